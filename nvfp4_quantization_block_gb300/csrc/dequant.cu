@@ -1,0 +1,103 @@
+// BF16 dequantization of MXFP8 / NVFP4 operands (the dequantized-backward mode).
+//
+// Definition [Miles-zh = page "Miles 在 Blackwell GPU 上实现低精度强化学习，降低训练成本", section
+// "高精度反向和去量化反向": the backward GEMMs run in BF16 on the dequantization of the exact
+// low-precision operands produced by the forward pass]: out = RN_bf16(exact value).
+//   MXFP8: E4M3(q) * 2^(sf-127) is an exact fp32 product (4 significant bits times a power of
+//          two), so one hardware bf16 conversion rounds it once.
+//   NVFP4: E2M1(q) * E4M3(sf) is exact in fp32; its product with the fp32 coarse scale s has up to
+//          30 significant bits. It is formed as t = RZ(p * s) plus the exact remainder
+//          fma(p, s, -t); the remainder's sign sets the last bit of t (round to odd), after which
+//          the bf16 conversion yields the single rounding of the exact product (Boldo & Melquiond,
+//          IEEE TC 2008). Tiny products, where the remainder could underflow, use fp64.
+// One thread produces one 32-element (MXFP8) or 16-element (NVFP4) block: 16- or 8-byte loads,
+// 64- or 32-byte stores, one scale byte, streaming through HBM once.
+#include "nvq_device.cuh"
+#include "nvq_internal.h"
+
+namespace nvq {
+
+__device__ __forceinline__ int64_t sf_index(int64_t row, int64_t kb, int64_t nkb, int mma_layout) {
+    return mma_layout ? mma_sf_offset(row, kb, nkb) : row * nkb + kb;
+}
+
+__global__ void __launch_bounds__(256)
+dequant_mxfp8_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ sf, int64_t rows,
+                     int64_t cols, int mma_layout, uint16_t* __restrict__ out) {
+    const int64_t nkb = cols >> 5;
+    const int64_t blk = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (blk >= rows * nkb) return;
+    const int64_t row = blk / nkb, kb = blk - row * nkb;
+    const float scale = e8m0_scale(sf[sf_index(row, kb, nkb, mma_layout)]);
+    const uint8_t* src = q + row * cols + kb * 32;
+    const uint4 a = ld_stream_v4(src), b = ld_stream_v4(src + 16);
+    const uint32_t in[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    uint32_t o[16];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        float f0, f1, f2, f3;
+        e4m3x2_to_f32(in[i] & 0xFFFFu, f0, f1);
+        e4m3x2_to_f32(in[i] >> 16, f2, f3);
+        o[2 * i] = cvt_bf16x2(f0 * scale, f1 * scale);
+        o[2 * i + 1] = cvt_bf16x2(f2 * scale, f3 * scale);
+    }
+    uint4* dst = reinterpret_cast<uint4*>(out + row * cols + kb * 32);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+}
+
+// RN_bf16(p * s) for exact fp32 p and s (both finite).
+__device__ __forceinline__ float round_odd_product(float p, float s) {
+    const float t = __fmul_rz(p, s);
+    if (fabsf(t) >= 0x1p-96f) {
+        const float r = fmaf(p, s, -t);
+        return r != 0.0f ? __uint_as_float(__float_as_uint(t) | 1u) : t;
+    }
+    if (p == 0.0f || s == 0.0f) return t;
+    return f64_to_f32_round_odd((double)p * (double)s);
+}
+
+__global__ void __launch_bounds__(256)
+dequant_nvfp4_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ sf,
+                     const float* __restrict__ s, int64_t rows_per_group, int64_t total_rows,
+                     int64_t cols, int scope_matrix, int mma_layout, uint16_t* __restrict__ out) {
+    const int64_t nkb = cols >> 4;
+    const int64_t blk = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (blk >= total_rows * nkb) return;
+    const int64_t row = blk / nkb, kb = blk - row * nkb;
+    const float coarse = s[scope_matrix ? row / rows_per_group : row];
+    const float v_sf = e4m3_to_f32(sf[sf_index(row, kb, nkb, mma_layout)]);
+    const uint2 packed = *reinterpret_cast<const uint2*>(q + row * (cols >> 1) + kb * 8);
+    const uint32_t in[2] = {packed.x, packed.y};
+    uint32_t o[8];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            float e0, e1;
+            e2m1x2_to_f32((in[i] >> (8 * j)) & 0xFFu, e0, e1);
+            o[4 * i + j] = cvt_bf16x2(round_odd_product(e0 * v_sf, coarse), round_odd_product(e1 * v_sf, coarse));
+        }
+    }
+    uint4* dst = reinterpret_cast<uint4*>(out + row * cols + kb * 16);
+    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+cudaError_t launch_dequantize_bf16(int fmt_nvfp4, const uint8_t* q, const uint8_t* sf, const float* s,
+                                   int scope_matrix, int64_t groups, int64_t rows, int64_t cols,
+                                   int mma_layout, uint16_t* out, cudaStream_t stream) {
+    const int64_t total_rows = groups * rows;
+    if (!fmt_nvfp4) {
+        const int64_t nblk = total_rows * (cols >> 5);
+        dequant_mxfp8_kernel<<<(unsigned)((nblk + 255) / 256), 256, 0, stream>>>(q, sf, total_rows, cols,
+                                                                                  mma_layout, out);
+    } else {
+        const int64_t nblk = total_rows * (cols >> 4);
+        dequant_nvfp4_kernel<<<(unsigned)((nblk + 255) / 256), 256, 0, stream>>>(
+            q, sf, s, rows, total_rows, cols, scope_matrix, mma_layout, out);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace nvq

@@ -1,0 +1,634 @@
+// Block-scaled grouped GEMM for routed MoE experts on sm_103a tensor cores (tcgen05).
+//
+// Definition [Miles-zh = page "Miles 在 Blackwell GPU 上实现低精度强化学习，降低训练成本":
+// section "方案 1：端到端 MXFP8 强化学习" (forward, weight-gradient and data-gradient GEMMs run in
+// MXFP8, microscaling blocks along the reduction dimension); section "结果：在 8x B200 上对
+// Qwen3-30B-A3B 配方进行消融实验" (the per-token NVFP4 GEMM applies the FP32 per-token scaling in the
+// kernel epilogue instead of a separate op); NVFP4-ru = page "NVIDIA верифицировала 4-битный формат
+// NVFP4 ..." (FP4 GEMMs run natively on Blackwell tensor cores)]:
+//   GROUP_M: D[i, j] = s_a[i] s_b[e] sum_k deq(A)[i, k] deq(B[e])[j, k]   (rows i of group e)
+//   GROUP_K: D[e][i, j] = sum_{k in group e} deq(A)[i, k] deq(B)[j, k]
+//
+// Design (one CTA per SM, persistent, warp-specialised, 192 threads):
+//   warp 0 lane 0  TMA producer: 128x128-byte A tiles and 256x128-byte B tiles (128B swizzle)
+//                  plus the matching 512-byte scale tiles (bulk copies) into a ring of stages.
+//   warp 1 lane 0  MMA issuer: copies each stage's scale tiles smem -> TMEM (tcgen05.cp
+//                  32x128b.warpx4) and issues four tcgen05.mma block_scale instructions
+//                  (M=128, N=256; K=32 for MXFP8 E4M3 x UE8M0/32, K=64 for NVFP4 E2M1 x UE4M3/16),
+//                  accumulating in TMEM (fp32, 256 columns). Commits free smem stages and signal
+//                  the epilogue. Warp 1 also allocates and frees TMEM.
+//   warps 2-5      epilogue: tcgen05.ld 32 columns at a time, multiply by s_a[row] s_b[e], round
+//                  to bf16 (or keep fp32) and store with 16-byte vector stores.
+// Tiles are 128 rows x 256 columns; GROUP_M tiles start at the group's row offset (a multiple of
+// 32), so a tile's row scales span two 128-row scale tiles; both are copied to TMEM side by side
+// and the MMA's scale address starts at the tile's 32-row quarter within the first. GROUP_K
+// tiles iterate the group's reduction range in 32-element MMA steps (k-steps outside the group
+// inside a 128-element stage are skipped).
+//
+// Every wait on an mbarrier is bounded; a wait that runs out sets the caller's status word to
+// NVQ_DEV_TIMEOUT and a CTA-wide abort flag, and every role then leaves its loop, waits (bounded)
+// for the asynchronous work it issued, and the CTA frees its TMEM and exits.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/nvq.h"
+#include "nvq_device.cuh"
+
+namespace nvq {
+
+constexpr int GEMM_THREADS = 192;
+constexpr int BM = 128, BN = 256, BKB = 128;       // tile rows, tile columns, K bytes per stage
+constexpr int MAX_GROUPS = 1024;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t WAIT_LIMIT = 1u << 26;            // bounded spin: far beyond any legitimate wait
+
+template <bool FP4>
+struct GemmCfg {
+    static constexpr int STAGES = FP4 ? 3 : 4;
+    static constexpr int KGS = FP4 ? 4 : 1;            // 4-scale-column groups per stage
+    static constexpr int EPS = FP4 ? 256 : 128;        // reduction elements per stage
+    static constexpr int MMA_K = FP4 ? 64 : 32;        // reduction elements per MMA
+    static constexpr int A_BYTES = BM * BKB;
+    static constexpr int B_BYTES = BN * BKB;
+    static constexpr int SFA_BYTES = 2 * KGS * 512;
+    static constexpr int SFB_BYTES = 2 * KGS * 512;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+    static constexpr uint32_t SF_COLS = KGS * 8;       // TMEM columns per operand's scales
+    static constexpr uint32_t IDESC =
+        (FP4 ? ((1u << 7) | (1u << 10)) : 0u)         // A, B format: E2M1 (mxf4nvf4) or E4M3
+        | ((uint32_t)(BN >> 3) << 17)                  // N >> 3
+        | (FP4 ? 0u : (1u << 23))                      // scale type: UE4M3 (0) / UE8M0 (1)
+        | ((uint32_t)(BM >> 7) << 27);                 // M >> 7
+    static constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + 256 + 8 * (MAX_GROUPS + 1);
+};
+
+struct GemmParams {
+    int mode;
+    int out_f32;
+    int groups;
+    int64_t m, n, k;
+    const uint8_t* sfa;
+    const uint8_t* sfb;
+    const float* s_a;
+    const float* s_b;
+    const int64_t* offsets;
+    void* d;
+    int64_t ldd;
+    int32_t* status;
+    int64_t a_rowtiles;     // 128-row scale tiles of A
+    int64_t b_rowtiles;     // 128-row scale tiles of B (stacked rows)
+    int64_t sf_tiles_per_row;   // 4-column scale tiles per row (same for A and B)
+};
+
+// ------------------------------------------------------------------------------------------------
+// PTX wrappers
+// ------------------------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait; returns false (and raises the abort flag / status) when the limit is reached or
+// another role has already aborted.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          int32_t* status) {
+    for (uint32_t it = 0; it < WAIT_LIMIT; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 1023u) == 1023u && *abort_flag) return false;
+    }
+    *abort_flag = 1;
+    if (status) atomicExch(status, NVQ_DEV_TIMEOUT);
+    return false;
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int32_t x, int32_t y,
+                                            uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Shared-memory matrix descriptor (tcgen05): start >> 4, LBO >> 4, SBO >> 4, version 1, swizzle.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo, uint32_t swizzle) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)(lbo >> 4) << 16) | ((uint64_t)(sbo >> 4) << 32) |
+           (1ull << 46) | ((uint64_t)swizzle << 61);
+}
+
+template <bool FP4>
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    if constexpr (FP4) {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+            ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+            : "memory");
+    } else {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+            ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+            : "memory");
+    }
+}
+
+__device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// ------------------------------------------------------------------------------------------------
+// Tile schedule (identical in every role)
+// ------------------------------------------------------------------------------------------------
+struct Tile {
+    int e;
+    int64_t a_row0;     // first A row of the tile (GROUP_M: inside group e; GROUP_K: output row)
+    int64_t b_row0;     // first B row of the tile (stacked rows)
+    int64_t row_end;    // GROUP_M: end of group e's rows (exclusive); GROUP_K: m
+    int64_t n0;         // first output column
+    int64_t k_begin, k_end;   // reduction range (elements)
+    int64_t d_row0;     // first output row in D's row space
+};
+
+struct Schedule {
+    const int32_t* off;        // group offsets (smem, int32)
+    const int32_t* tile_start; // GROUP_M: prefix of tiles per group (smem)
+    int mode, groups;
+    int64_t m, n, k;
+    int n_tiles, m_tiles;      // GROUP_K: per-group tile grid
+    int64_t total;
+
+    __device__ Tile get(int64_t t) const {
+        Tile tl;
+        if (mode == NVQ_GEMM_GROUP_M) {
+            int lo = 0, hi = groups - 1;           // largest e with tile_start[e] <= t
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (tile_start[mid] <= t) lo = mid; else hi = mid - 1;
+            }
+            const int e = lo;
+            const int64_t local = t - tile_start[e];
+            const int64_t mt = local / n_tiles, nt = local - mt * n_tiles;
+            tl.e = e;
+            tl.a_row0 = off[e] + mt * BM;
+            tl.row_end = min((int64_t)off[e + 1], m);
+            tl.n0 = nt * BN;
+            tl.b_row0 = (int64_t)e * n + tl.n0;
+            tl.k_begin = 0;
+            tl.k_end = k;
+            tl.d_row0 = tl.a_row0;
+        } else {
+            const int64_t per = (int64_t)m_tiles * n_tiles;
+            const int e = (int)(t / per);
+            const int64_t local = t - (int64_t)e * per;
+            const int64_t mt = local / n_tiles, nt = local - mt * n_tiles;
+            tl.e = e;
+            tl.a_row0 = mt * BM;
+            tl.row_end = m;
+            tl.n0 = nt * BN;
+            tl.b_row0 = tl.n0;
+            tl.k_begin = off[e];
+            tl.k_end = off[e + 1];
+            tl.d_row0 = (int64_t)e * m + tl.a_row0;
+        }
+        return tl;
+    }
+};
+
+// ------------------------------------------------------------------------------------------------
+// Kernel
+// ------------------------------------------------------------------------------------------------
+template <bool FP4>
+__global__ void __launch_bounds__(GEMM_THREADS, 1)
+block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                         const GemmParams p) {
+    using C = GemmCfg<FP4>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* stage_base = smem;
+    uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
+    uint64_t* empty_bar = full_bar + C::STAGES;
+    uint64_t* tmem_full = empty_bar + C::STAGES;
+    uint64_t* tmem_empty = tmem_full + 1;
+    uint64_t* mma_done = tmem_empty + 1;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(mma_done + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+    int* bad_flag = reinterpret_cast<int*>(tmem_holder + 2);
+    int32_t* off32 = reinterpret_cast<int32_t*>(smem + C::STAGES * C::STAGE_BYTES + 256);
+    int32_t* tile_start = off32 + (MAX_GROUPS + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = p.groups;
+    const int n_tiles = (int)((p.n + BN - 1) / BN);
+
+    // ---- validate offsets and build the schedule (all threads see the same smem) ----
+    if (threadIdx.x == 0) {
+        *abort_flag = 0;
+        *bad_flag = 0;
+    }
+    __syncthreads();
+    const int64_t limit = (p.mode == NVQ_GEMM_GROUP_M) ? p.m : p.k;
+    for (int e = threadIdx.x; e <= G; e += blockDim.x) {
+        const int64_t o = p.offsets[e];
+        const bool ok = (o >= 0) && (o <= limit) && ((o & 31) == 0) && (e > 0 || o == 0) &&
+                        (e == 0 || p.offsets[e - 1] <= o);
+        if (!ok) *bad_flag = 1;
+        off32[e] = (int32_t)o;
+    }
+    __syncthreads();
+    if (*bad_flag) {
+        if (threadIdx.x == 0 && blockIdx.x == 0 && p.status) atomicExch(p.status, NVQ_DEV_BAD_OFFSETS);
+        return;
+    }
+    int64_t total;
+    Schedule sched;
+    sched.off = off32;
+    sched.tile_start = tile_start;
+    sched.mode = p.mode;
+    sched.groups = G;
+    sched.m = p.m;
+    sched.n = p.n;
+    sched.k = p.k;
+    sched.n_tiles = n_tiles;
+    sched.m_tiles = (int)((p.m + BM - 1) / BM);
+    if (p.mode == NVQ_GEMM_GROUP_M) {
+        if (threadIdx.x == 0) {
+            int32_t acc = 0;
+            for (int e = 0; e < G; ++e) {
+                tile_start[e] = acc;
+                acc += (int32_t)(((off32[e + 1] - off32[e]) + BM - 1) / BM) * n_tiles;
+            }
+            tile_start[G] = acc;
+        }
+        __syncthreads();
+        total = tile_start[G];
+    } else {
+        total = (int64_t)G * sched.m_tiles * n_tiles;
+    }
+    sched.total = total;
+
+    // ---- barriers and TMEM ----
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&empty_bar[s], 1);
+        }
+        mbar_init(tmem_full, 1);
+        mbar_init(tmem_empty, 128);
+        mbar_init(mma_done, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(smem_u32(tmem_holder)), "r"(TMEM_COLS) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+    const uint32_t tmem_acc = tmem_base;
+    const uint32_t tmem_sfa = tmem_base + BN;
+    const uint32_t tmem_sfb = tmem_base + BN + C::SF_COLS;
+
+    const int64_t k_stages_total = (p.k + C::EPS - 1) / C::EPS;   // stages over the whole K extent
+
+    if (warp == 0 && lane == 0) {
+        // =========================== TMA producer ===========================
+        int slot = 0;
+        uint32_t phase = 0;
+        int64_t issued = 0;
+        bool ok = true;
+        for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            const Tile tl = sched.get(t);
+            if (tl.k_end <= tl.k_begin) continue;
+            const int64_t ks0 = tl.k_begin / C::EPS, ks1 = (tl.k_end + C::EPS - 1) / C::EPS;
+            const int64_t rb_a = tl.a_row0 / BM;
+            const bool need_a2 = (tl.a_row0 % BM) != 0 && rb_a + 1 < p.a_rowtiles;
+            const int64_t rb_b = tl.b_row0 / BM;
+            const bool need_b2 = rb_b + 1 < p.b_rowtiles;
+            for (int64_t ks = ks0; ks < ks1; ++ks) {
+                if (!mbar_wait(&empty_bar[slot], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+                uint8_t* st = stage_base + (size_t)slot * C::STAGE_BYTES;
+                uint8_t* sa = st;
+                uint8_t* sb = st + C::A_BYTES;
+                uint8_t* ssfa = sb + C::B_BYTES;
+                uint8_t* ssfb = ssfa + C::SFA_BYTES;
+                const int64_t kg0 = ks * C::KGS;
+                const int64_t kgn = min((int64_t)C::KGS, p.sf_tiles_per_row - kg0);
+                const uint32_t sf_bytes = (uint32_t)kgn * 512u;
+                const uint32_t tx = C::A_BYTES + C::B_BYTES + sf_bytes * (1u + (need_a2 ? 1u : 0u)) +
+                                    sf_bytes * (1u + (need_b2 ? 1u : 0u));
+                mbar_arrive_expect_tx(&full_bar[slot], tx);
+                tma_load_2d(sa, &tmap_a, (int32_t)(ks * BKB), (int32_t)tl.a_row0, &full_bar[slot]);
+                tma_load_2d(sb, &tmap_b, (int32_t)(ks * BKB), (int32_t)tl.b_row0, &full_bar[slot]);
+                bulk_load(ssfa, p.sfa + ((rb_a * p.sf_tiles_per_row + kg0) << 9), sf_bytes, &full_bar[slot]);
+                if (need_a2)
+                    bulk_load(ssfa + C::KGS * 512, p.sfa + (((rb_a + 1) * p.sf_tiles_per_row + kg0) << 9), sf_bytes,
+                              &full_bar[slot]);
+                bulk_load(ssfb, p.sfb + ((rb_b * p.sf_tiles_per_row + kg0) << 9), sf_bytes, &full_bar[slot]);
+                if (need_b2)
+                    bulk_load(ssfb + C::KGS * 512, p.sfb + (((rb_b + 1) * p.sf_tiles_per_row + kg0) << 9), sf_bytes,
+                              &full_bar[slot]);
+                ++issued;
+                if (++slot == C::STAGES) { slot = 0; phase ^= 1u; }
+            }
+        }
+        // wait (bounded) until the copies of the last fill of every slot have landed
+        const int64_t n_last = issued < C::STAGES ? issued : C::STAGES;
+        for (int64_t i = 0; i < n_last; ++i) {
+            int s2 = slot - 1 - (int)i;
+            uint32_t ph = phase;
+            if (s2 < 0) { s2 += C::STAGES; ph ^= 1u; }
+            for (uint32_t it = 0; it < WAIT_LIMIT && !mbar_try_wait(&full_bar[s2], ph); ++it) {}
+        }
+    } else if (warp == 1 && lane == 0) {
+        // =========================== MMA issuer ===========================
+        int slot = 0;
+        uint32_t phase = 0;
+        uint32_t acc_phase = 0;
+        bool ok = true;
+        const uint32_t stage0 = smem_u32(stage_base);
+        for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            const Tile tl = sched.get(t);
+            if (tl.k_end <= tl.k_begin) continue;
+            if (!mbar_wait(tmem_empty, acc_phase ^ 1u, abort_flag, p.status)) break;
+            tc_fence_after();
+            const int64_t ks0 = tl.k_begin / C::EPS, ks1 = (tl.k_end + C::EPS - 1) / C::EPS;
+            const uint32_t g0 = (uint32_t)((tl.a_row0 % BM) / 32);
+            uint32_t accumulate = 0;
+            for (int64_t ks = ks0; ks < ks1; ++ks) {
+                if (!mbar_wait(&full_bar[slot], phase, abort_flag, p.status)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t sa = stage0 + (uint32_t)slot * C::STAGE_BYTES;
+                const uint32_t sb = sa + C::A_BYTES;
+                const uint32_t ssfa = sb + C::B_BYTES;
+                const uint32_t ssfb = ssfa + C::SFA_BYTES;
+                // scales -> TMEM: SFA k-group j at columns [8j, 8j+8) (two 128-row tiles), same for SFB
+#pragma unroll
+                for (int j = 0; j < C::KGS; ++j) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        tc_cp_sf(tmem_sfa + 8 * j + 4 * h, smem_desc(ssfa + (h * C::KGS + j) * 512, 0, 128, 0));
+                        tc_cp_sf(tmem_sfb + 8 * j + 4 * h, smem_desc(ssfb + (h * C::KGS + j) * 512, 0, 128, 0));
+                    }
+                }
+                const uint64_t adesc0 = smem_desc(sa, 16, 1024, 2);
+                const uint64_t bdesc0 = smem_desc(sb, 16, 1024, 2);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int64_t kel = ks * C::EPS + (int64_t)j * C::MMA_K;
+                    if (kel < tl.k_begin || kel >= tl.k_end) continue;
+                    const uint32_t kg = FP4 ? (uint32_t)j : 0u;
+                    const uint32_t sf_id = FP4 ? 0u : (uint32_t)j;
+                    const uint32_t idesc = C::IDESC | (sf_id << 4) | (sf_id << 29);
+                    // K advance inside the 128-byte swizzled row: 32 bytes per MMA (encoded >> 4)
+                    tc_mma<FP4>(tmem_acc, adesc0 + (uint64_t)(2 * j), bdesc0 + (uint64_t)(2 * j), idesc,
+                                tmem_sfa + 8 * kg + g0, tmem_sfb + 8 * kg, accumulate);
+                    accumulate = 1;
+                }
+                tc_commit(&empty_bar[slot]);
+                if (++slot == C::STAGES) { slot = 0; phase ^= 1u; }
+            }
+            if (!ok) break;
+            tc_commit(tmem_full);
+            acc_phase ^= 1u;
+        }
+        // wait (bounded) for every tcgen05 operation issued above before TMEM is released
+        tc_commit(mma_done);
+        for (uint32_t it = 0; it < WAIT_LIMIT && !mbar_try_wait(mma_done, 0); ++it) {}
+    } else if (warp >= 2) {
+        // =========================== epilogue ===========================
+        const int q = warp & 3;                       // TMEM lane quarter this warp may access
+        const int row_in_tile = q * 32 + lane;
+        uint32_t acc_phase = 0;
+        for (int64_t t = blockIdx.x; t < total; t += gridDim.x) {
+            const Tile tl = sched.get(t);
+            const int64_t row = tl.a_row0 + row_in_tile;
+            const bool row_ok = row < tl.row_end;
+            const int64_t drow = tl.d_row0 + row_in_tile;
+            float scale = 1.0f;
+            if (row_ok && p.s_a) scale = p.s_a[row];
+            if (p.s_b) scale *= p.s_b[tl.e];
+            const bool empty = tl.k_end <= tl.k_begin;
+            if (!empty) {
+                if (!mbar_wait(tmem_full, acc_phase, abort_flag, p.status)) break;
+                tc_fence_after();
+            }
+            for (int c = 0; c < BN / 32; ++c) {
+                const int64_t col = tl.n0 + c * 32;
+                uint32_t r[32];
+                if (!empty) {
+                    tmem_ld32(tmem_acc + ((uint32_t)(q * 32) << 16) + (uint32_t)(c * 32), r);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) r[j] = 0u;
+                }
+                if (!row_ok || col >= p.n) continue;
+                if (p.out_f32) {
+                    float* dst = reinterpret_cast<float*>(p.d) + drow * p.ldd + col;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        float4 v = make_float4(__uint_as_float(r[4 * j]) * scale, __uint_as_float(r[4 * j + 1]) * scale,
+                                               __uint_as_float(r[4 * j + 2]) * scale, __uint_as_float(r[4 * j + 3]) * scale);
+                        reinterpret_cast<float4*>(dst)[j] = v;
+                    }
+                } else {
+                    uint16_t* dst = reinterpret_cast<uint16_t*>(p.d) + drow * p.ldd + col;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        uint4 v;
+                        v.x = cvt_bf16x2(__uint_as_float(r[8 * j + 0]) * scale, __uint_as_float(r[8 * j + 1]) * scale);
+                        v.y = cvt_bf16x2(__uint_as_float(r[8 * j + 2]) * scale, __uint_as_float(r[8 * j + 3]) * scale);
+                        v.z = cvt_bf16x2(__uint_as_float(r[8 * j + 4]) * scale, __uint_as_float(r[8 * j + 5]) * scale);
+                        v.w = cvt_bf16x2(__uint_as_float(r[8 * j + 6]) * scale, __uint_as_float(r[8 * j + 7]) * scale);
+                        reinterpret_cast<uint4*>(dst)[j] = v;
+                    }
+                }
+            }
+            if (!empty) {
+                tc_fence_before();
+                mbar_arrive(tmem_empty);
+                acc_phase ^= 1u;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
+                     : "memory");
+    }
+}
+
+// ------------------------------------------------------------------------------------------------
+// Host side
+// ------------------------------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn get_encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+// 2-D uint8 tensor map over [rows, row_bytes] with a (box_rows x 128-byte) box, 128B swizzle,
+// zero fill out of bounds.
+static bool make_tmap(CUtensorMap* map, const void* base, int64_t rows, int64_t row_bytes, uint32_t box_rows) {
+    EncodeTiledFn enc = get_encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+    cuuint32_t box[2] = {(cuuint32_t)BKB, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+static int num_sms() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n;
+}
+
+template <bool FP4>
+static nvq_status launch_gemm(const nvq_gemm_args* a, cudaStream_t stream) {
+    using C = GemmCfg<FP4>;
+    const int64_t row_bytes = FP4 ? a->k / 2 : a->k;
+    const int64_t rows_a = a->m;
+    const int64_t rows_b = (a->mode == NVQ_GEMM_GROUP_M) ? a->groups * a->n : a->n;
+    CUtensorMap ta, tb;
+    if (!make_tmap(&ta, a->a, rows_a, row_bytes, BM) || !make_tmap(&tb, a->b, rows_b, row_bytes, BN))
+        return NVQ_ERR_CUDA;
+    GemmParams p;
+    p.mode = a->mode;
+    p.out_f32 = a->out_type == NVQ_OUT_F32;
+    p.groups = (int)a->groups;
+    p.m = a->m;
+    p.n = a->n;
+    p.k = a->k;
+    p.sfa = static_cast<const uint8_t*>(a->sfa);
+    p.sfb = static_cast<const uint8_t*>(a->sfb);
+    p.s_a = a->s_a;
+    p.s_b = a->s_b;
+    p.offsets = a->offsets;
+    p.d = a->d;
+    p.ldd = a->ldd;
+    p.status = a->status;
+    p.a_rowtiles = (rows_a + BM - 1) / BM;
+    p.b_rowtiles = (rows_b + BM - 1) / BM;
+    const int64_t kb = a->k / (FP4 ? 16 : 32);
+    p.sf_tiles_per_row = (kb + 3) / 4;
+
+    static bool attr_set[2] = {false, false};
+    if (!attr_set[FP4]) {
+        if (cudaFuncSetAttribute(block_scaled_gemm_kernel<FP4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)C::SMEM_BYTES) != cudaSuccess)
+            return NVQ_ERR_CUDA;
+        attr_set[FP4] = true;
+    }
+    const int grid = num_sms();
+    if (grid <= 0) return NVQ_ERR_CUDA;
+    block_scaled_gemm_kernel<FP4><<<grid, GEMM_THREADS, C::SMEM_BYTES, stream>>>(ta, tb, p);
+    return cudaGetLastError() == cudaSuccess ? NVQ_OK : NVQ_ERR_CUDA;
+}
+
+}  // namespace nvq
+
+namespace {
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+}  // namespace
+
+extern "C" nvq_status block_scaled_grouped_gemm(const nvq_gemm_args* a, void* stream) {
+    if (a == nullptr) return NVQ_ERR_INVALID_ARG;
+    if ((a->fmt != NVQ_MXFP8 && a->fmt != NVQ_NVFP4) || (a->mode != NVQ_GEMM_GROUP_M && a->mode != NVQ_GEMM_GROUP_K) ||
+        (a->out_type != NVQ_OUT_BF16 && a->out_type != NVQ_OUT_F32))
+        return NVQ_ERR_INVALID_ARG;
+    if (a->groups < 0 || a->m < 0 || a->n < 0 || a->k < 0) return NVQ_ERR_INVALID_ARG;
+    if (a->groups == 0 || a->m == 0 || a->n == 0) return NVQ_OK;
+    if (a->groups > nvq::MAX_GROUPS) return NVQ_ERR_UNSUPPORTED;
+    if (a->a == nullptr || a->b == nullptr || a->sfa == nullptr || a->sfb == nullptr || a->offsets == nullptr ||
+        a->d == nullptr)
+        return NVQ_ERR_INVALID_ARG;
+    if (a->k == 0 || a->k % 128 || a->n % 128) return NVQ_ERR_INVALID_ARG;
+    if (a->ldd < a->n || a->ldd % 8) return NVQ_ERR_INVALID_ARG;
+    if (a->m > INT32_MAX || a->k > INT32_MAX || a->groups * a->n > INT32_MAX) return NVQ_ERR_UNSUPPORTED;
+    if (a->mode == NVQ_GEMM_GROUP_K) {
+        if (a->fmt != NVQ_MXFP8) return NVQ_ERR_UNSUPPORTED;
+        if (a->m % 128 || a->s_a != nullptr) return NVQ_ERR_INVALID_ARG;
+    }
+    if (!aligned16(a->a) || !aligned16(a->b) || !aligned16(a->sfa) || !aligned16(a->sfb) || !aligned16(a->d) ||
+        (reinterpret_cast<uintptr_t>(a->offsets) & 7u))
+        return NVQ_ERR_MISALIGNED;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return a->fmt == NVQ_NVFP4 ? nvq::launch_gemm<true>(a, s) : nvq::launch_gemm<false>(a, s);
+}

@@ -1,0 +1,26 @@
+// Internal launch functions behind the C-ABI (include/nvq.h). Each enqueues kernels on `stream`
+// and returns the launch status; argument checking happens in api.cu before any of these runs.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace nvq {
+
+cudaError_t launch_mxfp8_quantize(const uint16_t* x, int64_t R, int64_t C, int64_t ldx,
+                                  uint8_t* q_row, uint8_t* sf_row, uint8_t* q_colT, uint8_t* sf_colT,
+                                  int mma_layout, cudaStream_t stream);
+
+cudaError_t launch_nvfp4_quantize_per_token(const uint16_t* x, int64_t R, int64_t C, int64_t ldx,
+                                            uint8_t* q, uint8_t* sf, float* s_tok, int mma_layout,
+                                            cudaStream_t stream);
+
+cudaError_t launch_nvfp4_quantize_weights(const uint16_t* w, int64_t E, int64_t K, int64_t N,
+                                          uint8_t* qT, uint8_t* sfT, float* s_w, int mma_layout,
+                                          cudaStream_t stream);
+
+cudaError_t launch_dequantize_bf16(int fmt_nvfp4, const uint8_t* q, const uint8_t* sf, const float* s,
+                                   int scope_matrix, int64_t groups, int64_t rows, int64_t cols,
+                                   int mma_layout, uint16_t* out, cudaStream_t stream);
+
+struct GemmLaunch;   // defined in gemm_sm103.cu
+}  // namespace nvq

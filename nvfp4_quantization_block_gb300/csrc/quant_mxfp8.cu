@@ -1,0 +1,147 @@
+// MXFP8 quantizer: rowwise 1x32 and columnwise 32x1 copies of a bf16 matrix in one pass.
+//
+// Definition [Miles-zh = page "Miles 在 Blackwell GPU 上实现低精度强化学习，降低训练成本",
+// section "为什么需要 Blackwell 原生方案？" (32 E4M3 values share an E8M0 power-of-two scale, rounded up
+// so the block maximum is not clipped) and section "方案 1：端到端 MXFP8 强化学习" (rowwise 1x32 and
+// columnwise 32x1 copies are numerically different and are both quantized from the original
+// full-precision data during quantization)].
+//
+// Design: one CTA per 128 x 128 bf16 tile (32 KB). Each warp streams two 256-byte row segments per
+// instruction with 128-bit loads; the rowwise copy is produced straight from registers (a 1x32
+// block is four lanes, amax by two xor-shuffles). The tile is parked in shared memory, and the
+// columnwise copy is produced from it by 256 threads, each owning a column pair of one 32-row
+// block (conflict-free: a warp reads 128 contiguous bytes of one tile row per access). The
+// columnwise codes are written transposed, 32 contiguous bytes per column and block. Input bytes
+// are read from HBM exactly once.
+#include "nvq_device.cuh"
+#include "nvq_internal.h"
+
+namespace nvq {
+
+constexpr int MX_TILE = 128;
+constexpr int MX_THREADS = 256;
+
+__global__ void __launch_bounds__(MX_THREADS)
+mxfp8_quant_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t C, int64_t ldx,
+                   uint8_t* __restrict__ q_row, uint8_t* __restrict__ sf_row,
+                   uint8_t* __restrict__ q_colT, uint8_t* __restrict__ sf_colT, int mma_layout) {
+    __shared__ __align__(16) uint32_t tile[MX_TILE][MX_TILE / 2];   // bf16 pairs
+    __shared__ __align__(4) uint8_t sfT_stage[MX_TILE][4];
+
+    const int64_t r0 = (int64_t)blockIdx.y * MX_TILE;
+    const int64_t c0 = (int64_t)blockIdx.x * MX_TILE;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const bool do_row = q_row != nullptr, do_col = q_colT != nullptr;
+    const int64_t kb_row = C >> 5;          // scale columns of the rowwise copy
+    const int64_t kb_col = R >> 5;          // scale columns of the columnwise copy
+
+    // ---- load: 8 instructions per thread, each 16 bytes = 8 bf16 of one row ----
+    uint4 v[8];
+    const int cc = (lane & 15) * 8;
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+        const int rr = it * 16 + warp * 2 + (lane >> 4);
+        const int64_t r = r0 + rr, c = c0 + cc;
+        v[it] = make_uint4(0u, 0u, 0u, 0u);
+        if (r < R && c < C) v[it] = ld_stream_v4(x + r * ldx + c);
+    }
+
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+        const int rr = it * 16 + warp * 2 + (lane >> 4);
+        const int64_t r = r0 + rr, c = c0 + cc;
+        if (do_col) *reinterpret_cast<uint4*>(&tile[rr][cc >> 1]) = v[it];
+        if (do_row) {
+            uint32_t m = absmax_bits_8(v[it]);
+            m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
+            m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
+            const uint32_t sf = e8m0_byte(m << 16);
+            const float inv = e8m0_inv_scale(sf);
+            const uint32_t w0 = v[it].x, w1 = v[it].y, w2 = v[it].z, w3 = v[it].w;
+            uint32_t o0 = cvt_e4m3x2(bf16_lo(w0) * inv, bf16_hi(w0) * inv) |
+                          (cvt_e4m3x2(bf16_lo(w1) * inv, bf16_hi(w1) * inv) << 16);
+            uint32_t o1 = cvt_e4m3x2(bf16_lo(w2) * inv, bf16_hi(w2) * inv) |
+                          (cvt_e4m3x2(bf16_lo(w3) * inv, bf16_hi(w3) * inv) << 16);
+            if (r < R && c < C) *reinterpret_cast<uint2*>(q_row + r * C + c) = make_uint2(o0, o1);
+            // gather the four block scales of this 128-column row segment into the segment's lane 0
+            const uint32_t s4 = __shfl_down_sync(0xffffffffu, sf, 4);
+            const uint32_t s8 = __shfl_down_sync(0xffffffffu, sf, 8);
+            const uint32_t s12 = __shfl_down_sync(0xffffffffu, sf, 12);
+            if ((lane & 15) == 0) {
+                const int64_t kb0 = c0 >> 5;
+                if (mma_layout) {
+                    if (r < ((R + 127) & ~int64_t(127))) {
+                        uint32_t word = sf | (s4 << 8) | (s8 << 16) | (s12 << 24);
+                        *reinterpret_cast<uint32_t*>(sf_row + mma_sf_offset(r, kb0, kb_row)) = word;
+                    }
+                } else if (r < R) {
+                    const uint32_t s[4] = {sf, s4, s8, s12};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        if (kb0 + j < kb_row) sf_row[r * kb_row + kb0 + j] = (uint8_t)s[j];
+                }
+            }
+        }
+    }
+    if (!do_col) return;
+    __syncthreads();
+
+    // ---- columnwise: thread = (column pair cp, 32-row block rb) ----
+    const int cp = threadIdx.x & 63, rb = threadIdx.x >> 6;
+    uint32_t w[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) w[i] = tile[rb * 32 + i][cp];
+    uint32_t m2 = 0;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) m2 = __vmaxu2(m2, w[i] & 0x7FFF7FFFu);
+    const uint32_t sf_lo = e8m0_byte((m2 & 0xFFFFu) << 16);
+    const uint32_t sf_hi = e8m0_byte(m2 & 0xFFFF0000u);
+    const float inv_lo = e8m0_inv_scale(sf_lo), inv_hi = e8m0_inv_scale(sf_hi);
+    const int64_t c = c0 + 2 * cp;
+    const int64_t rs = r0 + rb * 32;
+    if (c < C && rs < R) {
+        uint32_t olo[8], ohi[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t a0 = w[4 * i], a1 = w[4 * i + 1], a2 = w[4 * i + 2], a3 = w[4 * i + 3];
+            olo[i] = cvt_e4m3x2(bf16_lo(a0) * inv_lo, bf16_lo(a1) * inv_lo) |
+                     (cvt_e4m3x2(bf16_lo(a2) * inv_lo, bf16_lo(a3) * inv_lo) << 16);
+            ohi[i] = cvt_e4m3x2(bf16_hi(a0) * inv_hi, bf16_hi(a1) * inv_hi) |
+                     (cvt_e4m3x2(bf16_hi(a2) * inv_hi, bf16_hi(a3) * inv_hi) << 16);
+        }
+        uint4* plo = reinterpret_cast<uint4*>(q_colT + c * R + rs);
+        uint4* phi = reinterpret_cast<uint4*>(q_colT + (c + 1) * R + rs);
+        plo[0] = make_uint4(olo[0], olo[1], olo[2], olo[3]);
+        plo[1] = make_uint4(olo[4], olo[5], olo[6], olo[7]);
+        phi[0] = make_uint4(ohi[0], ohi[1], ohi[2], ohi[3]);
+        phi[1] = make_uint4(ohi[4], ohi[5], ohi[6], ohi[7]);
+    }
+    sfT_stage[2 * cp][rb] = (uint8_t)sf_lo;
+    sfT_stage[2 * cp + 1][rb] = (uint8_t)sf_hi;
+    __syncthreads();
+    if (threadIdx.x < MX_TILE) {
+        const int64_t cr = c0 + threadIdx.x;             // row of the transposed copy
+        const int64_t kb0 = r0 >> 5;
+        const uint32_t word = *reinterpret_cast<const uint32_t*>(&sfT_stage[threadIdx.x][0]);
+        if (mma_layout) {
+            if (cr < ((C + 127) & ~int64_t(127)))
+                *reinterpret_cast<uint32_t*>(sf_colT + mma_sf_offset(cr, kb0, kb_col)) = word;
+        } else if (cr < C) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (kb0 + j < kb_col) sf_colT[cr * kb_col + kb0 + j] = (uint8_t)(word >> (8 * j));
+        }
+    }
+}
+
+cudaError_t launch_mxfp8_quantize(const uint16_t* x, int64_t R, int64_t C, int64_t ldx,
+                                  uint8_t* q_row, uint8_t* sf_row, uint8_t* q_colT, uint8_t* sf_colT,
+                                  int mma_layout, cudaStream_t stream) {
+    // the MMA layout pads rows to 128: cover the padded rows so the padding gets zero scales
+    dim3 grid((unsigned)((C + MX_TILE - 1) / MX_TILE), (unsigned)((R + MX_TILE - 1) / MX_TILE));
+    mxfp8_quant_kernel<<<grid, MX_THREADS, 0, stream>>>(x, R, C, ldx, q_row, sf_row, q_colT, sf_colT,
+                                                        mma_layout);
+    return cudaGetLastError();
+}
+
+}  // namespace nvq

@@ -1,0 +1,249 @@
+// NVFP4 quantizers: per-token activations and per-expert-matrix weights.
+//
+// Definition [Miles-zh = page "Miles 在 Blackwell GPU 上实现低精度强化学习，降低训练成本":
+// section "为什么需要 Blackwell 原生方案？" (E2M1 values, one E4M3 scale per 16 values rounded to
+// nearest, a coarse FP32 scale on top); section "逐 Token 激活值缩放" (one FP32 scale per token computed
+// online, fused into the quantization call that also emits the packed FP4 values and the block
+// scales; gate/up weights share one FP32 scale); section "比特精确量化器合约" (bit-exact contract,
+// no fast math)]. Coarse scale s = RN(amax / 2688); block scale = E4M3 RNE of amax_b / (6 s);
+// code = E2M1 RNE (saturating) of x / (E4M3(sf) s). Exactness: see nvq_device.cuh.
+//
+// Per-token design: one warp per token row. The row (up to 2048 elements) is held in registers
+// after one coalesced 128-bit pass, reduced to its amax with warp shuffles, and encoded from
+// registers, so each input byte is read from HBM once. A 1x16 block is two adjacent lanes.
+#include "nvq_device.cuh"
+#include "nvq_internal.h"
+
+namespace nvq {
+
+constexpr int TOK_THREADS = 256;          // 8 rows per CTA
+constexpr int TOK_NREG = 8;               // 8 x 256 elements held in registers per row
+
+__device__ __forceinline__ void store_sf_group(uint8_t* sf, int64_t row, int64_t kb0, int64_t nkb,
+                                               uint32_t word, int mma_layout) {
+    if (mma_layout) {
+        *reinterpret_cast<uint32_t*>(sf + mma_sf_offset(row, kb0, nkb)) = word;
+    } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (kb0 + j < nkb) sf[row * nkb + kb0 + j] = (uint8_t)(word >> (8 * j));
+    }
+}
+
+// One 256-element step of a row: lane holds 8 elements; lanes (2j, 2j+1) form one 1x16 block.
+__device__ __forceinline__ void token_chunk(const uint4& vv, int i, int lane, int64_t row, bool real,
+                                            int64_t nchunk, int64_t nkb, int64_t C, const Nvfp4Scope& sc,
+                                            const E4M3InvTable& inv, uint8_t* __restrict__ q,
+                                            uint8_t* __restrict__ sf, int mma_layout) {
+    const int64_t ch = (int64_t)i * 32 + lane;
+    uint32_t mb = absmax_bits_8(vv);
+    mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
+    const uint32_t sfc = nvfp4_block_scale(__uint_as_float(mb << 16), sc);
+    const uint32_t codes = nvfp4_encode8(vv, sfc, sc, inv);
+    if (real && ch < nchunk) *reinterpret_cast<uint32_t*>(q + row * (C >> 1) + ch * 4) = codes;
+    const uint32_t s2 = __shfl_down_sync(0xffffffffu, sfc, 2);
+    const uint32_t s4 = __shfl_down_sync(0xffffffffu, sfc, 4);
+    const uint32_t s6 = __shfl_down_sync(0xffffffffu, sfc, 6);
+    if ((lane & 7) == 0) {
+        const int64_t kb0 = (int64_t)i * 16 + (lane >> 1);
+        if (kb0 < nkb) store_sf_group(sf, row, kb0, nkb, sfc | (s2 << 8) | (s4 << 16) | (s6 << 24), mma_layout);
+    }
+}
+
+__global__ void __launch_bounds__(TOK_THREADS)
+nvfp4_token_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t C, int64_t ldx,
+                   uint8_t* __restrict__ q, uint8_t* __restrict__ sf, float* __restrict__ s_tok,
+                   int mma_layout, int64_t rows_cover) {
+    __shared__ E4M3InvTable inv;
+    init_e4m3_inv_table(inv);
+    __syncthreads();
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t row = (int64_t)blockIdx.x * (TOK_THREADS / 32) + warp;
+    if (row >= rows_cover) return;
+    const bool real = row < R;
+    const int64_t nchunk = C >> 3;                       // 8-element chunks
+    const int iters = (int)((nchunk + 31) >> 5);
+    const int64_t nkb = C >> 4;
+    const uint16_t* xr = x + row * ldx;
+
+    // pass 1: load (into registers where possible) and reduce the row's amax
+    uint4 v[TOK_NREG];
+    uint32_t m = 0;
+#pragma unroll
+    for (int i = 0; i < TOK_NREG; ++i) {
+        v[i] = make_uint4(0u, 0u, 0u, 0u);
+        const int64_t ch = (int64_t)i * 32 + lane;
+        if (real && i < iters && ch < nchunk) v[i] = ld_stream_v4(xr + ch * 8);
+        m = max(m, absmax_bits_8(v[i]));
+    }
+    for (int i = TOK_NREG; i < iters; ++i) {
+        const int64_t ch = (int64_t)i * 32 + lane;
+        if (real && ch < nchunk) m = max(m, absmax_bits_8(ld_stream_v4(xr + ch * 8)));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+    const float s = nvfp4_coarse_scale(__uint_as_float(m << 16));
+    const Nvfp4Scope sc = make_nvfp4_scope(s);
+    if (real && lane == 0) s_tok[row] = s;
+
+    // pass 2: per 1x16 block scale and codes (register-resident chunks first, then any reloads)
+#pragma unroll
+    for (int i = 0; i < TOK_NREG; ++i)
+        if (i < iters) token_chunk(v[i], i, lane, row, real, nchunk, nkb, C, sc, inv, q, sf, mma_layout);
+    for (int i = TOK_NREG; i < iters; ++i) {
+        const int64_t ch = (int64_t)i * 32 + lane;
+        const uint4 vv = (real && ch < nchunk) ? ld_stream_v4(xr + ch * 8) : make_uint4(0u, 0u, 0u, 0u);
+        token_chunk(vv, i, lane, row, real, nchunk, nkb, C, sc, inv, q, sf, mma_layout);
+    }
+}
+
+cudaError_t launch_nvfp4_quantize_per_token(const uint16_t* x, int64_t R, int64_t C, int64_t ldx,
+                                            uint8_t* q, uint8_t* sf, float* s_tok, int mma_layout,
+                                            cudaStream_t stream) {
+    const int64_t cover = mma_layout ? ((R + 127) & ~int64_t(127)) : R;
+    const int rows_per_cta = TOK_THREADS / 32;
+    const int64_t grid = (cover + rows_per_cta - 1) / rows_per_cta;
+    nvfp4_token_kernel<<<(unsigned)grid, TOK_THREADS, 0, stream>>>(x, R, C, ldx, q, sf, s_tok, mma_layout, cover);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------------------------------------
+// Weights: W [E, K, N] -> qT [E, N, K/2], sfT [E, N, K/16], s_w [E]; coarse scope = expert matrix.
+// Three kernels: amax per expert (atomic max on the fp32 bits, kept in s_w), encode (tiles of
+// 64 k x 64 n transposed through shared memory), finalize (s_w <- RN(amax / 2688)).
+// ------------------------------------------------------------------------------------------------
+constexpr int WT_K = 64, WT_N = 64, WT_THREADS = 256;
+
+__global__ void __launch_bounds__(256)
+nvfp4_weight_amax_kernel(const uint16_t* __restrict__ w, int64_t per_expert, uint32_t* __restrict__ amax_bits) {
+    const int64_t e = blockIdx.y;
+    const uint16_t* we = w + e * per_expert;
+    const int64_t nvec = per_expert >> 3;
+    uint32_t m = 0;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += (int64_t)gridDim.x * blockDim.x)
+        m = max(m, absmax_bits_8(ld_stream_v4(we + i * 8)));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+    __shared__ uint32_t red[8];
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        uint32_t t = red[0];
+        for (int j = 1; j < (int)(blockDim.x >> 5); ++j) t = max(t, red[j]);
+        if (t) atomicMax(amax_bits + e, t << 16);    // non-negative floats order like their bits
+    }
+}
+
+__global__ void __launch_bounds__(WT_THREADS)
+nvfp4_weight_encode_kernel(const uint16_t* __restrict__ w, int64_t K, int64_t N,
+                           uint8_t* __restrict__ qT, uint8_t* __restrict__ sfT,
+                           const uint32_t* __restrict__ amax_bits, int mma_layout) {
+    __shared__ __align__(16) uint32_t tile[WT_K][WT_N / 2];
+    __shared__ E4M3InvTable inv;
+    init_e4m3_inv_table(inv);
+
+    const int64_t e = blockIdx.z;
+    const int64_t k0 = (int64_t)blockIdx.y * WT_K, n0 = (int64_t)blockIdx.x * WT_N;
+    const uint16_t* we = w + e * K * N;
+    // load 64 x 64 bf16: each row is 8 chunks of 16 bytes; chunk index xor-swizzled by (row/16)
+#pragma unroll
+    for (int it = 0; it < 2; ++it) {
+        const int idx = it * WT_THREADS + threadIdx.x;
+        const int rr = idx >> 3, chunk = idx & 7;
+        const int64_t k = k0 + rr, n = n0 + chunk * 8;
+        uint4 val = make_uint4(0u, 0u, 0u, 0u);
+        if (k < K && n < N) val = ld_stream_v4(we + k * N + n);
+        *reinterpret_cast<uint4*>(&tile[rr][(chunk ^ ((rr >> 4) & 3)) * 4]) = val;
+    }
+    __syncthreads();
+
+    const int kblk = threadIdx.x & 3, nl = threadIdx.x >> 2;       // 4 consecutive lanes = one n
+    const int64_t n = n0 + nl;
+    const float s = nvfp4_coarse_scale(__uint_as_float(amax_bits[e]));
+    const Nvfp4Scope sc = make_nvfp4_scope(s);
+    // gather the 16 k-values of column nl: element j of the block is row 16*kblk + j
+    const int wcol = ((nl >> 1) >> 2), wsub = (nl >> 1) & 3;      // 16-byte chunk and word in it
+    const int half = nl & 1;
+    uint32_t p[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int ra = 16 * kblk + 2 * j, rb2 = ra + 1;
+        const uint32_t wa = tile[ra][((wcol ^ ((ra >> 4) & 3)) << 2) + wsub];
+        const uint32_t wb = tile[rb2][((wcol ^ ((rb2 >> 4) & 3)) << 2) + wsub];
+        const uint32_t ea = half ? (wa >> 16) : (wa & 0xFFFFu);
+        const uint32_t eb = half ? (wb >> 16) : (wb & 0xFFFFu);
+        p[j] = ea | (eb << 16);
+    }
+    const uint4 lo = make_uint4(p[0], p[1], p[2], p[3]), hi = make_uint4(p[4], p[5], p[6], p[7]);
+    const uint32_t mb = max(absmax_bits_8(lo), absmax_bits_8(hi));
+    const uint32_t sfc = nvfp4_block_scale(__uint_as_float(mb << 16), sc);
+    const uint32_t c0 = nvfp4_encode8(lo, sfc, sc, inv);
+    const uint32_t c1 = nvfp4_encode8(hi, sfc, sc, inv);
+    const int64_t kb = (k0 >> 4) + kblk, nkb = K >> 4;
+    if (n < N && kb < nkb) {
+        *reinterpret_cast<uint2*>(qT + (e * N + n) * (K >> 1) + kb * 8) = make_uint2(c0, c1);
+    }
+    // scale bytes: the 4 lanes of one n hold 4 consecutive blocks
+    const uint32_t s1 = __shfl_down_sync(0xffffffffu, sfc, 1);
+    const uint32_t s2 = __shfl_down_sync(0xffffffffu, sfc, 2);
+    const uint32_t s3 = __shfl_down_sync(0xffffffffu, sfc, 3);
+    if (kblk == 0) {
+        const int64_t row = e * N + n;
+        const int64_t kb0 = k0 >> 4;
+        const uint32_t word = sfc | (s1 << 8) | (s2 << 16) | (s3 << 24);
+        if (mma_layout) {
+            if (n < N) *reinterpret_cast<uint32_t*>(sfT + mma_sf_offset(row, kb0, nkb)) = word;
+        } else if (n < N) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (kb0 + j < nkb) sfT[row * nkb + kb0 + j] = (uint8_t)(word >> (8 * j));
+        }
+    }
+}
+
+__global__ void nvfp4_weight_finalize_kernel(float* s_w, int64_t E) {
+    const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (e < E) s_w[e] = nvfp4_coarse_scale(__uint_as_float(reinterpret_cast<uint32_t*>(s_w)[e]));
+}
+
+// zero the padding rows of an MMA-layout scale buffer beyond `rows` (rows not multiple of 128)
+__global__ void zero_bytes_kernel(uint8_t* p, int64_t n) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < n) p[i] = 0;
+}
+
+cudaError_t launch_nvfp4_quantize_weights(const uint16_t* w, int64_t E, int64_t K, int64_t N,
+                                          uint8_t* qT, uint8_t* sfT, float* s_w, int mma_layout,
+                                          cudaStream_t stream) {
+    cudaError_t err = cudaMemsetAsync(s_w, 0, sizeof(float) * (size_t)E, stream);
+    if (err != cudaSuccess) return err;
+    const int64_t per_expert = K * N;
+    int64_t blocks = (per_expert / 8 + 255) / 256;
+    if (blocks > 64) blocks = 64;
+    if (blocks < 1) blocks = 1;
+    nvfp4_weight_amax_kernel<<<dim3((unsigned)blocks, (unsigned)E), 256, 0, stream>>>(
+        w, per_expert, reinterpret_cast<uint32_t*>(s_w));
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    if (mma_layout) {
+        // rows of the stacked [E*N, K/16] scale matrix are padded to 128; the encode kernel writes
+        // every real row's tile bytes (column padding included), so only trailing pad rows remain
+        const int64_t rows = E * N, kb = K >> 4;
+        const int64_t padded_rows = (rows + 127) & ~int64_t(127);
+        if (padded_rows > rows) {
+            const int64_t start = mma_sf_offset(padded_rows - 128, 0, kb);   // last row tile
+            const int64_t bytes = ((kb + 3) >> 2) * 512;
+            // the tile also holds real rows; rewrite it fully below by zeroing first
+            zero_bytes_kernel<<<(unsigned)((bytes + 255) / 256), 256, 0, stream>>>(sfT + start, bytes);
+            if ((err = cudaGetLastError()) != cudaSuccess) return err;
+        }
+    }
+    dim3 grid((unsigned)((N + WT_N - 1) / WT_N), (unsigned)((K + WT_K - 1) / WT_K), (unsigned)E);
+    nvfp4_weight_encode_kernel<<<grid, WT_THREADS, 0, stream>>>(w, K, N, qT, sfT,
+                                                               reinterpret_cast<const uint32_t*>(s_w), mma_layout);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    nvfp4_weight_finalize_kernel<<<(unsigned)((E + 255) / 256), 256, 0, stream>>>(s_w, E);
+    return cudaGetLastError();
+}
+
+}  // namespace nvq

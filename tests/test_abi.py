@@ -1,0 +1,82 @@
+"""The C-ABI library builds for sm_103a, loads, exports every entry point include/nvq.h declares,
+and rejects bad arguments on the host before any launch (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "nvq.h")
+LIB = os.path.join(ROOT, "nvfp4_quantization_block_gb300", "libnvq.so")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(LIB):
+        import __graft_entry__
+        __graft_entry__.build()
+    return ctypes.CDLL(LIB)
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return re.findall(r"^\s*(?:const\s+)?\w+\*?\s+\*?(\w+)\s*\(", text, flags=re.M)
+
+
+def test_header_declares_the_boundary():
+    names = set(declared_functions())
+    for required in ["mxfp8_quantize", "nvfp4_quantize_per_token", "nvfp4_quantize_weights",
+                     "dequantize_bf16", "block_scaled_grouped_gemm", "nvq_status_string", "nvq_sf_bytes"]:
+        assert required in names, required
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"libnvq.so does not export {name}"
+
+
+def test_sf_bytes_and_status_strings(lib):
+    f = lib.nvq_sf_bytes
+    f.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int32, ctypes.c_int]
+    f.restype = ctypes.c_int64
+    assert f(256, 512, 32, 0) == 256 * 16
+    assert f(256, 512, 32, 1) == 256 * 16
+    assert f(300, 512, 16, 1) == 384 * 32
+    assert f(300, 48, 16, 1) == 384 * 4          # 3 scale columns pad to 4
+    assert f(10, 33, 32, 0) == -1
+    s = lib.nvq_status_string
+    s.argtypes = [ctypes.c_int]
+    s.restype = ctypes.c_char_p
+    assert s(0) == b"NVQ_OK" and s(2) == b"NVQ_ERR_MISALIGNED"
+
+
+def test_host_validation_rejects_before_launch(lib):
+    q = lib.mxfp8_quantize
+    vp = ctypes.c_void_p
+    q.argtypes = [vp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, vp, vp, vp, vp, ctypes.c_int, vp]
+    q.restype = ctypes.c_int
+    fake = vp(0x10000)          # never dereferenced: every call below fails validation first
+    odd = vp(0x10008)
+    assert q(fake, -1, 64, 64, fake, fake, None, None, 1, None) == 1          # negative rows
+    assert q(fake, 64, 48, 64, fake, fake, None, None, 1, None) == 1          # cols % 32
+    assert q(fake, 48, 64, 64, None, None, fake, fake, 1, None) == 1          # colwise needs rows % 32
+    assert q(fake, 64, 64, 64, fake, None, None, None, 1, None) == 1          # q without sf
+    assert q(odd, 64, 64, 64, fake, fake, None, None, 1, None) == 2           # misaligned input
+    assert q(fake, 64, 64, 60, fake, fake, None, None, 1, None) == 1          # ld < cols
+    assert q(fake, 64, 64, 68, fake, fake, None, None, 1, None) == 2          # ld % 8
+    assert q(fake, 64, 64, 64, fake, fake, None, None, 7, None) == 1          # bad layout enum
+    assert q(fake, 0, 64, 64, fake, fake, None, None, 1, None) == 0           # empty is a no-op
+    t = lib.nvfp4_quantize_per_token
+    t.argtypes = [vp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, vp, vp, vp, ctypes.c_int, vp]
+    t.restype = ctypes.c_int
+    assert t(fake, 4, 40, 40, fake, fake, fake, 0, None) == 1                 # cols % 16
+    assert t(fake, 4, 64, 64, fake, fake, None, 0, None) == 1                 # missing s_tok
+    assert t(fake, 0, 64, 64, None, None, None, 0, None) == 0
+    d = lib.dequantize_bf16
+    d.argtypes = [ctypes.c_int, vp, vp, vp, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                  ctypes.c_int, vp, vp]
+    d.restype = ctypes.c_int
+    assert d(1, fake, fake, None, 0, 1, 4, 32, 0, fake, None) == 1            # NVFP4 needs s
+    assert d(5, fake, fake, None, 0, 1, 4, 32, 0, fake, None) == 1            # bad format

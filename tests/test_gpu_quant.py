@@ -1,0 +1,262 @@
+"""GPU parity: the sm_103a quantizers and dequantizer against the CPU oracle, byte for byte.
+
+Input families follow the upstream contract tests described on the pages ("random", "boundary",
+"zeros", "maxes" [Miles-zh = page "Miles 在 Blackwell GPU 上实现低精度强化学习，降低训练成本", section
+"比特精确量化器合约"]), at sizes spanning several tiles with ragged tails, in both scale layouts.
+"""
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def nvq():
+    import nvfp4_quantization_block_gb300 as m
+    return m
+
+
+def _seed(*parts):
+    return zlib.crc32(repr(parts).encode()) % 10007
+
+
+def _np(t):
+    return t.detach().cpu().numpy()
+
+
+def _bits_of(x_f64):
+    """Host bf16 bits of float64 values (exactly representable ones stay exact)."""
+    return oracle.f64_to_bf16_bits_rne(np.asarray(x_f64, dtype=np.float64))
+
+
+def _dev(bits):
+    return workloads.from_bits(bits, "cuda")
+
+
+# ------------------------------------------------------------------------------------------------
+# input families
+# ------------------------------------------------------------------------------------------------
+def family(name, shape, seed=0):
+    rng = np.random.default_rng(seed)
+    R, C = shape
+    if name == "random":
+        x = rng.standard_normal(shape) * np.exp(rng.uniform(-12, 12, (R, 1)))
+        x *= np.where(rng.random(shape) < 0.01, 100.0, 1.0)
+        return _bits_of(x)
+    if name == "zeros":
+        b = np.zeros(shape, dtype=np.uint16)
+        b[rng.random(shape) < 0.3] = 0x8000          # negative zeros keep their sign
+        return b
+    if name == "maxes":
+        b = np.full(shape, 0x7F7F, dtype=np.uint16)
+        b[rng.random(shape) < 0.5] |= 0x8000
+        return b
+    if name == "boundary":
+        # values on E4M3 / E2M1 rounding midpoints and their bf16 neighbours, scaled by powers of
+        # two and by the "nice" NVFP4 token scale 2^k (token amax 42*2^(k+6)), plus subnormals
+        mids4 = (oracle.E4M3_VALUES[:-1] + oracle.E4M3_VALUES[1:]) / 2
+        mids2 = (oracle.E2M1_VALUES[:-1] + oracle.E2M1_VALUES[1:]) / 2
+        base = np.concatenate([mids4, oracle.E4M3_VALUES, mids2 * 8, mids2 * 11, mids2 * 448, [448, 450, 449.5]])
+        v = rng.choice(base, shape) * np.ldexp(1.0, rng.integers(-20, 20, (R, 1)))
+        v = oracle.bf16_bits_to_f64(_bits_of(v))
+        ulp = np.ldexp(1.0, np.frexp(v)[1] - 8)
+        v = v + rng.choice([-1, 0, 0, 0, 1], shape) * ulp
+        v *= rng.choice([-1, 1], shape)
+        tiny = rng.random(shape) < 0.03
+        v[tiny] = rng.integers(1, 200, tiny.sum()) * 2.0 ** -133
+        b = _bits_of(v)
+        # rows whose amax gives an exact power-of-two token scale
+        nice = rng.random(R) < 0.5
+        col = rng.integers(0, C, R)
+        b[nice, col[nice]] = _bits_of(42.0 * np.ldexp(1.0, rng.integers(-10, 10, nice.sum())))
+        return b
+    raise ValueError(name)
+
+
+FAMILIES = ["random", "boundary", "zeros", "maxes"]
+
+
+# ------------------------------------------------------------------------------------------------
+# MXFP8
+# ------------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("fam", FAMILIES)
+@pytest.mark.parametrize("shape", [(256, 512), (320, 416), (96, 64), (32, 32), (416, 1056)])
+@pytest.mark.parametrize("layout", ["canonical", "mma"])
+def test_mxfp8_row_col_bit_exact(nvq, fam, shape, layout):
+    bits = family(fam, shape, seed=_seed(fam, shape))
+    ref = oracle.mxfp8_quantize(bits)
+    out = nvq.mxfp8_quantize(_dev(bits), sf_layout=layout)
+    torch.cuda.synchronize()
+    assert np.array_equal(_np(out["q_row"]), ref["q_row"])
+    assert np.array_equal(_np(out["q_colT"]), ref["q_colT"])
+    if layout == "canonical":
+        assert np.array_equal(_np(out["sf_row"]).reshape(ref["sf_row"].shape), ref["sf_row"])
+        assert np.array_equal(_np(out["sf_colT"]).reshape(ref["sf_colT"].shape), ref["sf_colT"])
+    else:
+        assert np.array_equal(_np(out["sf_row"]), oracle.sf_to_mma_layout(ref["sf_row"]))
+        assert np.array_equal(_np(out["sf_colT"]), oracle.sf_to_mma_layout(ref["sf_colT"]))
+
+
+@pytest.mark.parametrize("shape", [(33, 64), (1, 32), (7, 96)])
+def test_mxfp8_rowwise_only_ragged_rows(nvq, shape):
+    bits = family("random", shape, seed=3)
+    ref = oracle.mxfp8_quantize(bits, colwise=False)
+    for layout in ("canonical", "mma"):
+        out = nvq.mxfp8_quantize(_dev(bits), colwise=False, sf_layout=layout)
+        assert np.array_equal(_np(out["q_row"]), ref["q_row"])
+        want = ref["sf_row"] if layout == "canonical" else oracle.sf_to_mma_layout(ref["sf_row"])
+        assert np.array_equal(_np(out["sf_row"]).reshape(want.shape), want)
+
+
+def test_mxfp8_strided_input(nvq):
+    bits = family("random", (128, 256), seed=4)
+    big = torch.zeros((128, 320), dtype=torch.bfloat16, device="cuda")
+    big[:, :256] = _dev(bits)
+    ref = oracle.mxfp8_quantize(bits)
+    out = nvq.mxfp8_quantize(big[:, :256], sf_layout="canonical")
+    assert np.array_equal(_np(out["q_row"]), ref["q_row"])
+    assert np.array_equal(_np(out["q_colT"]), ref["q_colT"])
+
+
+# ------------------------------------------------------------------------------------------------
+# NVFP4 per token
+# ------------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("fam", FAMILIES)
+@pytest.mark.parametrize("shape", [(300, 768), (257, 2048), (64, 4096), (5, 48), (130, 272)])
+@pytest.mark.parametrize("layout", ["canonical", "mma"])
+def test_nvfp4_per_token_bit_exact(nvq, fam, shape, layout):
+    bits = family(fam, shape, seed=_seed(fam, shape, 1))
+    q_ref, sf_ref, s_ref = oracle.nvfp4_quantize_per_token(bits)
+    q, sf, s = nvq.nvfp4_quantize_per_token(_dev(bits), sf_layout=layout)
+    torch.cuda.synchronize()
+    assert np.array_equal(_np(s).view(np.uint32), s_ref.view(np.uint32))
+    assert np.array_equal(_np(q), q_ref)
+    want = sf_ref if layout == "canonical" else oracle.sf_to_mma_layout(sf_ref)
+    assert np.array_equal(_np(sf).reshape(want.shape), want)
+
+
+@pytest.mark.parametrize("k", [-149, -140, -127, -120, -100, -91, -89])
+def test_nvfp4_tiny_token_scales(nvq, k):
+    # tokens whose coarse scale is subnormal or just around the fp32 fast-path threshold
+    rng = np.random.default_rng(-k)
+    x = rng.standard_normal((64, 256)) * 2688.0 * 2.0 ** k
+    bits = _bits_of(x)
+    q_ref, sf_ref, s_ref = oracle.nvfp4_quantize_per_token(bits)
+    q, sf, s = nvq.nvfp4_quantize_per_token(_dev(bits), sf_layout="canonical")
+    assert np.array_equal(_np(s).view(np.uint32), s_ref.view(np.uint32))
+    assert np.array_equal(_np(q), q_ref)
+    assert np.array_equal(_np(sf).reshape(sf_ref.shape), sf_ref)
+
+
+def test_nvfp4_per_token_invariance_on_gpu(nvq):
+    # a token's bytes do not depend on the rest of the batch (the scope the pages require)
+    bits = family("random", (512, 768), seed=9)
+    q, sf, s = nvq.nvfp4_quantize_per_token(_dev(bits), sf_layout="canonical")
+    perm = np.random.default_rng(1).permutation(512)[:100]
+    q2, sf2, s2 = nvq.nvfp4_quantize_per_token(_dev(np.ascontiguousarray(bits[perm])), sf_layout="canonical")
+    assert torch.equal(q2, q[torch.from_numpy(perm).cuda()])
+    assert torch.equal(s2, s[torch.from_numpy(perm).cuda()])
+
+
+# ------------------------------------------------------------------------------------------------
+# NVFP4 weights
+# ------------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("shape", [(3, 256, 192), (2, 80, 72), (1, 512, 384), (4, 64, 128)])
+@pytest.mark.parametrize("layout", ["canonical", "mma"])
+def test_nvfp4_weights_bit_exact(nvq, shape, layout):
+    E, K, N = shape
+    rng = np.random.default_rng(E * K + N)
+    w = rng.standard_normal(shape) * 0.02 * np.exp(rng.uniform(-3, 3, (E, 1, 1)))
+    w[0, :, : N // 2] *= 30.0                      # gate half larger than up half for expert 0
+    bits = _bits_of(w)
+    q_ref, sf_ref, s_ref = oracle.nvfp4_quantize_weights(bits)
+    q, sf, s = nvq.nvfp4_quantize_weights(_dev(bits).contiguous(), sf_layout=layout)
+    torch.cuda.synchronize()
+    assert np.array_equal(_np(s).view(np.uint32), s_ref.view(np.uint32))
+    assert np.array_equal(_np(q), q_ref)
+    if layout == "canonical":
+        assert np.array_equal(_np(sf).reshape(sf_ref.shape), sf_ref)
+    else:
+        assert np.array_equal(_np(sf), oracle.sf_to_mma_layout(sf_ref.reshape(E * N, K // 16)))
+
+
+# ------------------------------------------------------------------------------------------------
+# Dequantize
+# ------------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("fam", FAMILIES)
+@pytest.mark.parametrize("layout", ["canonical", "mma"])
+def test_dequantize_mxfp8_bit_exact(nvq, fam, layout):
+    bits = family(fam, (160, 224), seed=5)
+    ref = oracle.mxfp8_quantize(bits, colwise=False)
+    want = oracle.dequantize_mxfp8(ref["q_row"], ref["sf_row"])
+    sf = ref["sf_row"] if layout == "canonical" else oracle.sf_to_mma_layout(ref["sf_row"])
+    out = nvq.dequantize_bf16(nvq.MXFP8, torch.from_numpy(ref["q_row"]).cuda(), torch.from_numpy(sf).cuda(),
+                              rows=160, cols=224, sf_layout=layout)
+    got = out.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("fam", FAMILIES + ["tiny"])
+@pytest.mark.parametrize("layout", ["canonical", "mma"])
+def test_dequantize_nvfp4_rows_bit_exact(nvq, fam, layout):
+    if fam == "tiny":
+        x = np.random.default_rng(6).standard_normal((96, 272)) * 2.0 ** -120
+        bits = _bits_of(x)
+    else:
+        bits = family(fam, (96, 272), seed=6)
+    q, sf, s = oracle.nvfp4_quantize_per_token(bits)
+    want = oracle.dequantize_nvfp4(q, sf, s)
+    sfl = sf if layout == "canonical" else oracle.sf_to_mma_layout(sf)
+    out = nvq.dequantize_bf16(nvq.NVFP4, torch.from_numpy(q).cuda(), torch.from_numpy(sfl).cuda(),
+                              torch.from_numpy(s).cuda(), nvq.SCOPE_ROW, rows=96, cols=272, sf_layout=layout)
+    got = out.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert np.array_equal(got, want)
+
+
+def test_dequantize_nvfp4_weights_matrix_scope(nvq):
+    E, K, N = 3, 128, 64
+    rng = np.random.default_rng(7)
+    bits = _bits_of(rng.standard_normal((E, K, N)) * 0.02)
+    q, sf, s_w = oracle.nvfp4_quantize_weights(bits)
+    want = oracle.dequantize_nvfp4(q.reshape(E * N, K // 2), sf.reshape(E * N, K // 16), np.repeat(s_w, N))
+    out = nvq.dequantize_bf16(nvq.NVFP4, torch.from_numpy(q).cuda(), torch.from_numpy(sf).cuda(),
+                              torch.from_numpy(s_w).cuda(), nvq.SCOPE_MATRIX, groups=E, rows=N, cols=K,
+                              sf_layout="canonical")
+    got = out.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert np.array_equal(got, want)
+
+
+# ------------------------------------------------------------------------------------------------
+# Full-size workloads, sampled against the oracle
+# ------------------------------------------------------------------------------------------------
+def test_full_size_moe_activation_quant_sampled(nvq):
+    counts, offsets = workloads.moe_routing()
+    x = workloads.routed_activations(counts, offsets, workloads.HIDDEN, seed=11, device="cuda")
+    q, sf, s = nvq.nvfp4_quantize_per_token(x, sf_layout="mma")
+    mx = nvq.mxfp8_quantize(x, sf_layout="mma")
+    torch.cuda.synchronize()
+    R = x.shape[0]
+    rng = np.random.default_rng(0)
+    rows = np.sort(rng.choice(R, 384, replace=False))
+    xb = workloads.to_bits(x[torch.from_numpy(rows).cuda()])
+    q_ref, sf_ref, s_ref = oracle.nvfp4_quantize_per_token(xb)
+    assert np.array_equal(_np(q[torch.from_numpy(rows).cuda()]), q_ref)
+    assert np.array_equal(_np(s[torch.from_numpy(rows).cuda()]).view(np.uint32), s_ref.view(np.uint32))
+    sf_all = _np(sf)
+    kb = workloads.HIDDEN // 16
+    r_idx, c_idx = np.meshgrid(rows, np.arange(kb), indexing="ij")
+    assert np.array_equal(sf_all[oracle.mma_layout_offset(r_idx, c_idx, kb)], sf_ref)
+    # MXFP8 rowwise on the same rows; columnwise on sampled 32-row bands
+    mref = oracle.mxfp8_quantize(xb, colwise=False)
+    assert np.array_equal(_np(mx["q_row"][torch.from_numpy(rows).cuda()]), mref["q_row"])
+    bands = rng.choice(R // 32, 24, replace=False)
+    for b in bands:
+        xb2 = workloads.to_bits(x[32 * b:32 * b + 32])
+        cref = oracle.mxfp8_quantize(xb2, rowwise=False)
+        assert np.array_equal(_np(mx["q_colT"][:, 32 * b:32 * b + 32]), cref["q_colT"])
