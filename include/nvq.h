@@ -186,8 +186,10 @@ typedef struct {
  * epilogue; NVFP4-ru: block-scaled FP4 GEMMs run natively on Blackwell tensor cores.]
  * Accuracy: |D - D_exact| <= 2e-3 * sum_k |s_a s_b deq(A) deq(B)| before the output rounding.
  *
- * Requires: k % 128 == 0; n % 128 == 0; GROUP_K: m % 128 == 0 and fmt == NVQ_MXFP8; s_a only
- * with GROUP_M; offsets are validated on the device (status NVQ_DEV_BAD_OFFSETS, nothing written).
+ * Requires: n % 128 == 0; GROUP_M: k % 128 == 0; GROUP_K: k % 32 == 0, m % 128 == 0,
+ * fmt == NVQ_MXFP8 and s_a == NULL; groups <= 1024. offsets are validated on the device (status
+ * NVQ_DEV_BAD_OFFSETS, nothing written). Scale buffers: sfa = MMA layout of [m, k/block],
+ * sfb = MMA layout of the stacked [groups*n, k/block] (GROUP_M) or [n, k/block] (GROUP_K).
  */
 nvq_status block_scaled_grouped_gemm(const nvq_gemm_args* args, void* stream);
 

@@ -108,7 +108,7 @@ def sf_bytes(rows, cols, block, sf_layout="mma"):
 def _check_input(x, ndim):
     if not x.is_cuda or x.dtype != torch.bfloat16 or x.dim() != ndim:
         raise ValueError(f"expected a {ndim}-D bf16 CUDA tensor")
-    if x.stride(-1) != 1:
+    if x.numel() and x.stride(-1) != 1:
         raise ValueError("innermost dimension must be contiguous")
 
 
@@ -129,7 +129,7 @@ def mxfp8_quantize(x, rowwise=True, colwise=True, sf_layout="mma", out=None):
     if colwise:
         o.setdefault("q_colT", torch.empty((K, M), dtype=torch.uint8, device=dev))
         o.setdefault("sf_colT", torch.empty(sf_bytes(K, M, 32, lay), dtype=torch.uint8, device=dev))
-    st = _mxfp8_quantize(_ptr(x), M, K, x.stride(0), _ptr(o.get("q_row")), _ptr(o.get("sf_row")),
+    st = _mxfp8_quantize(_ptr(x), M, K, x.stride(0) if M else K, _ptr(o.get("q_row")), _ptr(o.get("sf_row")),
                          _ptr(o.get("q_colT")), _ptr(o.get("sf_colT")), lay, _stream(dev))
     _check(st, "mxfp8_quantize")
     return o
@@ -146,7 +146,7 @@ def nvfp4_quantize_per_token(x, sf_layout="mma", out=None):
                torch.empty(sf_bytes(T, K, 16, lay), dtype=torch.uint8, device=dev),
                torch.empty(T, dtype=torch.float32, device=dev))
     q, sf, s = out
-    st = _nvfp4_quantize_per_token(_ptr(x), T, K, x.stride(0), _ptr(q), _ptr(sf), _ptr(s), lay, _stream(dev))
+    st = _nvfp4_quantize_per_token(_ptr(x), T, K, x.stride(0) if T else K, _ptr(q), _ptr(sf), _ptr(s), lay, _stream(dev))
     _check(st, "nvfp4_quantize_per_token")
     return q, sf, s
 

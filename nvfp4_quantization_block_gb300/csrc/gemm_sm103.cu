@@ -9,9 +9,13 @@
 //   GROUP_M: D[i, j] = s_a[i] s_b[e] sum_k deq(A)[i, k] deq(B[e])[j, k]   (rows i of group e)
 //   GROUP_K: D[e][i, j] = sum_{k in group e} deq(A)[i, k] deq(B)[j, k]
 //
-// Design (one CTA per SM, persistent, warp-specialised, 192 threads):
+// Design (one CTA per SM, persistent, warp-specialised, 224 threads):
 //   warp 0 lane 0  TMA producer: 128x128-byte A tiles and 256x128-byte B tiles (128B swizzle)
 //                  plus the matching 512-byte scale tiles (bulk copies) into a ring of stages.
+//   warp 6         A-scale transposer: a GROUP_M tile starts at its group's row offset (a multiple
+//                  of 32), so its 128 rows of A scales straddle two 128-row scale tiles; the warp
+//                  rebuilds the tile's own 512-byte scale tile in shared memory (one funnel shift
+//                  per 16-byte line) and hands the stage to the MMA warp.
 //   warp 1 lane 0  MMA issuer: copies each stage's scale tiles smem -> TMEM (tcgen05.cp
 //                  32x128b.warpx4) and issues four tcgen05.mma block_scale instructions
 //                  (M=128, N=256; K=32 for MXFP8 E4M3 x UE8M0/32, K=64 for NVFP4 E2M1 x UE4M3/16),
@@ -19,11 +23,8 @@
 //                  the epilogue. Warp 1 also allocates and frees TMEM.
 //   warps 2-5      epilogue: tcgen05.ld 32 columns at a time, multiply by s_a[row] s_b[e], round
 //                  to bf16 (or keep fp32) and store with 16-byte vector stores.
-// Tiles are 128 rows x 256 columns; GROUP_M tiles start at the group's row offset (a multiple of
-// 32), so a tile's row scales span two 128-row scale tiles; both are copied to TMEM side by side
-// and the MMA's scale address starts at the tile's 32-row quarter within the first. GROUP_K
-// tiles iterate the group's reduction range in 32-element MMA steps (k-steps outside the group
-// inside a 128-element stage are skipped).
+// GROUP_K tiles iterate the group's reduction range in 32-element MMA steps (k-steps outside the
+// group inside a 128-element stage are skipped).
 //
 // Every wait on an mbarrier is bounded; a wait that runs out sets the caller's status word to
 // NVQ_DEV_TIMEOUT and a CTA-wide abort flag, and every role then leaves its loop, waits (bounded)
@@ -39,11 +40,11 @@
 
 namespace nvq {
 
-constexpr int GEMM_THREADS = 192;
+constexpr int GEMM_THREADS = 224;
 constexpr int BM = 128, BN = 256, BKB = 128;       // tile rows, tile columns, K bytes per stage
 constexpr int MAX_GROUPS = 1024;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t WAIT_LIMIT = 1u << 26;            // bounded spin: far beyond any legitimate wait
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;    // 2 s: far beyond any legitimate wait
 
 template <bool FP4>
 struct GemmCfg {
@@ -53,10 +54,13 @@ struct GemmCfg {
     static constexpr int MMA_K = FP4 ? 64 : 32;        // reduction elements per MMA
     static constexpr int A_BYTES = BM * BKB;
     static constexpr int B_BYTES = BN * BKB;
-    static constexpr int SFA_BYTES = 2 * KGS * 512;
-    static constexpr int SFB_BYTES = 2 * KGS * 512;
-    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
-    static constexpr uint32_t SF_COLS = KGS * 8;       // TMEM columns per operand's scales
+    static constexpr int SFA_BYTES = KGS * 512;        // the tile's own 128 row scales
+    static constexpr int SFB_BYTES = 2 * KGS * 512;    // two 128-row scale tiles (N = 256)
+    static constexpr int SFA_RAW_BYTES = 2 * KGS * 512;  // the two row tiles a 32-aligned tile spans
+    static constexpr int STAGE_BYTES =
+        (A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES + SFA_RAW_BYTES + 1023) / 1024 * 1024;
+    static constexpr uint32_t SFA_COLS = KGS * 4;      // TMEM columns of A's scales
+    static constexpr uint32_t SFB_COLS = KGS * 8;      // TMEM columns of B's scales
     static constexpr uint32_t IDESC =
         (FP4 ? ((1u << 7) | (1u << 10)) : 0u)         // A, B format: E2M1 (mxf4nvf4) or E4M3
         | ((uint32_t)(BN >> 3) << 17)                  // N >> 3
@@ -115,17 +119,35 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Bounded wait; returns false (and raises the abort flag / status) when the limit is reached or
-// another role has already aborted.
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait; returns false (and raises the abort flag / status) when WAIT_LIMIT_NS of wall-clock
+// time pass without the phase completing, or when another role has already aborted.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                           int32_t* status) {
-    for (uint32_t it = 0; it < WAIT_LIMIT; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 1023u) == 1023u && *abort_flag) return false;
+        if ((it & 255u) == 0u) {
+            if (*abort_flag) return false;
+            if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) break;
+        }
     }
     *abort_flag = 1;
     if (status) atomicExch(status, NVQ_DEV_TIMEOUT);
     return false;
+}
+
+// Bounded drain used at teardown: wait for a phase without raising anything.
+__device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) return;
 }
 
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int32_t x, int32_t y,
@@ -263,7 +285,8 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
     uint8_t* stage_base = smem;
     uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
     uint64_t* empty_bar = full_bar + C::STAGES;
-    uint64_t* tmem_full = empty_bar + C::STAGES;
+    uint64_t* sfa_bar = empty_bar + C::STAGES;
+    uint64_t* tmem_full = sfa_bar + C::STAGES;
     uint64_t* tmem_empty = tmem_full + 1;
     uint64_t* mma_done = tmem_empty + 1;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(mma_done + 1);
@@ -325,8 +348,9 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
     // ---- barriers and TMEM ----
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
-            mbar_init(&full_bar[s], 1);
+            mbar_init(&full_bar[s], 2);       // producer (A, B, B scales) + scale transposer
             mbar_init(&empty_bar[s], 1);
+            mbar_init(&sfa_bar[s], 1);
         }
         mbar_init(tmem_full, 1);
         mbar_init(tmem_empty, 128);
@@ -344,7 +368,7 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
     const uint32_t tmem_base = *tmem_holder;
     const uint32_t tmem_acc = tmem_base;
     const uint32_t tmem_sfa = tmem_base + BN;
-    const uint32_t tmem_sfb = tmem_base + BN + C::SF_COLS;
+    const uint32_t tmem_sfb = tmem_base + BN + C::SFA_COLS;
 
     const int64_t k_stages_total = (p.k + C::EPS - 1) / C::EPS;   // stages over the whole K extent
 
@@ -367,20 +391,22 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
                 uint8_t* st = stage_base + (size_t)slot * C::STAGE_BYTES;
                 uint8_t* sa = st;
                 uint8_t* sb = st + C::A_BYTES;
-                uint8_t* ssfa = sb + C::B_BYTES;
-                uint8_t* ssfb = ssfa + C::SFA_BYTES;
+                uint8_t* ssfb = sb + C::B_BYTES + C::SFA_BYTES;
+                uint8_t* ssfa_raw = ssfb + C::SFB_BYTES;
                 const int64_t kg0 = ks * C::KGS;
                 const int64_t kgn = min((int64_t)C::KGS, p.sf_tiles_per_row - kg0);
                 const uint32_t sf_bytes = (uint32_t)kgn * 512u;
-                const uint32_t tx = C::A_BYTES + C::B_BYTES + sf_bytes * (1u + (need_a2 ? 1u : 0u)) +
-                                    sf_bytes * (1u + (need_b2 ? 1u : 0u));
+                // A scales (raw row tiles) complete on sfa_bar; the transposer turns them into the tile's
+                // own scale tile and then arrives on full_bar
+                mbar_arrive_expect_tx(&sfa_bar[slot], sf_bytes * (1u + (need_a2 ? 1u : 0u)));
+                bulk_load(ssfa_raw, p.sfa + ((rb_a * p.sf_tiles_per_row + kg0) << 9), sf_bytes, &sfa_bar[slot]);
+                if (need_a2)
+                    bulk_load(ssfa_raw + C::KGS * 512, p.sfa + (((rb_a + 1) * p.sf_tiles_per_row + kg0) << 9),
+                              sf_bytes, &sfa_bar[slot]);
+                const uint32_t tx = C::A_BYTES + C::B_BYTES + sf_bytes * (1u + (need_b2 ? 1u : 0u));
                 mbar_arrive_expect_tx(&full_bar[slot], tx);
                 tma_load_2d(sa, &tmap_a, (int32_t)(ks * BKB), (int32_t)tl.a_row0, &full_bar[slot]);
                 tma_load_2d(sb, &tmap_b, (int32_t)(ks * BKB), (int32_t)tl.b_row0, &full_bar[slot]);
-                bulk_load(ssfa, p.sfa + ((rb_a * p.sf_tiles_per_row + kg0) << 9), sf_bytes, &full_bar[slot]);
-                if (need_a2)
-                    bulk_load(ssfa + C::KGS * 512, p.sfa + (((rb_a + 1) * p.sf_tiles_per_row + kg0) << 9), sf_bytes,
-                              &full_bar[slot]);
                 bulk_load(ssfb, p.sfb + ((rb_b * p.sf_tiles_per_row + kg0) << 9), sf_bytes, &full_bar[slot]);
                 if (need_b2)
                     bulk_load(ssfb + C::KGS * 512, p.sfb + (((rb_b + 1) * p.sf_tiles_per_row + kg0) << 9), sf_bytes,
@@ -395,7 +421,8 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
             int s2 = slot - 1 - (int)i;
             uint32_t ph = phase;
             if (s2 < 0) { s2 += C::STAGES; ph ^= 1u; }
-            for (uint32_t it = 0; it < WAIT_LIMIT && !mbar_try_wait(&full_bar[s2], ph); ++it) {}
+            mbar_drain(&sfa_bar[s2], ph);
+            mbar_drain(&full_bar[s2], ph);
         }
     } else if (warp == 1 && lane == 0) {
         // =========================== MMA issuer ===========================
@@ -410,7 +437,6 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
             if (!mbar_wait(tmem_empty, acc_phase ^ 1u, abort_flag, p.status)) break;
             tc_fence_after();
             const int64_t ks0 = tl.k_begin / C::EPS, ks1 = (tl.k_end + C::EPS - 1) / C::EPS;
-            const uint32_t g0 = (uint32_t)((tl.a_row0 % BM) / 32);
             uint32_t accumulate = 0;
             for (int64_t ks = ks0; ks < ks1; ++ks) {
                 if (!mbar_wait(&full_bar[slot], phase, abort_flag, p.status)) { ok = false; break; }
@@ -419,14 +445,13 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
                 const uint32_t sb = sa + C::A_BYTES;
                 const uint32_t ssfa = sb + C::B_BYTES;
                 const uint32_t ssfb = ssfa + C::SFA_BYTES;
-                // scales -> TMEM: SFA k-group j at columns [8j, 8j+8) (two 128-row tiles), same for SFB
+                // scales -> TMEM: A's k-group j at columns [4j, 4j+4); B's at [8j, 8j+8) (two 128-row tiles)
 #pragma unroll
                 for (int j = 0; j < C::KGS; ++j) {
+                    tc_cp_sf(tmem_sfa + 4 * j, smem_desc(ssfa + j * 512, 0, 128, 0));
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        tc_cp_sf(tmem_sfa + 8 * j + 4 * h, smem_desc(ssfa + (h * C::KGS + j) * 512, 0, 128, 0));
+                    for (int h = 0; h < 2; ++h)
                         tc_cp_sf(tmem_sfb + 8 * j + 4 * h, smem_desc(ssfb + (h * C::KGS + j) * 512, 0, 128, 0));
-                    }
                 }
                 const uint64_t adesc0 = smem_desc(sa, 16, 1024, 2);
                 const uint64_t bdesc0 = smem_desc(sb, 16, 1024, 2);
@@ -439,7 +464,7 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
                     const uint32_t idesc = C::IDESC | (sf_id << 4) | (sf_id << 29);
                     // K advance inside the 128-byte swizzled row: 32 bytes per MMA (encoded >> 4)
                     tc_mma<FP4>(tmem_acc, adesc0 + (uint64_t)(2 * j), bdesc0 + (uint64_t)(2 * j), idesc,
-                                tmem_sfa + 8 * kg + g0, tmem_sfb + 8 * kg, accumulate);
+                                tmem_sfa + 4 * kg, tmem_sfb + 8 * kg, accumulate);
                     accumulate = 1;
                 }
                 tc_commit(&empty_bar[slot]);
@@ -451,7 +476,54 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
         }
         // wait (bounded) for every tcgen05 operation issued above before TMEM is released
         tc_commit(mma_done);
-        for (uint32_t it = 0; it < WAIT_LIMIT && !mbar_try_wait(mma_done, 0); ++it) {}
+        mbar_drain(mma_done, 0);
+    } else if (warp == 6) {
+        // ======================= A-scale transposer =======================
+        // A tile starting 32*g0 rows into a 128-row scale tile needs rows [32 g0, 128) of that tile
+        // followed by rows [0, 32 g0) of the next. In the 512-byte tile layout line l holds the
+        // scales of rows l, l+32, l+64, l+96 as four 4-byte words, so the tile's own line l is the
+        // 16-byte window starting g0 words into (line l of tile 0 ++ line l of tile 1).
+        int slot = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        const uint32_t stage0 = smem_u32(stage_base);
+        for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            const Tile tl = sched.get(t);
+            if (tl.k_end <= tl.k_begin) continue;
+            const int64_t ks0 = tl.k_begin / C::EPS, ks1 = (tl.k_end + C::EPS - 1) / C::EPS;
+            const int g0 = (int)((tl.a_row0 % BM) / 32);
+            for (int64_t ks = ks0; ks < ks1; ++ks) {
+                int good = 1;
+                if (lane == 0) good = mbar_wait(&sfa_bar[slot], phase, abort_flag, p.status) ? 1 : 0;
+                good = __shfl_sync(0xffffffffu, good, 0);
+                if (!good) { ok = false; break; }
+                const uint32_t st = stage0 + (uint32_t)slot * C::STAGE_BYTES;
+                const uint32_t dst = st + C::A_BYTES + C::B_BYTES;
+                const uint32_t raw = dst + C::SFA_BYTES + C::SFB_BYTES;
+#pragma unroll
+                for (int j = 0; j < C::KGS; ++j) {
+                    uint32_t w[8];
+                    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                                 : "r"(raw + j * 512 + lane * 16));
+                    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                                 : "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
+                                 : "r"(raw + (C::KGS + j) * 512 + lane * 16));
+                    uint32_t o0 = w[0], o1 = w[1], o2 = w[2], o3 = w[3];
+                    if (g0 == 1) { o0 = w[1]; o1 = w[2]; o2 = w[3]; o3 = w[4]; }
+                    else if (g0 == 2) { o0 = w[2]; o1 = w[3]; o2 = w[4]; o3 = w[5]; }
+                    else if (g0 == 3) { o0 = w[3]; o1 = w[4]; o2 = w[5]; o3 = w[6]; }
+                    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};"
+                                 ::"r"(dst + j * 512 + lane * 16), "r"(o0), "r"(o1), "r"(o2), "r"(o3)
+                                 : "memory");
+                }
+                // make the generic-proxy writes visible to tcgen05.cp (async proxy), then hand over
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&full_bar[slot]);
+                if (++slot == C::STAGES) { slot = 0; phase ^= 1u; }
+            }
+        }
     } else if (warp >= 2) {
         // =========================== epilogue ===========================
         const int q = warp & 3;                       // TMEM lane quarter this warp may access
@@ -619,7 +691,8 @@ extern "C" nvq_status block_scaled_grouped_gemm(const nvq_gemm_args* a, void* st
     if (a->a == nullptr || a->b == nullptr || a->sfa == nullptr || a->sfb == nullptr || a->offsets == nullptr ||
         a->d == nullptr)
         return NVQ_ERR_INVALID_ARG;
-    if (a->k == 0 || a->k % 128 || a->n % 128) return NVQ_ERR_INVALID_ARG;
+    if (a->k == 0 || a->n % 128) return NVQ_ERR_INVALID_ARG;
+    if (a->k % (a->mode == NVQ_GEMM_GROUP_M ? 128 : 32)) return NVQ_ERR_INVALID_ARG;
     if (a->ldd < a->n || a->ldd % 8) return NVQ_ERR_INVALID_ARG;
     if (a->m > INT32_MAX || a->k > INT32_MAX || a->groups * a->n > INT32_MAX) return NVQ_ERR_UNSUPPORTED;
     if (a->mode == NVQ_GEMM_GROUP_K) {

@@ -1,0 +1,269 @@
+"""GPU parity: the tcgen05 block-scaled grouped GEMM against the float64 oracle.
+
+Inputs are quantized independently on both sides (GPU kernels vs oracle) from the same seeded bf16
+data; the oracle multiplies its own dequantized operands in float64. Bound (method statement):
+|D_gpu - D| <= 2e-3 * sum_k |s_a s_b deq(A) deq(B)|, checked on the fp32 output; the bf16 output
+adds its own final rounding (at most 2^-8 |D|, half a bf16 ulp).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+TOL = 2e-3
+
+
+@pytest.fixture(scope="module")
+def nvq():
+    import nvfp4_quantization_block_gb300 as m
+    return m
+
+
+def _bits(x):
+    return oracle.f64_to_bf16_bits_rne(np.asarray(x, dtype=np.float64))
+
+
+def _check(d_gpu, D, bound, bf16_out):
+    d = d_gpu.detach().float().cpu().numpy().astype(np.float64)
+    err = np.abs(d - D)
+    allow = TOL * bound + (np.abs(D) * 2.0 ** -8 if bf16_out else 0.0)
+    bad = err > allow
+    assert not bad.any(), (f"{bad.sum()} of {bad.size} outside tolerance; worst err/bound "
+                           f"{(err / np.maximum(bound, 1e-300)).max():.3e}")
+
+
+def _routed(counts, k, seed, scale_rows=True):
+    offs = workloads.padded_offsets(counts, 32)
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((int(offs[-1]), k))
+    if scale_rows:
+        x *= np.exp(rng.uniform(-4, 4, (x.shape[0], 1)))
+    x[~workloads.valid_row_mask(counts, offs)] = 0
+    return offs, _bits(x)
+
+
+# ------------------------------------------------------------------------------------------------
+# forward / data-gradient (rows grouped by expert)
+# ------------------------------------------------------------------------------------------------
+def _run_m(nvq, fmt, counts, K, N, seed, out_type):
+    E = len(counts)
+    offs, xb = _routed(counts, K, seed)
+    rng = np.random.default_rng(seed + 1)
+    wb = _bits(rng.standard_normal((E, K, N)) * 0.02 * np.exp(rng.uniform(-2, 2, (E, 1, 1))))
+    x = workloads.from_bits(xb, "cuda")
+    w = workloads.from_bits(wb, "cuda")
+    M = x.shape[0]
+    offs_d = torch.from_numpy(offs).cuda()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    if fmt == "nvfp4":
+        qa, sfa, sa = nvq.nvfp4_quantize_per_token(x, sf_layout="mma")
+        qb, sfb, sb = nvq.nvfp4_quantize_weights(w.contiguous(), sf_layout="mma")
+        d = nvq.block_scaled_grouped_gemm(nvq.NVFP4, nvq.GEMM_GROUP_M, qa, sfa, qb, sfb, offs_d, m=M, n=N, k=K,
+                                          groups=E, s_a=sa, s_b=sb, out_type=out_type, status=status)
+        qa_r, sfa_r, sa_r = oracle.nvfp4_quantize_per_token(xb)
+        qb_r, sfb_r, sb_r = oracle.nvfp4_quantize_weights(wb)
+        a = oracle.deq_operand("nvfp4", qa_r, sfa_r)
+        b = np.stack([oracle.deq_operand("nvfp4", qb_r[e], sfb_r[e]) for e in range(E)])
+        D, bound = oracle.grouped_gemm_reference("m", a, b, offs, sa_r, sb_r)
+    else:
+        # forward: A = rowwise MXFP8 of X; B[e] = columnwise MXFP8 of W[e] (blocks along K), i.e. W[e]^T
+        qa = nvq.mxfp8_quantize(x, colwise=False, sf_layout="mma")
+        wt = w.transpose(1, 2).contiguous().view(E * N, K)          # [E*N, K]: rows are W[e] columns
+        qb = nvq.mxfp8_quantize(wt, colwise=False, sf_layout="mma")
+        d = nvq.block_scaled_grouped_gemm(nvq.MXFP8, nvq.GEMM_GROUP_M, qa["q_row"], qa["sf_row"], qb["q_row"],
+                                          qb["sf_row"], offs_d, m=M, n=N, k=K, groups=E, out_type=out_type,
+                                          status=status)
+        ra = oracle.mxfp8_quantize(xb, colwise=False)
+        a = oracle.deq_operand("mxfp8", ra["q_row"], ra["sf_row"])
+        b = []
+        for e in range(E):
+            rb = oracle.mxfp8_quantize(np.ascontiguousarray(wb[e]), rowwise=False)   # columnwise of W[e]
+            b.append(oracle.deq_operand("mxfp8", rb["q_colT"], rb["sf_colT"]))
+        D, bound = oracle.grouped_gemm_reference("m", a, np.stack(b), offs)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    rows = ~np.isnan(D[:, 0])
+    _check(d[torch.from_numpy(rows).cuda()], D[rows], bound[rows], out_type == nvq.OUT_BF16)
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4"])
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_contract_shape_single_group(nvq, fmt, out):
+    # 256 x 512 by 512 x 384: one group, N not a multiple of the 256-column tile
+    _run_m(nvq, fmt, [256], 512, 384, seed=0, out_type=nvq.OUT_F32 if out == "f32" else nvq.OUT_BF16)
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4"])
+@pytest.mark.parametrize("counts,K,N", [
+    ([96, 0, 160, 33, 300], 256, 256),       # group starts at 32-row offsets inside scale tiles
+    ([1, 31, 64, 0, 0, 129], 384, 512),      # K ragged against the FP4 stage (384 = 256 + 128)
+    ([200, 77], 768, 384),
+    ([0, 0, 0], 256, 256),                   # nothing to do
+])
+def test_grouped_rows(nvq, fmt, counts, K, N):
+    _run_m(nvq, fmt, counts, K, N, seed=sum(counts) + K, out_type=nvq.OUT_F32)
+
+
+def test_rows_outside_groups_untouched(nvq):
+    E, K, N = 2, 256, 256
+    counts = [40, 20]
+    offs = np.array([0, 64, 96], dtype=np.int64)       # 96 of 160 buffer rows belong to groups
+    rng = np.random.default_rng(3)
+    xb = _bits(rng.standard_normal((160, K)))
+    wb = _bits(rng.standard_normal((E, K, N)) * 0.02)
+    x = workloads.from_bits(xb, "cuda")
+    qa, sfa, sa = nvq.nvfp4_quantize_per_token(x, sf_layout="mma")
+    qb, sfb, sb = nvq.nvfp4_quantize_weights(workloads.from_bits(wb, "cuda").contiguous(), sf_layout="mma")
+    d = torch.full((160, N), 7.0, dtype=torch.float32, device="cuda")
+    nvq.block_scaled_grouped_gemm(nvq.NVFP4, nvq.GEMM_GROUP_M, qa, sfa, qb, sfb, torch.from_numpy(offs).cuda(),
+                                  m=160, n=N, k=K, groups=E, s_a=sa, s_b=sb, out=d, out_type=nvq.OUT_F32)
+    torch.cuda.synchronize()
+    assert torch.all(d[96:] == 7.0)
+    assert not torch.all(d[:96] == 7.0)
+    del counts
+
+
+def test_bad_offsets_set_status_and_write_nothing(nvq):
+    K, N = 256, 256
+    x = workloads.normal_bf16((64, K), device="cuda")
+    w = workloads.normal_bf16((1, K, N), 0.02, device="cuda")
+    qa, sfa, sa = nvq.nvfp4_quantize_per_token(x, sf_layout="mma")
+    qb, sfb, sb = nvq.nvfp4_quantize_weights(w, sf_layout="mma")
+    d = torch.full((64, N), 3.0, dtype=torch.float32, device="cuda")
+    for bad in ([0, 48], [0, 96], [16, 64]):            # not a multiple of 32 / past the buffer / [0] != 0
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        nvq.block_scaled_grouped_gemm(nvq.NVFP4, nvq.GEMM_GROUP_M, qa, sfa, qb, sfb,
+                                      torch.tensor(bad, dtype=torch.int64, device="cuda"), m=64, n=N, k=K,
+                                      groups=1, s_a=sa, s_b=sb, out=d, out_type=nvq.OUT_F32, status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == nvq.DEV_BAD_OFFSETS
+        assert torch.all(d == 3.0)
+
+
+def test_host_rejects_bad_shapes(nvq):
+    x = torch.zeros((64, 256), dtype=torch.uint8, device="cuda")
+    offs = torch.tensor([0, 64], dtype=torch.int64, device="cuda")
+    with pytest.raises(nvq.NvqError):        # k not a multiple of 128
+        nvq.block_scaled_grouped_gemm(nvq.MXFP8, nvq.GEMM_GROUP_M, x, x, x, x, offs, m=64, n=256, k=96, groups=1)
+    with pytest.raises(nvq.NvqError):        # n not a multiple of 128
+        nvq.block_scaled_grouped_gemm(nvq.MXFP8, nvq.GEMM_GROUP_M, x, x, x, x, offs, m=64, n=200, k=256, groups=1)
+    with pytest.raises(nvq.NvqError):        # NVFP4 weight gradient is not part of the method
+        nvq.block_scaled_grouped_gemm(nvq.NVFP4, nvq.GEMM_GROUP_K, x, x, x, x, offs, m=128, n=256, k=256, groups=1)
+
+
+# ------------------------------------------------------------------------------------------------
+# weight gradient (reduction grouped by expert), MXFP8 columnwise copies
+# ------------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("counts,Kin,Nout", [([64, 0, 96, 200], 256, 256), ([33, 300], 128, 384)])
+def test_weight_gradient_grouped_k(nvq, counts, Kin, Nout):
+    offs, xb = _routed(counts, Kin, seed=5)
+    rng = np.random.default_rng(6)
+    dy = rng.standard_normal((int(offs[-1]), Nout)) * 1e-3
+    dy[~workloads.valid_row_mask(counts, offs)] = 0
+    dyb = _bits(dy)
+    x = workloads.from_bits(xb, "cuda")
+    g = workloads.from_bits(dyb, "cuda")
+    Mtot = x.shape[0]
+    E = len(counts)
+    qx = nvq.mxfp8_quantize(x, rowwise=False, sf_layout="mma")
+    qg = nvq.mxfp8_quantize(g, rowwise=False, sf_layout="mma")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    d = nvq.block_scaled_grouped_gemm(nvq.MXFP8, nvq.GEMM_GROUP_K, qx["q_colT"], qx["sf_colT"], qg["q_colT"],
+                                      qg["sf_colT"], torch.from_numpy(offs).cuda(), m=Kin, n=Nout, k=Mtot,
+                                      groups=E, out_type=nvq.OUT_F32, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    rx = oracle.mxfp8_quantize(xb, rowwise=False)
+    rg = oracle.mxfp8_quantize(dyb, rowwise=False)
+    A = oracle.deq_operand("mxfp8", rx["q_colT"], rx["sf_colT"])
+    B = oracle.deq_operand("mxfp8", rg["q_colT"], rg["sf_colT"])
+    D, bound = oracle.grouped_gemm_reference("k", A, B, offs)
+    _check(d, D, bound, False)
+
+
+# ------------------------------------------------------------------------------------------------
+# Full-size workloads in the benchmark's launch configuration, sampled against the oracle
+# ------------------------------------------------------------------------------------------------
+def _sample_pairs(rng, rows, n, count):
+    return rng.choice(rows, count), rng.integers(0, n, count)
+
+
+def test_full_size_dense_mxfp8_sampled(nvq):
+    inp = workloads.dense_inputs(seed=0, device="cuda")
+    x, w = inp["x"], inp["w"]
+    M, K = x.shape
+    N = w.shape[1]
+    qa = nvq.mxfp8_quantize(x, colwise=False)
+    qb = nvq.mxfp8_quantize(w, rowwise=False)          # columnwise of W: [N, K], blocks along K
+    offs = torch.tensor([0, M], dtype=torch.int64, device="cuda")
+    d = nvq.block_scaled_grouped_gemm(nvq.MXFP8, nvq.GEMM_GROUP_M, qa["q_row"], qa["sf_row"], qb["q_colT"],
+                                      qb["sf_colT"], offs, m=M, n=N, k=K, groups=1)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(0)
+    ii, jj = _sample_pairs(rng, M, N, 2048)
+    xa = workloads.to_bits(x[torch.from_numpy(ii).cuda()])
+    wc = workloads.to_bits(w[:, torch.from_numpy(jj).cuda()].T.contiguous())
+    ra = oracle.mxfp8_quantize(xa, colwise=False)
+    rb = oracle.mxfp8_quantize(wc, colwise=False)      # rows of W^T = columns of W, blocks along K
+    A = oracle.deq_operand("mxfp8", ra["q_row"], ra["sf_row"])
+    B = oracle.deq_operand("mxfp8", rb["q_row"], rb["sf_row"])
+    Dv, bd = oracle.grouped_gemm_entries("m", A, B, np.tile([0, K], (len(ii), 1)), np.ones(len(ii)))
+    got = d[torch.from_numpy(ii).cuda(), torch.from_numpy(jj).cuda()]
+    _check(got, Dv, bd, True)
+
+
+def test_full_size_moe_nvfp4_sampled(nvq):
+    counts, offs = workloads.moe_routing()
+    K, N = workloads.HIDDEN, 2 * workloads.INTERMEDIATE
+    x = workloads.routed_activations(counts, offs, K, seed=1, device="cuda")
+    w = workloads.expert_weights(K, N, seed=2, device="cuda")
+    qa, sfa, sa = nvq.nvfp4_quantize_per_token(x)
+    qb, sfb, sb = nvq.nvfp4_quantize_weights(w)
+    M, E = x.shape[0], w.shape[0]
+    d = nvq.block_scaled_grouped_gemm(nvq.NVFP4, nvq.GEMM_GROUP_M, qa, sfa, qb, sfb, torch.from_numpy(offs).cuda(),
+                                      m=M, n=N, k=K, groups=E, s_a=sa, s_b=sb)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(1)
+    experts = rng.choice(E, 6, replace=False)
+    for e in experts:
+        if counts[e] == 0:
+            continue
+        rows = offs[e] + rng.integers(0, counts[e], 64)
+        cols = rng.integers(0, N, 64)
+        xa = workloads.to_bits(x[torch.from_numpy(rows).cuda()])
+        q_r, sf_r, s_r = oracle.nvfp4_quantize_per_token(xa)
+        wq_r, wsf_r, ws_r = oracle.nvfp4_quantize_weights(workloads.to_bits(w[int(e)])[None])
+        A = oracle.deq_operand("nvfp4", q_r, sf_r)
+        B = oracle.deq_operand("nvfp4", wq_r[0][cols], wsf_r[0][cols])
+        Dv, bd = oracle.grouped_gemm_entries("m", A, B, np.tile([0, K], (64, 1)), s_r.astype(np.float64) * float(ws_r[0]))
+        got = d[torch.from_numpy(rows).cuda(), torch.from_numpy(cols).cuda()]
+        _check(got, Dv, bd, True)
+
+
+def test_full_size_weight_gradient_sampled(nvq):
+    counts, offs = workloads.moe_routing()
+    Kin, Nout = workloads.HIDDEN, 2 * workloads.INTERMEDIATE
+    x = workloads.routed_activations(counts, offs, Kin, seed=3, device="cuda")
+    g = workloads.routed_activations(counts, offs, Nout, std=1e-3, seed=4, device="cuda")
+    qx = nvq.mxfp8_quantize(x, rowwise=False)
+    qg = nvq.mxfp8_quantize(g, rowwise=False)
+    E = len(counts)
+    d = nvq.block_scaled_grouped_gemm(nvq.MXFP8, nvq.GEMM_GROUP_K, qx["q_colT"], qx["sf_colT"], qg["q_colT"],
+                                      qg["sf_colT"], torch.from_numpy(offs).cuda(), m=Kin, n=Nout, k=x.shape[0],
+                                      groups=E)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(2)
+    S = 256
+    ee = rng.integers(0, E, S)
+    ii = rng.integers(0, Kin, S)
+    jj = rng.integers(0, Nout, S)
+    xa = workloads.to_bits(x[:, torch.from_numpy(ii).cuda()].T.contiguous())     # [S, Mtot] columns of X
+    ga = workloads.to_bits(g[:, torch.from_numpy(jj).cuda()].T.contiguous())
+    A = oracle.deq_operand("mxfp8", *oracle.mxfp8_quantize(xa, colwise=False).values())
+    B = oracle.deq_operand("mxfp8", *oracle.mxfp8_quantize(ga, colwise=False).values())
+    Dv, bd = oracle.grouped_gemm_entries("k", A, B, np.stack([offs[ee], offs[ee + 1]], 1), np.ones(S))
+    got = d[torch.from_numpy(ee).cuda(), torch.from_numpy(ii).cuda(), torch.from_numpy(jj).cuda()]
+    _check(got, Dv, bd, True)
