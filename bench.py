@@ -1,0 +1,747 @@
+"""Benchmark of the MXFP8 / per-token NVFP4 quantizer + block-scaled GEMM hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+Prints ONE JSON line (rank 0). Workloads (synthetic, seeded; shapes of the Qwen3-30B-A3B RL workload
+the pages ablate, see workloads.py):
+
+  dense    (default) X bf16 [8192, 2048] with per-row scales, W_qkv bf16 [2048, 5120]. One step is the
+           whole hot path on that batch: MXFP8 rowwise + columnwise quantization of X, MXFP8
+           columnwise quantization of W, per-token NVFP4 of X, NVFP4 of W (one matrix scope), the
+           MXFP8 and the NVFP4 block-scaled GEMM (bf16 out), and the BF16 dequantization of the NVFP4
+           W (dequantized-backward operand).
+  moe      16384 tokens, top-8 of 128 experts with Zipf(1.1) loads: per-token NVFP4 of the routed
+           gate_up input [R, 2048] and down input [R, 768], NVFP4 of W_gate_up [128, 2048, 1536] and
+           W_down [128, 768, 2048], and both grouped NVFP4 GEMMs.
+  backward the moe shapes in MXFP8 backward: row+col quantization of the routed X and dY, rowwise
+           MXFP8 of the expert weights, grouped data-gradient GEMMs and grouped weight-gradient GEMMs.
+  decode   256 tokens, uniform top-8 (2048 routed rows): per-token NVFP4 of the activations and the
+           grouped NVFP4 gate_up GEMM against resident NVFP4 weights, plus the BF16 dequantization of
+           all gate_up expert weights.
+
+value = block-scaled GEMM throughput of the step (GEMM flops of the step / device time of the whole
+step, quantizers included) in TFLOPS; the quantizers' GB/s and every kernel's fraction of its
+roofline are in "kernels". Inputs are resident in HBM when the timed region starts; L2 is flushed
+(256 MiB write) before every step, outside the step's events. "e2e" repeats the step through the
+same C-ABI with host-resident (pinned) inputs copied in and the GEMM outputs copied back inside the
+timed region. --impl reference times the CPU oracle (test infrastructure) on a bounded sample.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "quantize GB/s (% HBM peak); block-scaled MoE GEMM TFLOPS (% dense peak)"
+L2_FLUSH_BYTES = 256 << 20
+
+# ncu DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of the kernels timed
+# here, keyed by workload and kernel, with the sha256 of the source file the capture was taken
+# from. The command that produced each number is in profiles/. A changed source reports null.
+NCU_TRAFFIC = {}
+
+
+def _src_hash(name):
+    path = os.path.join(ROOT, "nvfp4_quantization_block_gb300", "csrc", name)
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def _load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ------------------------------------------------------------------------------------------------
+# CUDA path
+# ------------------------------------------------------------------------------------------------
+class Timer:
+    """CUDA events around each named launch group on the current stream; per-step totals."""
+
+    def __init__(self, torch):
+        self.torch = torch
+        self.records = {}
+        self.active = False
+
+    def run(self, name, fn):
+        if not self.active:
+            return fn()
+        t = self.torch
+        a, b = t.cuda.Event(enable_timing=True), t.cuda.Event(enable_timing=True)
+        a.record()
+        out = fn()
+        b.record()
+        self.records.setdefault(name, []).append((a, b))
+        return out
+
+    def durations_ms(self):
+        return {k: [a.elapsed_time(b) for a, b in v] for k, v in self.records.items()}
+
+
+class Kernel:
+    """Accounting for one timed launch group: algorithmic bytes or flops per step and its roofline."""
+
+    def __init__(self, name, bound, amount, src, peak_key, note):
+        self.name, self.bound, self.amount, self.src, self.peak_key, self.note = name, bound, amount, src, peak_key, note
+
+
+def _workload_dense(torch, nvq, wl, dev):
+    inp = wl.dense_inputs(seed=0, device=dev)
+    x, w = inp["x"], inp["w"]
+    M, K = x.shape
+    N = w.shape[1]
+    w3 = w.unsqueeze(0).contiguous()
+    offs = torch.tensor([0, M], dtype=torch.int64, device=dev)
+    bufs = {
+        "mx": {"q_row": torch.empty((M, K), dtype=torch.uint8, device=dev),
+               "sf_row": torch.empty(nvq.sf_bytes(M, K, 32), dtype=torch.uint8, device=dev),
+               "q_colT": torch.empty((K, M), dtype=torch.uint8, device=dev),
+               "sf_colT": torch.empty(nvq.sf_bytes(K, M, 32), dtype=torch.uint8, device=dev)},
+        "mw": {"q_colT": torch.empty((N, K), dtype=torch.uint8, device=dev),
+               "sf_colT": torch.empty(nvq.sf_bytes(N, K, 32), dtype=torch.uint8, device=dev)},
+        "nx": (torch.empty((M, K // 2), dtype=torch.uint8, device=dev),
+               torch.empty(nvq.sf_bytes(M, K, 16), dtype=torch.uint8, device=dev),
+               torch.empty(M, dtype=torch.float32, device=dev)),
+        "nw": (torch.empty((1, N, K // 2), dtype=torch.uint8, device=dev),
+               torch.empty(nvq.sf_bytes(N, K, 16), dtype=torch.uint8, device=dev),
+               torch.empty(1, dtype=torch.float32, device=dev)),
+        "d8": torch.empty((M, N), dtype=torch.bfloat16, device=dev),
+        "d4": torch.empty((M, N), dtype=torch.bfloat16, device=dev),
+        "wdq": torch.empty((N, K), dtype=torch.bfloat16, device=dev),
+    }
+    ne_x, ne_w = M * K, K * N
+    gemm_flops = 2.0 * M * N * K
+    kernels = [
+        Kernel("mxfp8_quantize X row+col", "hbm", ne_x * (2 + 2 * (1 + 1 / 32)), "quant_mxfp8.cu", "hbm", "4.0625 B/elem"),
+        Kernel("mxfp8_quantize W col", "hbm", ne_w * (2 + 1 + 1 / 32), "quant_mxfp8.cu", "hbm", "3.03125 B/elem"),
+        Kernel("nvfp4_quantize_per_token X", "hbm", ne_x * (2 + 0.5 + 1 / 16) + 4 * M, "quant_nvfp4.cu", "hbm",
+               "2.5625 B/elem + 4 B/row"),
+        Kernel("nvfp4_quantize_weights W", "hbm", ne_w * (2 + 0.5 + 1 / 16) + 4, "quant_nvfp4.cu", "hbm",
+               "2.5625 B/elem (one read; the kernel reads twice)"),
+        Kernel("block_scaled_gemm MXFP8", "tensor", gemm_flops, "gemm_sm103.cu", "fp8", "2*M*N*K"),
+        Kernel("block_scaled_gemm NVFP4", "tensor", gemm_flops, "gemm_sm103.cu", "fp4", "2*M*N*K"),
+        Kernel("dequantize_bf16 W", "hbm", ne_w * (0.5 + 1 / 16 + 2), "dequant.cu", "hbm", "2.5625 B/elem"),
+    ]
+
+    def step(timer, xin=None, win=None):
+        xx = x if xin is None else xin
+        ww = w if win is None else win
+        ww3 = w3 if win is None else win.unsqueeze(0)
+        timer.run(kernels[0].name, lambda: nvq.mxfp8_quantize(xx, out=bufs["mx"]))
+        timer.run(kernels[1].name, lambda: nvq.mxfp8_quantize(ww, rowwise=False, out=bufs["mw"]))
+        timer.run(kernels[2].name, lambda: nvq.nvfp4_quantize_per_token(xx, out=bufs["nx"]))
+        timer.run(kernels[3].name, lambda: nvq.nvfp4_quantize_weights(ww3, out=bufs["nw"]))
+        mx, mw, nx, nw = bufs["mx"], bufs["mw"], bufs["nx"], bufs["nw"]
+        timer.run(kernels[4].name, lambda: nvq.block_scaled_grouped_gemm(
+            nvq.MXFP8, nvq.GEMM_GROUP_M, mx["q_row"], mx["sf_row"], mw["q_colT"], mw["sf_colT"], offs,
+            m=M, n=N, k=K, groups=1, out=bufs["d8"]))
+        timer.run(kernels[5].name, lambda: nvq.block_scaled_grouped_gemm(
+            nvq.NVFP4, nvq.GEMM_GROUP_M, nx[0], nx[1], nw[0], nw[1], offs, m=M, n=N, k=K, groups=1,
+            s_a=nx[2], s_b=nw[2], out=bufs["d4"]))
+        timer.run(kernels[6].name, lambda: nvq.dequantize_bf16(
+            nvq.NVFP4, nw[0], nw[1], nw[2], nvq.SCOPE_MATRIX, groups=1, rows=N, cols=K, out=bufs["wdq"]))
+        return [bufs["d8"], bufs["d4"]]
+
+    config = {"workload": "dense linear forward, Qwen3-30B-A3B attention QKV shape (full hot path)",
+              "x": [M, K], "w": [K, N], "x_rows": "N(0,1) x exp(U(ln 0.1, ln 10)) per row", "w_std": 0.02,
+              "gemm_out": "bf16"}
+    return {"step": step, "kernels": kernels, "gemm_flops": 2 * gemm_flops, "inputs": [x, w],
+            "config": config, "dtype": "mxfp8(e4m3+e8m0)/nvfp4(e2m1+e4m3+fp32) -> fp32 accumulate -> bf16"}
+
+
+def _workload_moe(torch, nvq, wl, dev):
+    counts, offs_np = wl.moe_routing()
+    offs = torch.from_numpy(offs_np).to(dev)
+    R = int(offs_np[-1])
+    E, H, I2, I = wl.EXPERTS, wl.HIDDEN, 2 * wl.INTERMEDIATE, wl.INTERMEDIATE
+    x1 = wl.routed_activations(counts, offs_np, H, seed=1, device=dev)
+    x2 = wl.routed_activations(counts, offs_np, I, seed=2, device=dev)
+    w1 = wl.expert_weights(H, I2, seed=3, device=dev)
+    w2 = wl.expert_weights(I, H, seed=4, device=dev)
+    real = float(counts.sum())
+    f1, f2 = 2.0 * real * I2 * H, 2.0 * real * H * I
+
+    def alloc_tok(rows, k):
+        return (torch.empty((rows, k // 2), dtype=torch.uint8, device=dev),
+                torch.empty(nvq.sf_bytes(rows, k, 16), dtype=torch.uint8, device=dev),
+                torch.empty(rows, dtype=torch.float32, device=dev))
+
+    def alloc_w(e, k, n):
+        return (torch.empty((e, n, k // 2), dtype=torch.uint8, device=dev),
+                torch.empty(nvq.sf_bytes(e * n, k, 16), dtype=torch.uint8, device=dev),
+                torch.empty(e, dtype=torch.float32, device=dev))
+
+    b = {"a1": alloc_tok(R, H), "a2": alloc_tok(R, I), "b1": alloc_w(E, H, I2), "b2": alloc_w(E, I, H),
+         "d1": torch.empty((R, I2), dtype=torch.bfloat16, device=dev),
+         "d2": torch.empty((R, H), dtype=torch.bfloat16, device=dev)}
+    kernels = [
+        Kernel("nvfp4_quantize_per_token gate_up input", "hbm", R * H * 2.5625 + 4 * R, "quant_nvfp4.cu", "hbm", "2.5625 B/elem + 4 B/row"),
+        Kernel("nvfp4_quantize_weights gate_up", "hbm", E * H * I2 * 2.5625 + 4 * E, "quant_nvfp4.cu", "hbm", "2.5625 B/elem"),
+        Kernel("block_scaled_gemm NVFP4 gate_up", "tensor", f1, "gemm_sm103.cu", "fp4", "2*sum_e M_e*N*K"),
+        Kernel("nvfp4_quantize_per_token down input", "hbm", R * I * 2.5625 + 4 * R, "quant_nvfp4.cu", "hbm", "2.5625 B/elem + 4 B/row"),
+        Kernel("nvfp4_quantize_weights down", "hbm", E * I * H * 2.5625 + 4 * E, "quant_nvfp4.cu", "hbm", "2.5625 B/elem"),
+        Kernel("block_scaled_gemm NVFP4 down", "tensor", f2, "gemm_sm103.cu", "fp4", "2*sum_e M_e*N*K"),
+    ]
+
+    def step(timer, xin=None, win=None):
+        xa, xb = (x1, x2) if xin is None else xin
+        wa, wb = (w1, w2) if win is None else win
+        timer.run(kernels[0].name, lambda: nvq.nvfp4_quantize_per_token(xa, out=b["a1"]))
+        timer.run(kernels[1].name, lambda: nvq.nvfp4_quantize_weights(wa, out=b["b1"]))
+        timer.run(kernels[2].name, lambda: nvq.block_scaled_grouped_gemm(
+            nvq.NVFP4, nvq.GEMM_GROUP_M, b["a1"][0], b["a1"][1], b["b1"][0], b["b1"][1], offs, m=R, n=I2, k=H,
+            groups=E, s_a=b["a1"][2], s_b=b["b1"][2], out=b["d1"]))
+        timer.run(kernels[3].name, lambda: nvq.nvfp4_quantize_per_token(xb, out=b["a2"]))
+        timer.run(kernels[4].name, lambda: nvq.nvfp4_quantize_weights(wb, out=b["b2"]))
+        timer.run(kernels[5].name, lambda: nvq.block_scaled_grouped_gemm(
+            nvq.NVFP4, nvq.GEMM_GROUP_M, b["a2"][0], b["a2"][1], b["b2"][0], b["b2"][1], offs, m=R, n=H, k=I,
+            groups=E, s_a=b["a2"][2], s_b=b["b2"][2], out=b["d2"]))
+        return [b["d1"], b["d2"]]
+
+    config = {"workload": "per-token NVFP4 MoE expert forward (gate_up and down), Qwen3-30B-A3B shapes",
+              "tokens": 16384, "experts": E, "topk": 8, "routing": "Gumbel-top-8, p_r ~ r^-1.1",
+              "routed_rows": int(real), "buffer_rows": R, "row_alignment": 32,
+              "expert_rows_min_max": [int(counts.min()), int(counts.max())]}
+    return {"step": step, "kernels": kernels, "gemm_flops": f1 + f2, "inputs": [x1, x2, w1, w2],
+            "input_groups": ([0, 1], [2, 3]), "config": config,
+            "dtype": "nvfp4(e2m1+e4m3+fp32) -> fp32 accumulate -> bf16"}
+
+
+def _workload_backward(torch, nvq, wl, dev):
+    counts, offs_np = wl.moe_routing()
+    offs = torch.from_numpy(offs_np).to(dev)
+    R = int(offs_np[-1])
+    E, H, I2, I = wl.EXPERTS, wl.HIDDEN, 2 * wl.INTERMEDIATE, wl.INTERMEDIATE
+    real = float(counts.sum())
+    # layer 1 (gate_up): X1 [R, H] -> Y1 [R, I2], W1 [E, H, I2]; layer 2 (down): X2 [R, I] -> [R, H]
+    x1 = wl.routed_activations(counts, offs_np, H, seed=1, device=dev)
+    g1 = wl.routed_activations(counts, offs_np, I2, std=1e-3, seed=5, device=dev)
+    x2 = wl.routed_activations(counts, offs_np, I, seed=2, device=dev)
+    g2 = wl.routed_activations(counts, offs_np, H, std=1e-3, seed=6, device=dev)
+    # dgrad needs W[e] with its rows = the layer's input features and blocks along the output dim
+    w1 = wl.expert_weights(H, I2, seed=3, device=dev).view(E * H, I2)
+    w2 = wl.expert_weights(I, H, seed=4, device=dev).view(E * I, H)
+
+    def q_alloc(rows, cols, row, col):
+        o = {}
+        if row:
+            o["q_row"] = torch.empty((rows, cols), dtype=torch.uint8, device=dev)
+            o["sf_row"] = torch.empty(nvq.sf_bytes(rows, cols, 32), dtype=torch.uint8, device=dev)
+        if col:
+            o["q_colT"] = torch.empty((cols, rows), dtype=torch.uint8, device=dev)
+            o["sf_colT"] = torch.empty(nvq.sf_bytes(cols, rows, 32), dtype=torch.uint8, device=dev)
+        return o
+
+    b = {"x1": q_alloc(R, H, False, True), "g1": q_alloc(R, I2, True, True), "w1": q_alloc(E * H, I2, True, False),
+         "x2": q_alloc(R, I, False, True), "g2": q_alloc(R, H, True, True), "w2": q_alloc(E * I, H, True, False),
+         "dx1": torch.empty((R, H), dtype=torch.bfloat16, device=dev),
+         "dw1": torch.empty((E, H, I2), dtype=torch.bfloat16, device=dev),
+         "dx2": torch.empty((R, I), dtype=torch.bfloat16, device=dev),
+         "dw2": torch.empty((E, I, H), dtype=torch.bfloat16, device=dev)}
+    f1 = 2.0 * real * H * I2
+    f2 = 2.0 * real * I * H
+    kernels = [
+        Kernel("mxfp8_quantize X1 col", "hbm", R * H * 3.03125, "quant_mxfp8.cu", "hbm", "3.03125 B/elem"),
+        Kernel("mxfp8_quantize dY1 row+col", "hbm", R * I2 * 4.0625, "quant_mxfp8.cu", "hbm", "4.0625 B/elem"),
+        Kernel("mxfp8_quantize W1 row", "hbm", E * H * I2 * 3.03125, "quant_mxfp8.cu", "hbm", "3.03125 B/elem"),
+        Kernel("block_scaled_gemm MXFP8 dgrad gate_up", "tensor", f1, "gemm_sm103.cu", "fp8", "2*sum_e M_e*N*K"),
+        Kernel("block_scaled_gemm MXFP8 wgrad gate_up", "tensor", f1, "gemm_sm103.cu", "fp8", "2*sum_e M_e*N*K"),
+        Kernel("mxfp8_quantize X2 col", "hbm", R * I * 3.03125, "quant_mxfp8.cu", "hbm", "3.03125 B/elem"),
+        Kernel("mxfp8_quantize dY2 row+col", "hbm", R * H * 4.0625, "quant_mxfp8.cu", "hbm", "4.0625 B/elem"),
+        Kernel("mxfp8_quantize W2 row", "hbm", E * I * H * 3.03125, "quant_mxfp8.cu", "hbm", "3.03125 B/elem"),
+        Kernel("block_scaled_gemm MXFP8 dgrad down", "tensor", f2, "gemm_sm103.cu", "fp8", "2*sum_e M_e*N*K"),
+        Kernel("block_scaled_gemm MXFP8 wgrad down", "tensor", f2, "gemm_sm103.cu", "fp8", "2*sum_e M_e*N*K"),
+    ]
+
+    def step(timer, xin=None, win=None):
+        xa, ga, xb, gb = (x1, g1, x2, g2) if xin is None else xin
+        wa, wb = (w1, w2) if win is None else win
+        k = kernels
+        timer.run(k[0].name, lambda: nvq.mxfp8_quantize(xa, rowwise=False, out=b["x1"]))
+        timer.run(k[1].name, lambda: nvq.mxfp8_quantize(ga, out=b["g1"]))
+        timer.run(k[2].name, lambda: nvq.mxfp8_quantize(wa, colwise=False, out=b["w1"]))
+        timer.run(k[3].name, lambda: nvq.block_scaled_grouped_gemm(
+            nvq.MXFP8, nvq.GEMM_GROUP_M, b["g1"]["q_row"], b["g1"]["sf_row"], b["w1"]["q_row"], b["w1"]["sf_row"],
+            offs, m=R, n=H, k=I2, groups=E, out=b["dx1"]))
+        timer.run(k[4].name, lambda: nvq.block_scaled_grouped_gemm(
+            nvq.MXFP8, nvq.GEMM_GROUP_K, b["x1"]["q_colT"], b["x1"]["sf_colT"], b["g1"]["q_colT"], b["g1"]["sf_colT"],
+            offs, m=H, n=I2, k=R, groups=E, out=b["dw1"]))
+        timer.run(k[5].name, lambda: nvq.mxfp8_quantize(xb, rowwise=False, out=b["x2"]))
+        timer.run(k[6].name, lambda: nvq.mxfp8_quantize(gb, out=b["g2"]))
+        timer.run(k[7].name, lambda: nvq.mxfp8_quantize(wb, colwise=False, out=b["w2"]))
+        timer.run(k[8].name, lambda: nvq.block_scaled_grouped_gemm(
+            nvq.MXFP8, nvq.GEMM_GROUP_M, b["g2"]["q_row"], b["g2"]["sf_row"], b["w2"]["q_row"], b["w2"]["sf_row"],
+            offs, m=R, n=I, k=H, groups=E, out=b["dx2"]))
+        timer.run(k[9].name, lambda: nvq.block_scaled_grouped_gemm(
+            nvq.MXFP8, nvq.GEMM_GROUP_K, b["x2"]["q_colT"], b["x2"]["sf_colT"], b["g2"]["q_colT"], b["g2"]["sf_colT"],
+            offs, m=I, n=H, k=R, groups=E, out=b["dw2"]))
+        return [b["dx1"], b["dw1"], b["dx2"], b["dw2"]]
+
+    config = {"workload": "MXFP8 MoE backward (data and weight gradients of gate_up and down), Qwen3-30B-A3B",
+              "tokens": 16384, "experts": E, "topk": 8, "routing": "Gumbel-top-8, p_r ~ r^-1.1",
+              "routed_rows": int(real), "buffer_rows": R, "row_alignment": 32, "dy_std": 1e-3}
+    return {"step": step, "kernels": kernels, "gemm_flops": 2 * (f1 + f2), "inputs": [x1, g1, x2, g2, w1, w2],
+            "input_groups": ([0, 1, 2, 3], [4, 5]), "config": config,
+            "dtype": "mxfp8(e4m3+e8m0) -> fp32 accumulate -> bf16"}
+
+
+def _workload_decode(torch, nvq, wl, dev):
+    counts = wl.route_counts(256, zipf_s=0.0, seed=0)
+    offs_np = wl.padded_offsets(counts, 32)
+    offs = torch.from_numpy(offs_np).to(dev)
+    R = int(offs_np[-1])
+    E, H, I2 = wl.EXPERTS, wl.HIDDEN, 2 * wl.INTERMEDIATE
+    x = wl.routed_activations(counts, offs_np, H, seed=1, device=dev)
+    w = wl.expert_weights(H, I2, seed=3, device=dev)
+    wq = nvq.nvfp4_quantize_weights(w)          # resident NVFP4 weights (quantized once, untimed)
+    del w
+    real = float(counts.sum())
+    flops = 2.0 * real * I2 * H
+    a = (torch.empty((R, H // 2), dtype=torch.uint8, device=dev),
+         torch.empty(nvq.sf_bytes(R, H, 16), dtype=torch.uint8, device=dev),
+         torch.empty(R, dtype=torch.float32, device=dev))
+    d = torch.empty((R, I2), dtype=torch.bfloat16, device=dev)
+    wdq = torch.empty((E * I2, H), dtype=torch.bfloat16, device=dev)
+    wbytes = E * I2 * H * (0.5 + 1 / 16) + 4 * E
+    kernels = [
+        Kernel("nvfp4_quantize_per_token decode activations", "hbm", R * H * 2.5625 + 4 * R, "quant_nvfp4.cu", "hbm", "2.5625 B/elem + 4 B/row"),
+        Kernel("block_scaled_gemm NVFP4 decode gate_up", "hbm", wbytes + R * H * 0.5625 + real * I2 * 2, "gemm_sm103.cu", "hbm",
+               "NVFP4 weight bytes + activation bytes + bf16 output (memory-bound)"),
+        Kernel("dequantize_bf16 gate_up weights", "hbm", E * I2 * H * (0.5625 + 2), "dequant.cu", "hbm", "2.5625 B/elem"),
+    ]
+
+    def step(timer, xin=None, win=None):
+        xx = x if xin is None else xin[0]
+        timer.run(kernels[0].name, lambda: nvq.nvfp4_quantize_per_token(xx, out=a))
+        timer.run(kernels[1].name, lambda: nvq.block_scaled_grouped_gemm(
+            nvq.NVFP4, nvq.GEMM_GROUP_M, a[0], a[1], wq[0], wq[1], offs, m=R, n=I2, k=H, groups=E,
+            s_a=a[2], s_b=wq[2], out=d))
+        timer.run(kernels[2].name, lambda: nvq.dequantize_bf16(
+            nvq.NVFP4, wq[0], wq[1], wq[2], nvq.SCOPE_MATRIX, groups=E, rows=I2, cols=H, out=wdq))
+        return [d]
+
+    config = {"workload": "rollout-decode NVFP4 expert GEMM (256 tokens, uniform top-8) + dequantize all gate_up weights",
+              "tokens": 256, "experts": E, "routed_rows": int(real), "buffer_rows": R,
+              "weights_nvfp4_mb": round(wbytes / 1e6, 1)}
+    return {"step": step, "kernels": kernels, "gemm_flops": flops, "inputs": [x], "input_groups": ([0], []),
+            "config": config, "dtype": "nvfp4(e2m1+e4m3+fp32) -> fp32 accumulate -> bf16"}
+
+
+def _workload_quant(torch, nvq, wl, dev):
+    """Quantizers alone on a routed activation batch larger than L2 (the quantize GB/s metric)."""
+    counts, offs_np = wl.moe_routing()
+    R = int(offs_np[-1])
+    H = wl.HIDDEN
+    x = wl.routed_activations(counts, offs_np, H, seed=1, device=dev)
+    mx = {"q_row": torch.empty((R, H), dtype=torch.uint8, device=dev),
+          "sf_row": torch.empty(nvq.sf_bytes(R, H, 32), dtype=torch.uint8, device=dev),
+          "q_colT": torch.empty((H, R), dtype=torch.uint8, device=dev),
+          "sf_colT": torch.empty(nvq.sf_bytes(H, R, 32), dtype=torch.uint8, device=dev)}
+    nx = (torch.empty((R, H // 2), dtype=torch.uint8, device=dev),
+          torch.empty(nvq.sf_bytes(R, H, 16), dtype=torch.uint8, device=dev),
+          torch.empty(R, dtype=torch.float32, device=dev))
+    kernels = [
+        Kernel("mxfp8_quantize X row+col", "hbm", R * H * 4.0625, "quant_mxfp8.cu", "hbm", "4.0625 B/elem"),
+        Kernel("nvfp4_quantize_per_token X", "hbm", R * H * 2.5625 + 4 * R, "quant_nvfp4.cu", "hbm", "2.5625 B/elem + 4 B/row"),
+    ]
+
+    def step(timer, xin=None, win=None):
+        xx = x if xin is None else xin[0]
+        timer.run(kernels[0].name, lambda: nvq.mxfp8_quantize(xx, out=mx))
+        timer.run(kernels[1].name, lambda: nvq.nvfp4_quantize_per_token(xx, out=nx))
+        return [nx[0], nx[1], nx[2]]
+
+    config = {"workload": "quantizers on the routed gate_up input (Qwen3-30B-A3B, 16384 tokens top-8)",
+              "x": [R, H]}
+    return {"step": step, "kernels": kernels, "gemm_flops": 0.0, "inputs": [x], "input_groups": ([0], []),
+            "config": config, "dtype": "bf16 -> mxfp8 / nvfp4", "unit": "GB/s"}
+
+
+WORKLOADS = {"dense": _workload_dense, "quant": _workload_quant, "moe": _workload_moe, "backward": _workload_backward,
+             "decode": _workload_decode}
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"nvq_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "samples": len(rows), "reasons": reasons}
+
+
+def _peak(kind, peaks):
+    if kind == "hbm":
+        return peaks["hbm_gbs"], "GB/s"
+    ratio = {"fp8": 2.0, "fp4": 6.0}[kind]      # dense FP8 = 2x BF16, FP4 = 6x BF16 on GB300
+    return peaks["bf16_tflops"] * ratio, "TFLOP/s"
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import nvfp4_quantization_block_gb300 as nvq
+    import workloads as wl
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    peaks = _load_peaks()
+    W = WORKLOADS[args.workload](torch, nvq, wl, dev)
+    if args.steps is None:
+        # size the timed region to ~2 s (clock sampling needs it), from one untimed probe step
+        W["step"](timer)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        W["step"](timer)
+        b.record()
+        torch.cuda.synchronize()
+        args.steps = int(max(20, min(5000, 2000.0 / max(a.elapsed_time(b), 1e-3))))
+    timer = Timer(torch)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    # warm-up
+    for _ in range(args.warmup):
+        flush.zero_()
+        W["step"](timer)
+    barrier()
+
+    # timed region: K steps, per-kernel and per-step CUDA events, L2 flushed before each step
+    step_ev = []
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.5)                              # let the sampler start before the timed region
+    launches0 = nvq.launch_count()
+    timer.active = True
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        W["step"](timer)
+        b.record()
+        step_ev.append((a, b))
+    barrier()
+    wall = time.perf_counter() - t0
+    timer.active = False
+    launches = nvq.launch_count() - launches0
+    clk = clocks.stop()
+    step_ms = [a.elapsed_time(b) for a, b in step_ev]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    if W.get("unit") == "GB/s":
+        amount = sum(k.amount for k in W["kernels"])
+        value = amount * args.steps * world / (total_ms * 1e-3) / 1e9
+    else:
+        value = W["gemm_flops"] * args.steps * world / (total_ms * 1e-3) / 1e12
+
+    # per-kernel roofline
+    durs = timer.durations_ms()
+    kern = []
+    for k in W["kernels"]:
+        d = durs.get(k.name, [])
+        avg_ms = sum(d) / len(d) if d else float("nan")
+        peak, unit = _peak(k.peak_key, peaks)
+        achieved = (k.amount / (avg_ms * 1e-3)) / (1e9 if unit == "GB/s" else 1e12)
+        tr = NCU_TRAFFIC.get(args.workload, {}).get(k.name)
+        traffic = tr["bytes"] if tr and tr.get("src_sha") == _src_hash(k.src) else None
+        kern.append({"kernel": k.name, "bound": k.bound, "avg_ms": round(avg_ms, 5),
+                     "share": None, "achieved": round(achieved, 1), "peak": round(peak, 1), "unit": unit,
+                     "frac": round(achieved / peak, 4), "algorithmic": k.note,
+                     "amount_per_launch": k.amount, "traffic": traffic})
+    kt = sum(x["avg_ms"] for x in kern)
+    for x in kern:
+        x["share"] = round(x["avg_ms"] / kt, 4)
+    dom = max(kern, key=lambda x: x["avg_ms"])
+    q = [x for x in kern if x["kernel"].startswith(("mxfp8_quantize", "nvfp4_quantize"))]
+    quant_gbs = (sum(k.amount for k in W["kernels"] if any(k.name == x["kernel"] for x in q)) /
+                 (sum(x["avg_ms"] for x in q) * 1e-3) / 1e9) if q else None
+
+    # end to end: pinned host inputs copied in, step through the C-ABI, GEMM outputs copied out
+    e2e = None
+    if not args.no_e2e:
+        host_in = [t.detach().cpu().pin_memory() for t in W["inputs"]]
+        dev_in = [torch.empty_like(t) for t in W["inputs"]]
+        outs = W["step"](Timer(torch))
+        host_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+        h2d = sum(t.numel() * t.element_size() for t in host_in)
+        d2h = sum(t.numel() * t.element_size() for t in host_out)
+        groups = W.get("input_groups")
+
+        def e2e_step():
+            for h, dv in zip(host_in, dev_in):
+                dv.copy_(h, non_blocking=True)
+            if groups is None:
+                res = W["step"](Timer(torch), dev_in[0], dev_in[1])
+            else:
+                xi = [dev_in[i] for i in groups[0]]
+                wi = [dev_in[i] for i in groups[1]] or None
+                res = W["step"](Timer(torch), xi, wi)
+            for o, h in zip(res, host_out):
+                h.copy_(o, non_blocking=True)
+
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        barrier()
+        e2e_steps = min(args.steps, 100)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(e2e_steps):
+            e2e_step()
+        b.record()
+        barrier()
+        e2e_ms = a.elapsed_time(b)
+        if world > 1:
+            t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        scale_amt = (sum(k.amount for k in W["kernels"]) / 1e9) if W.get("unit") == "GB/s" else W["gemm_flops"] / 1e12
+        e2e = {"value": round(scale_amt * e2e_steps * world / (e2e_ms * 1e-3), 2),
+               "unit": W.get("unit", "TFLOPS"), "ms_per_step": round(e2e_ms / e2e_steps, 4), "steps": e2e_steps,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(args.workload)
+
+    if world > 1:
+        dist.barrier()
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": W.get("unit", "TFLOPS"), "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": W["dtype"], "data": "synthetic (seeded)",
+            "config": dict(W["config"], parallelism=f"replicas x{world}" if world > 1 else "single GPU",
+                           l2="256 MiB flush before every step, outside the step events",
+                           gemm_flops_per_step=W["gemm_flops"]),
+            "quantize_gbs": round(quant_gbs, 1) if quant_gbs else None,
+            "quantize_frac_hbm": round(quant_gbs / peaks["hbm_gbs"], 4) if quant_gbs else None,
+            "roofline": {"kernel": dom["kernel"], "bound": dom["bound"], "achieved": dom["achieved"],
+                         "peak": dom["peak"], "unit": dom["unit"], "frac": dom["frac"], "traffic": dom["traffic"],
+                         "peak_source": f"{peaks['source']} (bf16 burst x {'6' if 'NVFP4' in dom['kernel'] else '2'}"
+                                        f" for tensor; STREAM copy for HBM)"},
+            "kernels": kern,
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches),
+            "clocks": clk, "wall_s_timed_region": round(wall, 4),
+        }
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------------------------------------------
+# CPU oracle (test infrastructure): cpu_baseline leg and the reference arm
+# ------------------------------------------------------------------------------------------------
+def _oracle_sample(workload, rows, cols):
+    """Run the oracle on a bounded sample of the workload; returns (seconds, gemm flops, description)."""
+    import numpy as np
+
+    import oracle
+    import workloads as wl
+
+    rng = np.random.default_rng(0)
+    t0 = time.perf_counter()
+    flops = 0.0
+    if workload == "dense":
+        inp = wl.dense_inputs(seed=0, device="cpu")
+        xb = wl.to_bits(inp["x"][:rows])
+        wb = wl.to_bits(inp["w"][:, :cols].T.contiguous())          # W columns as rows
+        t0 = time.perf_counter()
+        mx = oracle.mxfp8_quantize(xb)
+        mw = oracle.mxfp8_quantize(wb, colwise=False)
+        nq, nsf, ns = oracle.nvfp4_quantize_per_token(xb)
+        amax_w = np.abs(oracle.bf16_bits_to_f64(wl.to_bits(inp["w"]))).max()
+        sw = oracle.nvfp4_token_scale(np.array([amax_w]))
+        wq, wsf = oracle.nvfp4_quantize_rows(oracle.bf16_bits_to_f64(wb), np.repeat(sw, cols))
+        a8 = oracle.deq_operand("mxfp8", mx["q_row"], mx["sf_row"])
+        b8 = oracle.deq_operand("mxfp8", mw["q_row"], mw["sf_row"])
+        d8, _ = oracle.grouped_gemm_reference("m", a8, b8[None], [0, rows])
+        a4 = oracle.deq_operand("nvfp4", nq, nsf)
+        b4 = oracle.deq_operand("nvfp4", wq, wsf)
+        d4, _ = oracle.grouped_gemm_reference("m", a4, b4[None], [0, rows], ns, sw)
+        oracle.dequantize_nvfp4(wq, wsf, np.repeat(sw, cols))
+        K = xb.shape[1]
+        flops = 2 * 2.0 * rows * cols * K
+        desc = f"oracle on X rows [{rows} x {K}] and W columns [{K} x {cols}]: every quantizer, both GEMMs, dequant"
+    elif workload == "quant":
+        import torch
+        K = wl.HIDDEN
+        x = rng.standard_normal((rows, K)).astype(np.float32)
+        xb = wl.to_bits(torch.from_numpy(x).to(torch.bfloat16))
+        t0 = time.perf_counter()
+        oracle.mxfp8_quantize(xb)
+        oracle.nvfp4_quantize_per_token(xb)
+        flops = rows * K * (4.0625 + 2.5625) + 4 * rows            # algorithmic bytes, not flops
+        desc = f"oracle MXFP8 row+col and per-token NVFP4 of {rows} rows x {K}"
+    else:
+        counts, offs = wl.moe_routing() if workload != "decode" else (None, None)
+        K = wl.HIDDEN
+        N = 2 * wl.INTERMEDIATE
+        x = rng.standard_normal((rows, K)).astype(np.float32)
+        w = (rng.standard_normal((K, N)) * 0.02).astype(np.float32)
+        import torch
+        xb = wl.to_bits(torch.from_numpy(x).to(torch.bfloat16))
+        wb = wl.to_bits(torch.from_numpy(w).to(torch.bfloat16))
+        t0 = time.perf_counter()
+        if workload == "backward":
+            mx = oracle.mxfp8_quantize(xb)
+            mw = oracle.mxfp8_quantize(wb[:, :cols].copy(), colwise=False)
+            a = oracle.deq_operand("mxfp8", mx["q_row"], mx["sf_row"])
+            b = oracle.deq_operand("mxfp8", oracle.mxfp8_quantize(np.ascontiguousarray(wb[:, :cols].T), colwise=False)["q_row"],
+                                   oracle.mxfp8_quantize(np.ascontiguousarray(wb[:, :cols].T), colwise=False)["sf_row"])
+            oracle.grouped_gemm_reference("m", a, b[None], [0, rows])
+            del mw
+        else:
+            q, sf, s = oracle.nvfp4_quantize_per_token(xb)
+            wq, wsf, sw = oracle.nvfp4_quantize_weights(wb[None, :, :cols].copy())
+            a = oracle.deq_operand("nvfp4", q, sf)
+            b = oracle.deq_operand("nvfp4", wq[0], wsf[0])
+            oracle.grouped_gemm_reference("m", a, b[None], [0, rows], s, sw)
+        flops = 2.0 * rows * cols * K
+        desc = f"oracle on {rows} routed rows x {cols} output columns, K={K} (one expert's GEMM block + its quantizers)"
+        del counts, offs
+    return time.perf_counter() - t0, flops, desc
+
+
+def cpu_baseline(workload, rows=2048, cols=1536):
+    """Time the oracle in a single-threaded child process (BLAS threads pinned to 1)."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    cmd = [sys.executable, os.path.abspath(__file__), "--oracle-sample", workload, "--rows", str(rows),
+           "--cols", str(cols)]
+    try:
+        out = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=600)
+        res = json.loads(out.stdout.strip().splitlines()[-1])
+    except (subprocess.SubprocessError, ValueError, IndexError) as e:
+        return {"value": None, "unit": "TFLOPS", "cores": 1, "kind": "oracle", "sample": f"failed: {e}"}
+    if workload == "quant":
+        return {"value": res["flops"] / res["seconds"] / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                "sample": res["sample"], "seconds": round(res["seconds"], 3)}
+    return {"value": res["flops"] / res["seconds"] / 1e12, "unit": "TFLOPS", "cores": 1, "kind": "oracle",
+            "sample": res["sample"], "seconds": round(res["seconds"], 3)}
+
+
+def run_reference(args):
+    if args.steps is None:
+        args.steps = 5
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return
+    rows, cols = 256, 256
+    for _ in range(args.warmup):
+        _oracle_sample(args.workload, rows, cols)
+    times, flops, desc = [], 0.0, ""
+    for _ in range(args.steps):
+        t, flops, desc = _oracle_sample(args.workload, rows, cols)
+        times.append(t)
+    total = sum(times)
+    unit = "GB/s" if args.workload == "quant" else "TFLOPS"
+    value = flops * len(times) / total / (1e9 if unit == "GB/s" else 1e12)
+    line = {"metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(1e3 * total / len(times), 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic (seeded)",
+            "impl": "reference",
+            "config": {"workload": args.workload, "sample": desc},
+            "cpu_baseline": {"value": value, "unit": unit, "cores": 1, "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: enough for about 2 s of device time, at least 20)")
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="dense")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--oracle-sample", default=None, help=argparse.SUPPRESS)
+    ap.add_argument("--rows", type=int, default=512, help=argparse.SUPPRESS)
+    ap.add_argument("--cols", type=int, default=512, help=argparse.SUPPRESS)
+    args = ap.parse_args()
+    if args.oracle_sample:
+        t, f, d = _oracle_sample(args.oracle_sample, args.rows, args.cols)
+        print(json.dumps({"seconds": t, "flops": f, "sample": d}))
+        return
+    if args.warmup < 3 and args.impl == "ours":
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -50,6 +50,10 @@ typedef enum { NVQ_SCOPE_ROW = 0, NVQ_SCOPE_MATRIX = 1 } nvq_scope;
 /* Human-readable name of a status code (static string). */
 const char* nvq_status_string(nvq_status s);
 
+/* Number of kernels this library has enqueued since it was loaded, counted on the host at each
+ * successful launch (diagnostics: lets a caller confirm which work ran in these kernels). */
+uint64_t nvq_launch_count(void);
+
 /* Bytes of a scale matrix for `rows` rows and `cols` elements per row quantized in blocks of
  * `block` (32 for MXFP8, 16 for NVFP4): rows*cols/block (CANONICAL) or the padded tile size (MMA).
  * Returns -1 on invalid arguments. Host-only; touches no device state. */

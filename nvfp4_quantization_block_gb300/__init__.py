@@ -44,6 +44,7 @@ def _sig(name, args, res=ctypes.c_int):
 
 _status_string = _sig("nvq_status_string", [ctypes.c_int], ctypes.c_char_p)
 _sf_bytes = _sig("nvq_sf_bytes", [_i64, _i64, _i32, ctypes.c_int], _i64)
+_launch_count = _sig("nvq_launch_count", [], ctypes.c_uint64)
 _mxfp8_quantize = _sig("mxfp8_quantize", [_vp, _i64, _i64, _i64, _vp, _vp, _vp, _vp, ctypes.c_int, _vp])
 _nvfp4_quantize_per_token = _sig("nvfp4_quantize_per_token", [_vp, _i64, _i64, _i64, _vp, _vp, _vp, ctypes.c_int, _vp])
 _nvfp4_quantize_weights = _sig("nvfp4_quantize_weights", [_vp, _i64, _i64, _i64, _vp, _vp, _vp, ctypes.c_int, _vp])
@@ -96,6 +97,11 @@ def _layout(sf_layout):
     if sf_layout in ("canonical", SF_CANONICAL):
         return SF_CANONICAL
     raise ValueError(sf_layout)
+
+
+def launch_count():
+    """Kernels enqueued by the library so far (host-side counter)."""
+    return int(_launch_count())
 
 
 def sf_bytes(rows, cols, block, sf_layout="mma"):

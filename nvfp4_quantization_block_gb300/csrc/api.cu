@@ -1,10 +1,16 @@
 // C-ABI entry points (include/nvq.h): argument validation on the host, then kernel launches.
 // Nothing here allocates, frees or synchronises.
+#include <atomic>
 #include <cstdint>
 #include <cuda_runtime.h>
 
 #include "../../include/nvq.h"
 #include "nvq_internal.h"
+
+namespace nvq {
+static std::atomic<uint64_t> g_launches{0};
+void count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+}  // namespace nvq
 
 namespace {
 
@@ -29,6 +35,8 @@ const char* nvq_status_string(nvq_status s) {
     }
     return "NVQ_ERR_UNKNOWN";
 }
+
+uint64_t nvq_launch_count(void) { return nvq::g_launches.load(std::memory_order_relaxed); }
 
 int64_t nvq_sf_bytes(int64_t rows, int64_t cols, int32_t block, nvq_sf_layout layout) {
     if (rows < 0 || cols < 0 || (block != 16 && block != 32) || cols % block || !valid_layout(layout))

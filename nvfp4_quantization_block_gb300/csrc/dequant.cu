@@ -97,7 +97,9 @@ cudaError_t launch_dequantize_bf16(int fmt_nvfp4, const uint8_t* q, const uint8_
         dequant_nvfp4_kernel<<<(unsigned)((nblk + 255) / 256), 256, 0, stream>>>(
             q, sf, s, rows, total_rows, cols, scope_matrix, mma_layout, out);
     }
-    return cudaGetLastError();
+    const cudaError_t err = cudaGetLastError();
+    if (err == cudaSuccess) count_launches(1);
+    return err;
 }
 
 }  // namespace nvq

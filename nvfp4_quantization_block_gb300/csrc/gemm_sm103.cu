@@ -37,6 +37,7 @@
 
 #include "../../include/nvq.h"
 #include "nvq_device.cuh"
+#include "nvq_internal.h"
 
 namespace nvq {
 
@@ -671,7 +672,9 @@ static nvq_status launch_gemm(const nvq_gemm_args* a, cudaStream_t stream) {
     const int grid = num_sms();
     if (grid <= 0) return NVQ_ERR_CUDA;
     block_scaled_gemm_kernel<FP4><<<grid, GEMM_THREADS, C::SMEM_BYTES, stream>>>(ta, tb, p);
-    return cudaGetLastError() == cudaSuccess ? NVQ_OK : NVQ_ERR_CUDA;
+    if (cudaGetLastError() != cudaSuccess) return NVQ_ERR_CUDA;
+    count_launches(1);
+    return NVQ_OK;
 }
 
 }  // namespace nvq

@@ -22,5 +22,6 @@ cudaError_t launch_dequantize_bf16(int fmt_nvfp4, const uint8_t* q, const uint8_
                                    int scope_matrix, int64_t groups, int64_t rows, int64_t cols,
                                    int mma_layout, uint16_t* out, cudaStream_t stream);
 
-struct GemmLaunch;   // defined in gemm_sm103.cu
+// Host-side count of kernels this library has enqueued (diagnostics; see nvq_launch_count).
+void count_launches(int n);
 }  // namespace nvq

@@ -141,7 +141,9 @@ cudaError_t launch_mxfp8_quantize(const uint16_t* x, int64_t R, int64_t C, int64
     dim3 grid((unsigned)((C + MX_TILE - 1) / MX_TILE), (unsigned)((R + MX_TILE - 1) / MX_TILE));
     mxfp8_quant_kernel<<<grid, MX_THREADS, 0, stream>>>(x, R, C, ldx, q_row, sf_row, q_colT, sf_colT,
                                                         mma_layout);
-    return cudaGetLastError();
+    const cudaError_t err = cudaGetLastError();
+    if (err == cudaSuccess) count_launches(1);
+    return err;
 }
 
 }  // namespace nvq

@@ -105,7 +105,9 @@ cudaError_t launch_nvfp4_quantize_per_token(const uint16_t* x, int64_t R, int64_
     const int rows_per_cta = TOK_THREADS / 32;
     const int64_t grid = (cover + rows_per_cta - 1) / rows_per_cta;
     nvfp4_token_kernel<<<(unsigned)grid, TOK_THREADS, 0, stream>>>(x, R, C, ldx, q, sf, s_tok, mma_layout, cover);
-    return cudaGetLastError();
+    const cudaError_t err = cudaGetLastError();
+    if (err == cudaSuccess) count_launches(1);
+    return err;
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -216,8 +218,12 @@ __global__ void zero_bytes_kernel(uint8_t* p, int64_t n) {
 cudaError_t launch_nvfp4_quantize_weights(const uint16_t* w, int64_t E, int64_t K, int64_t N,
                                           uint8_t* qT, uint8_t* sfT, float* s_w, int mma_layout,
                                           cudaStream_t stream) {
-    cudaError_t err = cudaMemsetAsync(s_w, 0, sizeof(float) * (size_t)E, stream);
-    if (err != cudaSuccess) return err;
+    int launched = 0;
+    cudaError_t err;
+    // s_w accumulates the amax bits per expert: clear it first
+    zero_bytes_kernel<<<(unsigned)((4 * E + 255) / 256), 256, 0, stream>>>(reinterpret_cast<uint8_t*>(s_w), 4 * E);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    ++launched;
     const int64_t per_expert = K * N;
     int64_t blocks = (per_expert / 8 + 255) / 256;
     if (blocks > 64) blocks = 64;
@@ -225,25 +231,30 @@ cudaError_t launch_nvfp4_quantize_weights(const uint16_t* w, int64_t E, int64_t 
     nvfp4_weight_amax_kernel<<<dim3((unsigned)blocks, (unsigned)E), 256, 0, stream>>>(
         w, per_expert, reinterpret_cast<uint32_t*>(s_w));
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    ++launched;
     if (mma_layout) {
         // rows of the stacked [E*N, K/16] scale matrix are padded to 128; the encode kernel writes
-        // every real row's tile bytes (column padding included), so only trailing pad rows remain
+        // every real row's tile bytes (column padding included), so only trailing pad rows remain:
+        // zero the last row tile before the encode kernel fills its real rows
         const int64_t rows = E * N, kb = K >> 4;
         const int64_t padded_rows = (rows + 127) & ~int64_t(127);
         if (padded_rows > rows) {
-            const int64_t start = mma_sf_offset(padded_rows - 128, 0, kb);   // last row tile
+            const int64_t start = mma_sf_offset(padded_rows - 128, 0, kb);
             const int64_t bytes = ((kb + 3) >> 2) * 512;
-            // the tile also holds real rows; rewrite it fully below by zeroing first
             zero_bytes_kernel<<<(unsigned)((bytes + 255) / 256), 256, 0, stream>>>(sfT + start, bytes);
             if ((err = cudaGetLastError()) != cudaSuccess) return err;
+            ++launched;
         }
     }
     dim3 grid((unsigned)((N + WT_N - 1) / WT_N), (unsigned)((K + WT_K - 1) / WT_K), (unsigned)E);
     nvfp4_weight_encode_kernel<<<grid, WT_THREADS, 0, stream>>>(w, K, N, qT, sfT,
                                                                reinterpret_cast<const uint32_t*>(s_w), mma_layout);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    ++launched;
     nvfp4_weight_finalize_kernel<<<(unsigned)((E + 255) / 256), 256, 0, stream>>>(s_w, E);
-    return cudaGetLastError();
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    count_launches(launched + 1);
+    return cudaSuccess;
 }
 
 }  // namespace nvq
