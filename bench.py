@@ -445,6 +445,7 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     peaks = _load_peaks()
     W = WORKLOADS[args.workload](torch, nvq, wl, dev)
+    timer = Timer(torch)
     if args.steps is None:
         # size the timed region to ~2 s (clock sampling needs it), from one untimed probe step
         W["step"](timer)
@@ -455,7 +456,6 @@ def run_ours(args):
         b.record()
         torch.cuda.synchronize()
         args.steps = int(max(20, min(5000, 2000.0 / max(a.elapsed_time(b), 1e-3))))
-    timer = Timer(torch)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
     def barrier():
@@ -691,6 +691,9 @@ def cpu_baseline(workload, rows=2048, cols=1536):
 
 
 def run_reference(args):
+    # the oracle runs single-threaded (numpy is first imported below, after this)
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[var] = "1"
     if args.steps is None:
         args.steps = 5
     rank = int(os.environ.get("RANK", "0"))

@@ -11,7 +11,9 @@
 //          the bf16 conversion yields the single rounding of the exact product (Boldo & Melquiond,
 //          IEEE TC 2008). Tiny products, where the remainder could underflow, use fp64.
 // One thread produces one 32-element (MXFP8) or 16-element (NVFP4) block: 16- or 8-byte loads,
-// 64- or 32-byte stores, one scale byte, streaming through HBM once.
+// 64- or 32-byte stores, one scale byte, streaming through HBM once. NVFP4 blocks look their 16
+// results up in a per-block table of the 8 possible bf16 values (byte permutes), so the E2M1
+// conversion instruction, which issues on a low-throughput pipe, is not used per element.
 #include "nvq_device.cuh"
 #include "nvq_internal.h"
 
@@ -57,6 +59,9 @@ __device__ __forceinline__ float round_odd_product(float p, float s) {
     return f64_to_f32_round_odd((double)p * (double)s);
 }
 
+// One 16-element block: every element takes one of 8 magnitudes times the block's scale product,
+// so the block's 8 possible bf16 results are computed once (round-to-odd products) and the codes
+// select them with byte permutes; the sign bit is copied from the code. No per-element conversion.
 __global__ void __launch_bounds__(256)
 dequant_nvfp4_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ sf,
                      const float* __restrict__ s, int64_t rows_per_group, int64_t total_rows,
@@ -68,16 +73,22 @@ dequant_nvfp4_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ 
     const float coarse = s[scope_matrix ? row / rows_per_group : row];
     const float v_sf = e4m3_to_f32(sf[sf_index(row, kb, nkb, mma_layout)]);
     const uint2 packed = *reinterpret_cast<const uint2*>(q + row * (cols >> 1) + kb * 8);
-    const uint32_t in[2] = {packed.x, packed.y};
+    // bf16 results for magnitude codes 0..7 = {0, .5, 1, 1.5, 2, 3, 4, 6} x v_sf x coarse
+    const uint32_t p01 = cvt_bf16x2(0.0f, round_odd_product(0.5f * v_sf, coarse));
+    const uint32_t p23 = cvt_bf16x2(round_odd_product(v_sf, coarse), round_odd_product(1.5f * v_sf, coarse));
+    const uint32_t p45 = cvt_bf16x2(round_odd_product(2.0f * v_sf, coarse), round_odd_product(3.0f * v_sf, coarse));
+    const uint32_t p67 = cvt_bf16x2(round_odd_product(4.0f * v_sf, coarse), round_odd_product(6.0f * v_sf, coarse));
+    const uint32_t lo_a = __byte_perm(p01, p23, 0x6420), hi_a = __byte_perm(p01, p23, 0x7531);
+    const uint32_t lo_b = __byte_perm(p45, p67, 0x6420), hi_b = __byte_perm(p45, p67, 0x7531);
     uint32_t o[8];
+    const uint32_t in[2] = {packed.x, packed.y};
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            float e0, e1;
-            e2m1x2_to_f32((in[i] >> (8 * j)) & 0xFFu, e0, e1);
-            o[4 * i + j] = cvt_bf16x2(round_odd_product(e0 * v_sf, coarse), round_odd_product(e1 * v_sf, coarse));
-        }
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t qq = in[i >> 1] >> (16 * (i & 1));       // codes of elements 4i .. 4i+3
+        const uint32_t sel = qq & 0x7777u;
+        const uint32_t lo = __byte_perm(lo_a, lo_b, sel), hi = __byte_perm(hi_a, hi_b, sel);
+        o[2 * i] = __byte_perm(lo, hi, 0x5140) | ((qq << 12) & 0x8000u) | ((qq << 24) & 0x80000000u);
+        o[2 * i + 1] = __byte_perm(lo, hi, 0x7362) | ((qq << 4) & 0x8000u) | ((qq << 16) & 0x80000000u);
     }
     uint4* dst = reinterpret_cast<uint4*>(out + row * cols + kb * 16);
     dst[0] = make_uint4(o[0], o[1], o[2], o[3]);

@@ -378,13 +378,16 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
         int slot = 0;
         uint32_t phase = 0;
         int64_t issued = 0;
+        uint32_t sfa_fills[C::STAGES];          // shifted-tile fills of each slot's sfa_bar
+        for (int i = 0; i < C::STAGES; ++i) sfa_fills[i] = 0;
         bool ok = true;
         for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
             const Tile tl = sched.get(t);
             if (tl.k_end <= tl.k_begin) continue;
             const int64_t ks0 = tl.k_begin / C::EPS, ks1 = (tl.k_end + C::EPS - 1) / C::EPS;
             const int64_t rb_a = tl.a_row0 / BM;
-            const bool need_a2 = (tl.a_row0 % BM) != 0 && rb_a + 1 < p.a_rowtiles;
+            const bool shifted = (tl.a_row0 % BM) != 0;
+            const bool need_a2 = shifted && rb_a + 1 < p.a_rowtiles;
             const int64_t rb_b = tl.b_row0 / BM;
             const bool need_b2 = rb_b + 1 < p.b_rowtiles;
             for (int64_t ks = ks0; ks < ks1; ++ks) {
@@ -397,21 +400,30 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
                 const int64_t kg0 = ks * C::KGS;
                 const int64_t kgn = min((int64_t)C::KGS, p.sf_tiles_per_row - kg0);
                 const uint32_t sf_bytes = (uint32_t)kgn * 512u;
-                // A scales (raw row tiles) complete on sfa_bar; the transposer turns them into the tile's
-                // own scale tile and then arrives on full_bar
-                mbar_arrive_expect_tx(&sfa_bar[slot], sf_bytes * (1u + (need_a2 ? 1u : 0u)));
-                bulk_load(ssfa_raw, p.sfa + ((rb_a * p.sf_tiles_per_row + kg0) << 9), sf_bytes, &sfa_bar[slot]);
-                if (need_a2)
-                    bulk_load(ssfa_raw + C::KGS * 512, p.sfa + (((rb_a + 1) * p.sf_tiles_per_row + kg0) << 9),
-                              sf_bytes, &sfa_bar[slot]);
-                const uint32_t tx = C::A_BYTES + C::B_BYTES + sf_bytes * (1u + (need_b2 ? 1u : 0u));
+                // full_bar completes after two arrivals and all bytes: the producer's expect_tx arrival
+                // (A, B, B scales, and the A scales of an aligned tile) plus either the producer's
+                // second arrival (aligned tile) or the transposer's (tile starting inside a scale tile)
+                const uint32_t tx = C::A_BYTES + C::B_BYTES + sf_bytes * (1u + (need_b2 ? 1u : 0u)) +
+                                    (shifted ? 0u : sf_bytes);
                 mbar_arrive_expect_tx(&full_bar[slot], tx);
+                if (shifted) {
+                    mbar_arrive_expect_tx(&sfa_bar[slot], sf_bytes * (1u + (need_a2 ? 1u : 0u)));
+                    ++sfa_fills[slot];
+                    bulk_load(ssfa_raw, p.sfa + ((rb_a * p.sf_tiles_per_row + kg0) << 9), sf_bytes, &sfa_bar[slot]);
+                    if (need_a2)
+                        bulk_load(ssfa_raw + C::KGS * 512, p.sfa + (((rb_a + 1) * p.sf_tiles_per_row + kg0) << 9),
+                                  sf_bytes, &sfa_bar[slot]);
+                } else {
+                    bulk_load(ssfb - C::SFA_BYTES, p.sfa + ((rb_a * p.sf_tiles_per_row + kg0) << 9), sf_bytes,
+                              &full_bar[slot]);
+                }
                 tma_load_2d(sa, &tmap_a, (int32_t)(ks * BKB), (int32_t)tl.a_row0, &full_bar[slot]);
                 tma_load_2d(sb, &tmap_b, (int32_t)(ks * BKB), (int32_t)tl.b_row0, &full_bar[slot]);
                 bulk_load(ssfb, p.sfb + ((rb_b * p.sf_tiles_per_row + kg0) << 9), sf_bytes, &full_bar[slot]);
                 if (need_b2)
                     bulk_load(ssfb + C::KGS * 512, p.sfb + (((rb_b + 1) * p.sf_tiles_per_row + kg0) << 9), sf_bytes,
                               &full_bar[slot]);
+                if (!shifted) mbar_arrive(&full_bar[slot]);
                 ++issued;
                 if (++slot == C::STAGES) { slot = 0; phase ^= 1u; }
             }
@@ -422,9 +434,10 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
             int s2 = slot - 1 - (int)i;
             uint32_t ph = phase;
             if (s2 < 0) { s2 += C::STAGES; ph ^= 1u; }
-            mbar_drain(&sfa_bar[s2], ph);
             mbar_drain(&full_bar[s2], ph);
         }
+        for (int s2 = 0; s2 < C::STAGES; ++s2)
+            if (sfa_fills[s2]) mbar_drain(&sfa_bar[s2], (sfa_fills[s2] - 1u) & 1u);
     } else if (warp == 1 && lane == 0) {
         // =========================== MMA issuer ===========================
         int slot = 0;
@@ -485,7 +498,7 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
         // scales of rows l, l+32, l+64, l+96 as four 4-byte words, so the tile's own line l is the
         // 16-byte window starting g0 words into (line l of tile 0 ++ line l of tile 1).
         int slot = 0;
-        uint32_t phase = 0;
+        uint32_t sfa_phase = 0;                 // bit s: parity of the next sfa_bar[s] phase
         bool ok = true;
         const uint32_t stage0 = smem_u32(stage_base);
         for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
@@ -493,9 +506,15 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
             if (tl.k_end <= tl.k_begin) continue;
             const int64_t ks0 = tl.k_begin / C::EPS, ks1 = (tl.k_end + C::EPS - 1) / C::EPS;
             const int g0 = (int)((tl.a_row0 % BM) / 32);
+            if (g0 == 0) {
+                // aligned tile: the producer loaded the scales in place; only keep the ring position
+                slot = (int)((slot + (ks1 - ks0)) % C::STAGES);
+                continue;
+            }
             for (int64_t ks = ks0; ks < ks1; ++ks) {
                 int good = 1;
-                if (lane == 0) good = mbar_wait(&sfa_bar[slot], phase, abort_flag, p.status) ? 1 : 0;
+                if (lane == 0)
+                    good = mbar_wait(&sfa_bar[slot], (sfa_phase >> slot) & 1u, abort_flag, p.status) ? 1 : 0;
                 good = __shfl_sync(0xffffffffu, good, 0);
                 if (!good) { ok = false; break; }
                 const uint32_t st = stage0 + (uint32_t)slot * C::STAGE_BYTES;
@@ -522,7 +541,8 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&full_bar[slot]);
-                if (++slot == C::STAGES) { slot = 0; phase ^= 1u; }
+                sfa_phase ^= 1u << slot;
+                if (++slot == C::STAGES) slot = 0;
             }
         }
     } else if (warp >= 2) {

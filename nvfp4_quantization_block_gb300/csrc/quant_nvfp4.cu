@@ -8,16 +8,15 @@
 // no fast math)]. Coarse scale s = RN(amax / 2688); block scale = E4M3 RNE of amax_b / (6 s);
 // code = E2M1 RNE (saturating) of x / (E4M3(sf) s). Exactness: see nvq_device.cuh.
 //
-// Per-token design: one warp per token row. The row (up to 2048 elements) is held in registers
-// after one coalesced 128-bit pass, reduced to its amax with warp shuffles, and encoded from
-// registers, so each input byte is read from HBM once. A 1x16 block is two adjacent lanes.
+// Per-token design: one warp per token row, one 16-element block per lane per step (see the
+// kernel). Weights: one thread per (column, 16-row block) after a shared-memory transpose.
 #include "nvq_device.cuh"
 #include "nvq_internal.h"
 
 namespace nvq {
 
 constexpr int TOK_THREADS = 256;          // 8 rows per CTA
-constexpr int TOK_NREG = 8;               // 8 x 256 elements held in registers per row
+constexpr int TOK_NREG = 4;               // 4 x 32 blocks of 16 = 2048 elements held in registers per row
 
 __device__ __forceinline__ void store_sf_group(uint8_t* sf, int64_t row, int64_t kb0, int64_t nkb,
                                                uint32_t word, int mma_layout) {
@@ -30,56 +29,67 @@ __device__ __forceinline__ void store_sf_group(uint8_t* sf, int64_t row, int64_t
     }
 }
 
-// One 256-element step of a row: lane holds 8 elements; lanes (2j, 2j+1) form one 1x16 block.
-__device__ __forceinline__ void token_chunk(const uint4& vv, int i, int lane, int64_t row, bool real,
-                                            int64_t nchunk, int64_t nkb, int64_t C, const Nvfp4Scope& sc,
-                                            const E4M3InvTable& inv, uint8_t* __restrict__ q,
-                                            uint8_t* __restrict__ sf, int mma_layout) {
-    const int64_t ch = (int64_t)i * 32 + lane;
-    uint32_t mb = absmax_bits_8(vv);
-    mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
-    const uint32_t sfc = nvfp4_block_scale(__uint_as_float(mb << 16), sc);
-    const uint32_t codes = nvfp4_encode8(vv, sfc, sc, inv);
-    if (real && ch < nchunk) *reinterpret_cast<uint32_t*>(q + row * (C >> 1) + ch * 4) = codes;
-    const uint32_t s2 = __shfl_down_sync(0xffffffffu, sfc, 2);
-    const uint32_t s4 = __shfl_down_sync(0xffffffffu, sfc, 4);
-    const uint32_t s6 = __shfl_down_sync(0xffffffffu, sfc, 6);
-    if ((lane & 7) == 0) {
-        const int64_t kb0 = (int64_t)i * 16 + (lane >> 1);
-        if (kb0 < nkb) store_sf_group(sf, row, kb0, nkb, sfc | (s2 << 8) | (s4 << 16) | (s6 << 24), mma_layout);
+template <bool V8>
+__device__ __forceinline__ void load_block(const uint16_t* p, uint4& a, uint4& b) {
+    if (V8) {
+        ld_v8(p, a, b);
+    } else {
+        a = ld_stream_v4(p);
+        b = ld_stream_v4(p + 8);
     }
 }
 
+// One 16-element block per lane: block kb = 32 i + lane of the row.
+__device__ __forceinline__ void token_block(const uint4& a, const uint4& b, int i, int lane, int64_t row,
+                                            bool real, int64_t nkb, int64_t C, const Nvfp4Scope& sc,
+                                            uint8_t* __restrict__ q, uint8_t* __restrict__ sf, int mma_layout) {
+    const int64_t kb = (int64_t)i * 32 + lane;
+    const uint32_t mb = max(absmax_bits_8(a), absmax_bits_8(b));
+    const uint32_t sfc = nvfp4_block_scale(__uint_as_float(mb << 16), sc);
+    E2M1Bounds bd;
+    if (sfc != 0u && !sc.exact) bd = nvfp4_bounds(sfc, sc);
+    const uint32_t c0 = nvfp4_encode8(a, sfc, sc, bd);
+    const uint32_t c1 = nvfp4_encode8(b, sfc, sc, bd);
+    if (real && kb < nkb) *reinterpret_cast<uint2*>(q + row * (C >> 1) + kb * 8) = make_uint2(c0, c1);
+    const uint32_t s1 = __shfl_down_sync(0xffffffffu, sfc, 1);
+    const uint32_t s2 = __shfl_down_sync(0xffffffffu, sfc, 2);
+    const uint32_t s3 = __shfl_down_sync(0xffffffffu, sfc, 3);
+    if ((lane & 3) == 0 && kb < nkb) store_sf_group(sf, row, kb, nkb, sfc | (s1 << 8) | (s2 << 16) | (s3 << 24), mma_layout);
+}
+
+// One warp per token row, one 16-element block per lane per step: the row (up to 2048 elements) is
+// loaded once with 32-byte coalesced loads, reduced to its amax with warp shuffles, and encoded
+// from registers, so each input byte is read from HBM once.
+template <bool V8>
 __global__ void __launch_bounds__(TOK_THREADS)
 nvfp4_token_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t C, int64_t ldx,
                    uint8_t* __restrict__ q, uint8_t* __restrict__ sf, float* __restrict__ s_tok,
                    int mma_layout, int64_t rows_cover) {
-    __shared__ E4M3InvTable inv;
-    init_e4m3_inv_table(inv);
-    __syncthreads();
-
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t row = (int64_t)blockIdx.x * (TOK_THREADS / 32) + warp;
     if (row >= rows_cover) return;
     const bool real = row < R;
-    const int64_t nchunk = C >> 3;                       // 8-element chunks
-    const int iters = (int)((nchunk + 31) >> 5);
-    const int64_t nkb = C >> 4;
+    const int64_t nkb = C >> 4;                          // 16-element blocks
+    const int iters = (int)((nkb + 31) >> 5);
     const uint16_t* xr = x + row * ldx;
 
     // pass 1: load (into registers where possible) and reduce the row's amax
-    uint4 v[TOK_NREG];
+    uint4 va[TOK_NREG], vb[TOK_NREG];
     uint32_t m = 0;
 #pragma unroll
     for (int i = 0; i < TOK_NREG; ++i) {
-        v[i] = make_uint4(0u, 0u, 0u, 0u);
-        const int64_t ch = (int64_t)i * 32 + lane;
-        if (real && i < iters && ch < nchunk) v[i] = ld_stream_v4(xr + ch * 8);
-        m = max(m, absmax_bits_8(v[i]));
+        va[i] = vb[i] = make_uint4(0u, 0u, 0u, 0u);
+        const int64_t kb = (int64_t)i * 32 + lane;
+        if (real && i < iters && kb < nkb) load_block<V8>(xr + kb * 16, va[i], vb[i]);
+        m = max(m, max(absmax_bits_8(va[i]), absmax_bits_8(vb[i])));
     }
     for (int i = TOK_NREG; i < iters; ++i) {
-        const int64_t ch = (int64_t)i * 32 + lane;
-        if (real && ch < nchunk) m = max(m, absmax_bits_8(ld_stream_v4(xr + ch * 8)));
+        const int64_t kb = (int64_t)i * 32 + lane;
+        if (real && kb < nkb) {
+            uint4 a, b;
+            load_block<V8>(xr + kb * 16, a, b);
+            m = max(m, max(absmax_bits_8(a), absmax_bits_8(b)));
+        }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -87,14 +97,15 @@ nvfp4_token_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t C, int64_t
     const Nvfp4Scope sc = make_nvfp4_scope(s);
     if (real && lane == 0) s_tok[row] = s;
 
-    // pass 2: per 1x16 block scale and codes (register-resident chunks first, then any reloads)
+    // pass 2: per 1x16 block scale and codes (register-resident blocks first, then any reloads)
 #pragma unroll
     for (int i = 0; i < TOK_NREG; ++i)
-        if (i < iters) token_chunk(v[i], i, lane, row, real, nchunk, nkb, C, sc, inv, q, sf, mma_layout);
+        if (i < iters) token_block(va[i], vb[i], i, lane, row, real, nkb, C, sc, q, sf, mma_layout);
     for (int i = TOK_NREG; i < iters; ++i) {
-        const int64_t ch = (int64_t)i * 32 + lane;
-        const uint4 vv = (real && ch < nchunk) ? ld_stream_v4(xr + ch * 8) : make_uint4(0u, 0u, 0u, 0u);
-        token_chunk(vv, i, lane, row, real, nchunk, nkb, C, sc, inv, q, sf, mma_layout);
+        const int64_t kb = (int64_t)i * 32 + lane;
+        uint4 a = make_uint4(0u, 0u, 0u, 0u), b = a;
+        if (real && kb < nkb) load_block<V8>(xr + kb * 16, a, b);
+        token_block(a, b, i, lane, row, real, nkb, C, sc, q, sf, mma_layout);
     }
 }
 
@@ -104,7 +115,11 @@ cudaError_t launch_nvfp4_quantize_per_token(const uint16_t* x, int64_t R, int64_
     const int64_t cover = mma_layout ? ((R + 127) & ~int64_t(127)) : R;
     const int rows_per_cta = TOK_THREADS / 32;
     const int64_t grid = (cover + rows_per_cta - 1) / rows_per_cta;
-    nvfp4_token_kernel<<<(unsigned)grid, TOK_THREADS, 0, stream>>>(x, R, C, ldx, q, sf, s_tok, mma_layout, cover);
+    const bool v8 = ((reinterpret_cast<uintptr_t>(x) & 31u) == 0) && (ldx % 16 == 0);
+    if (v8)
+        nvfp4_token_kernel<true><<<(unsigned)grid, TOK_THREADS, 0, stream>>>(x, R, C, ldx, q, sf, s_tok, mma_layout, cover);
+    else
+        nvfp4_token_kernel<false><<<(unsigned)grid, TOK_THREADS, 0, stream>>>(x, R, C, ldx, q, sf, s_tok, mma_layout, cover);
     const cudaError_t err = cudaGetLastError();
     if (err == cudaSuccess) count_launches(1);
     return err;
@@ -142,8 +157,6 @@ nvfp4_weight_encode_kernel(const uint16_t* __restrict__ w, int64_t K, int64_t N,
                            uint8_t* __restrict__ qT, uint8_t* __restrict__ sfT,
                            const uint32_t* __restrict__ amax_bits, int mma_layout) {
     __shared__ __align__(16) uint32_t tile[WT_K][WT_N / 2];
-    __shared__ E4M3InvTable inv;
-    init_e4m3_inv_table(inv);
 
     const int64_t e = blockIdx.z;
     const int64_t k0 = (int64_t)blockIdx.y * WT_K, n0 = (int64_t)blockIdx.x * WT_N;
@@ -180,8 +193,10 @@ nvfp4_weight_encode_kernel(const uint16_t* __restrict__ w, int64_t K, int64_t N,
     const uint4 lo = make_uint4(p[0], p[1], p[2], p[3]), hi = make_uint4(p[4], p[5], p[6], p[7]);
     const uint32_t mb = max(absmax_bits_8(lo), absmax_bits_8(hi));
     const uint32_t sfc = nvfp4_block_scale(__uint_as_float(mb << 16), sc);
-    const uint32_t c0 = nvfp4_encode8(lo, sfc, sc, inv);
-    const uint32_t c1 = nvfp4_encode8(hi, sfc, sc, inv);
+    E2M1Bounds bd;
+    if (sfc != 0u && !sc.exact) bd = nvfp4_bounds(sfc, sc);
+    const uint32_t c0 = nvfp4_encode8(lo, sfc, sc, bd);
+    const uint32_t c1 = nvfp4_encode8(hi, sfc, sc, bd);
     const int64_t kb = (k0 >> 4) + kblk, nkb = K >> 4;
     if (n < N && kb < nkb) {
         *reinterpret_cast<uint2*>(qT + (e * N + n) * (K >> 1) + kb * 8) = make_uint2(c0, c1);
