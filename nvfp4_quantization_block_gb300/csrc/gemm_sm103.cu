@@ -22,7 +22,9 @@
 //                  accumulating in TMEM (fp32, 256 columns). Commits free smem stages and signal
 //                  the epilogue. Warp 1 also allocates and frees TMEM.
 //   warps 2-5      epilogue: tcgen05.ld 32 columns at a time, multiply by s_a[row] s_b[e], round
-//                  to bf16 (or keep fp32) and store with 16-byte vector stores.
+//                  to bf16 into registers (the whole 256-column row of each thread), hand TMEM
+//                  back to the MMA warp, then store with 256-bit stores while the next tile's
+//                  MMAs run (fp32 output: stored chunk by chunk).
 // GROUP_K tiles iterate the group's reduction range in 32-element MMA steps (k-steps outside the
 // group inside a 128-element stage are skipped).
 //
@@ -82,6 +84,7 @@ struct GemmParams {
     const int64_t* offsets;
     void* d;
     int64_t ldd;
+    int d_aligned32;        // d and every row of it start on 32 bytes: 256-bit stores
     int32_t* status;
     int64_t a_rowtiles;     // 128-row scale tiles of A
     int64_t b_rowtiles;     // 128-row scale tiles of B (stacked rows)
@@ -213,6 +216,14 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
           "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(taddr));
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// 32 bytes to a 32-byte aligned global address in one 256-bit store.
+__device__ __forceinline__ void st_v8(void* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d, uint32_t e,
+                                      uint32_t f, uint32_t g, uint32_t h) {
+    asm volatile("st.global.v8.u32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+                 ::"l"(p), "r"(a), "r"(b), "r"(c), "r"(d), "r"(e), "r"(f), "r"(g), "r"(h)
+                 : "memory");
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -563,17 +574,18 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
                 if (!mbar_wait(tmem_full, acc_phase, abort_flag, p.status)) break;
                 tc_fence_after();
             }
-            for (int c = 0; c < BN / 32; ++c) {
-                const int64_t col = tl.n0 + c * 32;
-                uint32_t r[32];
-                if (!empty) {
-                    tmem_ld32(tmem_acc + ((uint32_t)(q * 32) << 16) + (uint32_t)(c * 32), r);
-                } else {
+            if (p.out_f32) {
+                // fp32 output: store each 32-column chunk as it leaves TMEM
+                for (int c = 0; c < BN / 32; ++c) {
+                    const int64_t col = tl.n0 + c * 32;
+                    uint32_t r[32];
+                    if (!empty) {
+                        tmem_ld32(tmem_acc + ((uint32_t)(q * 32) << 16) + (uint32_t)(c * 32), r);
+                    } else {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) r[j] = 0u;
-                }
-                if (!row_ok || col >= p.n) continue;
-                if (p.out_f32) {
+                        for (int j = 0; j < 32; ++j) r[j] = 0u;
+                    }
+                    if (!row_ok || col >= p.n) continue;
                     float* dst = reinterpret_cast<float*>(p.d) + drow * p.ldd + col;
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
@@ -581,23 +593,52 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
                                                __uint_as_float(r[4 * j + 2]) * scale, __uint_as_float(r[4 * j + 3]) * scale);
                         reinterpret_cast<float4*>(dst)[j] = v;
                     }
-                } else {
-                    uint16_t* dst = reinterpret_cast<uint16_t*>(p.d) + drow * p.ldd + col;
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        uint4 v;
-                        v.x = cvt_bf16x2(__uint_as_float(r[8 * j + 0]) * scale, __uint_as_float(r[8 * j + 1]) * scale);
-                        v.y = cvt_bf16x2(__uint_as_float(r[8 * j + 2]) * scale, __uint_as_float(r[8 * j + 3]) * scale);
-                        v.z = cvt_bf16x2(__uint_as_float(r[8 * j + 4]) * scale, __uint_as_float(r[8 * j + 5]) * scale);
-                        v.w = cvt_bf16x2(__uint_as_float(r[8 * j + 6]) * scale, __uint_as_float(r[8 * j + 7]) * scale);
-                        reinterpret_cast<uint4*>(dst)[j] = v;
-                    }
                 }
+                if (!empty) {
+                    tc_fence_before();
+                    mbar_arrive(tmem_empty);
+                    acc_phase ^= 1u;
+                }
+                continue;
+            }
+            // bf16 output: drain the whole accumulator row into registers as packed bf16 and hand
+            // TMEM back to the MMA warp before storing, so the stores overlap the next tile's MMAs
+            uint32_t pk[BN / 32][16];
+#pragma unroll
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t r[32];
+                if (!empty) {
+                    tmem_ld32(tmem_acc + ((uint32_t)(q * 32) << 16) + (uint32_t)(c * 32), r);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) r[j] = 0u;
+                }
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    pk[c][j] = cvt_bf16x2(__uint_as_float(r[2 * j]) * scale, __uint_as_float(r[2 * j + 1]) * scale);
             }
             if (!empty) {
                 tc_fence_before();
                 mbar_arrive(tmem_empty);
                 acc_phase ^= 1u;
+            }
+            if (row_ok) {
+                uint16_t* dst = reinterpret_cast<uint16_t*>(p.d) + drow * p.ldd + tl.n0;
+#pragma unroll
+                for (int c = 0; c < BN / 32; ++c) {
+                    if (tl.n0 + c * 32 >= p.n) break;
+                    if (p.d_aligned32) {
+#pragma unroll
+                        for (int h = 0; h < 2; ++h)
+                            st_v8(dst + c * 32 + h * 16, pk[c][8 * h], pk[c][8 * h + 1], pk[c][8 * h + 2], pk[c][8 * h + 3],
+                                  pk[c][8 * h + 4], pk[c][8 * h + 5], pk[c][8 * h + 6], pk[c][8 * h + 7]);
+                    } else {
+#pragma unroll
+                        for (int h = 0; h < 4; ++h)
+                            reinterpret_cast<uint4*>(dst + c * 32)[h] =
+                                make_uint4(pk[c][4 * h], pk[c][4 * h + 1], pk[c][4 * h + 2], pk[c][4 * h + 3]);
+                    }
+                }
             }
         }
     }
@@ -676,6 +717,7 @@ static nvq_status launch_gemm(const nvq_gemm_args* a, cudaStream_t stream) {
     p.offsets = a->offsets;
     p.d = a->d;
     p.ldd = a->ldd;
+    p.d_aligned32 = ((reinterpret_cast<uintptr_t>(a->d) & 31u) == 0) && (a->ldd % 16 == 0);
     p.status = a->status;
     p.a_rowtiles = (rows_a + BM - 1) / BM;
     p.b_rowtiles = (rows_b + BM - 1) / BM;
