@@ -44,8 +44,23 @@ L2_FLUSH_BYTES = 256 << 20
 
 # ncu DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of the kernels timed
 # here, keyed by workload and kernel, with the sha256 of the source file the capture was taken
-# from. The command that produced each number is in profiles/. A changed source reports null.
-NCU_TRAFFIC = {}
+# from. The commands that produced them are in profiles/launches_dense_step.md (dense) and
+# profiles/quant_routed_batch.md (quant). A changed source reports null.
+NCU_TRAFFIC = {
+    "dense": {
+        "mxfp8_quantize X row+col": {"bytes": 33600000, "src_sha": "3352a1d55c39ef58"},
+        "mxfp8_quantize W col": {"bytes": 21000000, "src_sha": "3352a1d55c39ef58"},
+        "nvfp4_quantize_per_token X": {"bytes": 33610000, "src_sha": "a0f791a42e9522ac"},
+        "nvfp4_quantize_weights W": {"bytes": 41980000, "src_sha": "a0f791a42e9522ac"},
+        "block_scaled_gemm MXFP8": {"bytes": 58490000, "src_sha": "cdf0360aff984fab"},
+        "block_scaled_gemm NVFP4": {"bytes": 42680000, "src_sha": "cdf0360aff984fab"},
+        "dequantize_bf16 W": {"bytes": 5910000, "src_sha": "def12a43bb80c45b"},
+    },
+    "quant": {
+        "mxfp8_quantize X row+col": {"bytes": 1050810000, "src_sha": "3352a1d55c39ef58"},
+        "nvfp4_quantize_per_token X": {"bytes": 679180000, "src_sha": "a0f791a42e9522ac"},
+    },
+}
 
 
 def _src_hash(name):
