@@ -240,8 +240,13 @@ cudaError_t launch_nvfp4_quantize_weights(const uint16_t* w, int64_t E, int64_t 
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     ++launched;
     const int64_t per_expert = K * N;
-    int64_t blocks = (per_expert / 8 + 255) / 256;
-    if (blocks > 64) blocks = 64;
+    // enough CTAs in total to fill the GPU a few times over, at least one per expert
+    int sms = 0, dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        sms = 148;
+    int64_t blocks = ((int64_t)sms * 8 + E - 1) / E;
+    const int64_t max_blocks = (per_expert / 8 + 255) / 256;
+    if (blocks > max_blocks) blocks = max_blocks;
     if (blocks < 1) blocks = 1;
     nvfp4_weight_amax_kernel<<<dim3((unsigned)blocks, (unsigned)E), 256, 0, stream>>>(
         w, per_expert, reinterpret_cast<uint32_t*>(s_w));
