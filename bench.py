@@ -107,6 +107,23 @@ class Timer:
         return {k: [a.elapsed_time(b) for a, b in v] for k, v in self.records.items()}
 
 
+def max_over_ranks(value_ms, world, device=None):
+    """Slowest rank's time (the whole job ends when the last replica ends); plain value at world 1."""
+    if world <= 1:
+        return float(value_ms)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value_ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(amount_per_step, steps, world, total_ms, scale):
+    """Whole-job throughput: every rank processes its own batch (weak scaling), so the units of all
+    ranks divided by the slowest rank's time; ``scale`` converts to the reported unit."""
+    return amount_per_step * steps * world / (total_ms * 1e-3) / scale
+
+
 class Kernel:
     """Accounting for one timed launch group: algorithmic bytes or flops per step and its roofline."""
 
@@ -506,17 +523,12 @@ def run_ours(args):
     launches = nvq.launch_count() - launches0
     clk = clocks.stop()
     step_ms = [a.elapsed_time(b) for a, b in step_ev]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), world, dev)
     ms_per_step = total_ms / args.steps
     if W.get("unit") == "GB/s":
-        amount = sum(k.amount for k in W["kernels"])
-        value = amount * args.steps * world / (total_ms * 1e-3) / 1e9
+        value = job_throughput(sum(k.amount for k in W["kernels"]), args.steps, world, total_ms, 1e9)
     else:
-        value = W["gemm_flops"] * args.steps * world / (total_ms * 1e-3) / 1e12
+        value = job_throughput(W["gemm_flops"], args.steps, world, total_ms, 1e12)
 
     # per-kernel roofline
     durs = timer.durations_ms()
@@ -573,13 +585,12 @@ def run_ours(args):
             e2e_step()
         b.record()
         barrier()
-        e2e_ms = a.elapsed_time(b)
-        if world > 1:
-            t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
-        scale_amt = (sum(k.amount for k in W["kernels"]) / 1e9) if W.get("unit") == "GB/s" else W["gemm_flops"] / 1e12
-        e2e = {"value": round(scale_amt * e2e_steps * world / (e2e_ms * 1e-3), 2),
+        e2e_ms = max_over_ranks(a.elapsed_time(b), world, dev)
+        if W.get("unit") == "GB/s":
+            e2e_val = job_throughput(sum(k.amount for k in W["kernels"]), e2e_steps, world, e2e_ms, 1e9)
+        else:
+            e2e_val = job_throughput(W["gemm_flops"], e2e_steps, world, e2e_ms, 1e12)
+        e2e = {"value": round(e2e_val, 2),
                "unit": W.get("unit", "TFLOPS"), "ms_per_step": round(e2e_ms / e2e_steps, 4), "steps": e2e_steps,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
