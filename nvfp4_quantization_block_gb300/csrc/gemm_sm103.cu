@@ -9,22 +9,31 @@
 //   GROUP_M: D[i, j] = s_a[i] s_b[e] sum_k deq(A)[i, k] deq(B[e])[j, k]   (rows i of group e)
 //   GROUP_K: D[e][i, j] = sum_{k in group e} deq(A)[i, k] deq(B)[j, k]
 //
-// Design (one CTA per SM, persistent, warp-specialised, 224 threads):
-//   warp 0 lane 0  TMA producer: 128x128-byte A tiles and 256x128-byte B tiles (128B swizzle)
-//                  plus the matching 512-byte scale tiles (bulk copies) into a ring of stages.
+// Design (persistent, warp-specialised, 224 threads per CTA). Two tilings share one kernel body:
+//   128-row tiles: one CTA per SM computes a 128 x 256 output tile (tcgen05 cta_group::1, M = 128).
+//   256-row tiles: a 2-CTA cluster (an SM pair) computes a 256 x 256 tile with cta_group::2 MMAs
+//                  (M = 256): each CTA stages its own 128 A rows and its own 128 of the 256 B rows,
+//                  so each SM takes in a third less operand data per flop; the even CTA issues the
+//                  MMAs and each CTA's TMEM holds its own 128 accumulator rows.
+// Roles:
+//   warp 0 lane 0  TMA producer: 128x128-byte A tiles and (256 or 128)x128-byte B tiles (128B
+//                  swizzle) plus the matching 512-byte scale tiles (bulk copies) into a ring of stages.
 //   warp 6         A-scale transposer: a GROUP_M tile starts at its group's row offset (a multiple
 //                  of 32), so its 128 rows of A scales straddle two 128-row scale tiles; the warp
 //                  rebuilds the tile's own 512-byte scale tile in shared memory (one funnel shift
-//                  per 16-byte line) and hands the stage to the MMA warp.
-//   warp 1 lane 0  MMA issuer: copies each stage's scale tiles smem -> TMEM (tcgen05.cp
-//                  32x128b.warpx4) and issues four tcgen05.mma block_scale instructions
-//                  (M=128, N=256; K=32 for MXFP8 E4M3 x UE8M0/32, K=64 for NVFP4 E2M1 x UE4M3/16),
+//                  per 16-byte line) and hands the stage on.
+//   warp 1 lane 0  MMA issuer (the even CTA of a pair): copies each stage's scale tiles smem -> TMEM
+//                  (tcgen05.cp 32x128b.warpx4) and issues four tcgen05.mma block_scale instructions
+//                  (N = 256; K = 32 for MXFP8 E4M3 x UE8M0/32, K = 64 for NVFP4 E2M1 x UE4M3/16),
 //                  accumulating in TMEM (fp32, 256 columns). Commits free smem stages and signal
-//                  the epilogue. Warp 1 also allocates and frees TMEM.
-//   warps 2-5      epilogue: tcgen05.ld 32 columns at a time, multiply by s_a[row] s_b[e], round
-//                  to bf16 into registers (the whole 256-column row of each thread), hand TMEM
-//                  back to the MMA warp, then store with 256-bit stores while the next tile's
-//                  MMAs run (fp32 output: stored chunk by chunk).
+//                  the epilogue (multicast to both CTAs of a pair). In the odd CTA of a pair this
+//                  lane forwards each completed stage to the even CTA's stage barrier instead.
+//                  Warp 1 also allocates and frees TMEM.
+//   warps 2-5      epilogue: tcgen05.ld 32 columns at a time (the next load in flight while the
+//                  current chunk converts), multiply by s_a[row] s_b[e], round to bf16 into
+//                  registers (the whole 256-column row of each thread), hand TMEM back to the MMA
+//                  warp, then store with 256-bit stores while the next tile's MMAs run (fp32
+//                  output: stored chunk by chunk).
 // GROUP_K tiles iterate the group's reduction range in 32-element MMA steps (k-steps outside the
 // group inside a 128-element stage are skipped).
 //
@@ -44,21 +53,23 @@
 namespace nvq {
 
 constexpr int GEMM_THREADS = 224;
-constexpr int BM = 128, BN = 256, BKB = 128;       // tile rows, tile columns, K bytes per stage
+constexpr int BM = 128, BN = 256, BKB = 128;       // rows per CTA, tile columns, K bytes per stage
 constexpr int MAX_GROUPS = 1024;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;    // 2 s: far beyond any legitimate wait
 
-template <bool FP4>
+template <bool FP4, bool PAIR>
 struct GemmCfg {
-    static constexpr int STAGES = FP4 ? 3 : 4;
+    static constexpr int STAGES = PAIR ? (FP4 ? 5 : 6) : (FP4 ? 3 : 4);
     static constexpr int KGS = FP4 ? 4 : 1;            // 4-scale-column groups per stage
     static constexpr int EPS = FP4 ? 256 : 128;        // reduction elements per stage
     static constexpr int MMA_K = FP4 ? 64 : 32;        // reduction elements per MMA
+    static constexpr int TILE_M = PAIR ? 2 * BM : BM;  // output rows of a scheduled tile
+    static constexpr int B_ROWS = PAIR ? BN / 2 : BN;  // B rows this CTA stages
     static constexpr int A_BYTES = BM * BKB;
-    static constexpr int B_BYTES = BN * BKB;
-    static constexpr int SFA_BYTES = KGS * 512;        // the tile's own 128 row scales
-    static constexpr int SFB_BYTES = 2 * KGS * 512;    // two 128-row scale tiles (N = 256)
+    static constexpr int B_BYTES = B_ROWS * BKB;
+    static constexpr int SFA_BYTES = KGS * 512;        // the CTA's own 128 row scales
+    static constexpr int SFB_BYTES = 2 * KGS * 512;    // two 128-row scale tiles (all N = 256 columns)
     static constexpr int SFA_RAW_BYTES = 2 * KGS * 512;  // the two row tiles a 32-aligned tile spans
     static constexpr int STAGE_BYTES =
         (A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES + SFA_RAW_BYTES + 1023) / 1024 * 1024;
@@ -68,7 +79,8 @@ struct GemmCfg {
         (FP4 ? ((1u << 7) | (1u << 10)) : 0u)         // A, B format: E2M1 (mxf4nvf4) or E4M3
         | ((uint32_t)(BN >> 3) << 17)                  // N >> 3
         | (FP4 ? 0u : (1u << 23))                      // scale type: UE4M3 (0) / UE8M0 (1)
-        | ((uint32_t)(BM >> 7) << 27);                 // M >> 7
+        | ((uint32_t)(TILE_M >> 4) << 24);             // M >> 4
+    static constexpr uint32_t EPI_ARRIVALS = PAIR ? 8u : 4u;   // tmem_empty: one per epilogue warp
     static constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + 256 + 8 * (MAX_GROUPS + 1);
 };
 
@@ -98,6 +110,23 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// shared::cluster address of the variable at local shared address `saddr` in cluster CTA `rank`
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
 }
@@ -111,15 +140,31 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// arrive on a barrier given by its shared::cluster address (this CTA's or the peer's)
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t caddr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
+}
+
+template <bool CLUSTER>
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
+    if constexpr (CLUSTER) {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(smem_u32(bar)), "r"(parity)
+            : "memory");
+    } else {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(smem_u32(bar)), "r"(parity)
+            : "memory");
+    }
     return ok != 0;
 }
 
@@ -131,12 +176,13 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 
 // Bounded wait; returns false (and raises the abort flag / status) when WAIT_LIMIT_NS of wall-clock
 // time pass without the phase completing, or when another role has already aborted.
+template <bool CLUSTER>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                           int32_t* status) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait<CLUSTER>(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait<CLUSTER>(bar, parity)) return true;
         if ((it & 255u) == 0u) {
             if (*abort_flag) return false;
             if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) break;
@@ -148,9 +194,10 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
 }
 
 // Bounded drain used at teardown: wait for a phase without raising anything.
+template <bool CLUSTER>
 __device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
     const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(bar, parity))
+    while (!mbar_try_wait<CLUSTER>(bar, parity))
         if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) return;
 }
 
@@ -172,9 +219,41 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-__device__ __forceinline__ void tc_commit(uint64_t* bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
-                 ::"r"(smem_u32(bar)) : "memory");
+// All tcgen05 instructions of one kernel use the same CTA group: ::1 for 128-row tiles, ::2 for
+// 256-row tiles on an SM pair. A pair's commits arrive on the barrier at the same shared address
+// in every CTA of `mask`.
+template <bool PAIR>
+__device__ __forceinline__ void tc_commit(uint64_t* bar, uint16_t mask) {
+    if constexpr (PAIR) {
+        asm volatile(
+            "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+            ::"r"(smem_u32(bar)), "h"(mask) : "memory");
+    } else {
+        (void)mask;
+        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                     ::"r"(smem_u32(bar)) : "memory");
+    }
+}
+
+template <bool PAIR>
+__device__ __forceinline__ void tmem_alloc(uint32_t* holder) {
+    if constexpr (PAIR) {
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(smem_u32(holder)), "r"(TMEM_COLS) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    } else {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(smem_u32(holder)), "r"(TMEM_COLS) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+}
+
+template <bool PAIR>
+__device__ __forceinline__ void tmem_dealloc(uint32_t base) {
+    if constexpr (PAIR)
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(base), "r"(TMEM_COLS) : "memory");
+    else
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(base), "r"(TMEM_COLS) : "memory");
 }
 
 // Shared-memory matrix descriptor (tcgen05): start >> 4, LBO >> 4, SBO >> 4, version 1, swizzle.
@@ -183,29 +262,32 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
            (1ull << 46) | ((uint64_t)swizzle << 61);
 }
 
-template <bool FP4>
+template <bool FP4, bool PAIR>
 __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                        uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
-    if constexpr (FP4) {
-        asm volatile(
-            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
-            "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
-            ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
-            : "memory");
-    } else {
-        asm volatile(
-            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
-            "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
-            ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
-            : "memory");
-    }
+#define NVQ_MMA(GROUP, KIND)                                                                                  \
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"                                            \
+                 "tcgen05.mma.cta_group::" GROUP ".kind::" KIND " [%0], %1, %2, %3, [%4], [%5], p;\n\t}"      \
+                 ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem),             \
+                 "r"(accumulate)                                                                              \
+                 : "memory")
+    if constexpr (FP4 && PAIR) NVQ_MMA("2", "mxf4nvf4.block_scale.scale_vec::4X");
+    else if constexpr (FP4) NVQ_MMA("1", "mxf4nvf4.block_scale.scale_vec::4X");
+    else if constexpr (PAIR) NVQ_MMA("2", "mxf8f6f4.block_scale.scale_vec::1X");
+    else NVQ_MMA("1", "mxf8f6f4.block_scale.scale_vec::1X");
+#undef NVQ_MMA
 }
 
+template <bool PAIR>
 __device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
-    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+    if constexpr (PAIR)
+        asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+    else
+        asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+// Start a 32-lane x 32-column TMEM load into r; the registers are valid after tmem_wait_ld(r).
+__device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
         "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
@@ -215,7 +297,19 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
           "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
           "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Wait for every outstanding TMEM load of this thread; r is threaded through so that no use of the
+// loaded registers can be scheduled before the wait.
+__device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                   "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                   "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
+                   "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+                 :
+                 : "memory");
 }
 
 // 32 bytes to a 32-byte aligned global address in one 256-bit store.
@@ -226,8 +320,14 @@ __device__ __forceinline__ void st_v8(void* p, uint32_t a, uint32_t b, uint32_t 
                  : "memory");
 }
 
+__device__ __forceinline__ void pack_scaled(const uint32_t (&r)[32], float scale, uint32_t (&pk)[16]) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+        pk[j] = cvt_bf16x2(__uint_as_float(r[2 * j]) * scale, __uint_as_float(r[2 * j + 1]) * scale);
+}
+
 // ------------------------------------------------------------------------------------------------
-// Tile schedule (identical in every role)
+// Tile schedule (identical in every role and in both CTAs of a pair)
 // ------------------------------------------------------------------------------------------------
 struct Tile {
     int e;
@@ -243,6 +343,7 @@ struct Schedule {
     const int32_t* off;        // group offsets (smem, int32)
     const int32_t* tile_start; // GROUP_M: prefix of tiles per group (smem)
     int mode, groups;
+    int tile_m;                // rows per scheduled tile (128, or 256 for an SM pair)
     int64_t m, n, k;
     int n_tiles, m_tiles;      // GROUP_K: per-group tile grid
     int64_t total;
@@ -259,7 +360,7 @@ struct Schedule {
             const int64_t local = t - tile_start[e];
             const int64_t mt = local / n_tiles, nt = local - mt * n_tiles;
             tl.e = e;
-            tl.a_row0 = off[e] + mt * BM;
+            tl.a_row0 = off[e] + mt * tile_m;
             tl.row_end = min((int64_t)off[e + 1], m);
             tl.n0 = nt * BN;
             tl.b_row0 = (int64_t)e * n + tl.n0;
@@ -272,7 +373,7 @@ struct Schedule {
             const int64_t local = t - (int64_t)e * per;
             const int64_t mt = local / n_tiles, nt = local - mt * n_tiles;
             tl.e = e;
-            tl.a_row0 = mt * BM;
+            tl.a_row0 = mt * tile_m;
             tl.row_end = m;
             tl.n0 = nt * BN;
             tl.b_row0 = tl.n0;
@@ -287,11 +388,11 @@ struct Schedule {
 // ------------------------------------------------------------------------------------------------
 // Kernel
 // ------------------------------------------------------------------------------------------------
-template <bool FP4>
+template <bool FP4, bool PAIR>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
 block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                          const GemmParams p) {
-    using C = GemmCfg<FP4>;
+    using C = GemmCfg<FP4, PAIR>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* stage_base = smem;
@@ -310,6 +411,12 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = p.groups;
     const int n_tiles = (int)((p.n + BN - 1) / BN);
+    // a pair's even CTA (rank 0) issues the MMAs; the odd one holds rows [128, 256) of each tile
+    const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+    const bool leader = rank == 0u;
+    const int64_t tile_first = PAIR ? (int64_t)(blockIdx.x >> 1) : (int64_t)blockIdx.x;
+    const int64_t tile_step = PAIR ? (int64_t)(gridDim.x >> 1) : (int64_t)gridDim.x;
+    const int64_t row_in_pair = (int64_t)rank * BM;
 
     // ---- validate offsets and build the schedule (all threads see the same smem) ----
     if (threadIdx.x == 0) {
@@ -326,7 +433,7 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
         off32[e] = (int32_t)o;
     }
     __syncthreads();
-    if (*bad_flag) {
+    if (*bad_flag) {    // both CTAs of a pair read the same offsets and leave here together
         if (threadIdx.x == 0 && blockIdx.x == 0 && p.status) atomicExch(p.status, NVQ_DEV_BAD_OFFSETS);
         return;
     }
@@ -336,17 +443,18 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
     sched.tile_start = tile_start;
     sched.mode = p.mode;
     sched.groups = G;
+    sched.tile_m = C::TILE_M;
     sched.m = p.m;
     sched.n = p.n;
     sched.k = p.k;
     sched.n_tiles = n_tiles;
-    sched.m_tiles = (int)((p.m + BM - 1) / BM);
+    sched.m_tiles = (int)((p.m + C::TILE_M - 1) / C::TILE_M);
     if (p.mode == NVQ_GEMM_GROUP_M) {
         if (threadIdx.x == 0) {
             int32_t acc = 0;
             for (int e = 0; e < G; ++e) {
                 tile_start[e] = acc;
-                acc += (int32_t)(((off32[e + 1] - off32[e]) + BM - 1) / BM) * n_tiles;
+                acc += (int32_t)(((off32[e + 1] - off32[e]) + C::TILE_M - 1) / C::TILE_M) * n_tiles;
             }
             tile_start[G] = acc;
         }
@@ -360,29 +468,26 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
     // ---- barriers and TMEM ----
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
-            mbar_init(&full_bar[s], 2);       // producer (A, B, B scales) + scale transposer
+            // producer (A, B, scales) + its second arrival or the scale transposer's; the even CTA
+            // of a pair also waits for the odd CTA's forwarded stage
+            mbar_init(&full_bar[s], (PAIR && leader) ? 3u : 2u);
             mbar_init(&empty_bar[s], 1);
             mbar_init(&sfa_bar[s], 1);
         }
         mbar_init(tmem_full, 1);
-        mbar_init(tmem_empty, 128);
+        mbar_init(tmem_empty, C::EPI_ARRIVALS);
         mbar_init(mma_done, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
-                     ::"r"(smem_u32(tmem_holder)), "r"(TMEM_COLS) : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    }
+    if (warp == 1) tmem_alloc<PAIR>(tmem_holder);
     tc_fence_before();
-    __syncthreads();
+    if constexpr (PAIR) cluster_sync(); else __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
     const uint32_t tmem_acc = tmem_base;
     const uint32_t tmem_sfa = tmem_base + BN;
     const uint32_t tmem_sfb = tmem_base + BN + C::SFA_COLS;
-
-    const int64_t k_stages_total = (p.k + C::EPS - 1) / C::EPS;   // stages over the whole K extent
+    constexpr uint16_t PAIR_MASK = 3;
 
     if (warp == 0 && lane == 0) {
         // =========================== TMA producer ===========================
@@ -392,17 +497,21 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
         uint32_t sfa_fills[C::STAGES];          // shifted-tile fills of each slot's sfa_bar
         for (int i = 0; i < C::STAGES; ++i) sfa_fills[i] = 0;
         bool ok = true;
-        for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        for (int64_t t = tile_first; t < total && ok; t += tile_step) {
             const Tile tl = sched.get(t);
             if (tl.k_end <= tl.k_begin) continue;
             const int64_t ks0 = tl.k_begin / C::EPS, ks1 = (tl.k_end + C::EPS - 1) / C::EPS;
-            const int64_t rb_a = tl.a_row0 / BM;
-            const bool shifted = (tl.a_row0 % BM) != 0;
+            const int64_t a_row0 = tl.a_row0 + row_in_pair;
+            const int64_t rb_a = a_row0 / BM;
+            // the odd CTA's rows of a pair tile can lie wholly past the buffer: TMA fills zeros,
+            // the scale copies (no bounds check of their own) are skipped
+            const bool a_in = rb_a < p.a_rowtiles;
+            const bool shifted = (a_row0 % BM) != 0;
             const bool need_a2 = shifted && rb_a + 1 < p.a_rowtiles;
             const int64_t rb_b = tl.b_row0 / BM;
             const bool need_b2 = rb_b + 1 < p.b_rowtiles;
             for (int64_t ks = ks0; ks < ks1; ++ks) {
-                if (!mbar_wait(&empty_bar[slot], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+                if (!mbar_wait<PAIR>(&empty_bar[slot], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
                 uint8_t* st = stage_base + (size_t)slot * C::STAGE_BYTES;
                 uint8_t* sa = st;
                 uint8_t* sb = st + C::A_BYTES;
@@ -415,21 +524,24 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
                 // (A, B, B scales, and the A scales of an aligned tile) plus either the producer's
                 // second arrival (aligned tile) or the transposer's (tile starting inside a scale tile)
                 const uint32_t tx = C::A_BYTES + C::B_BYTES + sf_bytes * (1u + (need_b2 ? 1u : 0u)) +
-                                    (shifted ? 0u : sf_bytes);
+                                    ((shifted || !a_in) ? 0u : sf_bytes);
                 mbar_arrive_expect_tx(&full_bar[slot], tx);
                 if (shifted) {
-                    mbar_arrive_expect_tx(&sfa_bar[slot], sf_bytes * (1u + (need_a2 ? 1u : 0u)));
+                    const uint32_t raw = a_in ? sf_bytes * (1u + (need_a2 ? 1u : 0u)) : 0u;
+                    mbar_arrive_expect_tx(&sfa_bar[slot], raw);
                     ++sfa_fills[slot];
-                    bulk_load(ssfa_raw, p.sfa + ((rb_a * p.sf_tiles_per_row + kg0) << 9), sf_bytes, &sfa_bar[slot]);
+                    if (a_in)
+                        bulk_load(ssfa_raw, p.sfa + ((rb_a * p.sf_tiles_per_row + kg0) << 9), sf_bytes, &sfa_bar[slot]);
                     if (need_a2)
                         bulk_load(ssfa_raw + C::KGS * 512, p.sfa + (((rb_a + 1) * p.sf_tiles_per_row + kg0) << 9),
                                   sf_bytes, &sfa_bar[slot]);
-                } else {
+                } else if (a_in) {
                     bulk_load(ssfb - C::SFA_BYTES, p.sfa + ((rb_a * p.sf_tiles_per_row + kg0) << 9), sf_bytes,
                               &full_bar[slot]);
                 }
-                tma_load_2d(sa, &tmap_a, (int32_t)(ks * BKB), (int32_t)tl.a_row0, &full_bar[slot]);
-                tma_load_2d(sb, &tmap_b, (int32_t)(ks * BKB), (int32_t)tl.b_row0, &full_bar[slot]);
+                tma_load_2d(sa, &tmap_a, (int32_t)(ks * BKB), (int32_t)a_row0, &full_bar[slot]);
+                tma_load_2d(sb, &tmap_b, (int32_t)(ks * BKB), (int32_t)(tl.b_row0 + (PAIR ? row_in_pair : 0)),
+                            &full_bar[slot]);
                 bulk_load(ssfb, p.sfb + ((rb_b * p.sf_tiles_per_row + kg0) << 9), sf_bytes, &full_bar[slot]);
                 if (need_b2)
                     bulk_load(ssfb + C::KGS * 512, p.sfb + (((rb_b + 1) * p.sf_tiles_per_row + kg0) << 9), sf_bytes,
@@ -445,10 +557,27 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
             int s2 = slot - 1 - (int)i;
             uint32_t ph = phase;
             if (s2 < 0) { s2 += C::STAGES; ph ^= 1u; }
-            mbar_drain(&full_bar[s2], ph);
+            mbar_drain<PAIR>(&full_bar[s2], ph);
         }
         for (int s2 = 0; s2 < C::STAGES; ++s2)
-            if (sfa_fills[s2]) mbar_drain(&sfa_bar[s2], (sfa_fills[s2] - 1u) & 1u);
+            if (sfa_fills[s2]) mbar_drain<PAIR>(&sfa_bar[s2], (sfa_fills[s2] - 1u) & 1u);
+    } else if (warp == 1 && lane == 0 && !leader) {
+        // ===================== stage forwarder (odd CTA of a pair) =====================
+        // Each stage of this CTA's ring that is complete (its copies landed and its A scales are in
+        // place) is announced on the even CTA's barrier of the same slot.
+        int slot = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int64_t t = tile_first; t < total && ok; t += tile_step) {
+            const Tile tl = sched.get(t);
+            if (tl.k_end <= tl.k_begin) continue;
+            const int64_t ks0 = tl.k_begin / C::EPS, ks1 = (tl.k_end + C::EPS - 1) / C::EPS;
+            for (int64_t ks = ks0; ks < ks1; ++ks) {
+                if (!mbar_wait<PAIR>(&full_bar[slot], phase, abort_flag, p.status)) { ok = false; break; }
+                mbar_arrive_cluster(mapa_shared(smem_u32(&full_bar[slot]), 0));
+                if (++slot == C::STAGES) { slot = 0; phase ^= 1u; }
+            }
+        }
     } else if (warp == 1 && lane == 0) {
         // =========================== MMA issuer ===========================
         int slot = 0;
@@ -456,27 +585,28 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
         uint32_t acc_phase = 0;
         bool ok = true;
         const uint32_t stage0 = smem_u32(stage_base);
-        for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        for (int64_t t = tile_first; t < total && ok; t += tile_step) {
             const Tile tl = sched.get(t);
             if (tl.k_end <= tl.k_begin) continue;
-            if (!mbar_wait(tmem_empty, acc_phase ^ 1u, abort_flag, p.status)) break;
+            if (!mbar_wait<PAIR>(tmem_empty, acc_phase ^ 1u, abort_flag, p.status)) break;
             tc_fence_after();
             const int64_t ks0 = tl.k_begin / C::EPS, ks1 = (tl.k_end + C::EPS - 1) / C::EPS;
             uint32_t accumulate = 0;
             for (int64_t ks = ks0; ks < ks1; ++ks) {
-                if (!mbar_wait(&full_bar[slot], phase, abort_flag, p.status)) { ok = false; break; }
+                if (!mbar_wait<PAIR>(&full_bar[slot], phase, abort_flag, p.status)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t sa = stage0 + (uint32_t)slot * C::STAGE_BYTES;
                 const uint32_t sb = sa + C::A_BYTES;
                 const uint32_t ssfa = sb + C::B_BYTES;
                 const uint32_t ssfb = ssfa + C::SFA_BYTES;
-                // scales -> TMEM: A's k-group j at columns [4j, 4j+4); B's at [8j, 8j+8) (two 128-row tiles)
+                // scales -> TMEM: A's k-group j at columns [4j, 4j+4); B's at [8j, 8j+8) (two 128-row
+                // tiles). For a pair each CTA's copy reads its own shared memory into its own TMEM.
 #pragma unroll
                 for (int j = 0; j < C::KGS; ++j) {
-                    tc_cp_sf(tmem_sfa + 4 * j, smem_desc(ssfa + j * 512, 0, 128, 0));
+                    tc_cp_sf<PAIR>(tmem_sfa + 4 * j, smem_desc(ssfa + j * 512, 0, 128, 0));
 #pragma unroll
                     for (int h = 0; h < 2; ++h)
-                        tc_cp_sf(tmem_sfb + 8 * j + 4 * h, smem_desc(ssfb + (h * C::KGS + j) * 512, 0, 128, 0));
+                        tc_cp_sf<PAIR>(tmem_sfb + 8 * j + 4 * h, smem_desc(ssfb + (h * C::KGS + j) * 512, 0, 128, 0));
                 }
                 const uint64_t adesc0 = smem_desc(sa, 16, 1024, 2);
                 const uint64_t bdesc0 = smem_desc(sb, 16, 1024, 2);
@@ -488,20 +618,20 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
                     const uint32_t sf_id = FP4 ? 0u : (uint32_t)j;
                     const uint32_t idesc = C::IDESC | (sf_id << 4) | (sf_id << 29);
                     // K advance inside the 128-byte swizzled row: 32 bytes per MMA (encoded >> 4)
-                    tc_mma<FP4>(tmem_acc, adesc0 + (uint64_t)(2 * j), bdesc0 + (uint64_t)(2 * j), idesc,
-                                tmem_sfa + 4 * kg, tmem_sfb + 8 * kg, accumulate);
+                    tc_mma<FP4, PAIR>(tmem_acc, adesc0 + (uint64_t)(2 * j), bdesc0 + (uint64_t)(2 * j), idesc,
+                                      tmem_sfa + 4 * kg, tmem_sfb + 8 * kg, accumulate);
                     accumulate = 1;
                 }
-                tc_commit(&empty_bar[slot]);
+                tc_commit<PAIR>(&empty_bar[slot], PAIR_MASK);
                 if (++slot == C::STAGES) { slot = 0; phase ^= 1u; }
             }
             if (!ok) break;
-            tc_commit(tmem_full);
+            tc_commit<PAIR>(tmem_full, PAIR_MASK);
             acc_phase ^= 1u;
         }
         // wait (bounded) for every tcgen05 operation issued above before TMEM is released
-        tc_commit(mma_done);
-        mbar_drain(mma_done, 0);
+        tc_commit<PAIR>(mma_done, 1);
+        mbar_drain<PAIR>(mma_done, 0);
     } else if (warp == 6) {
         // ======================= A-scale transposer =======================
         // A tile starting 32*g0 rows into a 128-row scale tile needs rows [32 g0, 128) of that tile
@@ -512,11 +642,11 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
         uint32_t sfa_phase = 0;                 // bit s: parity of the next sfa_bar[s] phase
         bool ok = true;
         const uint32_t stage0 = smem_u32(stage_base);
-        for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        for (int64_t t = tile_first; t < total && ok; t += tile_step) {
             const Tile tl = sched.get(t);
             if (tl.k_end <= tl.k_begin) continue;
             const int64_t ks0 = tl.k_begin / C::EPS, ks1 = (tl.k_end + C::EPS - 1) / C::EPS;
-            const int g0 = (int)((tl.a_row0 % BM) / 32);
+            const int g0 = (int)(((tl.a_row0 + row_in_pair) % BM) / 32);
             if (g0 == 0) {
                 // aligned tile: the producer loaded the scales in place; only keep the ring position
                 slot = (int)((slot + (ks1 - ks0)) % C::STAGES);
@@ -525,7 +655,7 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
             for (int64_t ks = ks0; ks < ks1; ++ks) {
                 int good = 1;
                 if (lane == 0)
-                    good = mbar_wait(&sfa_bar[slot], (sfa_phase >> slot) & 1u, abort_flag, p.status) ? 1 : 0;
+                    good = mbar_wait<PAIR>(&sfa_bar[slot], (sfa_phase >> slot) & 1u, abort_flag, p.status) ? 1 : 0;
                 good = __shfl_sync(0xffffffffu, good, 0);
                 if (!good) { ok = false; break; }
                 const uint32_t st = stage0 + (uint32_t)slot * C::STAGE_BYTES;
@@ -556,22 +686,26 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
                 if (++slot == C::STAGES) slot = 0;
             }
         }
-    } else if (warp >= 2) {
+    } else if (warp >= 2 && warp < 6) {
         // =========================== epilogue ===========================
         const int q = warp & 3;                       // TMEM lane quarter this warp may access
         const int row_in_tile = q * 32 + lane;
+        const uint32_t tbase = tmem_acc + ((uint32_t)(q * 32) << 16);
+        // the MMA issuer's tmem_empty barrier (in the even CTA of a pair)
+        const uint32_t empty_addr = PAIR ? mapa_shared(smem_u32(tmem_empty), 0) : 0u;
         uint32_t acc_phase = 0;
-        for (int64_t t = blockIdx.x; t < total; t += gridDim.x) {
+        for (int64_t t = tile_first; t < total; t += tile_step) {
             const Tile tl = sched.get(t);
-            const int64_t row = tl.a_row0 + row_in_tile;
+            const int64_t a_row0 = tl.a_row0 + row_in_pair;
+            const int64_t row = a_row0 + row_in_tile;
             const bool row_ok = row < tl.row_end;
-            const int64_t drow = tl.d_row0 + row_in_tile;
+            const int64_t drow = tl.d_row0 + row_in_pair + row_in_tile;
             float scale = 1.0f;
             if (row_ok && p.s_a) scale = p.s_a[row];
             if (p.s_b) scale *= p.s_b[tl.e];
             const bool empty = tl.k_end <= tl.k_begin;
             if (!empty) {
-                if (!mbar_wait(tmem_full, acc_phase, abort_flag, p.status)) break;
+                if (!mbar_wait<PAIR>(tmem_full, acc_phase, abort_flag, p.status)) break;
                 tc_fence_after();
             }
             if (p.out_f32) {
@@ -580,7 +714,8 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
                     const int64_t col = tl.n0 + c * 32;
                     uint32_t r[32];
                     if (!empty) {
-                        tmem_ld32(tmem_acc + ((uint32_t)(q * 32) << 16) + (uint32_t)(c * 32), r);
+                        tmem_ld32_async(tbase + (uint32_t)(c * 32), r);
+                        tmem_wait_ld(r);
                     } else {
 #pragma unroll
                         for (int j = 0; j < 32; ++j) r[j] = 0u;
@@ -594,62 +729,76 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
                         reinterpret_cast<float4*>(dst)[j] = v;
                     }
                 }
+            } else {
+                // bf16 output: drain the whole accumulator row into registers as packed bf16 (the
+                // next 32-column load in flight while the current one converts) and hand TMEM back
+                // to the MMA warp before storing, so the stores overlap the next tile's MMAs
+                uint32_t pk[BN / 32][16];
+                if (!empty) {
+                    uint32_t ra[32], rb[32];
+                    tmem_ld32_async(tbase, ra);
+                    tmem_wait_ld(ra);
+#pragma unroll
+                    for (int c = 0; c < BN / 32; c += 2) {
+                        tmem_ld32_async(tbase + (uint32_t)((c + 1) * 32), rb);
+                        pack_scaled(ra, scale, pk[c]);
+                        tmem_wait_ld(rb);
+                        if (c + 2 < BN / 32) tmem_ld32_async(tbase + (uint32_t)((c + 2) * 32), ra);
+                        pack_scaled(rb, scale, pk[c + 1]);
+                        if (c + 2 < BN / 32) tmem_wait_ld(ra);
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < BN / 32; ++c)
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) pk[c][j] = 0u;
+                }
                 if (!empty) {
                     tc_fence_before();
-                    mbar_arrive(tmem_empty);
+                    __syncwarp();
+                    if (lane == 0) {
+                        if constexpr (PAIR) mbar_arrive_cluster(empty_addr); else mbar_arrive(tmem_empty);
+                    }
                     acc_phase ^= 1u;
+                }
+                if (row_ok) {
+                    uint16_t* dst = reinterpret_cast<uint16_t*>(p.d) + drow * p.ldd + tl.n0;
+#pragma unroll
+                    for (int c = 0; c < BN / 32; ++c) {
+                        if (tl.n0 + c * 32 >= p.n) break;
+                        if (p.d_aligned32) {
+#pragma unroll
+                            for (int h = 0; h < 2; ++h)
+                                st_v8(dst + c * 32 + h * 16, pk[c][8 * h], pk[c][8 * h + 1], pk[c][8 * h + 2],
+                                      pk[c][8 * h + 3], pk[c][8 * h + 4], pk[c][8 * h + 5], pk[c][8 * h + 6],
+                                      pk[c][8 * h + 7]);
+                        } else {
+#pragma unroll
+                            for (int h = 0; h < 4; ++h)
+                                reinterpret_cast<uint4*>(dst + c * 32)[h] =
+                                    make_uint4(pk[c][4 * h], pk[c][4 * h + 1], pk[c][4 * h + 2], pk[c][4 * h + 3]);
+                        }
+                    }
                 }
                 continue;
             }
-            // bf16 output: drain the whole accumulator row into registers as packed bf16 and hand
-            // TMEM back to the MMA warp before storing, so the stores overlap the next tile's MMAs
-            uint32_t pk[BN / 32][16];
-#pragma unroll
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t r[32];
-                if (!empty) {
-                    tmem_ld32(tmem_acc + ((uint32_t)(q * 32) << 16) + (uint32_t)(c * 32), r);
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) r[j] = 0u;
-                }
-#pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    pk[c][j] = cvt_bf16x2(__uint_as_float(r[2 * j]) * scale, __uint_as_float(r[2 * j + 1]) * scale);
-            }
             if (!empty) {
                 tc_fence_before();
-                mbar_arrive(tmem_empty);
-                acc_phase ^= 1u;
-            }
-            if (row_ok) {
-                uint16_t* dst = reinterpret_cast<uint16_t*>(p.d) + drow * p.ldd + tl.n0;
-#pragma unroll
-                for (int c = 0; c < BN / 32; ++c) {
-                    if (tl.n0 + c * 32 >= p.n) break;
-                    if (p.d_aligned32) {
-#pragma unroll
-                        for (int h = 0; h < 2; ++h)
-                            st_v8(dst + c * 32 + h * 16, pk[c][8 * h], pk[c][8 * h + 1], pk[c][8 * h + 2], pk[c][8 * h + 3],
-                                  pk[c][8 * h + 4], pk[c][8 * h + 5], pk[c][8 * h + 6], pk[c][8 * h + 7]);
-                    } else {
-#pragma unroll
-                        for (int h = 0; h < 4; ++h)
-                            reinterpret_cast<uint4*>(dst + c * 32)[h] =
-                                make_uint4(pk[c][4 * h], pk[c][4 * h + 1], pk[c][4 * h + 2], pk[c][4 * h + 3]);
-                    }
+                __syncwarp();
+                if (lane == 0) {
+                    if constexpr (PAIR) mbar_arrive_cluster(empty_addr); else mbar_arrive(tmem_empty);
                 }
+                acc_phase ^= 1u;
             }
         }
     }
 
+    // teardown: every role of both CTAs is done (and the MMA issuer has drained its tcgen05 work)
+    // before the pair frees its TMEM and its shared memory goes away
     tc_fence_before();
-    __syncthreads();
+    if constexpr (PAIR) cluster_sync(); else __syncthreads();
     tc_fence_after();
-    if (warp == 1) {
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
-                     : "memory");
-    }
+    if (warp == 1) tmem_dealloc<PAIR>(tmem_base);
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -694,14 +843,14 @@ static int num_sms() {
     return n;
 }
 
-template <bool FP4>
+template <bool FP4, bool PAIR>
 static nvq_status launch_gemm(const nvq_gemm_args* a, cudaStream_t stream) {
-    using C = GemmCfg<FP4>;
+    using C = GemmCfg<FP4, PAIR>;
     const int64_t row_bytes = FP4 ? a->k / 2 : a->k;
     const int64_t rows_a = a->m;
     const int64_t rows_b = (a->mode == NVQ_GEMM_GROUP_M) ? a->groups * a->n : a->n;
     CUtensorMap ta, tb;
-    if (!make_tmap(&ta, a->a, rows_a, row_bytes, BM) || !make_tmap(&tb, a->b, rows_b, row_bytes, BN))
+    if (!make_tmap(&ta, a->a, rows_a, row_bytes, BM) || !make_tmap(&tb, a->b, rows_b, row_bytes, C::B_ROWS))
         return NVQ_ERR_CUDA;
     GemmParams p;
     p.mode = a->mode;
@@ -724,16 +873,58 @@ static nvq_status launch_gemm(const nvq_gemm_args* a, cudaStream_t stream) {
     const int64_t kb = a->k / (FP4 ? 16 : 32);
     p.sf_tiles_per_row = (kb + 3) / 4;
 
-    static bool attr_set[2] = {false, false};
-    if (!attr_set[FP4]) {
-        if (cudaFuncSetAttribute(block_scaled_gemm_kernel<FP4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    // one-time setup per kernel instance: shared-memory opt-in and the persistent grid (for pairs,
+    // as many 2-CTA clusters as the GPU can hold at once)
+    static int grid_cache = 0;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        if (cudaFuncSetAttribute(block_scaled_gemm_kernel<FP4, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)C::SMEM_BYTES) != cudaSuccess)
-            return NVQ_ERR_CUDA;
-        attr_set[FP4] = true;
-    }
-    const int grid = num_sms();
+            return;
+        const int sms = num_sms();
+        if (!PAIR) {
+            grid_cache = sms;
+            return;
+        }
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(2 * (sms / 2), 1, 1);
+        cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
+        cfg.dynamicSmemBytes = C::SMEM_BYTES;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, block_scaled_gemm_kernel<FP4, PAIR>, &cfg) != cudaSuccess ||
+            clusters <= 0) {
+            (void)cudaGetLastError();
+            return;
+        }
+        grid_cache = 2 * min(clusters, sms / 2);
+    });
+    const int grid = grid_cache;
     if (grid <= 0) return NVQ_ERR_CUDA;
-    block_scaled_gemm_kernel<FP4><<<grid, GEMM_THREADS, C::SMEM_BYTES, stream>>>(ta, tb, p);
+    if constexpr (PAIR) {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(grid, 1, 1);
+        cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
+        cfg.dynamicSmemBytes = C::SMEM_BYTES;
+        cfg.stream = stream;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, block_scaled_gemm_kernel<FP4, PAIR>, ta, tb, p) != cudaSuccess)
+            return NVQ_ERR_CUDA;
+    } else {
+        block_scaled_gemm_kernel<FP4, PAIR><<<grid, GEMM_THREADS, C::SMEM_BYTES, stream>>>(ta, tb, p);
+    }
     if (cudaGetLastError() != cudaSuccess) return NVQ_ERR_CUDA;
     count_launches(1);
     return NVQ_OK;
@@ -748,7 +939,8 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 extern "C" nvq_status block_scaled_grouped_gemm(const nvq_gemm_args* a, void* stream) {
     if (a == nullptr) return NVQ_ERR_INVALID_ARG;
     if ((a->fmt != NVQ_MXFP8 && a->fmt != NVQ_NVFP4) || (a->mode != NVQ_GEMM_GROUP_M && a->mode != NVQ_GEMM_GROUP_K) ||
-        (a->out_type != NVQ_OUT_BF16 && a->out_type != NVQ_OUT_F32))
+        (a->out_type != NVQ_OUT_BF16 && a->out_type != NVQ_OUT_F32) ||
+        (a->tiles != NVQ_TILES_AUTO && a->tiles != NVQ_TILES_128 && a->tiles != NVQ_TILES_256))
         return NVQ_ERR_INVALID_ARG;
     if (a->groups < 0 || a->m < 0 || a->n < 0 || a->k < 0) return NVQ_ERR_INVALID_ARG;
     if (a->groups == 0 || a->m == 0 || a->n == 0) return NVQ_OK;
@@ -768,5 +960,11 @@ extern "C" nvq_status block_scaled_grouped_gemm(const nvq_gemm_args* a, void* st
         (reinterpret_cast<uintptr_t>(a->offsets) & 7u))
         return NVQ_ERR_MISALIGNED;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    return a->fmt == NVQ_NVFP4 ? nvq::launch_gemm<true>(a, s) : nvq::launch_gemm<false>(a, s);
+    // Measured on GB300 (dense 8192x5120x2048 and the 128-expert MoE shapes), the 256-row pair
+    // tiles run slower than 128-row tiles: the pair's stage ring couples two SMs, and every stage
+    // then waits on the slower SM's copies plus a cross-SM hop. AUTO therefore takes 128-row tiles.
+    const bool pair = a->tiles == NVQ_TILES_256;
+    if (a->fmt == NVQ_NVFP4)
+        return pair ? nvq::launch_gemm<true, true>(a, s) : nvq::launch_gemm<true, false>(a, s);
+    return pair ? nvq::launch_gemm<false, true>(a, s) : nvq::launch_gemm<false, false>(a, s);
 }
