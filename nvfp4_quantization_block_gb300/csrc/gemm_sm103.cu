@@ -52,7 +52,9 @@
 
 namespace nvq {
 
-constexpr int GEMM_THREADS = 224;
+constexpr int GEMM_THREADS = 256;
+constexpr int SCALE_WARP = 7;                      // copies the scale tiles smem -> TMEM
+constexpr uint32_t SF_SETS = 2;                    // TMEM scale sets: copies of fill f+1 overlap MMAs of f
 constexpr int BM = 128, BN = 256, BKB = 128;       // rows per CTA, tile columns, K bytes per stage
 constexpr int MAX_GROUPS = 1024;
 constexpr uint32_t TMEM_COLS = 512;
@@ -402,7 +404,10 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
     uint64_t* tmem_full = sfa_bar + C::STAGES;
     uint64_t* tmem_empty = tmem_full + 1;
     uint64_t* mma_done = tmem_empty + 1;
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(mma_done + 1);
+    uint64_t* sf_ready = mma_done + 1;                 // [SF_SETS] scale set copied into TMEM
+    uint64_t* sf_free = sf_ready + SF_SETS;            // [SF_SETS] MMAs reading the set are done
+    uint64_t* cp_done = sf_free + SF_SETS;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(cp_done + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
     int* bad_flag = reinterpret_cast<int*>(tmem_holder + 2);
     int32_t* off32 = reinterpret_cast<int32_t*>(smem + C::STAGES * C::STAGE_BYTES + 256);
@@ -477,6 +482,11 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
         mbar_init(tmem_full, 1);
         mbar_init(tmem_empty, C::EPI_ARRIVALS);
         mbar_init(mma_done, 1);
+        for (uint32_t k = 0; k < SF_SETS; ++k) {
+            mbar_init(&sf_ready[k], 1);
+            mbar_init(&sf_free[k], 1);
+        }
+        mbar_init(cp_done, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) tmem_alloc<PAIR>(tmem_holder);
@@ -485,8 +495,10 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
     const uint32_t tmem_acc = tmem_base;
-    const uint32_t tmem_sfa = tmem_base + BN;
-    const uint32_t tmem_sfb = tmem_base + BN + C::SFA_COLS;
+    // scale set k: A's scales at tmem_sf(k), B's right after them
+    constexpr uint32_t SF_SET_COLS = C::SFA_COLS + C::SFB_COLS;
+    auto tmem_sfa = [&](uint32_t k) { return tmem_base + BN + k * SF_SET_COLS; };
+    auto tmem_sfb = [&](uint32_t k) { return tmem_base + BN + k * SF_SET_COLS + C::SFA_COLS; };
     constexpr uint16_t PAIR_MASK = 3;
 
     if (warp == 0 && lane == 0) {
@@ -583,6 +595,7 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
         int slot = 0;
         uint32_t phase = 0;
         uint32_t acc_phase = 0;
+        uint32_t fill = 0;                       // stage fills consumed (selects the scale set)
         bool ok = true;
         const uint32_t stage0 = smem_u32(stage_base);
         for (int64_t t = tile_first; t < total && ok; t += tile_step) {
@@ -593,21 +606,15 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
             const int64_t ks0 = tl.k_begin / C::EPS, ks1 = (tl.k_end + C::EPS - 1) / C::EPS;
             uint32_t accumulate = 0;
             for (int64_t ks = ks0; ks < ks1; ++ks) {
-                if (!mbar_wait<PAIR>(&full_bar[slot], phase, abort_flag, p.status)) { ok = false; break; }
+                const uint32_t set = fill % SF_SETS, use = fill / SF_SETS;
+                if (!mbar_wait<PAIR>(&full_bar[slot], phase, abort_flag, p.status) ||
+                    !mbar_wait<PAIR>(&sf_ready[set], use & 1u, abort_flag, p.status)) {
+                    ok = false;
+                    break;
+                }
                 tc_fence_after();
                 const uint32_t sa = stage0 + (uint32_t)slot * C::STAGE_BYTES;
                 const uint32_t sb = sa + C::A_BYTES;
-                const uint32_t ssfa = sb + C::B_BYTES;
-                const uint32_t ssfb = ssfa + C::SFA_BYTES;
-                // scales -> TMEM: A's k-group j at columns [4j, 4j+4); B's at [8j, 8j+8) (two 128-row
-                // tiles). For a pair each CTA's copy reads its own shared memory into its own TMEM.
-#pragma unroll
-                for (int j = 0; j < C::KGS; ++j) {
-                    tc_cp_sf<PAIR>(tmem_sfa + 4 * j, smem_desc(ssfa + j * 512, 0, 128, 0));
-#pragma unroll
-                    for (int h = 0; h < 2; ++h)
-                        tc_cp_sf<PAIR>(tmem_sfb + 8 * j + 4 * h, smem_desc(ssfb + (h * C::KGS + j) * 512, 0, 128, 0));
-                }
                 const uint64_t adesc0 = smem_desc(sa, 16, 1024, 2);
                 const uint64_t bdesc0 = smem_desc(sb, 16, 1024, 2);
 #pragma unroll
@@ -619,10 +626,12 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
                     const uint32_t idesc = C::IDESC | (sf_id << 4) | (sf_id << 29);
                     // K advance inside the 128-byte swizzled row: 32 bytes per MMA (encoded >> 4)
                     tc_mma<FP4, PAIR>(tmem_acc, adesc0 + (uint64_t)(2 * j), bdesc0 + (uint64_t)(2 * j), idesc,
-                                      tmem_sfa + 4 * kg, tmem_sfb + 8 * kg, accumulate);
+                                      tmem_sfa(set) + 4 * kg, tmem_sfb(set) + 8 * kg, accumulate);
                     accumulate = 1;
                 }
                 tc_commit<PAIR>(&empty_bar[slot], PAIR_MASK);
+                tc_commit<PAIR>(&sf_free[set], 1);
+                ++fill;
                 if (++slot == C::STAGES) { slot = 0; phase ^= 1u; }
             }
             if (!ok) break;
@@ -632,6 +641,48 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
         // wait (bounded) for every tcgen05 operation issued above before TMEM is released
         tc_commit<PAIR>(mma_done, 1);
         mbar_drain<PAIR>(mma_done, 0);
+    } else if (warp == SCALE_WARP && lane == 0 && leader) {
+        // ======================= scale copier =======================
+        // Copies each stage's scale tiles smem -> TMEM into scale set fill % SF_SETS (A's k-group j
+        // at columns [4j, 4j+4) of the set, B's at [8j, 8j+8): two 128-row tiles), so that the
+        // copies of the next fill run while the MMA issuer works on this one. For a pair each CTA's
+        // copy reads its own shared memory into its own TMEM.
+        int slot = 0;
+        uint32_t phase = 0;
+        uint32_t fill = 0;
+        bool ok = true;
+        const uint32_t stage0 = smem_u32(stage_base);
+        for (int64_t t = tile_first; t < total && ok; t += tile_step) {
+            const Tile tl = sched.get(t);
+            if (tl.k_end <= tl.k_begin) continue;
+            const int64_t ks0 = tl.k_begin / C::EPS, ks1 = (tl.k_end + C::EPS - 1) / C::EPS;
+            for (int64_t ks = ks0; ks < ks1; ++ks) {
+                const uint32_t set = fill % SF_SETS, use = fill / SF_SETS;
+                // the stage's scales are in place, and the MMAs of the set's previous use are done
+                if (!mbar_wait<PAIR>(&full_bar[slot], phase, abort_flag, p.status) ||
+                    !mbar_wait<PAIR>(&sf_free[set], (use & 1u) ^ 1u, abort_flag, p.status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t ssfa = stage0 + (uint32_t)slot * C::STAGE_BYTES + C::A_BYTES + C::B_BYTES;
+                const uint32_t ssfb = ssfa + C::SFA_BYTES;
+#pragma unroll
+                for (int j = 0; j < C::KGS; ++j) {
+                    tc_cp_sf<PAIR>(tmem_sfa(set) + 4 * j, smem_desc(ssfa + j * 512, 0, 128, 0));
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+                        tc_cp_sf<PAIR>(tmem_sfb(set) + 8 * j + 4 * h,
+                                       smem_desc(ssfb + (h * C::KGS + j) * 512, 0, 128, 0));
+                }
+                tc_commit<PAIR>(&sf_ready[set], 1);
+                ++fill;
+                if (++slot == C::STAGES) { slot = 0; phase ^= 1u; }
+            }
+        }
+        // wait (bounded) for the copies issued above before TMEM is released
+        tc_commit<PAIR>(cp_done, 1);
+        mbar_drain<PAIR>(cp_done, 0);
     } else if (warp == 6) {
         // ======================= A-scale transposer =======================
         // A tile starting 32*g0 rows into a 128-row scale tile needs rows [32 g0, 128) of that tile

@@ -148,6 +148,52 @@ def test_tilings_agree_bitwise(nvq, fmt):
     assert torch.equal(a.view(torch.int32), b.view(torch.int32))
 
 
+@pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4"])
+def test_many_tiles_per_cta(nvq, fmt):
+    # More tiles than CTAs: each CTA runs several tiles, so every stage ring wraps repeatedly, with
+    # tiles starting inside a scale tile (32-row group offsets) mixed among aligned ones.
+    counts = [150, 33, 260, 0, 121, 97, 201, 64, 180, 5, 140, 230]
+    E, K, N = len(counts), 1024, 2560
+    offs, xb = _routed(counts, K, seed=21)
+    rng = np.random.default_rng(22)
+    wb = _bits(rng.standard_normal((E, K, N)) * 0.02 * np.exp(rng.uniform(-2, 2, (E, 1, 1))))
+    x = workloads.from_bits(xb, "cuda")
+    w = workloads.from_bits(wb, "cuda")
+    M = x.shape[0]
+    offs_d = torch.from_numpy(offs).cuda()
+    tiles_128 = sum(-(-int(r) // 128) for r in np.diff(offs)) * (N // 256)
+    assert tiles_128 > 152                      # more tiles than a GB300 has SMs
+    if fmt == "nvfp4":
+        qa, sfa, sa = nvq.nvfp4_quantize_per_token(x)
+        qb, sfb, sb = nvq.nvfp4_quantize_weights(w.contiguous())
+        args, kw = (nvq.NVFP4, nvq.GEMM_GROUP_M, qa, sfa, qb, sfb, offs_d), dict(s_a=sa, s_b=sb)
+        qa_r, sfa_r, sa_r = oracle.nvfp4_quantize_per_token(xb)
+        qb_r, sfb_r, sb_r = oracle.nvfp4_quantize_weights(wb)
+        a = oracle.deq_operand("nvfp4", qa_r, sfa_r)
+        b = np.stack([oracle.deq_operand("nvfp4", qb_r[e], sfb_r[e]) for e in range(E)])
+        D, bound = oracle.grouped_gemm_reference("m", a, b, offs, sa_r, sb_r)
+    else:
+        qa = nvq.mxfp8_quantize(x, colwise=False)
+        qb = nvq.mxfp8_quantize(w.transpose(1, 2).contiguous().view(E * N, K), colwise=False)
+        args, kw = (nvq.MXFP8, nvq.GEMM_GROUP_M, qa["q_row"], qa["sf_row"], qb["q_row"], qb["sf_row"], offs_d), {}
+        ra = oracle.mxfp8_quantize(xb, colwise=False)
+        a = oracle.deq_operand("mxfp8", ra["q_row"], ra["sf_row"])
+        b = np.stack([oracle.deq_operand("mxfp8", *oracle.mxfp8_quantize(np.ascontiguousarray(wb[e]),
+                                                                          rowwise=False).values())
+                      for e in range(E)])
+        D, bound = oracle.grouped_gemm_reference("m", a, b, offs)
+    outs = []
+    for tiles in (1, 2):
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        d = nvq.block_scaled_grouped_gemm(*args, m=M, n=N, k=K, groups=E, out_type=nvq.OUT_F32, status=status,
+                                          tiles=tiles, **kw)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        _check(d, D, bound, False)
+        outs.append(d)
+    assert torch.equal(outs[0].view(torch.int32), outs[1].view(torch.int32))
+
+
 @pytest.mark.parametrize("tiles", [1, 2])
 def test_rows_outside_groups_untouched(nvq, tiles):
     E, K, N = 2, 256, 256
