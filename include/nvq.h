@@ -155,14 +155,6 @@ typedef enum { NVQ_OUT_BF16 = 0, NVQ_OUT_F32 = 1 } nvq_out_type;
 #define NVQ_DEV_TIMEOUT 1          /* a pipeline wait exceeded its iteration limit */
 #define NVQ_DEV_BAD_OFFSETS 2      /* offsets not monotone, not multiples of 32, or past the buffer */
 
-/* Output tiling of block_scaled_grouped_gemm. Both tilings compute the same values (the fp32
- * accumulation order over k is the same); they differ in speed only. */
-typedef enum {
-    NVQ_TILES_AUTO = 0,     /* the library's choice (currently 128-row tiles: measured faster)     */
-    NVQ_TILES_128 = 1,      /* 128 x 256 output tiles, one SM each                                  */
-    NVQ_TILES_256 = 2       /* 256 x 256 output tiles, each on a pair of SMs (2-CTA cluster): each
-                               SM stages half of the A rows and half of the B rows               */
-} nvq_gemm_tiles;
 
 typedef struct {
     nvq_format fmt;          /* NVQ_MXFP8 (E4M3 x E8M0 / 32) or NVQ_NVFP4 (E2M1 x E4M3 / 16)       */
@@ -185,7 +177,6 @@ typedef struct {
                                 GROUP_K: [groups, m, n] (empty groups are written as zeros)        */
     int64_t ldd;             /* leading dimension of d in elements (>= n, multiple of 8)           */
     int32_t* status;         /* optional device int32: NVQ_DEV_* after the call (set, never cleared) */
-    nvq_gemm_tiles tiles;    /* output tiling (NVQ_TILES_AUTO unless a caller needs a specific one) */
 } nvq_gemm_args;
 
 /*

@@ -31,7 +31,6 @@ SCOPE_ROW, SCOPE_MATRIX = 0, 1
 GEMM_GROUP_M, GEMM_GROUP_K = 0, 1
 OUT_BF16, OUT_F32 = 0, 1
 DEV_OK, DEV_TIMEOUT, DEV_BAD_OFFSETS = 0, 1, 2
-TILES_AUTO, TILES_128, TILES_256 = 0, 1, 2
 
 _vp, _i64, _i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32
 
@@ -60,7 +59,7 @@ class GemmArgs(ctypes.Structure):
         ("groups", _i64), ("m", _i64), ("n", _i64), ("k", _i64),
         ("a", _vp), ("sfa", _vp), ("s_a", _vp),
         ("b", _vp), ("sfb", _vp), ("s_b", _vp),
-        ("offsets", _vp), ("d", _vp), ("ldd", _i64), ("status", _vp), ("tiles", ctypes.c_int),
+        ("offsets", _vp), ("d", _vp), ("ldd", _i64), ("status", _vp),
     ]
 
 
@@ -193,11 +192,10 @@ def dequantize_bf16(fmt, q, sf, s=None, scope=SCOPE_ROW, groups=1, rows=None, co
 
 
 def block_scaled_grouped_gemm(fmt, mode, a, sfa, b, sfb, offsets, m, n, k, groups, s_a=None, s_b=None,
-                              out=None, out_type=OUT_BF16, status=None, tiles=TILES_AUTO):
+                              out=None, out_type=OUT_BF16, status=None):
     """Block-scaled grouped GEMM (include/nvq.h). ``offsets`` is a device int64 tensor [groups+1].
 
-    mode GEMM_GROUP_M: D [m, n]; mode GEMM_GROUP_K: D [groups, m, n]. ``tiles`` picks the output
-    tiling (TILES_AUTO, TILES_128 or TILES_256; same values, different speed). Returns D.
+    mode GEMM_GROUP_M: D [m, n]; mode GEMM_GROUP_K: D [groups, m, n]. Returns D.
     """
     if _gemm is None:
         raise NvqError(NVQ_ERR_UNSUPPORTED, "block_scaled_grouped_gemm (not built)")
@@ -211,7 +209,7 @@ def block_scaled_grouped_gemm(fmt, mode, a, sfa, b, sfb, offsets, m, n, k, group
     args = GemmArgs(fmt=int(fmt), mode=int(mode), out_type=int(out_type), groups=int(groups), m=int(m),
                     n=int(n), k=int(k), a=_ptr(a), sfa=_ptr(sfa), s_a=_ptr(s_a), b=_ptr(b), sfb=_ptr(sfb),
                     s_b=_ptr(s_b), offsets=_ptr(offsets), d=_ptr(out), ldd=int(out.stride(-2)),
-                    status=_ptr(status), tiles=int(tiles))
+                    status=_ptr(status))
     st = _gemm(ctypes.byref(args), _stream(dev))
     _check(st, "block_scaled_grouped_gemm")
     return out

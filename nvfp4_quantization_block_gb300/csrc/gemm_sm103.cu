@@ -9,25 +9,21 @@
 //   GROUP_M: D[i, j] = s_a[i] s_b[e] sum_k deq(A)[i, k] deq(B[e])[j, k]   (rows i of group e)
 //   GROUP_K: D[e][i, j] = sum_{k in group e} deq(A)[i, k] deq(B)[j, k]
 //
-// Design (persistent, warp-specialised, 224 threads per CTA). Two tilings share one kernel body:
-//   128-row tiles: one CTA per SM computes a 128 x 256 output tile (tcgen05 cta_group::1, M = 128).
-//   256-row tiles: a 2-CTA cluster (an SM pair) computes a 256 x 256 tile with cta_group::2 MMAs
-//                  (M = 256): each CTA stages its own 128 A rows and its own 128 of the 256 B rows,
-//                  so each SM takes in a third less operand data per flop; the even CTA issues the
-//                  MMAs and each CTA's TMEM holds its own 128 accumulator rows.
-// Roles:
-//   warp 0 lane 0  TMA producer: 128x128-byte A tiles and (256 or 128)x128-byte B tiles (128B
-//                  swizzle) plus the matching 512-byte scale tiles (bulk copies) into a ring of stages.
+// Design (one CTA per SM, persistent, warp-specialised, 256 threads). A CTA computes 128 x 256
+// output tiles (tcgen05 M = 128, N = 256) from a ring of stages (MXFP8: 4 x 50 KB, NVFP4: 3 x 58 KB),
+// each holding a 128x128-byte A tile, a 256x128-byte B tile (128B swizzle) and their 512-byte
+// scale tiles. Roles:
+//   warp 0 lane 0  TMA producer: A and B tiles (tensor copies) and the scale tiles (bulk copies).
 //   warp 6         A-scale transposer: a GROUP_M tile starts at its group's row offset (a multiple
-//                  of 32), so its 128 rows of A scales straddle two 128-row scale tiles; the warp
-//                  rebuilds the tile's own 512-byte scale tile in shared memory (one funnel shift
-//                  per 16-byte line) and hands the stage on.
-//   warp 1 lane 0  MMA issuer (the even CTA of a pair): copies each stage's scale tiles smem -> TMEM
-//                  (tcgen05.cp 32x128b.warpx4) and issues four tcgen05.mma block_scale instructions
-//                  (N = 256; K = 32 for MXFP8 E4M3 x UE8M0/32, K = 64 for NVFP4 E2M1 x UE4M3/16),
-//                  accumulating in TMEM (fp32, 256 columns). Commits free smem stages and signal
-//                  the epilogue (multicast to both CTAs of a pair). In the odd CTA of a pair this
-//                  lane forwards each completed stage to the even CTA's stage barrier instead.
+//                  of 32), so its 128 rows of A scales straddle two 128-row scale tiles; the producer
+//                  loads both into the stage and the warp rebuilds the tile's own 512-byte scale tile
+//                  (one funnel shift per 16-byte line).
+//   warp 7 lane 0  scale warp: copies each stage's scale tiles smem -> TMEM (tcgen05.cp
+//                  32x128b.warpx4) into one of two TMEM scale sets, so that the copies of the next
+//                  stage are queued while the MMAs of this one run.
+//   warp 1 lane 0  MMA issuer: four tcgen05.mma block_scale instructions per stage (K = 32 for
+//                  MXFP8 E4M3 x UE8M0/32, K = 64 for NVFP4 E2M1 x UE4M3/16) into a 256-column fp32
+//                  TMEM accumulator; commits free stages and scale sets and signal the epilogue.
 //                  Warp 1 also allocates and frees TMEM.
 //   warps 2-5      epilogue: tcgen05.ld 32 columns at a time (the next load in flight while the
 //                  current chunk converts), multiply by s_a[row] s_b[e], round to bf16 into
@@ -53,37 +49,38 @@
 namespace nvq {
 
 constexpr int GEMM_THREADS = 256;
-constexpr int SCALE_WARP = 7;                      // copies the scale tiles smem -> TMEM
-constexpr uint32_t SF_SETS = 2;                    // TMEM scale sets: copies of fill f+1 overlap MMAs of f
-constexpr int BM = 128, BN = 256, BKB = 128;       // rows per CTA, tile columns, K bytes per stage
+constexpr int W_PRODUCER = 0, W_MMA = 1, W_EPI0 = 2, W_TRANSPOSER = 6, W_SCALE = 7;
+constexpr int BM = 128, BN = 256, BKB = 128;       // tile rows, tile columns, K bytes per stage
 constexpr int MAX_GROUPS = 1024;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;    // 2 s: far beyond any legitimate wait
 
-template <bool FP4, bool PAIR>
+template <bool FP4>
 struct GemmCfg {
-    static constexpr int STAGES = PAIR ? (FP4 ? 5 : 6) : (FP4 ? 3 : 4);
+    static constexpr int STAGES = FP4 ? 3 : 4;
     static constexpr int KGS = FP4 ? 4 : 1;            // 4-scale-column groups per stage
     static constexpr int EPS = FP4 ? 256 : 128;        // reduction elements per stage
     static constexpr int MMA_K = FP4 ? 64 : 32;        // reduction elements per MMA
-    static constexpr int TILE_M = PAIR ? 2 * BM : BM;  // output rows of a scheduled tile
-    static constexpr int B_ROWS = PAIR ? BN / 2 : BN;  // B rows this CTA stages
     static constexpr int A_BYTES = BM * BKB;
-    static constexpr int B_BYTES = B_ROWS * BKB;
-    static constexpr int SFA_BYTES = KGS * 512;        // the CTA's own 128 row scales
-    static constexpr int SFB_BYTES = 2 * KGS * 512;    // two 128-row scale tiles (all N = 256 columns)
+    static constexpr int B_BYTES = BN * BKB;
+    static constexpr int SFA_BYTES = KGS * 512;        // the tile's own 128 row scales
+    static constexpr int SFB_BYTES = 2 * KGS * 512;    // two 128-row scale tiles (N = 256)
     static constexpr int SFA_RAW_BYTES = 2 * KGS * 512;  // the two row tiles a 32-aligned tile spans
     static constexpr int STAGE_BYTES =
         (A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES + SFA_RAW_BYTES + 1023) / 1024 * 1024;
+    static constexpr uint32_t SF_SETS = 2;             // TMEM scale sets
     static constexpr uint32_t SFA_COLS = KGS * 4;      // TMEM columns of A's scales
     static constexpr uint32_t SFB_COLS = KGS * 8;      // TMEM columns of B's scales
+    static constexpr uint32_t SF_SET_COLS = SFA_COLS + SFB_COLS;
     static constexpr uint32_t IDESC =
         (FP4 ? ((1u << 7) | (1u << 10)) : 0u)         // A, B format: E2M1 (mxf4nvf4) or E4M3
         | ((uint32_t)(BN >> 3) << 17)                  // N >> 3
         | (FP4 ? 0u : (1u << 23))                      // scale type: UE4M3 (0) / UE8M0 (1)
-        | ((uint32_t)(TILE_M >> 4) << 24);             // M >> 4
-    static constexpr uint32_t EPI_ARRIVALS = PAIR ? 8u : 4u;   // tmem_empty: one per epilogue warp
-    static constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + 256 + 8 * (MAX_GROUPS + 1);
+        | ((uint32_t)(BM >> 4) << 24);                 // M >> 4
+    static constexpr int BAR_BYTES = 256;
+    static constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + BAR_BYTES + 8 * (MAX_GROUPS + 1);
+    static_assert(BN + SF_SETS * SF_SET_COLS <= TMEM_COLS, "TMEM columns");
+    static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 };
 
 struct GemmParams {
@@ -112,23 +109,6 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-// shared::cluster address of the variable at local shared address `saddr` in cluster CTA `rank`
-__device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
-    return r;
-}
-
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
-}
-
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
 }
@@ -142,31 +122,15 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
-// arrive on a barrier given by its shared::cluster address (this CTA's or the peer's)
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t caddr) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
-}
-
-template <bool CLUSTER>
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     uint32_t ok;
-    if constexpr (CLUSTER) {
-        asm volatile(
-            "{\n\t.reg .pred p;\n\t"
-            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-            "selp.u32 %0, 1, 0, p;\n\t}"
-            : "=r"(ok)
-            : "r"(smem_u32(bar)), "r"(parity)
-            : "memory");
-    } else {
-        asm volatile(
-            "{\n\t.reg .pred p;\n\t"
-            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-            "selp.u32 %0, 1, 0, p;\n\t}"
-            : "=r"(ok)
-            : "r"(smem_u32(bar)), "r"(parity)
-            : "memory");
-    }
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
     return ok != 0;
 }
 
@@ -178,13 +142,11 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 
 // Bounded wait; returns false (and raises the abort flag / status) when WAIT_LIMIT_NS of wall-clock
 // time pass without the phase completing, or when another role has already aborted.
-template <bool CLUSTER>
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          int32_t* status) {
-    if (mbar_try_wait<CLUSTER>(bar, parity)) return true;
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int32_t* status) {
+    if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait<CLUSTER>(bar, parity)) return true;
+        if (mbar_try_wait(bar, parity)) return true;
         if ((it & 255u) == 0u) {
             if (*abort_flag) return false;
             if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) break;
@@ -196,10 +158,9 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
 }
 
 // Bounded drain used at teardown: wait for a phase without raising anything.
-template <bool CLUSTER>
 __device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
     const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait<CLUSTER>(bar, parity))
+    while (!mbar_try_wait(bar, parity))
         if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) return;
 }
 
@@ -221,41 +182,10 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// All tcgen05 instructions of one kernel use the same CTA group: ::1 for 128-row tiles, ::2 for
-// 256-row tiles on an SM pair. A pair's commits arrive on the barrier at the same shared address
-// in every CTA of `mask`.
-template <bool PAIR>
-__device__ __forceinline__ void tc_commit(uint64_t* bar, uint16_t mask) {
-    if constexpr (PAIR) {
-        asm volatile(
-            "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
-            ::"r"(smem_u32(bar)), "h"(mask) : "memory");
-    } else {
-        (void)mask;
-        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
-                     ::"r"(smem_u32(bar)) : "memory");
-    }
-}
-
-template <bool PAIR>
-__device__ __forceinline__ void tmem_alloc(uint32_t* holder) {
-    if constexpr (PAIR) {
-        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"
-                     ::"r"(smem_u32(holder)), "r"(TMEM_COLS) : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-    } else {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
-                     ::"r"(smem_u32(holder)), "r"(TMEM_COLS) : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    }
-}
-
-template <bool PAIR>
-__device__ __forceinline__ void tmem_dealloc(uint32_t base) {
-    if constexpr (PAIR)
-        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(base), "r"(TMEM_COLS) : "memory");
-    else
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(base), "r"(TMEM_COLS) : "memory");
+// Arrives on `bar` once every tcgen05 operation this thread issued before has completed.
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 ::"r"(smem_u32(bar)) : "memory");
 }
 
 // Shared-memory matrix descriptor (tcgen05): start >> 4, LBO >> 4, SBO >> 4, version 1, swizzle.
@@ -264,28 +194,26 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
            (1ull << 46) | ((uint64_t)swizzle << 61);
 }
 
-template <bool FP4, bool PAIR>
+template <bool FP4>
 __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                        uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
-#define NVQ_MMA(GROUP, KIND)                                                                                  \
-    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"                                            \
-                 "tcgen05.mma.cta_group::" GROUP ".kind::" KIND " [%0], %1, %2, %3, [%4], [%5], p;\n\t}"      \
-                 ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem),             \
-                 "r"(accumulate)                                                                              \
-                 : "memory")
-    if constexpr (FP4 && PAIR) NVQ_MMA("2", "mxf4nvf4.block_scale.scale_vec::4X");
-    else if constexpr (FP4) NVQ_MMA("1", "mxf4nvf4.block_scale.scale_vec::4X");
-    else if constexpr (PAIR) NVQ_MMA("2", "mxf8f6f4.block_scale.scale_vec::1X");
-    else NVQ_MMA("1", "mxf8f6f4.block_scale.scale_vec::1X");
-#undef NVQ_MMA
+    if constexpr (FP4) {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+            ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+            : "memory");
+    } else {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+            ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+            : "memory");
+    }
 }
 
-template <bool PAIR>
 __device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
-    if constexpr (PAIR)
-        asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
-    else
-        asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
 // Start a 32-lane x 32-column TMEM load into r; the registers are valid after tmem_wait_ld(r).
@@ -329,7 +257,7 @@ __device__ __forceinline__ void pack_scaled(const uint32_t (&r)[32], float scale
 }
 
 // ------------------------------------------------------------------------------------------------
-// Tile schedule (identical in every role and in both CTAs of a pair)
+// Tile schedule (identical in every role)
 // ------------------------------------------------------------------------------------------------
 struct Tile {
     int e;
@@ -345,7 +273,6 @@ struct Schedule {
     const int32_t* off;        // group offsets (smem, int32)
     const int32_t* tile_start; // GROUP_M: prefix of tiles per group (smem)
     int mode, groups;
-    int tile_m;                // rows per scheduled tile (128, or 256 for an SM pair)
     int64_t m, n, k;
     int n_tiles, m_tiles;      // GROUP_K: per-group tile grid
     int64_t total;
@@ -362,7 +289,7 @@ struct Schedule {
             const int64_t local = t - tile_start[e];
             const int64_t mt = local / n_tiles, nt = local - mt * n_tiles;
             tl.e = e;
-            tl.a_row0 = off[e] + mt * tile_m;
+            tl.a_row0 = off[e] + mt * BM;
             tl.row_end = min((int64_t)off[e + 1], m);
             tl.n0 = nt * BN;
             tl.b_row0 = (int64_t)e * n + tl.n0;
@@ -375,7 +302,7 @@ struct Schedule {
             const int64_t local = t - (int64_t)e * per;
             const int64_t mt = local / n_tiles, nt = local - mt * n_tiles;
             tl.e = e;
-            tl.a_row0 = mt * tile_m;
+            tl.a_row0 = mt * BM;
             tl.row_end = m;
             tl.n0 = nt * BN;
             tl.b_row0 = tl.n0;
@@ -387,41 +314,67 @@ struct Schedule {
     }
 };
 
+// Walks the stages (k-steps of non-empty tiles) of one CTA in schedule order, for roles that run
+// ahead of the stage they are working on.
+template <int EPS>
+struct StageCursor {
+    const Schedule* sched;
+    int64_t t, step, ks, ks1;
+    Tile tl;
+    bool valid;
+
+    __device__ void seek(int64_t from) {
+        for (t = from; t < sched->total; t += step) {
+            tl = sched->get(t);
+            if (tl.k_end > tl.k_begin) {
+                ks = tl.k_begin / EPS;
+                ks1 = (tl.k_end + EPS - 1) / EPS;
+                valid = true;
+                return;
+            }
+        }
+        valid = false;
+    }
+    __device__ void begin(const Schedule* s, int64_t first, int64_t stride) {
+        sched = s;
+        step = stride;
+        seek(first);
+    }
+    __device__ void next() {
+        if (++ks < ks1) return;
+        seek(t + step);
+    }
+};
+
 // ------------------------------------------------------------------------------------------------
 // Kernel
 // ------------------------------------------------------------------------------------------------
-template <bool FP4, bool PAIR>
+template <bool FP4>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
 block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                          const GemmParams p) {
-    using C = GemmCfg<FP4, PAIR>;
+    using C = GemmCfg<FP4>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* stage_base = smem;
     uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
     uint64_t* empty_bar = full_bar + C::STAGES;
-    uint64_t* sfa_bar = empty_bar + C::STAGES;
-    uint64_t* tmem_full = sfa_bar + C::STAGES;
+    uint64_t* sfa_bar = empty_bar + C::STAGES;         // [STAGES] raw A scales of a shifted tile landed
+    uint64_t* sf_ready = sfa_bar + C::STAGES;          // [SF_SETS] scale set copied into TMEM
+    uint64_t* sf_free = sf_ready + C::SF_SETS;         // [SF_SETS] MMAs reading the set are done
+    uint64_t* tmem_full = sf_free + C::SF_SETS;
     uint64_t* tmem_empty = tmem_full + 1;
     uint64_t* mma_done = tmem_empty + 1;
-    uint64_t* sf_ready = mma_done + 1;                 // [SF_SETS] scale set copied into TMEM
-    uint64_t* sf_free = sf_ready + SF_SETS;            // [SF_SETS] MMAs reading the set are done
-    uint64_t* cp_done = sf_free + SF_SETS;
+    uint64_t* cp_done = mma_done + 1;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(cp_done + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
     int* bad_flag = reinterpret_cast<int*>(tmem_holder + 2);
-    int32_t* off32 = reinterpret_cast<int32_t*>(smem + C::STAGES * C::STAGE_BYTES + 256);
+    int32_t* off32 = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(full_bar) + C::BAR_BYTES);
     int32_t* tile_start = off32 + (MAX_GROUPS + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = p.groups;
     const int n_tiles = (int)((p.n + BN - 1) / BN);
-    // a pair's even CTA (rank 0) issues the MMAs; the odd one holds rows [128, 256) of each tile
-    const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
-    const bool leader = rank == 0u;
-    const int64_t tile_first = PAIR ? (int64_t)(blockIdx.x >> 1) : (int64_t)blockIdx.x;
-    const int64_t tile_step = PAIR ? (int64_t)(gridDim.x >> 1) : (int64_t)gridDim.x;
-    const int64_t row_in_pair = (int64_t)rank * BM;
 
     // ---- validate offsets and build the schedule (all threads see the same smem) ----
     if (threadIdx.x == 0) {
@@ -438,130 +391,117 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
         off32[e] = (int32_t)o;
     }
     __syncthreads();
-    if (*bad_flag) {    // both CTAs of a pair read the same offsets and leave here together
+    if (*bad_flag) {
         if (threadIdx.x == 0 && blockIdx.x == 0 && p.status) atomicExch(p.status, NVQ_DEV_BAD_OFFSETS);
         return;
     }
-    int64_t total;
     Schedule sched;
     sched.off = off32;
     sched.tile_start = tile_start;
     sched.mode = p.mode;
     sched.groups = G;
-    sched.tile_m = C::TILE_M;
     sched.m = p.m;
     sched.n = p.n;
     sched.k = p.k;
     sched.n_tiles = n_tiles;
-    sched.m_tiles = (int)((p.m + C::TILE_M - 1) / C::TILE_M);
+    sched.m_tiles = (int)((p.m + BM - 1) / BM);
     if (p.mode == NVQ_GEMM_GROUP_M) {
         if (threadIdx.x == 0) {
             int32_t acc = 0;
             for (int e = 0; e < G; ++e) {
                 tile_start[e] = acc;
-                acc += (int32_t)(((off32[e + 1] - off32[e]) + C::TILE_M - 1) / C::TILE_M) * n_tiles;
+                acc += (int32_t)(((off32[e + 1] - off32[e]) + BM - 1) / BM) * n_tiles;
             }
             tile_start[G] = acc;
         }
         __syncthreads();
-        total = tile_start[G];
+        sched.total = tile_start[G];
     } else {
-        total = (int64_t)G * sched.m_tiles * n_tiles;
+        sched.total = (int64_t)G * sched.m_tiles * n_tiles;
     }
-    sched.total = total;
+    const int64_t total = sched.total;
 
     // ---- barriers and TMEM ----
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
-            // producer (A, B, scales) + its second arrival or the scale transposer's; the even CTA
-            // of a pair also waits for the odd CTA's forwarded stage
-            mbar_init(&full_bar[s], (PAIR && leader) ? 3u : 2u);
+            // the producer's expect_tx arrival + its second arrival or the scale transposer's
+            mbar_init(&full_bar[s], 2);
             mbar_init(&empty_bar[s], 1);
             mbar_init(&sfa_bar[s], 1);
         }
-        mbar_init(tmem_full, 1);
-        mbar_init(tmem_empty, C::EPI_ARRIVALS);
-        mbar_init(mma_done, 1);
-        for (uint32_t k = 0; k < SF_SETS; ++k) {
+        for (uint32_t k = 0; k < C::SF_SETS; ++k) {
             mbar_init(&sf_ready[k], 1);
             mbar_init(&sf_free[k], 1);
         }
+        mbar_init(tmem_full, 1);
+        mbar_init(tmem_empty, 4);              // one arrival per epilogue warp
+        mbar_init(mma_done, 1);
         mbar_init(cp_done, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == 1) tmem_alloc<PAIR>(tmem_holder);
+    if (warp == W_MMA) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(smem_u32(tmem_holder)), "r"(TMEM_COLS) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
     tc_fence_before();
-    if constexpr (PAIR) cluster_sync(); else __syncthreads();
+    __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
     const uint32_t tmem_acc = tmem_base;
-    // scale set k: A's scales at tmem_sf(k), B's right after them
-    constexpr uint32_t SF_SET_COLS = C::SFA_COLS + C::SFB_COLS;
-    auto tmem_sfa = [&](uint32_t k) { return tmem_base + BN + k * SF_SET_COLS; };
-    auto tmem_sfb = [&](uint32_t k) { return tmem_base + BN + k * SF_SET_COLS + C::SFA_COLS; };
-    constexpr uint16_t PAIR_MASK = 3;
+    // scale set k: A's scales at tmem_sfa(k) (k-group j at +4j), B's at tmem_sfb(k) (+8j)
+    auto tmem_sfa = [&](uint32_t k) { return tmem_base + BN + k * C::SF_SET_COLS; };
+    auto tmem_sfb = [&](uint32_t k) { return tmem_base + BN + k * C::SF_SET_COLS + C::SFA_COLS; };
+    const int64_t first = blockIdx.x, stride = gridDim.x;
 
-    if (warp == 0 && lane == 0) {
+    if (warp == W_PRODUCER && lane == 0) {
         // =========================== TMA producer ===========================
         int slot = 0;
         uint32_t phase = 0;
         int64_t issued = 0;
         uint32_t sfa_fills[C::STAGES];          // shifted-tile fills of each slot's sfa_bar
         for (int i = 0; i < C::STAGES; ++i) sfa_fills[i] = 0;
-        bool ok = true;
-        for (int64_t t = tile_first; t < total && ok; t += tile_step) {
-            const Tile tl = sched.get(t);
-            if (tl.k_end <= tl.k_begin) continue;
-            const int64_t ks0 = tl.k_begin / C::EPS, ks1 = (tl.k_end + C::EPS - 1) / C::EPS;
-            const int64_t a_row0 = tl.a_row0 + row_in_pair;
-            const int64_t rb_a = a_row0 / BM;
-            // the odd CTA's rows of a pair tile can lie wholly past the buffer: TMA fills zeros,
-            // the scale copies (no bounds check of their own) are skipped
-            const bool a_in = rb_a < p.a_rowtiles;
-            const bool shifted = (a_row0 % BM) != 0;
+        StageCursor<C::EPS> cur;
+        for (cur.begin(&sched, first, stride); cur.valid; cur.next()) {
+            if (!mbar_wait(&empty_bar[slot], phase ^ 1u, abort_flag, p.status)) break;
+            const Tile& tl = cur.tl;
+            const int64_t rb_a = tl.a_row0 / BM;
+            const bool shifted = (tl.a_row0 % BM) != 0;
             const bool need_a2 = shifted && rb_a + 1 < p.a_rowtiles;
             const int64_t rb_b = tl.b_row0 / BM;
             const bool need_b2 = rb_b + 1 < p.b_rowtiles;
-            for (int64_t ks = ks0; ks < ks1; ++ks) {
-                if (!mbar_wait<PAIR>(&empty_bar[slot], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
-                uint8_t* st = stage_base + (size_t)slot * C::STAGE_BYTES;
-                uint8_t* sa = st;
-                uint8_t* sb = st + C::A_BYTES;
-                uint8_t* ssfb = sb + C::B_BYTES + C::SFA_BYTES;
-                uint8_t* ssfa_raw = ssfb + C::SFB_BYTES;
-                const int64_t kg0 = ks * C::KGS;
-                const int64_t kgn = min((int64_t)C::KGS, p.sf_tiles_per_row - kg0);
-                const uint32_t sf_bytes = (uint32_t)kgn * 512u;
-                // full_bar completes after two arrivals and all bytes: the producer's expect_tx arrival
-                // (A, B, B scales, and the A scales of an aligned tile) plus either the producer's
-                // second arrival (aligned tile) or the transposer's (tile starting inside a scale tile)
-                const uint32_t tx = C::A_BYTES + C::B_BYTES + sf_bytes * (1u + (need_b2 ? 1u : 0u)) +
-                                    ((shifted || !a_in) ? 0u : sf_bytes);
-                mbar_arrive_expect_tx(&full_bar[slot], tx);
-                if (shifted) {
-                    const uint32_t raw = a_in ? sf_bytes * (1u + (need_a2 ? 1u : 0u)) : 0u;
-                    mbar_arrive_expect_tx(&sfa_bar[slot], raw);
-                    ++sfa_fills[slot];
-                    if (a_in)
-                        bulk_load(ssfa_raw, p.sfa + ((rb_a * p.sf_tiles_per_row + kg0) << 9), sf_bytes, &sfa_bar[slot]);
-                    if (need_a2)
-                        bulk_load(ssfa_raw + C::KGS * 512, p.sfa + (((rb_a + 1) * p.sf_tiles_per_row + kg0) << 9),
-                                  sf_bytes, &sfa_bar[slot]);
-                } else if (a_in) {
-                    bulk_load(ssfb - C::SFA_BYTES, p.sfa + ((rb_a * p.sf_tiles_per_row + kg0) << 9), sf_bytes,
-                              &full_bar[slot]);
-                }
-                tma_load_2d(sa, &tmap_a, (int32_t)(ks * BKB), (int32_t)a_row0, &full_bar[slot]);
-                tma_load_2d(sb, &tmap_b, (int32_t)(ks * BKB), (int32_t)(tl.b_row0 + (PAIR ? row_in_pair : 0)),
-                            &full_bar[slot]);
-                bulk_load(ssfb, p.sfb + ((rb_b * p.sf_tiles_per_row + kg0) << 9), sf_bytes, &full_bar[slot]);
-                if (need_b2)
-                    bulk_load(ssfb + C::KGS * 512, p.sfb + (((rb_b + 1) * p.sf_tiles_per_row + kg0) << 9), sf_bytes,
-                              &full_bar[slot]);
-                if (!shifted) mbar_arrive(&full_bar[slot]);
-                ++issued;
-                if (++slot == C::STAGES) { slot = 0; phase ^= 1u; }
+            uint8_t* st = stage_base + (size_t)slot * C::STAGE_BYTES;
+            uint8_t* ssfa = st + C::A_BYTES + C::B_BYTES;
+            uint8_t* ssfb = ssfa + C::SFA_BYTES;
+            uint8_t* ssfa_raw = ssfb + C::SFB_BYTES;
+            const int64_t kg0 = cur.ks * C::KGS;
+            const int64_t kgn = min((int64_t)C::KGS, p.sf_tiles_per_row - kg0);
+            const uint32_t sf_bytes = (uint32_t)kgn * 512u;
+            // full_bar completes after two arrivals and all bytes: the producer's expect_tx arrival
+            // (A, B, B scales, and the A scales of an aligned tile) plus either the producer's second
+            // arrival (aligned tile) or the transposer's (tile starting inside a scale tile)
+            const uint32_t tx = C::A_BYTES + C::B_BYTES + sf_bytes * (1u + (need_b2 ? 1u : 0u)) +
+                                (shifted ? 0u : sf_bytes);
+            mbar_arrive_expect_tx(&full_bar[slot], tx);
+            if (shifted) {
+                mbar_arrive_expect_tx(&sfa_bar[slot], sf_bytes * (1u + (need_a2 ? 1u : 0u)));
+                ++sfa_fills[slot];
+                bulk_load(ssfa_raw, p.sfa + ((rb_a * p.sf_tiles_per_row + kg0) << 9), sf_bytes, &sfa_bar[slot]);
+                if (need_a2)
+                    bulk_load(ssfa_raw + C::KGS * 512, p.sfa + (((rb_a + 1) * p.sf_tiles_per_row + kg0) << 9),
+                              sf_bytes, &sfa_bar[slot]);
+            } else {
+                bulk_load(ssfa, p.sfa + ((rb_a * p.sf_tiles_per_row + kg0) << 9), sf_bytes, &full_bar[slot]);
             }
+            tma_load_2d(st, &tmap_a, (int32_t)(cur.ks * BKB), (int32_t)tl.a_row0, &full_bar[slot]);
+            tma_load_2d(st + C::A_BYTES, &tmap_b, (int32_t)(cur.ks * BKB), (int32_t)tl.b_row0, &full_bar[slot]);
+            bulk_load(ssfb, p.sfb + ((rb_b * p.sf_tiles_per_row + kg0) << 9), sf_bytes, &full_bar[slot]);
+            if (need_b2)
+                bulk_load(ssfb + C::KGS * 512, p.sfb + (((rb_b + 1) * p.sf_tiles_per_row + kg0) << 9), sf_bytes,
+                          &full_bar[slot]);
+            if (!shifted) mbar_arrive(&full_bar[slot]);
+            ++issued;
+            if (++slot == C::STAGES) { slot = 0; phase ^= 1u; }
         }
         // wait (bounded) until the copies of the last fill of every slot have landed
         const int64_t n_last = issued < C::STAGES ? issued : C::STAGES;
@@ -569,54 +509,68 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
             int s2 = slot - 1 - (int)i;
             uint32_t ph = phase;
             if (s2 < 0) { s2 += C::STAGES; ph ^= 1u; }
-            mbar_drain<PAIR>(&full_bar[s2], ph);
+            mbar_drain(&full_bar[s2], ph);
         }
         for (int s2 = 0; s2 < C::STAGES; ++s2)
-            if (sfa_fills[s2]) mbar_drain<PAIR>(&sfa_bar[s2], (sfa_fills[s2] - 1u) & 1u);
-    } else if (warp == 1 && lane == 0 && !leader) {
-        // ===================== stage forwarder (odd CTA of a pair) =====================
-        // Each stage of this CTA's ring that is complete (its copies landed and its A scales are in
-        // place) is announced on the even CTA's barrier of the same slot.
+            if (sfa_fills[s2]) mbar_drain(&sfa_bar[s2], (sfa_fills[s2] - 1u) & 1u);
+    } else if (warp == W_SCALE && lane == 0) {
+        // =========================== scale warp ===========================
+        // Copies stage `fill`'s scale tiles into scale set fill % SF_SETS (A's k-group j at columns
+        // [4j, 4j+4) of the set, B's at [8j, 8j+8): two 128-row tiles) once the stage has landed and
+        // the MMAs of the set's previous use are done.
         int slot = 0;
         uint32_t phase = 0;
-        bool ok = true;
-        for (int64_t t = tile_first; t < total && ok; t += tile_step) {
-            const Tile tl = sched.get(t);
-            if (tl.k_end <= tl.k_begin) continue;
-            const int64_t ks0 = tl.k_begin / C::EPS, ks1 = (tl.k_end + C::EPS - 1) / C::EPS;
-            for (int64_t ks = ks0; ks < ks1; ++ks) {
-                if (!mbar_wait<PAIR>(&full_bar[slot], phase, abort_flag, p.status)) { ok = false; break; }
-                mbar_arrive_cluster(mapa_shared(smem_u32(&full_bar[slot]), 0));
-                if (++slot == C::STAGES) { slot = 0; phase ^= 1u; }
+        uint32_t fill = 0;
+        const uint32_t stage0 = smem_u32(stage_base);
+        StageCursor<C::EPS> cur;
+        for (cur.begin(&sched, first, stride); cur.valid; cur.next()) {
+            const uint32_t set = fill % C::SF_SETS;
+            if (!mbar_wait(&full_bar[slot], phase, abort_flag, p.status) ||
+                !mbar_wait(&sf_free[set], ((fill / C::SF_SETS) & 1u) ^ 1u, abort_flag, p.status))
+                break;
+            tc_fence_after();
+            const uint32_t ssfa = stage0 + (uint32_t)slot * C::STAGE_BYTES + C::A_BYTES + C::B_BYTES;
+            const uint32_t ssfb = ssfa + C::SFA_BYTES;
+#pragma unroll
+            for (int j = 0; j < C::KGS; ++j) {
+                tc_cp_sf(tmem_sfa(set) + 4 * j, smem_desc(ssfa + j * 512, 0, 128, 0));
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                    tc_cp_sf(tmem_sfb(set) + 8 * j + 4 * h, smem_desc(ssfb + (h * C::KGS + j) * 512, 0, 128, 0));
             }
+            tc_commit(&sf_ready[set]);
+            ++fill;
+            if (++slot == C::STAGES) { slot = 0; phase ^= 1u; }
         }
-    } else if (warp == 1 && lane == 0) {
+        // wait (bounded) for the copies issued above before TMEM is released
+        tc_commit(cp_done);
+        mbar_drain(cp_done, 0);
+    } else if (warp == W_MMA && lane == 0) {
         // =========================== MMA issuer ===========================
         int slot = 0;
         uint32_t phase = 0;
         uint32_t acc_phase = 0;
-        uint32_t fill = 0;                       // stage fills consumed (selects the scale set)
+        uint32_t fill = 0;                       // stages consumed (selects the scale set)
         bool ok = true;
         const uint32_t stage0 = smem_u32(stage_base);
-        for (int64_t t = tile_first; t < total && ok; t += tile_step) {
+        for (int64_t t = first; t < total && ok; t += stride) {
             const Tile tl = sched.get(t);
             if (tl.k_end <= tl.k_begin) continue;
-            if (!mbar_wait<PAIR>(tmem_empty, acc_phase ^ 1u, abort_flag, p.status)) break;
+            if (!mbar_wait(tmem_empty, acc_phase ^ 1u, abort_flag, p.status)) break;
             tc_fence_after();
             const int64_t ks0 = tl.k_begin / C::EPS, ks1 = (tl.k_end + C::EPS - 1) / C::EPS;
             uint32_t accumulate = 0;
             for (int64_t ks = ks0; ks < ks1; ++ks) {
-                const uint32_t set = fill % SF_SETS, use = fill / SF_SETS;
-                if (!mbar_wait<PAIR>(&full_bar[slot], phase, abort_flag, p.status) ||
-                    !mbar_wait<PAIR>(&sf_ready[set], use & 1u, abort_flag, p.status)) {
+                const uint32_t set = fill % C::SF_SETS;
+                if (!mbar_wait(&full_bar[slot], phase, abort_flag, p.status) ||
+                    !mbar_wait(&sf_ready[set], (fill / C::SF_SETS) & 1u, abort_flag, p.status)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const uint32_t sa = stage0 + (uint32_t)slot * C::STAGE_BYTES;
-                const uint32_t sb = sa + C::A_BYTES;
                 const uint64_t adesc0 = smem_desc(sa, 16, 1024, 2);
-                const uint64_t bdesc0 = smem_desc(sb, 16, 1024, 2);
+                const uint64_t bdesc0 = smem_desc(sa + C::A_BYTES, 16, 1024, 2);
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const int64_t kel = ks * C::EPS + (int64_t)j * C::MMA_K;
@@ -625,65 +579,23 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
                     const uint32_t sf_id = FP4 ? 0u : (uint32_t)j;
                     const uint32_t idesc = C::IDESC | (sf_id << 4) | (sf_id << 29);
                     // K advance inside the 128-byte swizzled row: 32 bytes per MMA (encoded >> 4)
-                    tc_mma<FP4, PAIR>(tmem_acc, adesc0 + (uint64_t)(2 * j), bdesc0 + (uint64_t)(2 * j), idesc,
-                                      tmem_sfa(set) + 4 * kg, tmem_sfb(set) + 8 * kg, accumulate);
+                    tc_mma<FP4>(tmem_acc, adesc0 + (uint64_t)(2 * j), bdesc0 + (uint64_t)(2 * j), idesc,
+                                tmem_sfa(set) + 4 * kg, tmem_sfb(set) + 8 * kg, accumulate);
                     accumulate = 1;
                 }
-                tc_commit<PAIR>(&empty_bar[slot], PAIR_MASK);
-                tc_commit<PAIR>(&sf_free[set], 1);
+                tc_commit(&empty_bar[slot]);
+                tc_commit(&sf_free[set]);
                 ++fill;
                 if (++slot == C::STAGES) { slot = 0; phase ^= 1u; }
             }
             if (!ok) break;
-            tc_commit<PAIR>(tmem_full, PAIR_MASK);
+            tc_commit(tmem_full);
             acc_phase ^= 1u;
         }
         // wait (bounded) for every tcgen05 operation issued above before TMEM is released
-        tc_commit<PAIR>(mma_done, 1);
-        mbar_drain<PAIR>(mma_done, 0);
-    } else if (warp == SCALE_WARP && lane == 0 && leader) {
-        // ======================= scale copier =======================
-        // Copies each stage's scale tiles smem -> TMEM into scale set fill % SF_SETS (A's k-group j
-        // at columns [4j, 4j+4) of the set, B's at [8j, 8j+8): two 128-row tiles), so that the
-        // copies of the next fill run while the MMA issuer works on this one. For a pair each CTA's
-        // copy reads its own shared memory into its own TMEM.
-        int slot = 0;
-        uint32_t phase = 0;
-        uint32_t fill = 0;
-        bool ok = true;
-        const uint32_t stage0 = smem_u32(stage_base);
-        for (int64_t t = tile_first; t < total && ok; t += tile_step) {
-            const Tile tl = sched.get(t);
-            if (tl.k_end <= tl.k_begin) continue;
-            const int64_t ks0 = tl.k_begin / C::EPS, ks1 = (tl.k_end + C::EPS - 1) / C::EPS;
-            for (int64_t ks = ks0; ks < ks1; ++ks) {
-                const uint32_t set = fill % SF_SETS, use = fill / SF_SETS;
-                // the stage's scales are in place, and the MMAs of the set's previous use are done
-                if (!mbar_wait<PAIR>(&full_bar[slot], phase, abort_flag, p.status) ||
-                    !mbar_wait<PAIR>(&sf_free[set], (use & 1u) ^ 1u, abort_flag, p.status)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t ssfa = stage0 + (uint32_t)slot * C::STAGE_BYTES + C::A_BYTES + C::B_BYTES;
-                const uint32_t ssfb = ssfa + C::SFA_BYTES;
-#pragma unroll
-                for (int j = 0; j < C::KGS; ++j) {
-                    tc_cp_sf<PAIR>(tmem_sfa(set) + 4 * j, smem_desc(ssfa + j * 512, 0, 128, 0));
-#pragma unroll
-                    for (int h = 0; h < 2; ++h)
-                        tc_cp_sf<PAIR>(tmem_sfb(set) + 8 * j + 4 * h,
-                                       smem_desc(ssfb + (h * C::KGS + j) * 512, 0, 128, 0));
-                }
-                tc_commit<PAIR>(&sf_ready[set], 1);
-                ++fill;
-                if (++slot == C::STAGES) { slot = 0; phase ^= 1u; }
-            }
-        }
-        // wait (bounded) for the copies issued above before TMEM is released
-        tc_commit<PAIR>(cp_done, 1);
-        mbar_drain<PAIR>(cp_done, 0);
-    } else if (warp == 6) {
+        tc_commit(mma_done);
+        mbar_drain(mma_done, 0);
+    } else if (warp == W_TRANSPOSER) {
         // ======================= A-scale transposer =======================
         // A tile starting 32*g0 rows into a 128-row scale tile needs rows [32 g0, 128) of that tile
         // followed by rows [0, 32 g0) of the next. In the 512-byte tile layout line l holds the
@@ -693,11 +605,11 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
         uint32_t sfa_phase = 0;                 // bit s: parity of the next sfa_bar[s] phase
         bool ok = true;
         const uint32_t stage0 = smem_u32(stage_base);
-        for (int64_t t = tile_first; t < total && ok; t += tile_step) {
+        for (int64_t t = first; t < total && ok; t += stride) {
             const Tile tl = sched.get(t);
             if (tl.k_end <= tl.k_begin) continue;
             const int64_t ks0 = tl.k_begin / C::EPS, ks1 = (tl.k_end + C::EPS - 1) / C::EPS;
-            const int g0 = (int)(((tl.a_row0 + row_in_pair) % BM) / 32);
+            const int g0 = (int)((tl.a_row0 % BM) / 32);
             if (g0 == 0) {
                 // aligned tile: the producer loaded the scales in place; only keep the ring position
                 slot = (int)((slot + (ks1 - ks0)) % C::STAGES);
@@ -705,12 +617,10 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
             }
             for (int64_t ks = ks0; ks < ks1; ++ks) {
                 int good = 1;
-                if (lane == 0)
-                    good = mbar_wait<PAIR>(&sfa_bar[slot], (sfa_phase >> slot) & 1u, abort_flag, p.status) ? 1 : 0;
+                if (lane == 0) good = mbar_wait(&sfa_bar[slot], (sfa_phase >> slot) & 1u, abort_flag, p.status) ? 1 : 0;
                 good = __shfl_sync(0xffffffffu, good, 0);
                 if (!good) { ok = false; break; }
-                const uint32_t st = stage0 + (uint32_t)slot * C::STAGE_BYTES;
-                const uint32_t dst = st + C::A_BYTES + C::B_BYTES;
+                const uint32_t dst = stage0 + (uint32_t)slot * C::STAGE_BYTES + C::A_BYTES + C::B_BYTES;
                 const uint32_t raw = dst + C::SFA_BYTES + C::SFB_BYTES;
 #pragma unroll
                 for (int j = 0; j < C::KGS; ++j) {
@@ -737,26 +647,23 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
                 if (++slot == C::STAGES) slot = 0;
             }
         }
-    } else if (warp >= 2 && warp < 6) {
+    } else if (warp >= W_EPI0 && warp < W_EPI0 + 4) {
         // =========================== epilogue ===========================
         const int q = warp & 3;                       // TMEM lane quarter this warp may access
         const int row_in_tile = q * 32 + lane;
         const uint32_t tbase = tmem_acc + ((uint32_t)(q * 32) << 16);
-        // the MMA issuer's tmem_empty barrier (in the even CTA of a pair)
-        const uint32_t empty_addr = PAIR ? mapa_shared(smem_u32(tmem_empty), 0) : 0u;
         uint32_t acc_phase = 0;
-        for (int64_t t = tile_first; t < total; t += tile_step) {
+        for (int64_t t = first; t < total; t += stride) {
             const Tile tl = sched.get(t);
-            const int64_t a_row0 = tl.a_row0 + row_in_pair;
-            const int64_t row = a_row0 + row_in_tile;
+            const int64_t row = tl.a_row0 + row_in_tile;
             const bool row_ok = row < tl.row_end;
-            const int64_t drow = tl.d_row0 + row_in_pair + row_in_tile;
+            const int64_t drow = tl.d_row0 + row_in_tile;
             float scale = 1.0f;
             if (row_ok && p.s_a) scale = p.s_a[row];
             if (p.s_b) scale *= p.s_b[tl.e];
             const bool empty = tl.k_end <= tl.k_begin;
             if (!empty) {
-                if (!mbar_wait<PAIR>(tmem_full, acc_phase, abort_flag, p.status)) break;
+                if (!mbar_wait(tmem_full, acc_phase, abort_flag, p.status)) break;
                 tc_fence_after();
             }
             if (p.out_f32) {
@@ -780,76 +687,71 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
                         reinterpret_cast<float4*>(dst)[j] = v;
                     }
                 }
-            } else {
-                // bf16 output: drain the whole accumulator row into registers as packed bf16 (the
-                // next 32-column load in flight while the current one converts) and hand TMEM back
-                // to the MMA warp before storing, so the stores overlap the next tile's MMAs
-                uint32_t pk[BN / 32][16];
-                if (!empty) {
-                    uint32_t ra[32], rb[32];
-                    tmem_ld32_async(tbase, ra);
-                    tmem_wait_ld(ra);
-#pragma unroll
-                    for (int c = 0; c < BN / 32; c += 2) {
-                        tmem_ld32_async(tbase + (uint32_t)((c + 1) * 32), rb);
-                        pack_scaled(ra, scale, pk[c]);
-                        tmem_wait_ld(rb);
-                        if (c + 2 < BN / 32) tmem_ld32_async(tbase + (uint32_t)((c + 2) * 32), ra);
-                        pack_scaled(rb, scale, pk[c + 1]);
-                        if (c + 2 < BN / 32) tmem_wait_ld(ra);
-                    }
-                } else {
-#pragma unroll
-                    for (int c = 0; c < BN / 32; ++c)
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) pk[c][j] = 0u;
-                }
                 if (!empty) {
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) {
-                        if constexpr (PAIR) mbar_arrive_cluster(empty_addr); else mbar_arrive(tmem_empty);
-                    }
+                    if (lane == 0) mbar_arrive(tmem_empty);
                     acc_phase ^= 1u;
-                }
-                if (row_ok) {
-                    uint16_t* dst = reinterpret_cast<uint16_t*>(p.d) + drow * p.ldd + tl.n0;
-#pragma unroll
-                    for (int c = 0; c < BN / 32; ++c) {
-                        if (tl.n0 + c * 32 >= p.n) break;
-                        if (p.d_aligned32) {
-#pragma unroll
-                            for (int h = 0; h < 2; ++h)
-                                st_v8(dst + c * 32 + h * 16, pk[c][8 * h], pk[c][8 * h + 1], pk[c][8 * h + 2],
-                                      pk[c][8 * h + 3], pk[c][8 * h + 4], pk[c][8 * h + 5], pk[c][8 * h + 6],
-                                      pk[c][8 * h + 7]);
-                        } else {
-#pragma unroll
-                            for (int h = 0; h < 4; ++h)
-                                reinterpret_cast<uint4*>(dst + c * 32)[h] =
-                                    make_uint4(pk[c][4 * h], pk[c][4 * h + 1], pk[c][4 * h + 2], pk[c][4 * h + 3]);
-                        }
-                    }
                 }
                 continue;
             }
+            // bf16 output: drain the whole accumulator row into registers as packed bf16 (the next
+            // 32-column load in flight while the current one converts) and hand TMEM back to the
+            // MMA warp before storing, so the stores overlap the next tile's MMAs
+            uint32_t pk[BN / 32][16];
             if (!empty) {
+                uint32_t ra[32], rb[32];
+                tmem_ld32_async(tbase, ra);
+                tmem_wait_ld(ra);
+#pragma unroll
+                for (int c = 0; c < BN / 32; c += 2) {
+                    tmem_ld32_async(tbase + (uint32_t)((c + 1) * 32), rb);
+                    pack_scaled(ra, scale, pk[c]);
+                    tmem_wait_ld(rb);
+                    if (c + 2 < BN / 32) tmem_ld32_async(tbase + (uint32_t)((c + 2) * 32), ra);
+                    pack_scaled(rb, scale, pk[c + 1]);
+                    if (c + 2 < BN / 32) tmem_wait_ld(ra);
+                }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) {
-                    if constexpr (PAIR) mbar_arrive_cluster(empty_addr); else mbar_arrive(tmem_empty);
-                }
+                if (lane == 0) mbar_arrive(tmem_empty);
                 acc_phase ^= 1u;
+            } else {
+#pragma unroll
+                for (int c = 0; c < BN / 32; ++c)
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) pk[c][j] = 0u;
+            }
+            if (row_ok) {
+                uint16_t* dst = reinterpret_cast<uint16_t*>(p.d) + drow * p.ldd + tl.n0;
+#pragma unroll
+                for (int c = 0; c < BN / 32; ++c) {
+                    if (tl.n0 + c * 32 >= p.n) break;
+                    if (p.d_aligned32) {
+#pragma unroll
+                        for (int h = 0; h < 2; ++h)
+                            st_v8(dst + c * 32 + h * 16, pk[c][8 * h], pk[c][8 * h + 1], pk[c][8 * h + 2],
+                                  pk[c][8 * h + 3], pk[c][8 * h + 4], pk[c][8 * h + 5], pk[c][8 * h + 6],
+                                  pk[c][8 * h + 7]);
+                    } else {
+#pragma unroll
+                        for (int h = 0; h < 4; ++h)
+                            reinterpret_cast<uint4*>(dst + c * 32)[h] =
+                                make_uint4(pk[c][4 * h], pk[c][4 * h + 1], pk[c][4 * h + 2], pk[c][4 * h + 3]);
+                    }
+                }
             }
         }
     }
 
-    // teardown: every role of both CTAs is done (and the MMA issuer has drained its tcgen05 work)
-    // before the pair frees its TMEM and its shared memory goes away
+    // teardown: every role is done (and has drained the asynchronous work it issued)
     tc_fence_before();
-    if constexpr (PAIR) cluster_sync(); else __syncthreads();
+    __syncthreads();
     tc_fence_after();
-    if (warp == 1) tmem_dealloc<PAIR>(tmem_base);
+    if (warp == W_MMA) {
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
+                     : "memory");
+    }
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -894,14 +796,14 @@ static int num_sms() {
     return n;
 }
 
-template <bool FP4, bool PAIR>
+template <bool FP4>
 static nvq_status launch_gemm(const nvq_gemm_args* a, cudaStream_t stream) {
-    using C = GemmCfg<FP4, PAIR>;
+    using C = GemmCfg<FP4>;
     const int64_t row_bytes = FP4 ? a->k / 2 : a->k;
     const int64_t rows_a = a->m;
     const int64_t rows_b = (a->mode == NVQ_GEMM_GROUP_M) ? a->groups * a->n : a->n;
     CUtensorMap ta, tb;
-    if (!make_tmap(&ta, a->a, rows_a, row_bytes, BM) || !make_tmap(&tb, a->b, rows_b, row_bytes, C::B_ROWS))
+    if (!make_tmap(&ta, a->a, rows_a, row_bytes, BM) || !make_tmap(&tb, a->b, rows_b, row_bytes, BN))
         return NVQ_ERR_CUDA;
     GemmParams p;
     p.mode = a->mode;
@@ -924,58 +826,16 @@ static nvq_status launch_gemm(const nvq_gemm_args* a, cudaStream_t stream) {
     const int64_t kb = a->k / (FP4 ? 16 : 32);
     p.sf_tiles_per_row = (kb + 3) / 4;
 
-    // one-time setup per kernel instance: shared-memory opt-in and the persistent grid (for pairs,
-    // as many 2-CTA clusters as the GPU can hold at once)
-    static int grid_cache = 0;
+    static bool attr_ok = false;
     static std::once_flag once;
     std::call_once(once, [] {
-        if (cudaFuncSetAttribute(block_scaled_gemm_kernel<FP4, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)C::SMEM_BYTES) != cudaSuccess)
-            return;
-        const int sms = num_sms();
-        if (!PAIR) {
-            grid_cache = sms;
-            return;
-        }
-        cudaLaunchConfig_t cfg = {};
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.gridDim = dim3(2 * (sms / 2), 1, 1);
-        cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
-        cfg.dynamicSmemBytes = C::SMEM_BYTES;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        int clusters = 0;
-        if (cudaOccupancyMaxActiveClusters(&clusters, block_scaled_gemm_kernel<FP4, PAIR>, &cfg) != cudaSuccess ||
-            clusters <= 0) {
-            (void)cudaGetLastError();
-            return;
-        }
-        grid_cache = 2 * min(clusters, sms / 2);
+        attr_ok = cudaFuncSetAttribute(block_scaled_gemm_kernel<FP4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)C::SMEM_BYTES) == cudaSuccess;
     });
-    const int grid = grid_cache;
+    if (!attr_ok) return NVQ_ERR_CUDA;
+    const int grid = num_sms();
     if (grid <= 0) return NVQ_ERR_CUDA;
-    if constexpr (PAIR) {
-        cudaLaunchConfig_t cfg = {};
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.gridDim = dim3(grid, 1, 1);
-        cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
-        cfg.dynamicSmemBytes = C::SMEM_BYTES;
-        cfg.stream = stream;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        if (cudaLaunchKernelEx(&cfg, block_scaled_gemm_kernel<FP4, PAIR>, ta, tb, p) != cudaSuccess)
-            return NVQ_ERR_CUDA;
-    } else {
-        block_scaled_gemm_kernel<FP4, PAIR><<<grid, GEMM_THREADS, C::SMEM_BYTES, stream>>>(ta, tb, p);
-    }
+    block_scaled_gemm_kernel<FP4><<<grid, GEMM_THREADS, C::SMEM_BYTES, stream>>>(ta, tb, p);
     if (cudaGetLastError() != cudaSuccess) return NVQ_ERR_CUDA;
     count_launches(1);
     return NVQ_OK;
@@ -990,8 +850,7 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 extern "C" nvq_status block_scaled_grouped_gemm(const nvq_gemm_args* a, void* stream) {
     if (a == nullptr) return NVQ_ERR_INVALID_ARG;
     if ((a->fmt != NVQ_MXFP8 && a->fmt != NVQ_NVFP4) || (a->mode != NVQ_GEMM_GROUP_M && a->mode != NVQ_GEMM_GROUP_K) ||
-        (a->out_type != NVQ_OUT_BF16 && a->out_type != NVQ_OUT_F32) ||
-        (a->tiles != NVQ_TILES_AUTO && a->tiles != NVQ_TILES_128 && a->tiles != NVQ_TILES_256))
+        (a->out_type != NVQ_OUT_BF16 && a->out_type != NVQ_OUT_F32))
         return NVQ_ERR_INVALID_ARG;
     if (a->groups < 0 || a->m < 0 || a->n < 0 || a->k < 0) return NVQ_ERR_INVALID_ARG;
     if (a->groups == 0 || a->m == 0 || a->n == 0) return NVQ_OK;
@@ -1011,11 +870,5 @@ extern "C" nvq_status block_scaled_grouped_gemm(const nvq_gemm_args* a, void* st
         (reinterpret_cast<uintptr_t>(a->offsets) & 7u))
         return NVQ_ERR_MISALIGNED;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // Measured on GB300 (dense 8192x5120x2048 and the 128-expert MoE shapes), the 256-row pair
-    // tiles run slower than 128-row tiles: the pair's stage ring couples two SMs, and every stage
-    // then waits on the slower SM's copies plus a cross-SM hop. AUTO therefore takes 128-row tiles.
-    const bool pair = a->tiles == NVQ_TILES_256;
-    if (a->fmt == NVQ_NVFP4)
-        return pair ? nvq::launch_gemm<true, true>(a, s) : nvq::launch_gemm<true, false>(a, s);
-    return pair ? nvq::launch_gemm<false, true>(a, s) : nvq::launch_gemm<false, false>(a, s);
+    return a->fmt == NVQ_NVFP4 ? nvq::launch_gemm<true>(a, s) : nvq::launch_gemm<false>(a, s);
 }

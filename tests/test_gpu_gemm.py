@@ -48,7 +48,7 @@ def _routed(counts, k, seed, scale_rows=True):
 # ------------------------------------------------------------------------------------------------
 # forward / data-gradient (rows grouped by expert)
 # ------------------------------------------------------------------------------------------------
-def _run_m(nvq, fmt, counts, K, N, seed, out_type, tiles=0):
+def _run_m(nvq, fmt, counts, K, N, seed, out_type):
     E = len(counts)
     offs, xb = _routed(counts, K, seed)
     rng = np.random.default_rng(seed + 1)
@@ -62,7 +62,7 @@ def _run_m(nvq, fmt, counts, K, N, seed, out_type, tiles=0):
         qa, sfa, sa = nvq.nvfp4_quantize_per_token(x, sf_layout="mma")
         qb, sfb, sb = nvq.nvfp4_quantize_weights(w.contiguous(), sf_layout="mma")
         d = nvq.block_scaled_grouped_gemm(nvq.NVFP4, nvq.GEMM_GROUP_M, qa, sfa, qb, sfb, offs_d, m=M, n=N, k=K,
-                                          groups=E, s_a=sa, s_b=sb, out_type=out_type, status=status, tiles=tiles)
+                                          groups=E, s_a=sa, s_b=sb, out_type=out_type, status=status)
         qa_r, sfa_r, sa_r = oracle.nvfp4_quantize_per_token(xb)
         qb_r, sfb_r, sb_r = oracle.nvfp4_quantize_weights(wb)
         a = oracle.deq_operand("nvfp4", qa_r, sfa_r)
@@ -75,7 +75,7 @@ def _run_m(nvq, fmt, counts, K, N, seed, out_type, tiles=0):
         qb = nvq.mxfp8_quantize(wt, colwise=False, sf_layout="mma")
         d = nvq.block_scaled_grouped_gemm(nvq.MXFP8, nvq.GEMM_GROUP_M, qa["q_row"], qa["sf_row"], qb["q_row"],
                                           qb["sf_row"], offs_d, m=M, n=N, k=K, groups=E, out_type=out_type,
-                                          status=status, tiles=tiles)
+                                          status=status)
         ra = oracle.mxfp8_quantize(xb, colwise=False)
         a = oracle.deq_operand("mxfp8", ra["q_row"], ra["sf_row"])
         b = []
@@ -89,69 +89,31 @@ def _run_m(nvq, fmt, counts, K, N, seed, out_type, tiles=0):
     _check(d[torch.from_numpy(rows).cuda()], D[rows], bound[rows], out_type == nvq.OUT_BF16)
 
 
-TILES = {"t128": 1, "t256": 2}
-
-
-@pytest.mark.parametrize("tiles", sorted(TILES))
 @pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4"])
 @pytest.mark.parametrize("out", ["f32", "bf16"])
-def test_contract_shape_single_group(nvq, fmt, out, tiles):
+def test_contract_shape_single_group(nvq, fmt, out):
     # 256 x 512 by 512 x 384: one group, N not a multiple of the 256-column tile
-    _run_m(nvq, fmt, [256], 512, 384, seed=0, out_type=nvq.OUT_F32 if out == "f32" else nvq.OUT_BF16,
-           tiles=TILES[tiles])
+    _run_m(nvq, fmt, [256], 512, 384, seed=0, out_type=nvq.OUT_F32 if out == "f32" else nvq.OUT_BF16)
 
 
-@pytest.mark.parametrize("tiles", sorted(TILES))
 @pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4"])
 @pytest.mark.parametrize("counts,K,N", [
     ([96, 0, 160, 33, 300], 256, 256),       # group starts at 32-row offsets inside scale tiles
     ([1, 31, 64, 0, 0, 129], 384, 512),      # K ragged against the FP4 stage (384 = 256 + 128)
     ([200, 77], 768, 384),
     ([0, 0, 0], 256, 256),                   # nothing to do
-    ([40], 256, 256),                        # 256-row tile: the second SM's rows all past the buffer
-    ([300, 40], 512, 256),                   # ... and starting inside a scale tile (rows 448..575)
+    ([40], 256, 256),                        # a single small group
+    ([300, 40], 512, 256),                   # the last tile starts inside a scale tile
 ])
-def test_grouped_rows(nvq, fmt, counts, K, N, tiles):
-    _run_m(nvq, fmt, counts, K, N, seed=sum(counts) + K, out_type=nvq.OUT_F32, tiles=TILES[tiles])
-
-
-@pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4"])
-def test_tilings_agree_bitwise(nvq, fmt):
-    # 128-row and 256-row tiles run the same MMA k-sequence for every output element: equal bits
-    counts = [700, 0, 33, 520, 96, 1000]
-    K, N = 1024, 768
-    E = len(counts)
-    offs, xb = _routed(counts, K, seed=11)
-    rng = np.random.default_rng(12)
-    x = workloads.from_bits(xb, "cuda")
-    w = workloads.from_bits(_bits(rng.standard_normal((E, K, N)) * 0.02), "cuda")
-    M = x.shape[0]
-    offs_d = torch.from_numpy(offs).cuda()
-    if fmt == "nvfp4":
-        qa, sfa, sa = nvq.nvfp4_quantize_per_token(x)
-        qb, sfb, sb = nvq.nvfp4_quantize_weights(w.contiguous())
-        args = (nvq.NVFP4, nvq.GEMM_GROUP_M, qa, sfa, qb, sfb, offs_d)
-        kw = dict(s_a=sa, s_b=sb)
-    else:
-        qa = nvq.mxfp8_quantize(x, colwise=False)
-        qb = nvq.mxfp8_quantize(w.transpose(1, 2).contiguous().view(E * N, K), colwise=False)
-        args = (nvq.MXFP8, nvq.GEMM_GROUP_M, qa["q_row"], qa["sf_row"], qb["q_row"], qb["sf_row"], offs_d)
-        kw = {}
-    outs = []
-    for tiles in (1, 2):
-        d = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
-        nvq.block_scaled_grouped_gemm(*args, m=M, n=N, k=K, groups=E, out=d, out_type=nvq.OUT_F32, tiles=tiles, **kw)
-        outs.append(d)
-    torch.cuda.synchronize()
-    a, b = outs                       # every buffer row belongs to a group (padded offsets)
-    assert not torch.isnan(a).any()
-    assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+def test_grouped_rows(nvq, fmt, counts, K, N):
+    _run_m(nvq, fmt, counts, K, N, seed=sum(counts) + K, out_type=nvq.OUT_F32)
 
 
 @pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4"])
 def test_many_tiles_per_cta(nvq, fmt):
     # More tiles than CTAs: each CTA runs several tiles, so every stage ring wraps repeatedly, with
-    # tiles starting inside a scale tile (32-row group offsets) mixed among aligned ones.
+    # tiles starting inside a scale tile (32-row group offsets) mixed among aligned ones, and the
+    # scale ring runs ahead of the operand ring across tile boundaries.
     counts = [150, 33, 260, 0, 121, 97, 201, 64, 180, 5, 140, 230]
     E, K, N = len(counts), 1024, 2560
     offs, xb = _routed(counts, K, seed=21)
@@ -182,20 +144,14 @@ def test_many_tiles_per_cta(nvq, fmt):
                                                                           rowwise=False).values())
                       for e in range(E)])
         D, bound = oracle.grouped_gemm_reference("m", a, b, offs)
-    outs = []
-    for tiles in (1, 2):
-        status = torch.zeros(1, dtype=torch.int32, device="cuda")
-        d = nvq.block_scaled_grouped_gemm(*args, m=M, n=N, k=K, groups=E, out_type=nvq.OUT_F32, status=status,
-                                          tiles=tiles, **kw)
-        torch.cuda.synchronize()
-        assert int(status.item()) == 0
-        _check(d, D, bound, False)
-        outs.append(d)
-    assert torch.equal(outs[0].view(torch.int32), outs[1].view(torch.int32))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    d = nvq.block_scaled_grouped_gemm(*args, m=M, n=N, k=K, groups=E, out_type=nvq.OUT_F32, status=status, **kw)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    _check(d, D, bound, False)
 
 
-@pytest.mark.parametrize("tiles", [1, 2])
-def test_rows_outside_groups_untouched(nvq, tiles):
+def test_rows_outside_groups_untouched(nvq):
     E, K, N = 2, 256, 256
     counts = [40, 20]
     offs = np.array([0, 64, 96], dtype=np.int64)       # 96 of 160 buffer rows belong to groups
@@ -207,16 +163,14 @@ def test_rows_outside_groups_untouched(nvq, tiles):
     qb, sfb, sb = nvq.nvfp4_quantize_weights(workloads.from_bits(wb, "cuda").contiguous(), sf_layout="mma")
     d = torch.full((160, N), 7.0, dtype=torch.float32, device="cuda")
     nvq.block_scaled_grouped_gemm(nvq.NVFP4, nvq.GEMM_GROUP_M, qa, sfa, qb, sfb, torch.from_numpy(offs).cuda(),
-                                  m=160, n=N, k=K, groups=E, s_a=sa, s_b=sb, out=d, out_type=nvq.OUT_F32,
-                                  tiles=tiles)
+                                  m=160, n=N, k=K, groups=E, s_a=sa, s_b=sb, out=d, out_type=nvq.OUT_F32)
     torch.cuda.synchronize()
     assert torch.all(d[96:] == 7.0)
     assert not torch.all(d[:96] == 7.0)
     del counts
 
 
-@pytest.mark.parametrize("tiles", [1, 2])
-def test_bad_offsets_set_status_and_write_nothing(nvq, tiles):
+def test_bad_offsets_set_status_and_write_nothing(nvq):
     K, N = 256, 256
     x = workloads.normal_bf16((64, K), device="cuda")
     w = workloads.normal_bf16((1, K, N), 0.02, device="cuda")
@@ -227,8 +181,7 @@ def test_bad_offsets_set_status_and_write_nothing(nvq, tiles):
         status = torch.zeros(1, dtype=torch.int32, device="cuda")
         nvq.block_scaled_grouped_gemm(nvq.NVFP4, nvq.GEMM_GROUP_M, qa, sfa, qb, sfb,
                                       torch.tensor(bad, dtype=torch.int64, device="cuda"), m=64, n=N, k=K,
-                                      groups=1, s_a=sa, s_b=sb, out=d, out_type=nvq.OUT_F32, status=status,
-                                      tiles=tiles)
+                                      groups=1, s_a=sa, s_b=sb, out=d, out_type=nvq.OUT_F32, status=status)
         torch.cuda.synchronize()
         assert int(status.item()) == nvq.DEV_BAD_OFFSETS
         assert torch.all(d == 3.0)
@@ -248,10 +201,9 @@ def test_host_rejects_bad_shapes(nvq):
 # ------------------------------------------------------------------------------------------------
 # weight gradient (reduction grouped by expert), MXFP8 columnwise copies
 # ------------------------------------------------------------------------------------------------
-@pytest.mark.parametrize("tiles", [1, 2])
 @pytest.mark.parametrize("counts,Kin,Nout", [([64, 0, 96, 200], 256, 256), ([33, 300], 128, 384),
                                              ([500, 40], 384, 256)])
-def test_weight_gradient_grouped_k(nvq, counts, Kin, Nout, tiles):
+def test_weight_gradient_grouped_k(nvq, counts, Kin, Nout):
     offs, xb = _routed(counts, Kin, seed=5)
     rng = np.random.default_rng(6)
     dy = rng.standard_normal((int(offs[-1]), Nout)) * 1e-3
@@ -266,7 +218,7 @@ def test_weight_gradient_grouped_k(nvq, counts, Kin, Nout, tiles):
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     d = nvq.block_scaled_grouped_gemm(nvq.MXFP8, nvq.GEMM_GROUP_K, qx["q_colT"], qx["sf_colT"], qg["q_colT"],
                                       qg["sf_colT"], torch.from_numpy(offs).cuda(), m=Kin, n=Nout, k=Mtot,
-                                      groups=E, out_type=nvq.OUT_F32, status=status, tiles=tiles)
+                                      groups=E, out_type=nvq.OUT_F32, status=status)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     rx = oracle.mxfp8_quantize(xb, rowwise=False)
@@ -284,8 +236,7 @@ def _sample_pairs(rng, rows, n, count):
     return rng.choice(rows, count), rng.integers(0, n, count)
 
 
-@pytest.mark.parametrize("tiles", [0, 1])
-def test_full_size_dense_mxfp8_sampled(nvq, tiles):
+def test_full_size_dense_mxfp8_sampled(nvq):
     inp = workloads.dense_inputs(seed=0, device="cuda")
     x, w = inp["x"], inp["w"]
     M, K = x.shape
@@ -294,7 +245,7 @@ def test_full_size_dense_mxfp8_sampled(nvq, tiles):
     qb = nvq.mxfp8_quantize(w, rowwise=False)          # columnwise of W: [N, K], blocks along K
     offs = torch.tensor([0, M], dtype=torch.int64, device="cuda")
     d = nvq.block_scaled_grouped_gemm(nvq.MXFP8, nvq.GEMM_GROUP_M, qa["q_row"], qa["sf_row"], qb["q_colT"],
-                                      qb["sf_colT"], offs, m=M, n=N, k=K, groups=1, tiles=tiles)
+                                      qb["sf_colT"], offs, m=M, n=N, k=K, groups=1)
     torch.cuda.synchronize()
     rng = np.random.default_rng(0)
     ii, jj = _sample_pairs(rng, M, N, 2048)
