@@ -18,17 +18,6 @@ namespace nvq {
 constexpr int TOK_THREADS = 256;          // 8 rows per CTA
 constexpr int TOK_NREG = 4;               // 4 x 32 blocks of 16 = 2048 elements held in registers per row
 
-__device__ __forceinline__ void store_sf_group(uint8_t* sf, int64_t row, int64_t kb0, int64_t nkb,
-                                               uint32_t word, int mma_layout) {
-    if (mma_layout) {
-        *reinterpret_cast<uint32_t*>(sf + mma_sf_offset(row, kb0, nkb)) = word;
-    } else {
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            if (kb0 + j < nkb) sf[row * nkb + kb0 + j] = (uint8_t)(word >> (8 * j));
-    }
-}
-
 template <bool V8>
 __device__ __forceinline__ void load_block(const uint16_t* p, uint4& a, uint4& b) {
     if (V8) {
@@ -39,22 +28,53 @@ __device__ __forceinline__ void load_block(const uint16_t* p, uint4& a, uint4& b
     }
 }
 
-// One 16-element block per lane: block kb = 32 i + lane of the row.
-__device__ __forceinline__ void token_block(const uint4& a, const uint4& b, int i, int lane, int64_t row,
-                                            bool real, int64_t nkb, int64_t C, const Nvfp4Scope& sc,
-                                            uint8_t* __restrict__ q, uint8_t* __restrict__ sf, int mma_layout) {
-    const int64_t kb = (int64_t)i * 32 + lane;
-    const uint32_t mb = max(absmax_bits_8(a), absmax_bits_8(b));
-    const uint32_t sfc = nvfp4_block_scale(__uint_as_float(mb << 16), sc);
+// Scale code and the 16 codes of one block (two uint4 of 8 bf16, magnitude maximum mb as bf16
+// bits): table-driven in the fast path, exact fp64 decisions for a scope with a tiny (or zero)
+// coarse scale.
+__device__ __forceinline__ uint32_t encode_block(const uint4& a, const uint4& b, uint32_t mb, const Nvfp4Scope& sc,
+                                                 const Nvfp4Table& T, uint32_t& c0, uint32_t& c1) {
+    uint32_t sfc;
     E2M1Bounds bd;
-    if (sfc != 0u && !sc.exact) bd = nvfp4_bounds(sfc, sc);
-    const uint32_t c0 = nvfp4_encode8(a, sfc, sc, bd);
-    const uint32_t c1 = nvfp4_encode8(b, sfc, sc, bd);
-    if (real && kb < nkb) *reinterpret_cast<uint2*>(q + row * (C >> 1) + kb * 8) = make_uint2(c0, c1);
+    if (!sc.exact) {
+        sfc = nvfp4_block_scale_t(mb, sc, T);
+        if (sfc != 0u) bd = nvfp4_block_bounds_t(sfc, T);
+    } else {
+        sfc = nvfp4_block_scale(__uint_as_float(mb << 16), sc);
+    }
+    c0 = nvfp4_encode8(a, sfc, sc, bd);
+    c1 = nvfp4_encode8(b, sfc, sc, bd);
+    return sfc;
+}
+
+// Where one token row's outputs go: its packed codes and its scale bytes (canonical row, or the
+// row's place in the MMA tile layout, to which a 4-block group adds (kb / 4) * 512).
+struct TokenRowOut {
+    uint8_t* q;          // row of packed codes
+    uint8_t* sf;         // canonical: row of scale bytes; MMA: row's base inside its tile column
+    int64_t nkb;
+    int mma_layout;
+};
+
+// One 16-element block per lane: block kb = 32 i + lane of the row.
+__device__ __forceinline__ void token_block(const uint4& a, const uint4& b, uint32_t mb, int i, int lane, bool real,
+                                            const Nvfp4Scope& sc, const Nvfp4Table& T, const TokenRowOut& o) {
+    const int64_t kb = (int64_t)i * 32 + lane;
+    uint32_t c0, c1;
+    const uint32_t sfc = encode_block(a, b, mb, sc, T, c0, c1);
+    if (real && kb < o.nkb) *reinterpret_cast<uint2*>(o.q + kb * 8) = make_uint2(c0, c1);
     const uint32_t s1 = __shfl_down_sync(0xffffffffu, sfc, 1);
     const uint32_t s2 = __shfl_down_sync(0xffffffffu, sfc, 2);
     const uint32_t s3 = __shfl_down_sync(0xffffffffu, sfc, 3);
-    if ((lane & 3) == 0 && kb < nkb) store_sf_group(sf, row, kb, nkb, sfc | (s1 << 8) | (s2 << 16) | (s3 << 24), mma_layout);
+    if ((lane & 3) == 0 && kb < o.nkb) {
+        const uint32_t word = sfc | (s1 << 8) | (s2 << 16) | (s3 << 24);
+        if (o.mma_layout) {
+            *reinterpret_cast<uint32_t*>(o.sf + ((kb >> 2) << 9)) = word;
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (kb + j < o.nkb) o.sf[kb + j] = (uint8_t)(word >> (8 * j));
+        }
+    }
 }
 
 // One warp per token row, one 16-element block per lane per step: the row (up to 2048 elements) is
@@ -65,9 +85,11 @@ __global__ void __launch_bounds__(TOK_THREADS)
 nvfp4_token_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t C, int64_t ldx,
                    uint8_t* __restrict__ q, uint8_t* __restrict__ sf, float* __restrict__ s_tok,
                    int mma_layout, int64_t rows_cover) {
+    __shared__ Nvfp4Table tables[TOK_THREADS / 32];          // one per warp (token row)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t row = (int64_t)blockIdx.x * (TOK_THREADS / 32) + warp;
     if (row >= rows_cover) return;
+    Nvfp4Table& T = tables[warp];
     const bool real = row < R;
     const int64_t nkb = C >> 4;                          // 16-element blocks
     const int iters = (int)((nkb + 31) >> 5);
@@ -75,13 +97,15 @@ nvfp4_token_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t C, int64_t
 
     // pass 1: load (into registers where possible) and reduce the row's amax
     uint4 va[TOK_NREG], vb[TOK_NREG];
+    uint32_t mbk[TOK_NREG];                              // block maxima of the register-resident blocks
     uint32_t m = 0;
 #pragma unroll
     for (int i = 0; i < TOK_NREG; ++i) {
         va[i] = vb[i] = make_uint4(0u, 0u, 0u, 0u);
         const int64_t kb = (int64_t)i * 32 + lane;
         if (real && i < iters && kb < nkb) load_block<V8>(xr + kb * 16, va[i], vb[i]);
-        m = max(m, max(absmax_bits_8(va[i]), absmax_bits_8(vb[i])));
+        mbk[i] = max(absmax_bits_8(va[i]), absmax_bits_8(vb[i]));
+        m = max(m, mbk[i]);
     }
     for (int i = TOK_NREG; i < iters; ++i) {
         const int64_t kb = (int64_t)i * 32 + lane;
@@ -96,16 +120,23 @@ nvfp4_token_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t C, int64_t
     const float s = nvfp4_coarse_scale(__uint_as_float(m << 16));
     const Nvfp4Scope sc = make_nvfp4_scope(s);
     if (real && lane == 0) s_tok[row] = s;
+    if (!sc.exact) nvfp4_table_build_warp(T, s, lane);
+    __syncwarp();
 
     // pass 2: per 1x16 block scale and codes (register-resident blocks first, then any reloads)
+    TokenRowOut o;
+    o.q = q + row * (C >> 1);
+    o.nkb = nkb;
+    o.mma_layout = mma_layout;
+    o.sf = mma_layout ? sf + mma_sf_offset(row, 0, nkb) : sf + row * nkb;
 #pragma unroll
     for (int i = 0; i < TOK_NREG; ++i)
-        if (i < iters) token_block(va[i], vb[i], i, lane, row, real, nkb, C, sc, q, sf, mma_layout);
+        if (i < iters) token_block(va[i], vb[i], mbk[i], i, lane, real, sc, T, o);
     for (int i = TOK_NREG; i < iters; ++i) {
         const int64_t kb = (int64_t)i * 32 + lane;
         uint4 a = make_uint4(0u, 0u, 0u, 0u), b = a;
         if (real && kb < nkb) load_block<V8>(xr + kb * 16, a, b);
-        token_block(a, b, i, lane, row, real, nkb, C, sc, q, sf, mma_layout);
+        token_block(a, b, max(absmax_bits_8(a), absmax_bits_8(b)), i, lane, real, sc, T, o);
     }
 }
 
@@ -157,6 +188,7 @@ nvfp4_weight_encode_kernel(const uint16_t* __restrict__ w, int64_t K, int64_t N,
                            uint8_t* __restrict__ qT, uint8_t* __restrict__ sfT,
                            const uint32_t* __restrict__ amax_bits, int mma_layout) {
     __shared__ __align__(16) uint32_t tile[WT_K][WT_N / 2];
+    __shared__ Nvfp4Table T;                                   // the expert matrix's scope table
 
     const int64_t e = blockIdx.z;
     const int64_t k0 = (int64_t)blockIdx.y * WT_K, n0 = (int64_t)blockIdx.x * WT_N;
@@ -171,12 +203,13 @@ nvfp4_weight_encode_kernel(const uint16_t* __restrict__ w, int64_t K, int64_t N,
         if (k < K && n < N) val = ld_stream_v4(we + k * N + n);
         *reinterpret_cast<uint4*>(&tile[rr][(chunk ^ ((rr >> 4) & 3)) * 4]) = val;
     }
+    const float s = nvfp4_coarse_scale(__uint_as_float(amax_bits[e]));
+    const Nvfp4Scope sc = make_nvfp4_scope(s);
+    if (!sc.exact && threadIdx.x < 32) nvfp4_table_build_warp(T, s, threadIdx.x);
     __syncthreads();
 
     const int kblk = threadIdx.x & 3, nl = threadIdx.x >> 2;       // 4 consecutive lanes = one n
     const int64_t n = n0 + nl;
-    const float s = nvfp4_coarse_scale(__uint_as_float(amax_bits[e]));
-    const Nvfp4Scope sc = make_nvfp4_scope(s);
     // gather the 16 k-values of column nl: element j of the block is row 16*kblk + j
     const int wcol = ((nl >> 1) >> 2), wsub = (nl >> 1) & 3;      // 16-byte chunk and word in it
     const int half = nl & 1;
@@ -191,12 +224,8 @@ nvfp4_weight_encode_kernel(const uint16_t* __restrict__ w, int64_t K, int64_t N,
         p[j] = ea | (eb << 16);
     }
     const uint4 lo = make_uint4(p[0], p[1], p[2], p[3]), hi = make_uint4(p[4], p[5], p[6], p[7]);
-    const uint32_t mb = max(absmax_bits_8(lo), absmax_bits_8(hi));
-    const uint32_t sfc = nvfp4_block_scale(__uint_as_float(mb << 16), sc);
-    E2M1Bounds bd;
-    if (sfc != 0u && !sc.exact) bd = nvfp4_bounds(sfc, sc);
-    const uint32_t c0 = nvfp4_encode8(lo, sfc, sc, bd);
-    const uint32_t c1 = nvfp4_encode8(hi, sfc, sc, bd);
+    uint32_t c0, c1;
+    const uint32_t sfc = encode_block(lo, hi, max(absmax_bits_8(lo), absmax_bits_8(hi)), sc, T, c0, c1);
     const int64_t kb = (k0 >> 4) + kblk, nkb = K >> 4;
     if (n < N && kb < nkb) {
         *reinterpret_cast<uint2*>(qT + (e * N + n) * (K >> 1) + kb * 8) = make_uint2(c0, c1);
