@@ -49,11 +49,11 @@ L2_FLUSH_BYTES = 256 << 20
 NCU_TRAFFIC = {
     "dense": {
         "mxfp8_quantize X row+col": {"bytes": 33600000, "src_sha": "3352a1d55c39ef58"},
-        "mxfp8_quantize W col": {"bytes": 21000000, "src_sha": "3352a1d55c39ef58"},
-        "nvfp4_quantize_per_token X": {"bytes": 33610000, "src_sha": "a0f791a42e9522ac"},
-        "nvfp4_quantize_weights W": {"bytes": 41980000, "src_sha": "a0f791a42e9522ac"},
-        "block_scaled_gemm MXFP8": {"bytes": 58490000, "src_sha": "cdf0360aff984fab"},
-        "block_scaled_gemm NVFP4": {"bytes": 42680000, "src_sha": "cdf0360aff984fab"},
+        "mxfp8_quantize W col": {"bytes": 21010000, "src_sha": "3352a1d55c39ef58"},
+        "nvfp4_quantize_per_token X": {"bytes": 33600000, "src_sha": "ef6116dee65ea977"},
+        "nvfp4_quantize_weights W": {"bytes": 41970000, "src_sha": "ef6116dee65ea977"},
+        "block_scaled_gemm MXFP8": {"bytes": 56980000, "src_sha": "437f71369e033858"},
+        "block_scaled_gemm NVFP4": {"bytes": 41770000, "src_sha": "437f71369e033858"},
         "dequantize_bf16 W": {"bytes": 5910000, "src_sha": "def12a43bb80c45b"},
     },
     "quant": {
