@@ -58,7 +58,7 @@ NCU_TRAFFIC = {
     },
     "quant": {
         "mxfp8_quantize X row+col": {"bytes": 1050810000, "src_sha": "3352a1d55c39ef58"},
-        "nvfp4_quantize_per_token X": {"bytes": 679180000, "src_sha": "a0f791a42e9522ac"},
+        "nvfp4_quantize_per_token X": {"bytes": 677110000, "src_sha": "ef6116dee65ea977"},
     },
 }
 

@@ -10,12 +10,15 @@
 //
 // Per-token design: one warp per token row, one 16-element block per lane per step (see the
 // kernel). Weights: one thread per (column, 16-row block) after a shared-memory transpose.
+#include <algorithm>
+#include <mutex>
+
 #include "nvq_device.cuh"
 #include "nvq_internal.h"
 
 namespace nvq {
 
-constexpr int TOK_THREADS = 256;          // 8 rows per CTA
+constexpr int TOK_THREADS = 128;          // 4 rows per CTA
 constexpr int TOK_NREG = 4;               // 4 x 32 blocks of 16 = 2048 elements held in registers per row
 
 template <bool V8>
@@ -29,20 +32,22 @@ __device__ __forceinline__ void load_block(const uint16_t* p, uint4& a, uint4& b
 }
 
 // Scale code and the 16 codes of one block (two uint4 of 8 bf16, magnitude maximum mb as bf16
-// bits): table-driven in the fast path, exact fp64 decisions for a scope with a tiny (or zero)
-// coarse scale.
+// bits): table-driven and branch-free in the fast path; exact fp64 decisions for a scope with a
+// tiny (or zero) coarse scale.
+template <bool EXACT>
 __device__ __forceinline__ uint32_t encode_block(const uint4& a, const uint4& b, uint32_t mb, const Nvfp4Scope& sc,
-                                                 const Nvfp4Table& T, uint32_t& c0, uint32_t& c1) {
-    uint32_t sfc;
-    E2M1Bounds bd;
-    if (!sc.exact) {
-        sfc = nvfp4_block_scale_t(mb, sc, T);
-        if (sfc != 0u) bd = nvfp4_block_bounds_t(sfc, T);
-    } else {
-        sfc = nvfp4_block_scale(__uint_as_float(mb << 16), sc);
+                                                 const Nvfp4Table& T, const Nvfp4CodeInfo& I, uint32_t& c0,
+                                                 uint32_t& c1) {
+    if (EXACT) {
+        const uint32_t sfc = nvfp4_block_scale(__uint_as_float(mb << 16), sc);
+        c0 = nvfp4_encode8_exact(a, sfc, sc);
+        c1 = nvfp4_encode8_exact(b, sfc, sc);
+        return sfc;
     }
-    c0 = nvfp4_encode8(a, sfc, sc, bd);
-    c1 = nvfp4_encode8(b, sfc, sc, bd);
+    const uint32_t sfc = nvfp4_block_scale_t(mb, sc, T);
+    const E2M1Bounds bd = nvfp4_block_bounds_t(sfc, T, I);
+    c0 = nvfp4_codes8(a, bd);
+    c1 = nvfp4_codes8(b, bd);
     return sfc;
 }
 
@@ -56,11 +61,13 @@ struct TokenRowOut {
 };
 
 // One 16-element block per lane: block kb = 32 i + lane of the row.
+template <bool EXACT>
 __device__ __forceinline__ void token_block(const uint4& a, const uint4& b, uint32_t mb, int i, int lane, bool real,
-                                            const Nvfp4Scope& sc, const Nvfp4Table& T, const TokenRowOut& o) {
+                                            const Nvfp4Scope& sc, const Nvfp4Table& T, const Nvfp4CodeInfo& I,
+                                            const TokenRowOut& o) {
     const int64_t kb = (int64_t)i * 32 + lane;
     uint32_t c0, c1;
-    const uint32_t sfc = encode_block(a, b, mb, sc, T, c0, c1);
+    const uint32_t sfc = encode_block<EXACT>(a, b, mb, sc, T, I, c0, c1);
     if (real && kb < o.nkb) *reinterpret_cast<uint2*>(o.q + kb * 8) = make_uint2(c0, c1);
     const uint32_t s1 = __shfl_down_sync(0xffffffffu, sfc, 1);
     const uint32_t s2 = __shfl_down_sync(0xffffffffu, sfc, 2);
@@ -86,7 +93,10 @@ nvfp4_token_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t C, int64_t
                    uint8_t* __restrict__ q, uint8_t* __restrict__ sf, float* __restrict__ s_tok,
                    int mma_layout, int64_t rows_cover) {
     __shared__ Nvfp4Table tables[TOK_THREADS / 32];          // one per warp (token row)
+    __shared__ Nvfp4CodeInfo info;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (uint32_t c = threadIdx.x; c < 128u; c += TOK_THREADS) nvfp4_code_info_build(info, c);
+    __syncthreads();
     const int64_t row = (int64_t)blockIdx.x * (TOK_THREADS / 32) + warp;
     if (row >= rows_cover) return;
     Nvfp4Table& T = tables[warp];
@@ -129,14 +139,22 @@ nvfp4_token_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t C, int64_t
     o.nkb = nkb;
     o.mma_layout = mma_layout;
     o.sf = mma_layout ? sf + mma_sf_offset(row, 0, nkb) : sf + row * nkb;
+    if (!sc.exact) {
 #pragma unroll
-    for (int i = 0; i < TOK_NREG; ++i)
-        if (i < iters) token_block(va[i], vb[i], mbk[i], i, lane, real, sc, T, o);
+        for (int i = 0; i < TOK_NREG; ++i)
+            if (i < iters) token_block<false>(va[i], vb[i], mbk[i], i, lane, real, sc, T, info, o);
+    } else {
+#pragma unroll
+        for (int i = 0; i < TOK_NREG; ++i)
+            if (i < iters) token_block<true>(va[i], vb[i], mbk[i], i, lane, real, sc, T, info, o);
+    }
     for (int i = TOK_NREG; i < iters; ++i) {
         const int64_t kb = (int64_t)i * 32 + lane;
         uint4 a = make_uint4(0u, 0u, 0u, 0u), b = a;
         if (real && kb < nkb) load_block<V8>(xr + kb * 16, a, b);
-        token_block(a, b, max(absmax_bits_8(a), absmax_bits_8(b)), i, lane, real, sc, T, o);
+        const uint32_t mb = max(absmax_bits_8(a), absmax_bits_8(b));
+        if (!sc.exact) token_block<false>(a, b, mb, i, lane, real, sc, T, info, o);
+        else token_block<true>(a, b, mb, i, lane, real, sc, T, info, o);
     }
 }
 
@@ -158,10 +176,11 @@ cudaError_t launch_nvfp4_quantize_per_token(const uint16_t* x, int64_t R, int64_
 
 // ------------------------------------------------------------------------------------------------
 // Weights: W [E, K, N] -> qT [E, N, K/2], sfT [E, N, K/16], s_w [E]; coarse scope = expert matrix.
-// Three kernels: amax per expert (atomic max on the fp32 bits, kept in s_w), encode (tiles of
-// 64 k x 64 n transposed through shared memory), finalize (s_w <- RN(amax / 2688)).
+// Three kernels: amax per expert (atomic max on the fp32 bits, kept in s_w), encode, finalize
+// (s_w <- RN(amax / 2688)).
 // ------------------------------------------------------------------------------------------------
 constexpr int WT_K = 64, WT_N = 64, WT_THREADS = 256;
+constexpr int WT_STRIDE = 36;            // words per transposed smem row (64 k = 32 k-pair words + 4)
 
 __global__ void __launch_bounds__(256)
 nvfp4_weight_amax_kernel(const uint16_t* __restrict__ w, int64_t per_expert, uint32_t* __restrict__ amax_bits) {
@@ -183,67 +202,111 @@ nvfp4_weight_amax_kernel(const uint16_t* __restrict__ w, int64_t per_expert, uin
     }
 }
 
+// Encode: a persistent loop over tiles of 64 k x 64 n. CTA b takes the contiguous range
+// [total b / G, total (b + 1) / G) of the (expert, k tile, n tile) sequence, so the load is even
+// for any expert count and a CTA rebuilds its scope table only when its range enters the next
+// expert. A tile arrives as row pairs (k, k + 1): byte permutes interleave them into words
+// (x[k][n], x[k+1][n]) stored transposed, [n][k pair], in shared memory, the k-pair index of row
+// n XOR-ed with 4 (n / 8) so that the stores and the 128-bit loads are free of bank conflicts.
+// Each thread then encodes one 16-k block of one column, read with two 128-bit loads. The next
+// tile's rows are in flight while the current tile is encoded (two buffers, one barrier a tile).
 __global__ void __launch_bounds__(WT_THREADS)
-nvfp4_weight_encode_kernel(const uint16_t* __restrict__ w, int64_t K, int64_t N,
-                           uint8_t* __restrict__ qT, uint8_t* __restrict__ sfT,
+nvfp4_weight_encode_kernel(const uint16_t* __restrict__ w, int64_t K, int64_t N, int64_t tiles_k, int64_t tiles_n,
+                           int64_t total, uint8_t* __restrict__ qT, uint8_t* __restrict__ sfT,
                            const uint32_t* __restrict__ amax_bits, int mma_layout) {
-    __shared__ __align__(16) uint32_t tile[WT_K][WT_N / 2];
-    __shared__ Nvfp4Table T;                                   // the expert matrix's scope table
+    __shared__ __align__(16) uint32_t tile[2][WT_N * WT_STRIDE];
+    __shared__ Nvfp4Table T;                                   // the current expert's scope table
+    __shared__ Nvfp4CodeInfo I;
+    if (threadIdx.x < 128) nvfp4_code_info_build(I, threadIdx.x);
 
-    const int64_t e = blockIdx.z;
-    const int64_t k0 = (int64_t)blockIdx.y * WT_K, n0 = (int64_t)blockIdx.x * WT_N;
-    const uint16_t* we = w + e * K * N;
-    // load 64 x 64 bf16: each row is 8 chunks of 16 bytes; chunk index xor-swizzled by (row/16)
-#pragma unroll
-    for (int it = 0; it < 2; ++it) {
-        const int idx = it * WT_THREADS + threadIdx.x;
-        const int rr = idx >> 3, chunk = idx & 7;
-        const int64_t k = k0 + rr, n = n0 + chunk * 8;
-        uint4 val = make_uint4(0u, 0u, 0u, 0u);
-        if (k < K && n < N) val = ld_stream_v4(we + k * N + n);
-        *reinterpret_cast<uint4*>(&tile[rr][(chunk ^ ((rr >> 4) & 3)) * 4]) = val;
-    }
-    const float s = nvfp4_coarse_scale(__uint_as_float(amax_bits[e]));
-    const Nvfp4Scope sc = make_nvfp4_scope(s);
-    if (!sc.exact && threadIdx.x < 32) nvfp4_table_build_warp(T, s, threadIdx.x);
-    __syncthreads();
+    const int64_t per_e = tiles_k * tiles_n;
+    const int64_t t_begin = total * blockIdx.x / gridDim.x, t_end = total * (blockIdx.x + 1) / gridDim.x;
+    const int lp = threadIdx.x >> 3, lc = threadIdx.x & 7;     // loader: k pair, 8-column chunk
+    const int en = threadIdx.x >> 2, ekb = threadIdx.x & 3;    // encoder: column, 16-k block
+    const int64_t nkb = K >> 4;
 
-    const int kblk = threadIdx.x & 3, nl = threadIdx.x >> 2;       // 4 consecutive lanes = one n
-    const int64_t n = n0 + nl;
-    // gather the 16 k-values of column nl: element j of the block is row 16*kblk + j
-    const int wcol = ((nl >> 1) >> 2), wsub = (nl >> 1) & 3;      // 16-byte chunk and word in it
-    const int half = nl & 1;
-    uint32_t p[8];
+    // tile cursor (expert, k tile, n tile), advanced without divisions
+    struct Cursor {
+        int64_t e, kt, nt;
+    };
+    auto advance = [&](Cursor& c) {
+        if (++c.nt == tiles_n) {
+            c.nt = 0;
+            if (++c.kt == tiles_k) {
+                c.kt = 0;
+                ++c.e;
+            }
+        }
+    };
+    auto load = [&](const Cursor& c, uint4& A, uint4& B) {
+        const int64_t k = c.kt * WT_K + 2 * lp, n = c.nt * WT_N + 8 * lc;
+        A = B = make_uint4(0u, 0u, 0u, 0u);
+        if (k < K && n < N) {                                  // K even: row k + 1 exists too
+            const uint16_t* src = w + (c.e * K + k) * N + n;
+            A = ld_stream_v4(src);
+            B = ld_stream_v4(src + N);
+        }
+    };
+
+    Cursor cur;
+    cur.e = t_begin / per_e;
+    cur.kt = (t_begin - cur.e * per_e) / tiles_n;
+    cur.nt = t_begin - cur.e * per_e - cur.kt * tiles_n;
+    Cursor nxt = cur;
+    uint4 A, B;
+    if (t_begin < t_end) load(cur, A, B);
+    int64_t cur_e = -1;
+    Nvfp4Scope sc = make_nvfp4_scope(0.0f);
+    for (int64_t t = t_begin; t < t_end; ++t) {
+        uint32_t* buf = tile[(t - t_begin) & 1];
+        {
+            const uint32_t a[4] = {A.x, A.y, A.z, A.w}, b[4] = {B.x, B.y, B.z, B.w};
+            const int col = lp ^ (4 * lc);                     // row n = 8 lc + m: n / 8 = lc
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const int ra = 16 * kblk + 2 * j, rb2 = ra + 1;
-        const uint32_t wa = tile[ra][((wcol ^ ((ra >> 4) & 3)) << 2) + wsub];
-        const uint32_t wb = tile[rb2][((wcol ^ ((rb2 >> 4) & 3)) << 2) + wsub];
-        const uint32_t ea = half ? (wa >> 16) : (wa & 0xFFFFu);
-        const uint32_t eb = half ? (wb >> 16) : (wb & 0xFFFFu);
-        p[j] = ea | (eb << 16);
-    }
-    const uint4 lo = make_uint4(p[0], p[1], p[2], p[3]), hi = make_uint4(p[4], p[5], p[6], p[7]);
-    uint32_t c0, c1;
-    const uint32_t sfc = encode_block(lo, hi, max(absmax_bits_8(lo), absmax_bits_8(hi)), sc, T, c0, c1);
-    const int64_t kb = (k0 >> 4) + kblk, nkb = K >> 4;
-    if (n < N && kb < nkb) {
-        *reinterpret_cast<uint2*>(qT + (e * N + n) * (K >> 1) + kb * 8) = make_uint2(c0, c1);
-    }
-    // scale bytes: the 4 lanes of one n hold 4 consecutive blocks
-    const uint32_t s1 = __shfl_down_sync(0xffffffffu, sfc, 1);
-    const uint32_t s2 = __shfl_down_sync(0xffffffffu, sfc, 2);
-    const uint32_t s3 = __shfl_down_sync(0xffffffffu, sfc, 3);
-    if (kblk == 0) {
+            for (int j = 0; j < 4; ++j) {
+                const int n0 = 8 * lc + 2 * j;                 // word j holds columns n0, n0 + 1
+                buf[n0 * WT_STRIDE + col] = __byte_perm(a[j], b[j], 0x5410);
+                buf[(n0 + 1) * WT_STRIDE + col] = __byte_perm(a[j], b[j], 0x7632);
+            }
+        }
+        cur = nxt;
+        advance(nxt);
+        if (t + 1 < t_end) load(nxt, A, B);
+        const int64_t e = cur.e;
+        if (e != cur_e) {                                      // uniform across the CTA
+            __syncthreads();                                   // the previous expert's table is done
+            cur_e = e;
+            const float s = nvfp4_coarse_scale(__uint_as_float(amax_bits[e]));
+            sc = make_nvfp4_scope(s);
+            if (!sc.exact && threadIdx.x < 32) nvfp4_table_build_warp(T, s, threadIdx.x);
+        }
+        __syncthreads();
+
+        const int64_t k0 = cur.kt * WT_K, n = cur.nt * WT_N + en;
+        const uint32_t* rowp = buf + en * WT_STRIDE;
+        const int sw = 4 * (en >> 3);
+        const uint4 lo = *reinterpret_cast<const uint4*>(rowp + ((8 * ekb) ^ sw));
+        const uint4 hi = *reinterpret_cast<const uint4*>(rowp + ((8 * ekb + 4) ^ sw));
+        uint32_t c0, c1;
+        const uint32_t mb = max(absmax_bits_8(lo), absmax_bits_8(hi));
+        const uint32_t sfc = sc.exact ? encode_block<true>(lo, hi, mb, sc, T, I, c0, c1)
+                                      : encode_block<false>(lo, hi, mb, sc, T, I, c0, c1);
+        const int64_t kb0 = k0 >> 4, kb = kb0 + ekb;
         const int64_t row = e * N + n;
-        const int64_t kb0 = k0 >> 4;
-        const uint32_t word = sfc | (s1 << 8) | (s2 << 16) | (s3 << 24);
-        if (mma_layout) {
-            if (n < N) *reinterpret_cast<uint32_t*>(sfT + mma_sf_offset(row, kb0, nkb)) = word;
-        } else if (n < N) {
+        if (n < N && kb < nkb) *reinterpret_cast<uint2*>(qT + row * (K >> 1) + kb * 8) = make_uint2(c0, c1);
+        // scale bytes: the 4 lanes of one column hold 4 consecutive blocks
+        const uint32_t s1 = __shfl_down_sync(0xffffffffu, sfc, 1);
+        const uint32_t s2 = __shfl_down_sync(0xffffffffu, sfc, 2);
+        const uint32_t s3 = __shfl_down_sync(0xffffffffu, sfc, 3);
+        if (ekb == 0 && n < N) {
+            const uint32_t word = sfc | (s1 << 8) | (s2 << 16) | (s3 << 24);
+            if (mma_layout) {
+                *reinterpret_cast<uint32_t*>(sfT + mma_sf_offset(row, kb0, nkb)) = word;
+            } else {
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-                if (kb0 + j < nkb) sfT[row * nkb + kb0 + j] = (uint8_t)(word >> (8 * j));
+                for (int j = 0; j < 4; ++j)
+                    if (kb0 + j < nkb) sfT[row * nkb + kb0 + j] = (uint8_t)(word >> (8 * j));
+            }
         }
     }
 }
@@ -295,9 +358,19 @@ cudaError_t launch_nvfp4_quantize_weights(const uint16_t* w, int64_t E, int64_t 
             ++launched;
         }
     }
-    dim3 grid((unsigned)((N + WT_N - 1) / WT_N), (unsigned)((K + WT_K - 1) / WT_K), (unsigned)E);
-    nvfp4_weight_encode_kernel<<<grid, WT_THREADS, 0, stream>>>(w, K, N, qT, sfT,
-                                                               reinterpret_cast<const uint32_t*>(s_w), mma_layout);
+    // one resident wave of encode CTAs over every tile of every expert
+    static int enc_per_sm = 0;
+    static std::once_flag enc_once;
+    std::call_once(enc_once, [] {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&enc_per_sm, nvfp4_weight_encode_kernel, WT_THREADS, 0) !=
+            cudaSuccess || enc_per_sm < 1)
+            enc_per_sm = 1;
+    });
+    const int64_t tiles_k = (K + WT_K - 1) / WT_K, tiles_n = (N + WT_N - 1) / WT_N;
+    const int64_t total = E * tiles_k * tiles_n;
+    const int64_t enc_grid = std::min<int64_t>(total, (int64_t)sms * enc_per_sm);
+    nvfp4_weight_encode_kernel<<<(unsigned)enc_grid, WT_THREADS, 0, stream>>>(
+        w, K, N, tiles_k, tiles_n, total, qT, sfT, reinterpret_cast<const uint32_t*>(s_w), mma_layout);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     ++launched;
     nvfp4_weight_finalize_kernel<<<(unsigned)((E + 255) / 256), 256, 0, stream>>>(s_w, E);

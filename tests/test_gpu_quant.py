@@ -186,6 +186,28 @@ def test_nvfp4_weights_bit_exact(nvq, shape, layout):
         assert np.array_equal(_np(sf), oracle.sf_to_mma_layout(sf_ref.reshape(E * N, K // 16)))
 
 
+@pytest.mark.parametrize("layout", ["canonical", "mma"])
+def test_nvfp4_weights_tile_ranges_cross_experts(nvq, layout):
+    """More 64 x 64 tiles (64 experts x 8 x 4) than encode CTAs, so each CTA's range of tiles
+    crosses expert boundaries; three experts have a tiny coarse scale (exact decisions) between
+    experts on the table-driven path."""
+    E, K, N = 64, 512, 256
+    rng = np.random.default_rng(7)
+    w = rng.standard_normal((E, K, N)) * 0.02 * np.exp(rng.uniform(-2, 2, (E, 1, 1)))
+    w[5:8] *= 2.0 ** -100
+    bits = _bits_of(w)
+    q_ref, sf_ref, s_ref = oracle.nvfp4_quantize_weights(bits)
+    assert (s_ref[5:8] < 2.0 ** -90).all() and (s_ref[8:] > 2.0 ** -90).all()
+    q, sf, s = nvq.nvfp4_quantize_weights(_dev(bits).contiguous(), sf_layout=layout)
+    torch.cuda.synchronize()
+    assert np.array_equal(_np(s).view(np.uint32), s_ref.view(np.uint32))
+    assert np.array_equal(_np(q), q_ref)
+    if layout == "canonical":
+        assert np.array_equal(_np(sf).reshape(sf_ref.shape), sf_ref)
+    else:
+        assert np.array_equal(_np(sf), oracle.sf_to_mma_layout(sf_ref.reshape(E * N, K // 16)))
+
+
 # ------------------------------------------------------------------------------------------------
 # Dequantize
 # ------------------------------------------------------------------------------------------------
