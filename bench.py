@@ -331,6 +331,84 @@ def _workload_backward(torch, nvq, wl, dev):
             "dtype": "mxfp8(e4m3+e8m0) -> fp32 accumulate -> bf16"}
 
 
+def _workload_dq_backward(torch, nvq, wl, dev):
+    """Dequantized backward of the MoE layers: the MXFP8 copies of the backward workload (made
+    untimed, as the forward would leave them) are dequantized to BF16 and the data and weight
+    gradients run as BF16 grouped GEMMs on them [Miles-zh, "高精度反向和去量化反向"]."""
+    counts, offs_np = wl.moe_routing()
+    offs = torch.from_numpy(offs_np).to(dev)
+    R = int(offs_np[-1])
+    E, H, I2, I = wl.EXPERTS, wl.HIDDEN, 2 * wl.INTERMEDIATE, wl.INTERMEDIATE
+    real = float(counts.sum())
+    x1 = wl.routed_activations(counts, offs_np, H, seed=1, device=dev)
+    g1 = wl.routed_activations(counts, offs_np, I2, std=1e-3, seed=5, device=dev)
+    x2 = wl.routed_activations(counts, offs_np, I, seed=2, device=dev)
+    g2 = wl.routed_activations(counts, offs_np, H, std=1e-3, seed=6, device=dev)
+    w1 = wl.expert_weights(H, I2, seed=3, device=dev).view(E * H, I2)
+    w2 = wl.expert_weights(I, H, seed=4, device=dev).view(E * I, H)
+    q = {"x1": nvq.mxfp8_quantize(x1, rowwise=False), "g1": nvq.mxfp8_quantize(g1),
+         "w1": nvq.mxfp8_quantize(w1, colwise=False), "x2": nvq.mxfp8_quantize(x2, rowwise=False),
+         "g2": nvq.mxfp8_quantize(g2), "w2": nvq.mxfp8_quantize(w2, colwise=False)}
+    del x1, g1, x2, g2, w1, w2
+
+    def bf(rows, cols):
+        return torch.empty((rows, cols), dtype=torch.bfloat16, device=dev)
+
+    # dequantized operands: dgrad A = dY rows, B = W rows; wgrad A = X^T, B = dY^T (columnwise copies)
+    d = {"g1r": bf(R, I2), "w1": bf(E * H, I2), "x1t": bf(H, R), "g1t": bf(I2, R),
+         "g2r": bf(R, H), "w2": bf(E * I, H), "x2t": bf(I, R), "g2t": bf(H, R),
+         "dx1": bf(R, H), "dw1": torch.empty((E, H, I2), dtype=torch.bfloat16, device=dev),
+         "dx2": bf(R, I), "dw2": torch.empty((E, I, H), dtype=torch.bfloat16, device=dev)}
+    f1 = 2.0 * real * H * I2
+    f2 = 2.0 * real * I * H
+    dq = 1 + 1 / 32 + 2
+    kernels = [
+        Kernel("dequantize_bf16 dY1 row", "hbm", R * I2 * dq, "dequant.cu", "hbm", "3.03125 B/elem"),
+        Kernel("dequantize_bf16 W1 row", "hbm", E * H * I2 * dq, "dequant.cu", "hbm", "3.03125 B/elem"),
+        Kernel("grouped_gemm BF16 dgrad gate_up", "tensor", f1, "gemm_sm103.cu", "bf16", "2*sum_e M_e*N*K"),
+        Kernel("dequantize_bf16 X1 col", "hbm", R * H * dq, "dequant.cu", "hbm", "3.03125 B/elem"),
+        Kernel("dequantize_bf16 dY1 col", "hbm", R * I2 * dq, "dequant.cu", "hbm", "3.03125 B/elem"),
+        Kernel("grouped_gemm BF16 wgrad gate_up", "tensor", f1, "gemm_sm103.cu", "bf16", "2*sum_e M_e*N*K"),
+        Kernel("dequantize_bf16 dY2 row", "hbm", R * H * dq, "dequant.cu", "hbm", "3.03125 B/elem"),
+        Kernel("dequantize_bf16 W2 row", "hbm", E * I * H * dq, "dequant.cu", "hbm", "3.03125 B/elem"),
+        Kernel("grouped_gemm BF16 dgrad down", "tensor", f2, "gemm_sm103.cu", "bf16", "2*sum_e M_e*N*K"),
+        Kernel("dequantize_bf16 X2 col", "hbm", R * I * dq, "dequant.cu", "hbm", "3.03125 B/elem"),
+        Kernel("dequantize_bf16 dY2 col", "hbm", R * H * dq, "dequant.cu", "hbm", "3.03125 B/elem"),
+        Kernel("grouped_gemm BF16 wgrad down", "tensor", f2, "gemm_sm103.cu", "bf16", "2*sum_e M_e*N*K"),
+    ]
+
+    def deq(src, key, rows, cols, out):
+        return lambda: nvq.dequantize_bf16(nvq.MXFP8, src["q_" + key], src["sf_" + key], rows=rows, cols=cols, out=out)
+
+    def step(timer, xin=None, win=None):
+        k = kernels
+        timer.run(k[0].name, deq(q["g1"], "row", R, I2, d["g1r"]))
+        timer.run(k[1].name, deq(q["w1"], "row", E * H, I2, d["w1"]))
+        timer.run(k[2].name, lambda: nvq.block_scaled_grouped_gemm(
+            nvq.BF16, nvq.GEMM_GROUP_M, d["g1r"], None, d["w1"], None, offs, m=R, n=H, k=I2, groups=E, out=d["dx1"]))
+        timer.run(k[3].name, deq(q["x1"], "colT", H, R, d["x1t"]))
+        timer.run(k[4].name, deq(q["g1"], "colT", I2, R, d["g1t"]))
+        timer.run(k[5].name, lambda: nvq.block_scaled_grouped_gemm(
+            nvq.BF16, nvq.GEMM_GROUP_K, d["x1t"], None, d["g1t"], None, offs, m=H, n=I2, k=R, groups=E, out=d["dw1"]))
+        timer.run(k[6].name, deq(q["g2"], "row", R, H, d["g2r"]))
+        timer.run(k[7].name, deq(q["w2"], "row", E * I, H, d["w2"]))
+        timer.run(k[8].name, lambda: nvq.block_scaled_grouped_gemm(
+            nvq.BF16, nvq.GEMM_GROUP_M, d["g2r"], None, d["w2"], None, offs, m=R, n=I, k=H, groups=E, out=d["dx2"]))
+        timer.run(k[9].name, deq(q["x2"], "colT", I, R, d["x2t"]))
+        timer.run(k[10].name, deq(q["g2"], "colT", H, R, d["g2t"]))
+        timer.run(k[11].name, lambda: nvq.block_scaled_grouped_gemm(
+            nvq.BF16, nvq.GEMM_GROUP_K, d["x2t"], None, d["g2t"], None, offs, m=I, n=H, k=R, groups=E, out=d["dw2"]))
+        return [d["dx1"], d["dw1"], d["dx2"], d["dw2"]]
+
+    config = {"workload": "dequantized MoE backward: MXFP8 copies dequantized to BF16, BF16 grouped data and "
+                          "weight gradients of gate_up and down, Qwen3-30B-A3B",
+              "tokens": 16384, "experts": E, "topk": 8, "routed_rows": int(real), "buffer_rows": R,
+              "row_alignment": 32, "dy_std": 1e-3}
+    # its inputs are the forward's quantized copies already on the device: no host round trip to time
+    return {"step": step, "kernels": kernels, "gemm_flops": 2 * (f1 + f2), "inputs": [], "e2e": False,
+            "config": config, "dtype": "mxfp8 -> bf16 (dequantized) -> fp32 accumulate -> bf16"}
+
+
 def _workload_decode(torch, nvq, wl, dev):
     counts = wl.route_counts(256, zipf_s=0.0, seed=0)
     offs_np = wl.padded_offsets(counts, 32)
@@ -403,8 +481,47 @@ def _workload_quant(torch, nvq, wl, dev):
             "config": config, "dtype": "bf16 -> mxfp8 / nvfp4", "unit": "GB/s"}
 
 
+def _workload_dispatch(torch, nvq, wl, dev):
+    """Quantize-once dispatch of the MoE gate_up input: per-token NVFP4 of the 16384 tokens, then the
+    gather of their quantized rows into the 132960 expert-sorted routed rows (32-row padded)."""
+    T, H = 16384, wl.HIDDEN
+    choices = wl.route_choices(T)
+    counts = wl.route_counts(T)
+    offs_np = wl.padded_offsets(counts, 32)
+    R = int(offs_np[-1])
+    idx = torch.from_numpy(wl.dispatch_index(choices, offs_np)).to(dev)
+    x = wl.normal_bf16((T, H), 1.0, seed=21, device=dev)
+    tok = (torch.empty((T, H // 2), dtype=torch.uint8, device=dev),
+           torch.empty(nvq.sf_bytes(T, H, 16), dtype=torch.uint8, device=dev),
+           torch.empty(T, dtype=torch.float32, device=dev))
+    routed = (torch.empty((R, H // 2), dtype=torch.uint8, device=dev),
+              torch.empty(nvq.sf_bytes(R, H, 16), dtype=torch.uint8, device=dev),
+              torch.empty(R, dtype=torch.float32, device=dev))
+    row_bytes = H // 2 + H // 16 + 4
+    kernels = [
+        Kernel("nvfp4_quantize_per_token tokens", "hbm", T * H * 2.5625 + 4 * T, "quant_nvfp4.cu", "hbm",
+               "2.5625 B/elem + 4 B/row"),
+        Kernel("quantized_gather_rows routed", "hbm", (int(counts.sum()) + R) * row_bytes, "layout_ops.cu", "hbm",
+               "read K/2 + K/16 + 4 B per real routed row, write the same per routed row"),
+    ]
+
+    def step(timer, xin=None, win=None):
+        xx = x if xin is None else xin[0]
+        timer.run(kernels[0].name, lambda: nvq.nvfp4_quantize_per_token(xx, out=tok))
+        timer.run(kernels[1].name, lambda: nvq.quantized_gather_rows(nvq.NVFP4, tok[0], tok[1], tok[2], idx, H,
+                                                                     out=routed))
+        return [routed[0], routed[1], routed[2]]
+
+    config = {"workload": "quantize-once dispatch: per-token NVFP4 of 16384 tokens x 2048, gathered into "
+                          "the top-8 expert-sorted routed rows (Zipf 1.1, 32-row padding)",
+              "tokens": [T, H], "routed_rows": R}
+    return {"step": step, "kernels": kernels, "gemm_flops": 0.0, "inputs": [x], "input_groups": ([0], []),
+            "config": config, "dtype": "bf16 -> nvfp4 (gathered)", "unit": "GB/s"}
+
+
 WORKLOADS = {"dense": _workload_dense, "quant": _workload_quant, "moe": _workload_moe, "backward": _workload_backward,
-             "decode": _workload_decode}
+             "decode": _workload_decode, "dispatch": _workload_dispatch, "dq_backward": _workload_dq_backward}
+GBS_WORKLOADS = ("quant", "dispatch")
 
 
 class ClockSampler:
@@ -457,7 +574,7 @@ class ClockSampler:
 def _peak(kind, peaks):
     if kind == "hbm":
         return peaks["hbm_gbs"], "GB/s"
-    ratio = {"fp8": 2.0, "fp4": 6.0}[kind]      # dense FP8 = 2x BF16, FP4 = 6x BF16 on GB300
+    ratio = {"bf16": 1.0, "fp8": 2.0, "fp4": 6.0}[kind]   # dense FP8 = 2x BF16, FP4 = 6x BF16 on GB300
     return peaks["bf16_tflops"] * ratio, "TFLOP/s"
 
 
@@ -554,7 +671,7 @@ def run_ours(args):
 
     # end to end: pinned host inputs copied in, step through the C-ABI, GEMM outputs copied out
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and W.get("e2e", True):
         host_in = [t.detach().cpu().pin_memory() for t in W["inputs"]]
         dev_in = [torch.empty_like(t) for t in W["inputs"]]
         outs = W["step"](Timer(torch))
@@ -658,6 +775,18 @@ def _oracle_sample(workload, rows, cols):
         K = xb.shape[1]
         flops = 2 * 2.0 * rows * cols * K
         desc = f"oracle on X rows [{rows} x {K}] and W columns [{K} x {cols}]: every quantizer, both GEMMs, dequant"
+    elif workload == "dispatch":
+        import torch
+        K = wl.HIDDEN
+        T = max(1, rows // 8)
+        x = rng.standard_normal((T, K)).astype(np.float32)
+        xb = wl.to_bits(torch.from_numpy(x).to(torch.bfloat16))
+        idx = rng.integers(0, T, rows)
+        t0 = time.perf_counter()
+        q, sf, s = oracle.nvfp4_quantize_per_token(xb)
+        q[idx], sf[idx], s[idx]
+        flops = T * K * 2.5625 + 4 * T + 2 * rows * (K // 2 + K // 16 + 4)   # algorithmic bytes
+        desc = f"oracle per-token NVFP4 of {T} tokens x {K}, gathered into {rows} rows"
     elif workload == "quant":
         import torch
         K = wl.HIDDEN
@@ -709,7 +838,7 @@ def cpu_baseline(workload, rows=2048, cols=1536):
         res = json.loads(out.stdout.strip().splitlines()[-1])
     except (subprocess.SubprocessError, ValueError, IndexError) as e:
         return {"value": None, "unit": "TFLOPS", "cores": 1, "kind": "oracle", "sample": f"failed: {e}"}
-    if workload == "quant":
+    if workload in GBS_WORKLOADS:
         return {"value": res["flops"] / res["seconds"] / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
                 "sample": res["sample"], "seconds": round(res["seconds"], 3)}
     return {"value": res["flops"] / res["seconds"] / 1e12, "unit": "TFLOPS", "cores": 1, "kind": "oracle",
@@ -734,7 +863,7 @@ def run_reference(args):
         t, flops, desc = _oracle_sample(args.workload, rows, cols)
         times.append(t)
     total = sum(times)
-    unit = "GB/s" if args.workload == "quant" else "TFLOPS"
+    unit = "GB/s" if args.workload in GBS_WORKLOADS else "TFLOPS"
     value = flops * len(times) / total / (1e9 if unit == "GB/s" else 1e12)
     line = {"metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(1e3 * total / len(times), 3), "higher_is_better": True,

@@ -44,7 +44,7 @@ typedef enum {
 } nvq_status;
 
 typedef enum { NVQ_SF_CANONICAL = 0, NVQ_SF_MMA = 1 } nvq_sf_layout;
-typedef enum { NVQ_MXFP8 = 0, NVQ_NVFP4 = 1 } nvq_format;
+typedef enum { NVQ_MXFP8 = 0, NVQ_NVFP4 = 1, NVQ_BF16 = 2 } nvq_format;   /* NVQ_BF16: GEMM operands only */
 typedef enum { NVQ_SCOPE_ROW = 0, NVQ_SCOPE_MATRIX = 1 } nvq_scope;
 
 /* Human-readable name of a status code (static string). */
@@ -150,25 +150,64 @@ typedef enum {
 
 typedef enum { NVQ_OUT_BF16 = 0, NVQ_OUT_F32 = 1 } nvq_out_type;
 
+/*
+ * sf_layout_convert — the explicit permutation between canonical scale bytes [rows, kb] and the
+ * tcgen05 tile layout described above (both directions).
+ *
+ * Defines: a pure permutation (NVQ_SF_MMA output: padding bytes zero). [Miles-zh, "重构权重更新接口":
+ * backend-specific swizzled layouts must stay explicit and verifiable, e.g. across a live weight
+ * update.]
+ *
+ *   src, src_layout   scales [rows, kb] in that layout (nvq_sf_bytes(rows, kb*block, block, layout)).
+ *   dst, dst_layout   the other layout; src_layout == dst_layout is rejected (NVQ_ERR_INVALID_ARG).
+ * rows = 0 or kb = 0 is a no-op. src and dst must not overlap.
+ */
+nvq_status sf_layout_convert(const uint8_t* src, nvq_sf_layout src_layout, int64_t rows, int64_t kb,
+                             uint8_t* dst, nvq_sf_layout dst_layout, void* stream);
+
+/*
+ * quantized_gather_rows — quantize-once dispatch: gather quantized rows (codes, block scales and,
+ * for NVFP4, token scales) into a new row order, e.g. tokens into expert-sorted routed rows.
+ *
+ * Defines: row i of the outputs = row index[i] of the inputs, byte for byte; index[i] = -1 gives
+ * a zero row (codes 0, scales 0, token scale 0 — what quantizing a zero padding row gives). Because
+ * per-token NVFP4 and rowwise MXFP8 bytes depend on their own row only, gathering quantized tokens
+ * equals quantizing the gathered bf16 rows. [Miles-zh, "逐 Token 激活值缩放": one FP32 scale per
+ * token computed online, so the rollout can quantize once; per-token invariance.]
+ *
+ *   fmt         NVQ_NVFP4 (codes cols/2 bytes per row, scales cols/16, token scales) or NVQ_MXFP8
+ *               (rowwise copy: codes cols bytes per row, scales cols/32; s and s_out ignored).
+ *   q, sf, s    source rows [src_rows] (s: float32 [src_rows], NVFP4 only), sf in src_layout.
+ *   index       device int32 [rows]; values in [-1, src_rows). An out-of-range value sets *status
+ *               to NVQ_DEV_BAD_INDEX (when status is non-NULL) and that row is written as a zero row.
+ *   q_out, sf_out, s_out  destination rows [rows], sf_out in dst_layout (MMA padding rows zeroed).
+ * Requires cols % 16 (NVFP4) or % 32 (MXFP8) == 0. rows = 0 is a no-op.
+ */
+nvq_status quantized_gather_rows(nvq_format fmt, const uint8_t* q, const uint8_t* sf, const float* s,
+                                 int64_t src_rows, int64_t cols, nvq_sf_layout src_layout,
+                                 const int32_t* index, int64_t rows, uint8_t* q_out, uint8_t* sf_out,
+                                 float* s_out, nvq_sf_layout dst_layout, int32_t* status, void* stream);
+
 /* Device status word values written by block_scaled_grouped_gemm (when `status` is non-NULL). */
 #define NVQ_DEV_OK 0
 #define NVQ_DEV_TIMEOUT 1          /* a pipeline wait exceeded its iteration limit */
 #define NVQ_DEV_BAD_OFFSETS 2      /* offsets not monotone, not multiples of 32, or past the buffer */
+#define NVQ_DEV_BAD_INDEX 3        /* quantized_gather_rows: an index outside [-1, src_rows) */
 
 
 typedef struct {
-    nvq_format fmt;          /* NVQ_MXFP8 (E4M3 x E8M0 / 32) or NVQ_NVFP4 (E2M1 x E4M3 / 16)       */
+    nvq_format fmt;          /* NVQ_MXFP8 (E4M3 x E8M0 / 32), NVQ_NVFP4 (E2M1 x E4M3 / 16), NVQ_BF16 */
     nvq_gemm_mode mode;
     nvq_out_type out_type;   /* bf16 (round to nearest even) or float32                           */
     int64_t groups;          /* E: experts                                                        */
     int64_t m;               /* GROUP_M: rows of the A buffer; GROUP_K: rows of A = output rows    */
     int64_t n;               /* GROUP_M: rows of each B[e]; GROUP_K: rows of B; = output columns   */
     int64_t k;               /* GROUP_M: reduction length; GROUP_K: columns of A and of B          */
-    const void* a;           /* [m, k] codes, K-major (NVFP4 packed: k/2 bytes per row)            */
-    const void* sfa;         /* scales of a in the MMA layout                                      */
+    const void* a;           /* [m, k] codes, K-major (NVFP4 packed: k/2 bytes per row; BF16: bf16) */
+    const void* sfa;         /* scales of a in the MMA layout (ignored for NVQ_BF16)               */
     const float* s_a;        /* [m] per-row FP32 scales (NVFP4 tokens) or NULL (= 1)               */
     const void* b;           /* GROUP_M: [groups, n, k]; GROUP_K: [n, k]; codes, K-major           */
-    const void* sfb;         /* scales of b (stacked rows) in the MMA layout                       */
+    const void* sfb;         /* scales of b (stacked rows) in the MMA layout (ignored for NVQ_BF16) */
     const float* s_b;        /* [groups] per-expert FP32 scales or NULL (= 1)                      */
     const int64_t* offsets;  /* device [groups+1]: group e owns rows (GROUP_M) or reduction columns
                                 (GROUP_K) offsets[e] .. offsets[e+1]-1; offsets[0] = 0, monotone,
@@ -192,9 +231,14 @@ typedef struct {
  * Accuracy: |D - D_exact| <= 2e-3 * sum_k |s_a s_b deq(A) deq(B)| before the output rounding.
  *
  * Requires: n % 128 == 0; GROUP_M: k % 128 == 0; GROUP_K: k % 32 == 0, m % 128 == 0,
- * fmt == NVQ_MXFP8 and s_a == NULL; groups <= 1024. offsets are validated on the device (status
- * NVQ_DEV_BAD_OFFSETS, nothing written). Scale buffers: sfa = MMA layout of [m, k/block],
+ * fmt == NVQ_MXFP8 or NVQ_BF16 and s_a == NULL; groups <= 1024. offsets are validated on the device
+ * (status NVQ_DEV_BAD_OFFSETS, nothing written). Scale buffers: sfa = MMA layout of [m, k/block],
  * sfb = MMA layout of the stacked [groups*n, k/block] (GROUP_M) or [n, k/block] (GROUP_K).
+ *
+ * fmt == NVQ_BF16: the same grouped GEMM on bf16 operands (a [m, k], b [groups*n, k] or [n, k],
+ * k-major) with fp32 accumulation; sfa and sfb are ignored (may be NULL); k % 16 == 0 in both
+ * modes. [Miles-zh, "高精度反向和去量化反向": the high-precision and the dequantized backward run BF16
+ * GEMMs, the latter on the BF16 dequantization (dequantize_bf16) of the low-precision operands.]
  */
 nvq_status block_scaled_grouped_gemm(const nvq_gemm_args* args, void* stream);
 

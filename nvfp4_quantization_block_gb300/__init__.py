@@ -26,11 +26,11 @@ _lib = ctypes.CDLL(LIB_PATH)
 
 NVQ_OK, NVQ_ERR_INVALID_ARG, NVQ_ERR_MISALIGNED, NVQ_ERR_UNSUPPORTED, NVQ_ERR_CUDA, NVQ_ERR_TIMEOUT = range(6)
 SF_CANONICAL, SF_MMA = 0, 1
-MXFP8, NVFP4 = 0, 1
+MXFP8, NVFP4, BF16 = 0, 1, 2
 SCOPE_ROW, SCOPE_MATRIX = 0, 1
 GEMM_GROUP_M, GEMM_GROUP_K = 0, 1
 OUT_BF16, OUT_F32 = 0, 1
-DEV_OK, DEV_TIMEOUT, DEV_BAD_OFFSETS = 0, 1, 2
+DEV_OK, DEV_TIMEOUT, DEV_BAD_OFFSETS, DEV_BAD_INDEX = 0, 1, 2, 3
 
 _vp, _i64, _i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32
 
@@ -48,6 +48,9 @@ _launch_count = _sig("nvq_launch_count", [], ctypes.c_uint64)
 _mxfp8_quantize = _sig("mxfp8_quantize", [_vp, _i64, _i64, _i64, _vp, _vp, _vp, _vp, ctypes.c_int, _vp])
 _nvfp4_quantize_per_token = _sig("nvfp4_quantize_per_token", [_vp, _i64, _i64, _i64, _vp, _vp, _vp, ctypes.c_int, _vp])
 _nvfp4_quantize_weights = _sig("nvfp4_quantize_weights", [_vp, _i64, _i64, _i64, _vp, _vp, _vp, ctypes.c_int, _vp])
+_sf_layout_convert = _sig("sf_layout_convert", [_vp, ctypes.c_int, _i64, _i64, _vp, ctypes.c_int, _vp])
+_quantized_gather_rows = _sig("quantized_gather_rows", [ctypes.c_int, _vp, _vp, _vp, _i64, _i64, ctypes.c_int, _vp,
+                                                        _i64, _vp, _vp, _vp, ctypes.c_int, _vp, _vp])
 _dequantize_bf16 = _sig("dequantize_bf16", [ctypes.c_int, _vp, _vp, _vp, ctypes.c_int, _i64, _i64, _i64,
                                             ctypes.c_int, _vp, _vp])
 
@@ -172,6 +175,37 @@ def nvfp4_quantize_weights(w, sf_layout="mma", out=None):
     st = _nvfp4_quantize_weights(_ptr(w), E, K, N, _ptr(q), _ptr(sf), _ptr(s), lay, _stream(dev))
     _check(st, "nvfp4_quantize_weights")
     return q, sf, s
+
+
+def sf_layout_convert(sf, rows, kb, src_layout, dst_layout, out=None):
+    """Permute block scales [rows, kb] between the canonical and the MMA tile layout."""
+    src, dst = _layout(src_layout), _layout(dst_layout)
+    if out is None:
+        n = rows * kb if dst == SF_CANONICAL else sf_bytes(rows, kb * 16, 16, SF_MMA)
+        out = torch.empty(n, dtype=torch.uint8, device=sf.device)
+    st = _sf_layout_convert(_ptr(sf), src, int(rows), int(kb), _ptr(out), dst, _stream(sf.device))
+    _check(st, "sf_layout_convert")
+    return out
+
+
+def quantized_gather_rows(fmt, q, sf, s, index, cols, src_layout="mma", dst_layout="mma", out=None, status=None):
+    """Rows ``index`` (int32 CUDA tensor, -1 = zero row) of quantized rows (q, sf[, s]) -> new
+    (q, sf, s) in ``dst_layout`` (s is None for MXFP8)."""
+    src_rows = q.shape[0]
+    rows = index.numel()
+    dev = index.device
+    block = 16 if fmt == NVFP4 else 32
+    qb = cols // 2 if fmt == NVFP4 else cols
+    dst = _layout(dst_layout)
+    if out is None:
+        out = (torch.empty((rows, qb), dtype=torch.uint8, device=dev),
+               torch.empty(sf_bytes(rows, cols, block, dst), dtype=torch.uint8, device=dev),
+               torch.empty(rows, dtype=torch.float32, device=dev) if fmt == NVFP4 else None)
+    qo, sfo, so = out
+    st = _quantized_gather_rows(int(fmt), _ptr(q), _ptr(sf), _ptr(s), int(src_rows), int(cols), _layout(src_layout),
+                                _ptr(index), int(rows), _ptr(qo), _ptr(sfo), _ptr(so), dst, _ptr(status), _stream(dev))
+    _check(st, "quantized_gather_rows")
+    return qo, sfo, so
 
 
 def dequantize_bf16(fmt, q, sf, s=None, scope=SCOPE_ROW, groups=1, rows=None, cols=None,

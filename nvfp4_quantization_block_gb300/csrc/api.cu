@@ -89,6 +89,40 @@ nvq_status nvfp4_quantize_weights(const void* w, int64_t experts, int64_t k, int
                                                         static_cast<cudaStream_t>(stream)));
 }
 
+nvq_status sf_layout_convert(const uint8_t* src, nvq_sf_layout src_layout, int64_t rows, int64_t kb, uint8_t* dst,
+                             nvq_sf_layout dst_layout, void* stream) {
+    if (!valid_layout(src_layout) || !valid_layout(dst_layout) || src_layout == dst_layout) return NVQ_ERR_INVALID_ARG;
+    if (rows < 0 || kb < 0) return NVQ_ERR_INVALID_ARG;
+    if (rows == 0 || kb == 0) return NVQ_OK;
+    if (src == nullptr || dst == nullptr) return NVQ_ERR_INVALID_ARG;
+    if (!aligned16(src) || !aligned16(dst)) return NVQ_ERR_MISALIGNED;
+    return from_cuda(nvq::launch_sf_layout_convert(src, dst_layout == NVQ_SF_MMA, rows, kb, dst,
+                                                   static_cast<cudaStream_t>(stream)));
+}
+
+nvq_status quantized_gather_rows(nvq_format fmt, const uint8_t* q, const uint8_t* sf, const float* s,
+                                 int64_t src_rows, int64_t cols, nvq_sf_layout src_layout, const int32_t* index,
+                                 int64_t rows, uint8_t* q_out, uint8_t* sf_out, float* s_out,
+                                 nvq_sf_layout dst_layout, int32_t* status, void* stream) {
+    if ((fmt != NVQ_MXFP8 && fmt != NVQ_NVFP4) || !valid_layout(src_layout) || !valid_layout(dst_layout))
+        return NVQ_ERR_INVALID_ARG;
+    if (src_rows < 0 || cols < 0 || rows < 0) return NVQ_ERR_INVALID_ARG;
+    if (rows == 0) return NVQ_OK;
+    const int64_t block = fmt == NVQ_NVFP4 ? 16 : 32;
+    if (cols == 0 || cols % block || q_out == nullptr || sf_out == nullptr || index == nullptr)
+        return NVQ_ERR_INVALID_ARG;
+    if (src_rows > 0 && (q == nullptr || sf == nullptr)) return NVQ_ERR_INVALID_ARG;
+    if (fmt == NVQ_NVFP4 && (s_out == nullptr || (src_rows > 0 && s == nullptr))) return NVQ_ERR_INVALID_ARG;
+    if ((q && !aligned16(q)) || (sf && !aligned16(sf)) || !aligned16(q_out) || !aligned16(sf_out))
+        return NVQ_ERR_MISALIGNED;
+    const int64_t qbytes = fmt == NVQ_NVFP4 ? cols / 2 : cols;
+    return from_cuda(nvq::launch_quantized_gather_rows(q, sf, fmt == NVQ_NVFP4 ? s : nullptr, src_rows, qbytes,
+                                                       cols / block, src_layout == NVQ_SF_MMA, index, rows, q_out,
+                                                       sf_out, fmt == NVQ_NVFP4 ? s_out : nullptr,
+                                                       dst_layout == NVQ_SF_MMA, status,
+                                                       static_cast<cudaStream_t>(stream)));
+}
+
 nvq_status dequantize_bf16(nvq_format fmt, const uint8_t* q, const uint8_t* sf, const float* s,
                            nvq_scope scope, int64_t groups, int64_t rows, int64_t cols,
                            nvq_sf_layout sf_layout, void* out, void* stream) {

@@ -55,27 +55,33 @@ constexpr int MAX_GROUPS = 1024;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;    // 2 s: far beyond any legitimate wait
 
-template <bool FP4>
+enum { F_MXFP8 = 0, F_NVFP4 = 1, F_BF16 = 2 };       // operand formats (the kernel's template argument)
+
+template <int FMT>
 struct GemmCfg {
+    static constexpr bool FP4 = FMT == F_NVFP4;
+    static constexpr bool SCALED = FMT != F_BF16;      // block-scaled MMA (scale tiles staged to TMEM)
     static constexpr int STAGES = FP4 ? 3 : 4;
     static constexpr int KGS = FP4 ? 4 : 1;            // 4-scale-column groups per stage
-    static constexpr int EPS = FP4 ? 256 : 128;        // reduction elements per stage
-    static constexpr int MMA_K = FP4 ? 64 : 32;        // reduction elements per MMA
+    static constexpr int EPS = FP4 ? 256 : (SCALED ? 128 : 64);   // reduction elements per stage (128 B)
+    static constexpr int MMA_K = FP4 ? 64 : (SCALED ? 32 : 16);   // reduction elements per MMA (32 B)
     static constexpr int A_BYTES = BM * BKB;
     static constexpr int B_BYTES = BN * BKB;
-    static constexpr int SFA_BYTES = KGS * 512;        // the tile's own 128 row scales
-    static constexpr int SFB_BYTES = 2 * KGS * 512;    // two 128-row scale tiles (N = 256)
-    static constexpr int SFA_RAW_BYTES = 2 * KGS * 512;  // the two row tiles a 32-aligned tile spans
+    static constexpr int SFA_BYTES = SCALED ? KGS * 512 : 0;        // the tile's own 128 row scales
+    static constexpr int SFB_BYTES = SCALED ? 2 * KGS * 512 : 0;    // two 128-row scale tiles (N = 256)
+    static constexpr int SFA_RAW_BYTES = SCALED ? 2 * KGS * 512 : 0;  // the two row tiles a 32-aligned tile spans
     static constexpr int STAGE_BYTES =
         (A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES + SFA_RAW_BYTES + 1023) / 1024 * 1024;
-    static constexpr uint32_t SF_SETS = 2;             // TMEM scale sets
+    static constexpr uint32_t SF_SETS = SCALED ? 2 : 0;             // TMEM scale sets
+    static constexpr uint32_t SF_SETS_NZ = SCALED ? SF_SETS : 1;    // divisor for set arithmetic
     static constexpr uint32_t SFA_COLS = KGS * 4;      // TMEM columns of A's scales
     static constexpr uint32_t SFB_COLS = KGS * 8;      // TMEM columns of B's scales
     static constexpr uint32_t SF_SET_COLS = SFA_COLS + SFB_COLS;
     static constexpr uint32_t IDESC =
-        (FP4 ? ((1u << 7) | (1u << 10)) : 0u)         // A, B format: E2M1 (mxf4nvf4) or E4M3
+        (SCALED ? ((FP4 ? ((1u << 7) | (1u << 10)) : 0u)   // A, B format: E2M1 (mxf4nvf4) or E4M3
+                   | (FP4 ? 0u : (1u << 23)))               // scale type: UE4M3 (0) / UE8M0 (1)
+                : ((1u << 4) | (1u << 7) | (1u << 10)))     // kind::f16: D F32, A and B BF16
         | ((uint32_t)(BN >> 3) << 17)                  // N >> 3
-        | (FP4 ? 0u : (1u << 23))                      // scale type: UE4M3 (0) / UE8M0 (1)
         | ((uint32_t)(BM >> 4) << 24);                 // M >> 4
     static constexpr int BAR_BYTES = 256;
     static constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + BAR_BYTES + 8 * (MAX_GROUPS + 1);
@@ -194,20 +200,26 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
            (1ull << 46) | ((uint64_t)swizzle << 61);
 }
 
-template <bool FP4>
+template <int FMT>
 __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                        uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
-    if constexpr (FP4) {
+    if constexpr (FMT == F_NVFP4) {
         asm volatile(
             "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
             "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
             ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
             : "memory");
-    } else {
+    } else if constexpr (FMT == F_MXFP8) {
         asm volatile(
             "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
             "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
             ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+            : "memory");
+    } else {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+            ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
             : "memory");
     }
 }
@@ -349,11 +361,11 @@ struct StageCursor {
 // ------------------------------------------------------------------------------------------------
 // Kernel
 // ------------------------------------------------------------------------------------------------
-template <bool FP4>
+template <int FMT>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
 block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                          const GemmParams p) {
-    using C = GemmCfg<FP4>;
+    using C = GemmCfg<FMT>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* stage_base = smem;
@@ -429,9 +441,11 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
             mbar_init(&empty_bar[s], 1);
             mbar_init(&sfa_bar[s], 1);
         }
-        for (uint32_t k = 0; k < C::SF_SETS; ++k) {
-            mbar_init(&sf_ready[k], 1);
-            mbar_init(&sf_free[k], 1);
+        if constexpr (C::SCALED) {
+            for (uint32_t k = 0; k < C::SF_SETS; ++k) {
+                mbar_init(&sf_ready[k], 1);
+                mbar_init(&sf_free[k], 1);
+            }
         }
         mbar_init(tmem_full, 1);
         mbar_init(tmem_empty, 4);              // one arrival per epilogue warp
@@ -466,7 +480,7 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
             if (!mbar_wait(&empty_bar[slot], phase ^ 1u, abort_flag, p.status)) break;
             const Tile& tl = cur.tl;
             const int64_t rb_a = tl.a_row0 / BM;
-            const bool shifted = (tl.a_row0 % BM) != 0;
+            const bool shifted = C::SCALED && (tl.a_row0 % BM) != 0;
             const bool need_a2 = shifted && rb_a + 1 < p.a_rowtiles;
             const int64_t rb_b = tl.b_row0 / BM;
             const bool need_b2 = rb_b + 1 < p.b_rowtiles;
@@ -480,10 +494,12 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
             // full_bar completes after two arrivals and all bytes: the producer's expect_tx arrival
             // (A, B, B scales, and the A scales of an aligned tile) plus either the producer's second
             // arrival (aligned tile) or the transposer's (tile starting inside a scale tile)
-            const uint32_t tx = C::A_BYTES + C::B_BYTES + sf_bytes * (1u + (need_b2 ? 1u : 0u)) +
-                                (shifted ? 0u : sf_bytes);
+            const uint32_t tx = C::A_BYTES + C::B_BYTES +
+                                (C::SCALED ? sf_bytes * (1u + (need_b2 ? 1u : 0u)) + (shifted ? 0u : sf_bytes) : 0u);
             mbar_arrive_expect_tx(&full_bar[slot], tx);
-            if (shifted) {
+            if (!C::SCALED) {
+                // no scales to stage
+            } else if (shifted) {
                 mbar_arrive_expect_tx(&sfa_bar[slot], sf_bytes * (1u + (need_a2 ? 1u : 0u)));
                 ++sfa_fills[slot];
                 bulk_load(ssfa_raw, p.sfa + ((rb_a * p.sf_tiles_per_row + kg0) << 9), sf_bytes, &sfa_bar[slot]);
@@ -495,10 +511,12 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
             }
             tma_load_2d(st, &tmap_a, (int32_t)(cur.ks * BKB), (int32_t)tl.a_row0, &full_bar[slot]);
             tma_load_2d(st + C::A_BYTES, &tmap_b, (int32_t)(cur.ks * BKB), (int32_t)tl.b_row0, &full_bar[slot]);
-            bulk_load(ssfb, p.sfb + ((rb_b * p.sf_tiles_per_row + kg0) << 9), sf_bytes, &full_bar[slot]);
-            if (need_b2)
-                bulk_load(ssfb + C::KGS * 512, p.sfb + (((rb_b + 1) * p.sf_tiles_per_row + kg0) << 9), sf_bytes,
-                          &full_bar[slot]);
+            if (C::SCALED) {
+                bulk_load(ssfb, p.sfb + ((rb_b * p.sf_tiles_per_row + kg0) << 9), sf_bytes, &full_bar[slot]);
+                if (need_b2)
+                    bulk_load(ssfb + C::KGS * 512, p.sfb + (((rb_b + 1) * p.sf_tiles_per_row + kg0) << 9), sf_bytes,
+                              &full_bar[slot]);
+            }
             if (!shifted) mbar_arrive(&full_bar[slot]);
             ++issued;
             if (++slot == C::STAGES) { slot = 0; phase ^= 1u; }
@@ -513,7 +531,7 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
         }
         for (int s2 = 0; s2 < C::STAGES; ++s2)
             if (sfa_fills[s2]) mbar_drain(&sfa_bar[s2], (sfa_fills[s2] - 1u) & 1u);
-    } else if (warp == W_SCALE && lane == 0) {
+    } else if (C::SCALED && warp == W_SCALE && lane == 0) {
         // =========================== scale warp ===========================
         // Copies stage `fill`'s scale tiles into scale set fill % SF_SETS (A's k-group j at columns
         // [4j, 4j+4) of the set, B's at [8j, 8j+8): two 128-row tiles) once the stage has landed and
@@ -524,9 +542,9 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
         const uint32_t stage0 = smem_u32(stage_base);
         StageCursor<C::EPS> cur;
         for (cur.begin(&sched, first, stride); cur.valid; cur.next()) {
-            const uint32_t set = fill % C::SF_SETS;
+            const uint32_t set = fill % C::SF_SETS_NZ;
             if (!mbar_wait(&full_bar[slot], phase, abort_flag, p.status) ||
-                !mbar_wait(&sf_free[set], ((fill / C::SF_SETS) & 1u) ^ 1u, abort_flag, p.status))
+                !mbar_wait(&sf_free[set], ((fill / C::SF_SETS_NZ) & 1u) ^ 1u, abort_flag, p.status))
                 break;
             tc_fence_after();
             const uint32_t ssfa = stage0 + (uint32_t)slot * C::STAGE_BYTES + C::A_BYTES + C::B_BYTES;
@@ -561,9 +579,9 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
             const int64_t ks0 = tl.k_begin / C::EPS, ks1 = (tl.k_end + C::EPS - 1) / C::EPS;
             uint32_t accumulate = 0;
             for (int64_t ks = ks0; ks < ks1; ++ks) {
-                const uint32_t set = fill % C::SF_SETS;
+                const uint32_t set = fill % C::SF_SETS_NZ;
                 if (!mbar_wait(&full_bar[slot], phase, abort_flag, p.status) ||
-                    !mbar_wait(&sf_ready[set], (fill / C::SF_SETS) & 1u, abort_flag, p.status)) {
+                    (C::SCALED && !mbar_wait(&sf_ready[set], (fill / C::SF_SETS_NZ) & 1u, abort_flag, p.status))) {
                     ok = false;
                     break;
                 }
@@ -575,16 +593,16 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
                 for (int j = 0; j < 4; ++j) {
                     const int64_t kel = ks * C::EPS + (int64_t)j * C::MMA_K;
                     if (kel < tl.k_begin || kel >= tl.k_end) continue;
-                    const uint32_t kg = FP4 ? (uint32_t)j : 0u;
-                    const uint32_t sf_id = FP4 ? 0u : (uint32_t)j;
+                    const uint32_t kg = C::FP4 ? (uint32_t)j : 0u;
+                    const uint32_t sf_id = (C::SCALED && !C::FP4) ? (uint32_t)j : 0u;
                     const uint32_t idesc = C::IDESC | (sf_id << 4) | (sf_id << 29);
                     // K advance inside the 128-byte swizzled row: 32 bytes per MMA (encoded >> 4)
-                    tc_mma<FP4>(tmem_acc, adesc0 + (uint64_t)(2 * j), bdesc0 + (uint64_t)(2 * j), idesc,
+                    tc_mma<FMT>(tmem_acc, adesc0 + (uint64_t)(2 * j), bdesc0 + (uint64_t)(2 * j), idesc,
                                 tmem_sfa(set) + 4 * kg, tmem_sfb(set) + 8 * kg, accumulate);
                     accumulate = 1;
                 }
                 tc_commit(&empty_bar[slot]);
-                tc_commit(&sf_free[set]);
+                if (C::SCALED) tc_commit(&sf_free[set]);
                 ++fill;
                 if (++slot == C::STAGES) { slot = 0; phase ^= 1u; }
             }
@@ -595,7 +613,7 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
         // wait (bounded) for every tcgen05 operation issued above before TMEM is released
         tc_commit(mma_done);
         mbar_drain(mma_done, 0);
-    } else if (warp == W_TRANSPOSER) {
+    } else if (C::SCALED && warp == W_TRANSPOSER) {
         // ======================= A-scale transposer =======================
         // A tile starting 32*g0 rows into a 128-row scale tile needs rows [32 g0, 128) of that tile
         // followed by rows [0, 32 g0) of the next. In the 512-byte tile layout line l holds the
@@ -796,10 +814,10 @@ static int num_sms() {
     return n;
 }
 
-template <bool FP4>
+template <int FMT>
 static nvq_status launch_gemm(const nvq_gemm_args* a, cudaStream_t stream) {
-    using C = GemmCfg<FP4>;
-    const int64_t row_bytes = FP4 ? a->k / 2 : a->k;
+    using C = GemmCfg<FMT>;
+    const int64_t row_bytes = C::FP4 ? a->k / 2 : (C::SCALED ? a->k : 2 * a->k);
     const int64_t rows_a = a->m;
     const int64_t rows_b = (a->mode == NVQ_GEMM_GROUP_M) ? a->groups * a->n : a->n;
     CUtensorMap ta, tb;
@@ -823,19 +841,19 @@ static nvq_status launch_gemm(const nvq_gemm_args* a, cudaStream_t stream) {
     p.status = a->status;
     p.a_rowtiles = (rows_a + BM - 1) / BM;
     p.b_rowtiles = (rows_b + BM - 1) / BM;
-    const int64_t kb = a->k / (FP4 ? 16 : 32);
+    const int64_t kb = a->k / (C::FP4 ? 16 : 32);
     p.sf_tiles_per_row = (kb + 3) / 4;
 
     static bool attr_ok = false;
     static std::once_flag once;
     std::call_once(once, [] {
-        attr_ok = cudaFuncSetAttribute(block_scaled_gemm_kernel<FP4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        attr_ok = cudaFuncSetAttribute(block_scaled_gemm_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)C::SMEM_BYTES) == cudaSuccess;
     });
     if (!attr_ok) return NVQ_ERR_CUDA;
     const int grid = num_sms();
     if (grid <= 0) return NVQ_ERR_CUDA;
-    block_scaled_gemm_kernel<FP4><<<grid, GEMM_THREADS, C::SMEM_BYTES, stream>>>(ta, tb, p);
+    block_scaled_gemm_kernel<FMT><<<grid, GEMM_THREADS, C::SMEM_BYTES, stream>>>(ta, tb, p);
     if (cudaGetLastError() != cudaSuccess) return NVQ_ERR_CUDA;
     count_launches(1);
     return NVQ_OK;
@@ -849,26 +867,30 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 extern "C" nvq_status block_scaled_grouped_gemm(const nvq_gemm_args* a, void* stream) {
     if (a == nullptr) return NVQ_ERR_INVALID_ARG;
-    if ((a->fmt != NVQ_MXFP8 && a->fmt != NVQ_NVFP4) || (a->mode != NVQ_GEMM_GROUP_M && a->mode != NVQ_GEMM_GROUP_K) ||
+    if ((a->fmt != NVQ_MXFP8 && a->fmt != NVQ_NVFP4 && a->fmt != NVQ_BF16) ||
+        (a->mode != NVQ_GEMM_GROUP_M && a->mode != NVQ_GEMM_GROUP_K) ||
         (a->out_type != NVQ_OUT_BF16 && a->out_type != NVQ_OUT_F32))
         return NVQ_ERR_INVALID_ARG;
     if (a->groups < 0 || a->m < 0 || a->n < 0 || a->k < 0) return NVQ_ERR_INVALID_ARG;
     if (a->groups == 0 || a->m == 0 || a->n == 0) return NVQ_OK;
     if (a->groups > nvq::MAX_GROUPS) return NVQ_ERR_UNSUPPORTED;
-    if (a->a == nullptr || a->b == nullptr || a->sfa == nullptr || a->sfb == nullptr || a->offsets == nullptr ||
-        a->d == nullptr)
+    const bool scaled = a->fmt != NVQ_BF16;
+    if (a->a == nullptr || a->b == nullptr || a->offsets == nullptr || a->d == nullptr ||
+        (scaled && (a->sfa == nullptr || a->sfb == nullptr)))
         return NVQ_ERR_INVALID_ARG;
     if (a->k == 0 || a->n % 128) return NVQ_ERR_INVALID_ARG;
-    if (a->k % (a->mode == NVQ_GEMM_GROUP_M ? 128 : 32)) return NVQ_ERR_INVALID_ARG;
+    if (scaled ? a->k % (a->mode == NVQ_GEMM_GROUP_M ? 128 : 32) : a->k % 16) return NVQ_ERR_INVALID_ARG;
     if (a->ldd < a->n || a->ldd % 8) return NVQ_ERR_INVALID_ARG;
     if (a->m > INT32_MAX || a->k > INT32_MAX || a->groups * a->n > INT32_MAX) return NVQ_ERR_UNSUPPORTED;
     if (a->mode == NVQ_GEMM_GROUP_K) {
-        if (a->fmt != NVQ_MXFP8) return NVQ_ERR_UNSUPPORTED;
+        if (a->fmt == NVQ_NVFP4) return NVQ_ERR_UNSUPPORTED;
         if (a->m % 128 || a->s_a != nullptr) return NVQ_ERR_INVALID_ARG;
     }
-    if (!aligned16(a->a) || !aligned16(a->b) || !aligned16(a->sfa) || !aligned16(a->sfb) || !aligned16(a->d) ||
-        (reinterpret_cast<uintptr_t>(a->offsets) & 7u))
+    if (!aligned16(a->a) || !aligned16(a->b) || (scaled && (!aligned16(a->sfa) || !aligned16(a->sfb))) ||
+        !aligned16(a->d) || (reinterpret_cast<uintptr_t>(a->offsets) & 7u))
         return NVQ_ERR_MISALIGNED;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    return a->fmt == NVQ_NVFP4 ? nvq::launch_gemm<true>(a, s) : nvq::launch_gemm<false>(a, s);
+    if (a->fmt == NVQ_NVFP4) return nvq::launch_gemm<nvq::F_NVFP4>(a, s);
+    if (a->fmt == NVQ_MXFP8) return nvq::launch_gemm<nvq::F_MXFP8>(a, s);
+    return nvq::launch_gemm<nvq::F_BF16>(a, s);
 }

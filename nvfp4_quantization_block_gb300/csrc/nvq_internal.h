@@ -22,6 +22,14 @@ cudaError_t launch_dequantize_bf16(int fmt_nvfp4, const uint8_t* q, const uint8_
                                    int scope_matrix, int64_t groups, int64_t rows, int64_t cols,
                                    int mma_layout, uint16_t* out, cudaStream_t stream);
 
+cudaError_t launch_sf_layout_convert(const uint8_t* src, int to_mma, int64_t rows, int64_t kb, uint8_t* dst,
+                                     cudaStream_t stream);
+
+cudaError_t launch_quantized_gather_rows(const uint8_t* q, const uint8_t* sf, const float* s, int64_t src_rows,
+                                         int64_t qbytes, int64_t kb, int src_mma, const int32_t* index, int64_t rows,
+                                         uint8_t* q_out, uint8_t* sf_out, float* s_out, int dst_mma,
+                                         int32_t* status, cudaStream_t stream);
+
 // Host-side count of kernels this library has enqueued (diagnostics; see nvq_launch_count).
 void count_launches(int n);
 }  // namespace nvq

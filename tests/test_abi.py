@@ -74,6 +74,22 @@ def test_host_validation_rejects_before_launch(lib):
     assert t(fake, 4, 40, 40, fake, fake, fake, 0, None) == 1                 # cols % 16
     assert t(fake, 4, 64, 64, fake, fake, None, 0, None) == 1                 # missing s_tok
     assert t(fake, 0, 64, 64, None, None, None, 0, None) == 0
+    cv = lib.sf_layout_convert
+    cv.argtypes = [vp, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, vp, ctypes.c_int, vp]
+    cv.restype = ctypes.c_int
+    assert cv(fake, 0, 8, 4, fake, 0, None) == 1                 # same layout both sides
+    assert cv(fake, 0, 8, 4, odd, 1, None) == 2                  # misaligned destination
+    assert cv(fake, 0, 0, 4, fake, 1, None) == 0                 # empty is a no-op
+    g = lib.quantized_gather_rows
+    g.argtypes = [ctypes.c_int, vp, vp, vp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, vp, ctypes.c_int64,
+                  vp, vp, vp, ctypes.c_int, vp, vp]
+    g.restype = ctypes.c_int
+    assert g(1, fake, fake, fake, 4, 40, 1, fake, 8, fake, fake, fake, 1, None, None) == 1   # cols % 16
+    assert g(1, fake, fake, None, 4, 64, 1, fake, 8, fake, fake, fake, 1, None, None) == 1   # NVFP4 needs s
+    assert g(0, fake, fake, None, 4, 48, 1, fake, 8, fake, fake, None, 1, None, None) == 1   # MXFP8 cols % 32
+    assert g(1, fake, fake, fake, 4, 64, 1, None, 8, fake, fake, fake, 1, None, None) == 1   # no index
+    assert g(1, odd, fake, fake, 4, 64, 1, fake, 8, fake, fake, fake, 1, None, None) == 2    # misaligned q
+    assert g(1, fake, fake, fake, 4, 64, 1, fake, 0, None, None, None, 1, None, None) == 0   # no rows
     d = lib.dequantize_bf16
     d.argtypes = [ctypes.c_int, vp, vp, vp, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                   ctypes.c_int, vp, vp]

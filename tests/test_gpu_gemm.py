@@ -312,3 +312,80 @@ def test_full_size_weight_gradient_sampled(nvq):
     Dv, bd = oracle.grouped_gemm_entries("k", A, B, np.stack([offs[ee], offs[ee + 1]], 1), np.ones(S))
     got = d[torch.from_numpy(ee).cuda(), torch.from_numpy(ii).cuda(), torch.from_numpy(jj).cuda()]
     _check(got, Dv, bd, True)
+
+
+# ------------------------------------------------------------------------------------------------
+# BF16 grouped GEMM (high-precision and dequantized backward) [Miles-zh, "高精度反向和去量化反向"]
+# ------------------------------------------------------------------------------------------------
+def _bf16_m(nvq, counts, K, N, seed, out_type):
+    E = len(counts)
+    offs, xb = _routed(counts, K, seed)
+    rng = np.random.default_rng(seed + 1)
+    wb = _bits(rng.standard_normal((E, N, K)) * 0.02 * np.exp(rng.uniform(-2, 2, (E, 1, 1))))   # B[e] [N, K]
+    x = workloads.from_bits(xb, "cuda")
+    w = workloads.from_bits(wb, "cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    d = nvq.block_scaled_grouped_gemm(nvq.BF16, nvq.GEMM_GROUP_M, x, None, w, None, torch.from_numpy(offs).cuda(),
+                                      m=x.shape[0], n=N, k=K, groups=E, out_type=out_type, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    D, bound = oracle.grouped_gemm_reference("m", oracle.bf16_bits_to_f64(xb), oracle.bf16_bits_to_f64(wb), offs)
+    rows = ~np.isnan(D[:, 0])
+    _check(d[torch.from_numpy(rows).cuda()], D[rows], bound[rows], out_type == nvq.OUT_BF16)
+
+
+@pytest.mark.parametrize("counts,K,N,out", [
+    ([256], 512, 384, "f32"),                    # one group, N ragged against the 256-column tile
+    ([256], 512, 384, "bf16"),
+    ([96, 0, 160, 33, 300], 256, 256, "f32"),    # group starts at 32-row offsets
+    ([1, 31, 64, 0, 0, 129], 80, 512, "f32"),    # K ragged against the 64-element stage
+    ([0, 0, 0], 256, 256, "f32"),
+])
+def test_bf16_grouped_rows(nvq, counts, K, N, out):
+    _bf16_m(nvq, counts, K, N, seed=sum(counts) + K, out_type=nvq.OUT_F32 if out == "f32" else nvq.OUT_BF16)
+
+
+def test_bf16_many_tiles_per_cta(nvq):
+    # more tiles than CTAs: the stage ring wraps across tiles of different groups
+    _bf16_m(nvq, [150, 33, 260, 0, 121, 97, 201, 64, 180, 5, 140, 230], 1024, 2560, seed=31, out_type=nvq.OUT_F32)
+
+
+@pytest.mark.parametrize("counts,Kin,Nout", [([500, 40], 384, 256), ([100, 0, 250, 33], 256, 384)])
+def test_bf16_weight_gradient_grouped_k(nvq, counts, Kin, Nout):
+    # dW[e] = X_e^T dY_e with X^T [Kin, R] and dY^T [Nout, R] (K-major over the routed rows)
+    offs, xb = _routed(counts, Kin, seed=7)
+    rng = np.random.default_rng(8)
+    dy = rng.standard_normal((int(offs[-1]), Nout)) * 1e-3
+    dy[~workloads.valid_row_mask(counts, offs)] = 0
+    xt, gt = np.ascontiguousarray(xb.T), np.ascontiguousarray(_bits(dy).T)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    d = nvq.block_scaled_grouped_gemm(nvq.BF16, nvq.GEMM_GROUP_K, workloads.from_bits(xt, "cuda"), None,
+                                      workloads.from_bits(gt, "cuda"), None, torch.from_numpy(offs).cuda(),
+                                      m=Kin, n=Nout, k=xt.shape[1], groups=len(counts), out_type=nvq.OUT_F32,
+                                      status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    D, bound = oracle.grouped_gemm_reference("k", oracle.bf16_bits_to_f64(xt), oracle.bf16_bits_to_f64(gt), offs)
+    _check(d, D, bound, False)
+
+
+def test_bf16_dequantized_backward_dgrad(nvq):
+    """Dequantized backward, data gradient: dX = dY W^T per expert with W the BF16 dequantization of
+    its MXFP8 rowwise copy (blocks along the output dimension, the reduction dimension here)."""
+    counts, Kin, Nout = [130, 0, 61, 200], 256, 384
+    E = len(counts)
+    offs, gb = _routed(counts, Nout, seed=12)
+    rng = np.random.default_rng(13)
+    wb = _bits(rng.standard_normal((E * Kin, Nout)) * 0.02)               # W[e] [Kin, Nout], stacked
+    qw = nvq.mxfp8_quantize(workloads.from_bits(wb, "cuda"), colwise=False, sf_layout="mma")
+    wdq = nvq.dequantize_bf16(nvq.MXFP8, qw["q_row"], qw["sf_row"], rows=E * Kin, cols=Nout)
+    g = workloads.from_bits(gb, "cuda")
+    d = nvq.block_scaled_grouped_gemm(nvq.BF16, nvq.GEMM_GROUP_M, g, None, wdq, None, torch.from_numpy(offs).cuda(),
+                                      m=g.shape[0], n=Kin, k=Nout, groups=E, out_type=nvq.OUT_F32)
+    torch.cuda.synchronize()
+    rw = oracle.mxfp8_quantize(wb, colwise=False)
+    wdq_ref = oracle.bf16_bits_to_f64(oracle.f64_to_bf16_bits_rne(oracle.deq_operand("mxfp8", rw["q_row"], rw["sf_row"])))
+    assert np.array_equal(workloads.to_bits(wdq.cpu()), oracle.f64_to_bf16_bits_rne(wdq_ref))   # the dequantization
+    D, bound = oracle.grouped_gemm_reference("m", oracle.bf16_bits_to_f64(gb), wdq_ref.reshape(E, Kin, Nout), offs)
+    rows = ~np.isnan(D[:, 0])
+    _check(d[torch.from_numpy(rows).cuda()], D[rows], bound[rows], False)

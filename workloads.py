@@ -61,21 +61,44 @@ def from_bits(bits, device="cpu"):
 # Routing
 # ----------------------------------------------------------------------------------------------
 
-def route_counts(tokens, experts=EXPERTS, topk=TOPK, zipf_s=1.1, seed=0):
-    """Rows per expert when each token takes ``topk`` distinct experts by Gumbel-top-k on log p_r.
+def route_choices(tokens, experts=EXPERTS, topk=TOPK, zipf_s=1.1, seed=0):
+    """The ``topk`` distinct experts of every token, by Gumbel-top-k on log p_r: int64 [tokens, topk].
 
-    zipf_s > 0: p_r ~ r^-s (r = 1..experts); zipf_s == 0: uniform. Returns int64 [experts].
+    zipf_s > 0: p_r ~ r^-s (r = 1..experts); zipf_s == 0: uniform.
     """
     rng = np.random.default_rng(seed)
     logp = -zipf_s * np.log(np.arange(1, experts + 1, dtype=np.float64))
-    counts = np.zeros(experts, dtype=np.int64)
+    out = np.empty((tokens, topk), dtype=np.int64)
     chunk = 4096
     for t0 in range(0, tokens, chunk):
         n = min(chunk, tokens - t0)
         gumbel = -np.log(-np.log(rng.random((n, experts))))
-        top = np.argpartition(-(logp + gumbel), topk - 1, axis=1)[:, :topk]
-        counts += np.bincount(top.reshape(-1), minlength=experts)
-    return counts
+        out[t0:t0 + n] = np.argpartition(-(logp + gumbel), topk - 1, axis=1)[:, :topk]
+    return out
+
+
+def route_counts(tokens, experts=EXPERTS, topk=TOPK, zipf_s=1.1, seed=0):
+    """Rows per expert of ``route_choices``: int64 [experts]."""
+    top = route_choices(tokens, experts, topk, zipf_s, seed)
+    return np.bincount(top.reshape(-1), minlength=experts).astype(np.int64)
+
+
+def dispatch_index(choices, offsets, experts=EXPERTS):
+    """Source token of every routed row (expert-sorted, each expert's tokens in token order, segments
+    starting at ``offsets``): int32 [offsets[-1]], -1 on padding rows."""
+    choices = np.asarray(choices)
+    tokens, topk = choices.shape
+    idx = np.full(int(offsets[-1]), -1, dtype=np.int32)
+    flat_e = choices.reshape(-1)
+    flat_t = np.repeat(np.arange(tokens, dtype=np.int32), topk)
+    order = np.argsort(flat_e, kind="stable")           # by expert, tokens in order within one
+    counts = np.bincount(flat_e, minlength=experts)
+    pos = 0
+    for e in range(experts):
+        c = int(counts[e])
+        idx[int(offsets[e]):int(offsets[e]) + c] = flat_t[order[pos:pos + c]]
+        pos += c
+    return idx
 
 
 def padded_offsets(counts, align):
