@@ -6,13 +6,17 @@
 // columnwise 32x1 copies are numerically different and are both quantized from the original
 // full-precision data during quantization)].
 //
-// Design: one CTA per 128 x 128 bf16 tile (32 KB). Each warp streams two 256-byte row segments per
-// instruction with 128-bit loads; the rowwise copy is produced straight from registers (a 1x32
-// block is four lanes, amax by two xor-shuffles). The tile is parked in shared memory, and the
-// columnwise copy is produced from it by 256 threads, each owning a column pair of one 32-row
-// block (conflict-free: a warp reads 128 contiguous bytes of one tile row per access). The
-// columnwise codes are written transposed, 32 contiguous bytes per column and block. Input bytes
-// are read from HBM exactly once.
+// Design: one CTA per 128 x 128 bf16 tile (32 KB). With a columnwise copy the tile is copied straight
+// into shared memory with cp.async (two 256-byte row segments per warp instruction, no registers
+// held while the loads are in flight, 5-6 CTAs per SM); the rowwise-only copy keeps the tile in
+// registers (4 CTAs per SM, no barrier). The rowwise copy is produced by the same lanes from 16-byte
+// pieces (a 1x32 block is four lanes, amax by two xor-shuffles); the columnwise copy by 256
+// threads, each owning a column pair of one 32-row block (conflict-free: a warp reads 128
+// contiguous bytes of one tile row per access), amax in one sweep of its 32 words and codes in a
+// second. The columnwise codes are written transposed, 32 contiguous bytes per column and block.
+// Input bytes are read from HBM exactly once.
+#include <mutex>
+
 #include "nvq_device.cuh"
 #include "nvq_internal.h"
 
@@ -21,7 +25,18 @@ namespace nvq {
 constexpr int MX_TILE = 128;
 constexpr int MX_THREADS = 256;
 
-__global__ void __launch_bounds__(MX_THREADS)
+// Resident CTAs per SM of each variant (measured on GB300). STAGED: the tile is copied to shared
+// memory by cp.async and both copies are made from there (5-6 CTAs per SM; best when the grid is
+// many waves deep); otherwise the tile is loaded into registers, the rowwise copy is made straight
+// from them and the tile is parked in shared memory for the columnwise copy (4 CTAs per SM; shorter
+// per-CTA latency, best for grids of one or two waves).
+template <bool ROW, bool COL, bool STAGED>
+struct MxOcc {
+    static constexpr int value = STAGED ? (ROW ? 6 : 5) : 4;
+};
+
+template <bool ROW, bool COL, bool STAGED>
+__global__ void __launch_bounds__(MX_THREADS, (MxOcc<ROW, COL, STAGED>::value))
 mxfp8_quant_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t C, int64_t ldx,
                    uint8_t* __restrict__ q_row, uint8_t* __restrict__ sf_row,
                    uint8_t* __restrict__ q_colT, uint8_t* __restrict__ sf_colT, int mma_layout) {
@@ -31,33 +46,47 @@ mxfp8_quant_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t C, int64_t
     const int64_t r0 = (int64_t)blockIdx.y * MX_TILE;
     const int64_t c0 = (int64_t)blockIdx.x * MX_TILE;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const bool do_row = q_row != nullptr, do_col = q_colT != nullptr;
+    constexpr bool do_row = ROW, do_col = COL;
     const int64_t kb_row = C >> 5;          // scale columns of the rowwise copy
     const int64_t kb_col = R >> 5;          // scale columns of the columnwise copy
 
-    // ---- load: 8 instructions per thread, each 16 bytes = 8 bf16 of one row ----
-    uint4 v[8];
+    // ---- load: 8 x 16 bytes per thread (zero outside the matrix), either straight to shared memory
+    // (cp.async: no registers held while the loads are in flight) or into registers ----
     const int cc = (lane & 15) * 8;
+    uint4 v_reg[STAGED ? 1 : 8];
 #pragma unroll
     for (int it = 0; it < 8; ++it) {
         const int rr = it * 16 + warp * 2 + (lane >> 4);
         const int64_t r = r0 + rr, c = c0 + cc;
-        v[it] = make_uint4(0u, 0u, 0u, 0u);
-        if (r < R && c < C) v[it] = ld_stream_v4(x + r * ldx + c);
+        const bool in = r < R && c < C;
+        if (STAGED) {
+            const uint16_t* src = in ? x + r * ldx + c : x;
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;"
+                         ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(&tile[rr][cc >> 1]))), "l"(src),
+                         "r"(in ? 16 : 0)
+                         : "memory");
+        } else {
+            v_reg[STAGED ? 0 : it] = in ? ld_stream_v4(x + r * ldx + c) : make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+    if (STAGED) {
+        asm volatile("cp.async.wait_all;" ::: "memory");
+        __syncthreads();
     }
 
-#pragma unroll
+#pragma unroll STAGED ? 2 : 8
     for (int it = 0; it < 8; ++it) {
         const int rr = it * 16 + warp * 2 + (lane >> 4);
         const int64_t r = r0 + rr, c = c0 + cc;
-        if (do_col) *reinterpret_cast<uint4*>(&tile[rr][cc >> 1]) = v[it];
+        if (!STAGED && do_col) *reinterpret_cast<uint4*>(&tile[rr][cc >> 1]) = v_reg[STAGED ? 0 : it];
         if (do_row) {
-            uint32_t m = absmax_bits_8(v[it]);
+            const uint4 v = STAGED ? *reinterpret_cast<const uint4*>(&tile[rr][cc >> 1]) : v_reg[STAGED ? 0 : it];
+            uint32_t m = absmax_bits_8(v);
             m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
             m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
             const uint32_t sf = e8m0_byte(m << 16);
             const float inv = e8m0_inv_scale(sf);
-            const uint32_t w0 = v[it].x, w1 = v[it].y, w2 = v[it].z, w3 = v[it].w;
+            const uint32_t w0 = v.x, w1 = v.y, w2 = v.z, w3 = v.w;
             uint32_t o0 = cvt_e4m3x2(bf16_lo(w0) * inv, bf16_hi(w0) * inv) |
                           (cvt_e4m3x2(bf16_lo(w1) * inv, bf16_hi(w1) * inv) << 16);
             uint32_t o1 = cvt_e4m3x2(bf16_lo(w2) * inv, bf16_hi(w2) * inv) |
@@ -84,16 +113,20 @@ mxfp8_quant_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t C, int64_t
         }
     }
     if (!do_col) return;
-    __syncthreads();
+    if (!STAGED) __syncthreads();
 
-    // ---- columnwise: thread = (column pair cp, 32-row block rb) ----
+    // ---- columnwise: thread = (column pair cp, 32-row block rb). Staged: the block's amax in a
+    // first sweep of its 32 words and the codes in a second (few registers); otherwise the 32 words
+    // are read once into registers. ----
     const int cp = threadIdx.x & 63, rb = threadIdx.x >> 6;
-    uint32_t w[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) w[i] = tile[rb * 32 + i][cp];
+    uint32_t w[STAGED ? 1 : 32];
     uint32_t m2 = 0;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) m2 = __vmaxu2(m2, w[i] & 0x7FFF7FFFu);
+    for (int i = 0; i < 32; ++i) {
+        const uint32_t wi = tile[rb * 32 + i][cp];
+        if (!STAGED) w[STAGED ? 0 : i] = wi;
+        m2 = __vmaxu2(m2, wi & 0x7FFF7FFFu);
+    }
     const uint32_t sf_lo = e8m0_byte((m2 & 0xFFFFu) << 16);
     const uint32_t sf_hi = e8m0_byte(m2 & 0xFFFF0000u);
     const float inv_lo = e8m0_inv_scale(sf_lo), inv_hi = e8m0_inv_scale(sf_hi);
@@ -103,11 +136,13 @@ mxfp8_quant_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t C, int64_t
         uint32_t olo[8], ohi[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const uint32_t a0 = w[4 * i], a1 = w[4 * i + 1], a2 = w[4 * i + 2], a3 = w[4 * i + 3];
-            olo[i] = cvt_e4m3x2(bf16_lo(a0) * inv_lo, bf16_lo(a1) * inv_lo) |
-                     (cvt_e4m3x2(bf16_lo(a2) * inv_lo, bf16_lo(a3) * inv_lo) << 16);
-            ohi[i] = cvt_e4m3x2(bf16_hi(a0) * inv_hi, bf16_hi(a1) * inv_hi) |
-                     (cvt_e4m3x2(bf16_hi(a2) * inv_hi, bf16_hi(a3) * inv_hi) << 16);
+            uint32_t a[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) a[j] = STAGED ? tile[rb * 32 + 4 * i + j][cp] : w[STAGED ? 0 : 4 * i + j];
+            olo[i] = cvt_e4m3x2(bf16_lo(a[0]) * inv_lo, bf16_lo(a[1]) * inv_lo) |
+                     (cvt_e4m3x2(bf16_lo(a[2]) * inv_lo, bf16_lo(a[3]) * inv_lo) << 16);
+            ohi[i] = cvt_e4m3x2(bf16_hi(a[0]) * inv_hi, bf16_hi(a[1]) * inv_hi) |
+                     (cvt_e4m3x2(bf16_hi(a[2]) * inv_hi, bf16_hi(a[3]) * inv_hi) << 16);
         }
         uint4* plo = reinterpret_cast<uint4*>(q_colT + c * R + rs);
         uint4* phi = reinterpret_cast<uint4*>(q_colT + (c + 1) * R + rs);
@@ -139,8 +174,27 @@ cudaError_t launch_mxfp8_quantize(const uint16_t* x, int64_t R, int64_t C, int64
                                   int mma_layout, cudaStream_t stream) {
     // the MMA layout pads rows to 128: cover the padded rows so the padding gets zero scales
     dim3 grid((unsigned)((C + MX_TILE - 1) / MX_TILE), (unsigned)((R + MX_TILE - 1) / MX_TILE));
-    mxfp8_quant_kernel<<<grid, MX_THREADS, 0, stream>>>(x, R, C, ldx, q_row, sf_row, q_colT, sf_colT,
-                                                        mma_layout);
+    static int sms = 0;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            sms = 0;
+    });
+    // grids deeper than two waves of the register variant are staged through shared memory
+    const bool staged = (int64_t)grid.x * grid.y > 2 * 4 * (int64_t)sms;
+#define NVQ_MX(RW, CL, ST) \
+    mxfp8_quant_kernel<RW, CL, ST><<<grid, MX_THREADS, 0, stream>>>(x, R, C, ldx, q_row, sf_row, q_colT, sf_colT, mma_layout)
+    if (q_row && q_colT) {
+        if (staged) NVQ_MX(true, true, true);
+        else NVQ_MX(true, true, false);
+    } else if (q_colT) {
+        if (staged) NVQ_MX(false, true, true);
+        else NVQ_MX(false, true, false);
+    } else {
+        NVQ_MX(true, false, false);
+    }
+#undef NVQ_MX
     const cudaError_t err = cudaGetLastError();
     if (err == cudaSuccess) count_launches(1);
     return err;

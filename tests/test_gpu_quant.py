@@ -103,6 +103,22 @@ def test_mxfp8_row_col_bit_exact(nvq, fam, shape, layout):
         assert np.array_equal(_np(out["sf_colT"]), oracle.sf_to_mma_layout(ref["sf_colT"]))
 
 
+@pytest.mark.parametrize("rowwise", [True, False])
+def test_mxfp8_deep_grid_staged_path(nvq, rowwise):
+    """A grid deeper than two waves (33 x 41 tiles of 128 x 128, ragged in both directions) takes
+    the shared-memory staged variant of the kernel; bit-exact against the oracle, both copies."""
+    shape = (4128, 5152)
+    bits = family("random", shape, seed=17)
+    ref = oracle.mxfp8_quantize(bits, rowwise=rowwise)
+    o = nvq.mxfp8_quantize(_dev(bits), rowwise=rowwise, sf_layout="mma")
+    torch.cuda.synchronize()
+    assert np.array_equal(_np(o["q_colT"]), ref["q_colT"])
+    assert np.array_equal(_np(o["sf_colT"]), oracle.sf_to_mma_layout(ref["sf_colT"]))
+    if rowwise:
+        assert np.array_equal(_np(o["q_row"]), ref["q_row"])
+        assert np.array_equal(_np(o["sf_row"]), oracle.sf_to_mma_layout(ref["sf_row"]))
+
+
 @pytest.mark.parametrize("shape", [(33, 64), (1, 32), (7, 96)])
 def test_mxfp8_rowwise_only_ragged_rows(nvq, shape):
     bits = family("random", shape, seed=3)
