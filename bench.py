@@ -519,9 +519,36 @@ def _workload_dispatch(torch, nvq, wl, dev):
             "config": config, "dtype": "bf16 -> nvfp4 (gathered)", "unit": "GB/s"}
 
 
+def _workload_swiglu(torch, nvq, wl, dev):
+    """The down projection's NVFP4 input straight from the gate_up GEMM output: SwiGLU + per-token
+    NVFP4 in one pass over the 132960 x (768 + 768) routed activation."""
+    counts, offs_np = wl.moe_routing()
+    R = int(offs_np[-1])
+    I = wl.INTERMEDIATE
+    x = wl.routed_activations(counts, offs_np, 2 * I, seed=12, device=dev)
+    out = (torch.empty((R, I // 2), dtype=torch.uint8, device=dev),
+           torch.empty(nvq.sf_bytes(R, I, 16), dtype=torch.uint8, device=dev),
+           torch.empty(R, dtype=torch.float32, device=dev))
+    kernels = [
+        Kernel("nvfp4_swiglu_quantize_per_token down input", "hbm", R * (2 * I * 2 + I / 2 + I / 16 + 4),
+               "quant_nvfp4.cu", "hbm", "4 B read per h element (gate and up bf16) + 0.5625 B written + 4 B/row"),
+    ]
+
+    def step(timer, xin=None, win=None):
+        xx = x if xin is None else xin[0]
+        timer.run(kernels[0].name, lambda: nvq.nvfp4_swiglu_quantize_per_token(xx, out=out))
+        return list(out)
+
+    config = {"workload": "fused SwiGLU + per-token NVFP4 of the MoE gate_up output (Qwen3-30B-A3B shapes)",
+              "gate_up": [R, 2 * I]}
+    return {"step": step, "kernels": kernels, "gemm_flops": 0.0, "inputs": [x], "input_groups": ([0], []),
+            "config": config, "dtype": "bf16 -> swiglu (fp32) -> nvfp4", "unit": "GB/s"}
+
+
 WORKLOADS = {"dense": _workload_dense, "quant": _workload_quant, "moe": _workload_moe, "backward": _workload_backward,
-             "decode": _workload_decode, "dispatch": _workload_dispatch, "dq_backward": _workload_dq_backward}
-GBS_WORKLOADS = ("quant", "dispatch")
+             "decode": _workload_decode, "dispatch": _workload_dispatch, "dq_backward": _workload_dq_backward,
+             "swiglu": _workload_swiglu}
+GBS_WORKLOADS = ("quant", "dispatch", "swiglu")
 
 
 class ClockSampler:

@@ -47,6 +47,8 @@ _sf_bytes = _sig("nvq_sf_bytes", [_i64, _i64, _i32, ctypes.c_int], _i64)
 _launch_count = _sig("nvq_launch_count", [], ctypes.c_uint64)
 _mxfp8_quantize = _sig("mxfp8_quantize", [_vp, _i64, _i64, _i64, _vp, _vp, _vp, _vp, ctypes.c_int, _vp])
 _nvfp4_quantize_per_token = _sig("nvfp4_quantize_per_token", [_vp, _i64, _i64, _i64, _vp, _vp, _vp, ctypes.c_int, _vp])
+_nvfp4_swiglu_quantize = _sig("nvfp4_swiglu_quantize_per_token", [_vp, _i64, _i64, _i64, _vp, _vp, _vp,
+                                                                  ctypes.c_int, _vp])
 _nvfp4_quantize_weights = _sig("nvfp4_quantize_weights", [_vp, _i64, _i64, _i64, _vp, _vp, _vp, ctypes.c_int, _vp])
 _sf_layout_convert = _sig("sf_layout_convert", [_vp, ctypes.c_int, _i64, _i64, _vp, ctypes.c_int, _vp])
 _quantized_gather_rows = _sig("quantized_gather_rows", [ctypes.c_int, _vp, _vp, _vp, _i64, _i64, ctypes.c_int, _vp,
@@ -157,6 +159,27 @@ def nvfp4_quantize_per_token(x, sf_layout="mma", out=None):
     q, sf, s = out
     st = _nvfp4_quantize_per_token(_ptr(x), T, K, x.stride(0) if T else K, _ptr(q), _ptr(sf), _ptr(s), lay, _stream(dev))
     _check(st, "nvfp4_quantize_per_token")
+    return q, sf, s
+
+
+def nvfp4_swiglu_quantize_per_token(gate_up, sf_layout="mma", out=None):
+    """SwiGLU of a fused gate||up activation [T, 2I] (bf16) quantized per token to NVFP4 ->
+    (q [T, I/2] u8, sf u8, s_tok [T] f32), without writing the bf16 activation."""
+    _check_input(gate_up, 2)
+    T, I2 = gate_up.shape
+    if I2 % 2:
+        raise ValueError("gate_up needs an even number of columns")
+    I = I2 // 2
+    lay = _layout(sf_layout)
+    dev = gate_up.device
+    if out is None:
+        out = (torch.empty((T, I // 2), dtype=torch.uint8, device=dev),
+               torch.empty(sf_bytes(T, I, 16, lay), dtype=torch.uint8, device=dev),
+               torch.empty(T, dtype=torch.float32, device=dev))
+    q, sf, s = out
+    st = _nvfp4_swiglu_quantize(_ptr(gate_up), T, I, gate_up.stride(0) if T else I2, _ptr(q), _ptr(sf), _ptr(s),
+                                lay, _stream(dev))
+    _check(st, "nvfp4_swiglu_quantize_per_token")
     return q, sf, s
 
 

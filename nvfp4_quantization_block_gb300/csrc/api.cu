@@ -77,6 +77,20 @@ nvq_status nvfp4_quantize_per_token(const void* x, int64_t rows, int64_t cols, i
                                                           static_cast<cudaStream_t>(stream)));
 }
 
+nvq_status nvfp4_swiglu_quantize_per_token(const void* gate_up, int64_t rows, int64_t cols, int64_t ld,
+                                           uint8_t* q, uint8_t* sf, float* s_tok, nvq_sf_layout sf_layout,
+                                           void* stream) {
+    if (rows < 0 || cols < 0 || !valid_layout(sf_layout)) return NVQ_ERR_INVALID_ARG;
+    if (rows == 0) return NVQ_OK;
+    if (gate_up == nullptr || q == nullptr || sf == nullptr || s_tok == nullptr) return NVQ_ERR_INVALID_ARG;
+    if (cols == 0 || cols % 16 || ld < 2 * cols) return NVQ_ERR_INVALID_ARG;
+    if (!aligned16(gate_up) || ld % 8 || !aligned16(q) || !aligned16(sf) || !aligned16(s_tok))
+        return NVQ_ERR_MISALIGNED;
+    return from_cuda(nvq::launch_nvfp4_swiglu_quantize(static_cast<const uint16_t*>(gate_up), rows, cols, ld, q, sf,
+                                                       s_tok, sf_layout == NVQ_SF_MMA,
+                                                       static_cast<cudaStream_t>(stream)));
+}
+
 nvq_status nvfp4_quantize_weights(const void* w, int64_t experts, int64_t k, int64_t n, uint8_t* qT,
                                   uint8_t* sfT, float* s_w, nvq_sf_layout sf_layout, void* stream) {
     if (experts < 0 || k < 0 || n < 0 || !valid_layout(sf_layout)) return NVQ_ERR_INVALID_ARG;

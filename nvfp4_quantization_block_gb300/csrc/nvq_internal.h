@@ -14,6 +14,9 @@ cudaError_t launch_nvfp4_quantize_per_token(const uint16_t* x, int64_t R, int64_
                                             uint8_t* q, uint8_t* sf, float* s_tok, int mma_layout,
                                             cudaStream_t stream);
 
+cudaError_t launch_nvfp4_swiglu_quantize(const uint16_t* gate_up, int64_t R, int64_t I, int64_t ld, uint8_t* q,
+                                         uint8_t* sf, float* s_tok, int mma_layout, cudaStream_t stream);
+
 cudaError_t launch_nvfp4_quantize_weights(const uint16_t* w, int64_t E, int64_t K, int64_t N,
                                           uint8_t* qT, uint8_t* sfT, float* s_w, int mma_layout,
                                           cudaStream_t stream);

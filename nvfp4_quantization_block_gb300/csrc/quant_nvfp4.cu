@@ -31,6 +31,50 @@ __device__ __forceinline__ void load_block(const uint16_t* p, uint4& a, uint4& b
     }
 }
 
+// SwiGLU of a fused gate||up activation, rounded to bf16 (the down projection's input). The pages'
+// SwiGLU experts run gate and up as one GEMM [Miles-zh, "逐 Token 激活值缩放"]; the activation is
+// silu(g) u with silu(g) = g / (1 + exp(-g)) (Shazeer 2020), computed in float32 with one rounding
+// per operation (no contraction: __f*_rn), so that it is reproducible bit for bit. exp is our own:
+// Cody and Waite's two-constant range reduction (clamped to [-87, 88] so 2^n stays normal) and a
+// degree-6 Taylor polynomial in Horner order.
+__device__ __forceinline__ float swiglu_exp(float x) {
+    x = fminf(fmaxf(x, -87.0f), 88.0f);
+    const float n = __fsub_rn(__fadd_rn(__fmul_rn(x, (float)1.4426950408889634), 12582912.0f), 12582912.0f);
+    const float r = __fsub_rn(__fsub_rn(x, __fmul_rn(n, 0.693145751953125f)),
+                              __fmul_rn(n, (float)(0.6931471805599453 - 0.693145751953125)));
+    float p = (float)(1.0 / 720.0);
+    p = __fadd_rn(__fmul_rn(p, r), (float)(1.0 / 120.0));
+    p = __fadd_rn(__fmul_rn(p, r), (float)(1.0 / 24.0));
+    p = __fadd_rn(__fmul_rn(p, r), (float)(1.0 / 6.0));
+    p = __fadd_rn(__fmul_rn(p, r), 0.5f);
+    p = __fadd_rn(__fmul_rn(p, r), 1.0f);
+    p = __fadd_rn(__fmul_rn(p, r), 1.0f);
+    return __fmul_rn(p, __int_as_float(((int)n + 127) << 23));
+}
+
+__device__ __forceinline__ float swiglu(float g, float u) {
+    const float d = __fadd_rn(1.0f, swiglu_exp(-g));
+    return __fmul_rn(__fdiv_rn(g, d), u);
+}
+
+// bf16x2 words of SwiGLU(gate, up) for two bf16x2 words
+__device__ __forceinline__ uint32_t swiglu2(uint32_t g, uint32_t u) {
+    return cvt_bf16x2(swiglu(bf16_lo(g), bf16_lo(u)), swiglu(bf16_hi(g), bf16_hi(u)));
+}
+
+// One 16-element block of the row: loaded as is, or (SWIGLU) formed from the gate block at p and
+// the up block at p + up.
+template <bool V8, bool SWIGLU>
+__device__ __forceinline__ void row_block(const uint16_t* p, int64_t up, uint4& a, uint4& b) {
+    load_block<V8>(p, a, b);
+    if (SWIGLU) {
+        uint4 ua, ub;
+        load_block<V8>(p + up, ua, ub);
+        a = make_uint4(swiglu2(a.x, ua.x), swiglu2(a.y, ua.y), swiglu2(a.z, ua.z), swiglu2(a.w, ua.w));
+        b = make_uint4(swiglu2(b.x, ub.x), swiglu2(b.y, ub.y), swiglu2(b.z, ub.z), swiglu2(b.w, ub.w));
+    }
+}
+
 // Scale code and the 16 codes of one block (two uint4 of 8 bf16, magnitude maximum mb as bf16
 // bits): table-driven and branch-free in the fast path; exact fp64 decisions for a scope with a
 // tiny (or zero) coarse scale.
@@ -87,7 +131,7 @@ __device__ __forceinline__ void token_block(const uint4& a, const uint4& b, uint
 // One warp per token row, one 16-element block per lane per step: the row (up to 2048 elements) is
 // loaded once with 32-byte coalesced loads, reduced to its amax with warp shuffles, and encoded
 // from registers, so each input byte is read from HBM once.
-template <bool V8>
+template <bool V8, bool SWIGLU>
 __global__ void __launch_bounds__(TOK_THREADS)
 nvfp4_token_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t C, int64_t ldx,
                    uint8_t* __restrict__ q, uint8_t* __restrict__ sf, float* __restrict__ s_tok,
@@ -113,7 +157,7 @@ nvfp4_token_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t C, int64_t
     for (int i = 0; i < TOK_NREG; ++i) {
         va[i] = vb[i] = make_uint4(0u, 0u, 0u, 0u);
         const int64_t kb = (int64_t)i * 32 + lane;
-        if (real && i < iters && kb < nkb) load_block<V8>(xr + kb * 16, va[i], vb[i]);
+        if (real && i < iters && kb < nkb) row_block<V8, SWIGLU>(xr + kb * 16, C, va[i], vb[i]);
         mbk[i] = max(absmax_bits_8(va[i]), absmax_bits_8(vb[i]));
         m = max(m, mbk[i]);
     }
@@ -121,7 +165,7 @@ nvfp4_token_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t C, int64_t
         const int64_t kb = (int64_t)i * 32 + lane;
         if (real && kb < nkb) {
             uint4 a, b;
-            load_block<V8>(xr + kb * 16, a, b);
+            row_block<V8, SWIGLU>(xr + kb * 16, C, a, b);
             m = max(m, max(absmax_bits_8(a), absmax_bits_8(b)));
         }
     }
@@ -151,27 +195,40 @@ nvfp4_token_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t C, int64_t
     for (int i = TOK_NREG; i < iters; ++i) {
         const int64_t kb = (int64_t)i * 32 + lane;
         uint4 a = make_uint4(0u, 0u, 0u, 0u), b = a;
-        if (real && kb < nkb) load_block<V8>(xr + kb * 16, a, b);
+        if (real && kb < nkb) row_block<V8, SWIGLU>(xr + kb * 16, C, a, b);
         const uint32_t mb = max(absmax_bits_8(a), absmax_bits_8(b));
         if (!sc.exact) token_block<false>(a, b, mb, i, lane, real, sc, T, info, o);
         else token_block<true>(a, b, mb, i, lane, real, sc, T, info, o);
     }
 }
 
-cudaError_t launch_nvfp4_quantize_per_token(const uint16_t* x, int64_t R, int64_t C, int64_t ldx,
-                                            uint8_t* q, uint8_t* sf, float* s_tok, int mma_layout,
-                                            cudaStream_t stream) {
+template <bool SWIGLU>
+static cudaError_t launch_token(const uint16_t* x, int64_t R, int64_t C, int64_t ldx, uint8_t* q, uint8_t* sf,
+                                float* s_tok, int mma_layout, cudaStream_t stream) {
     const int64_t cover = mma_layout ? ((R + 127) & ~int64_t(127)) : R;
     const int rows_per_cta = TOK_THREADS / 32;
     const int64_t grid = (cover + rows_per_cta - 1) / rows_per_cta;
-    const bool v8 = ((reinterpret_cast<uintptr_t>(x) & 31u) == 0) && (ldx % 16 == 0);
+    const bool v8 = ((reinterpret_cast<uintptr_t>(x) & 31u) == 0) && (ldx % 16 == 0) && (!SWIGLU || C % 16 == 0);
     if (v8)
-        nvfp4_token_kernel<true><<<(unsigned)grid, TOK_THREADS, 0, stream>>>(x, R, C, ldx, q, sf, s_tok, mma_layout, cover);
+        nvfp4_token_kernel<true, SWIGLU><<<(unsigned)grid, TOK_THREADS, 0, stream>>>(x, R, C, ldx, q, sf, s_tok,
+                                                                                    mma_layout, cover);
     else
-        nvfp4_token_kernel<false><<<(unsigned)grid, TOK_THREADS, 0, stream>>>(x, R, C, ldx, q, sf, s_tok, mma_layout, cover);
+        nvfp4_token_kernel<false, SWIGLU><<<(unsigned)grid, TOK_THREADS, 0, stream>>>(x, R, C, ldx, q, sf, s_tok,
+                                                                                     mma_layout, cover);
     const cudaError_t err = cudaGetLastError();
     if (err == cudaSuccess) count_launches(1);
     return err;
+}
+
+cudaError_t launch_nvfp4_quantize_per_token(const uint16_t* x, int64_t R, int64_t C, int64_t ldx,
+                                            uint8_t* q, uint8_t* sf, float* s_tok, int mma_layout,
+                                            cudaStream_t stream) {
+    return launch_token<false>(x, R, C, ldx, q, sf, s_tok, mma_layout, stream);
+}
+
+cudaError_t launch_nvfp4_swiglu_quantize(const uint16_t* gate_up, int64_t R, int64_t I, int64_t ld, uint8_t* q,
+                                         uint8_t* sf, float* s_tok, int mma_layout, cudaStream_t stream) {
+    return launch_token<true>(gate_up, R, I, ld, q, sf, s_tok, mma_layout, stream);
 }
 
 // ------------------------------------------------------------------------------------------------

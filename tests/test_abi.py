@@ -74,6 +74,13 @@ def test_host_validation_rejects_before_launch(lib):
     assert t(fake, 4, 40, 40, fake, fake, fake, 0, None) == 1                 # cols % 16
     assert t(fake, 4, 64, 64, fake, fake, None, 0, None) == 1                 # missing s_tok
     assert t(fake, 0, 64, 64, None, None, None, 0, None) == 0
+    sw = lib.nvfp4_swiglu_quantize_per_token
+    sw.argtypes = [vp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, vp, vp, vp, ctypes.c_int, vp]
+    sw.restype = ctypes.c_int
+    assert sw(fake, 4, 40, 80, fake, fake, fake, 0, None) == 1     # cols % 16
+    assert sw(fake, 4, 64, 100, fake, fake, fake, 0, None) == 1    # ld < 2 cols
+    assert sw(fake, 4, 64, 132, fake, fake, fake, 0, None) == 2    # ld % 8
+    assert sw(fake, 0, 64, 128, None, None, None, 0, None) == 0    # empty is a no-op
     cv = lib.sf_layout_convert
     cv.argtypes = [vp, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, vp, ctypes.c_int, vp]
     cv.restype = ctypes.c_int
