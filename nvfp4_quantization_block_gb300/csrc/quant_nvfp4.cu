@@ -104,19 +104,16 @@ struct TokenRowOut {
     int mma_layout;
 };
 
-// One 16-element block per lane: block kb = 32 i + lane of the row.
-template <bool EXACT>
-__device__ __forceinline__ void token_block(const uint4& a, const uint4& b, uint32_t mb, int i, int lane, bool real,
-                                            const Nvfp4Scope& sc, const Nvfp4Table& T, const Nvfp4CodeInfo& I,
+// Stores of one 16-element block kb of the row (codes c0, c1, scale code sfc), one block per lane:
+// the four lanes l..l+3 (l a multiple of 4 within the row's lanes) hold four consecutive blocks and
+// share one scale word. Called by all 32 lanes of the warp together (shuffles).
+__device__ __forceinline__ void token_store(uint32_t sfc, uint32_t c0, uint32_t c1, int64_t kb, int l, bool real,
                                             const TokenRowOut& o) {
-    const int64_t kb = (int64_t)i * 32 + lane;
-    uint32_t c0, c1;
-    const uint32_t sfc = encode_block<EXACT>(a, b, mb, sc, T, I, c0, c1);
     if (real && kb < o.nkb) *reinterpret_cast<uint2*>(o.q + kb * 8) = make_uint2(c0, c1);
     const uint32_t s1 = __shfl_down_sync(0xffffffffu, sfc, 1);
     const uint32_t s2 = __shfl_down_sync(0xffffffffu, sfc, 2);
     const uint32_t s3 = __shfl_down_sync(0xffffffffu, sfc, 3);
-    if ((lane & 3) == 0 && kb < o.nkb) {
+    if ((l & 3) == 0 && kb < o.nkb && o.sf != nullptr) {
         const uint32_t word = sfc | (s1 << 8) | (s2 << 16) | (s3 << 24);
         if (o.mma_layout) {
             *reinterpret_cast<uint32_t*>(o.sf + ((kb >> 2) << 9)) = word;
@@ -128,41 +125,97 @@ __device__ __forceinline__ void token_block(const uint4& a, const uint4& b, uint
     }
 }
 
-// One warp per token row, one 16-element block per lane per step: the row (up to 2048 elements) is
-// loaded once with 32-byte coalesced loads, reduced to its amax with warp shuffles, and encoded
-// from registers, so each input byte is read from HBM once.
-template <bool V8, bool SWIGLU>
+// Encode and store one block; the path (table-driven or exact) is the same for every lane.
+template <bool EXACT>
+__device__ __forceinline__ void token_block(const uint4& a, const uint4& b, uint32_t mb, int64_t kb, int l, bool real,
+                                            const Nvfp4Scope& sc, const Nvfp4Table& T, const Nvfp4CodeInfo& I,
+                                            const TokenRowOut& o) {
+    uint32_t c0, c1;
+    const uint32_t sfc = encode_block<EXACT>(a, b, mb, sc, T, I, c0, c1);
+    token_store(sfc, c0, c1, kb, l, real, o);
+}
+
+// Encode and store one block when the two rows of a warp may take different paths: the encoding
+// branches per row, the stores (shuffles) run with the whole warp.
+__device__ __forceinline__ void token_block_mixed(const uint4& a, const uint4& b, uint32_t mb, int64_t kb, int l,
+                                                  bool real, const Nvfp4Scope& sc, const Nvfp4Table& T,
+                                                  const Nvfp4CodeInfo& I, const TokenRowOut& o) {
+    uint32_t c0, c1, sfc;
+    if (!sc.exact) sfc = encode_block<false>(a, b, mb, sc, T, I, c0, c1);
+    else sfc = encode_block<true>(a, b, mb, sc, T, I, c0, c1);
+    __syncwarp();
+    token_store(sfc, c0, c1, kb, l, real, o);
+}
+
+// The scope table of a row built by its LPR lanes (32: nvfp4_table_build_warp; 16: each lane takes
+// the class boundaries of thresholds j and j + 2 (and their j + 4 partners) of class l & 7, and the
+// block-scale boundary of code l).
+template <int LPR>
+__device__ __forceinline__ void nvfp4_table_build_row(Nvfp4Table& T, float s, int l) {
+    if (LPR == 32) {
+        nvfp4_table_build_warp(T, s, l);
+        return;
+    }
+    const uint32_t f = (uint32_t)l & 7u;
+    const float v = (float)(8u + f) * 0x1p-9f;                     // value of E4M3 code 8 + f
+#pragma unroll
+    for (uint32_t t = 0; t < 2; ++t) {
+        const uint32_t j = ((uint32_t)l >> 3) + 2u * t;            // 0..3
+        uint32_t b = bf16_boundary((float)(2u * j + 1u) * 0.25f * v, s, (j & 1u) != 0u);
+        T.bp[f][j] = b | (b << 16);
+        if (j < 3u) T.bp[f][8u + j] = (b | (b << 16)) ^ 0x80008000u;
+        const uint32_t j2 = j + 4u;
+        if (j2 < 7u) {
+            const float m = (j2 == 6u) ? 5.0f : (float)j2 - 1.5f;
+            b = bf16_boundary(m * v, s, (j2 & 1u) != 0u);
+            T.bp[f][j2] = b | (b << 16);
+        }
+    }
+    T.bs[l] = bf16_boundary((float)(3 * (2 * l + 1)) * 0x1p-9f, s, (l & 1) != 0);
+    if (l < 12) T.bp[8][l] = l < 7 ? 0x7F007F00u : (l >= 8 && l < 11 ? 0xFF00FF00u : 0u);
+}
+
+// LPR lanes per token row (32: one row per warp; 16: two rows per warp, for rows of at most 64
+// blocks, so that rows of 48 blocks keep every lane busy), one 16-element block per lane per step:
+// the row is loaded once with 32-byte coalesced loads (held in registers up to TOK_NREG steps),
+// reduced to its amax with shuffles among the row's lanes, and encoded from registers, so each
+// input byte is read from HBM once.
+template <bool V8, bool SWIGLU, int LPR>
 __global__ void __launch_bounds__(TOK_THREADS)
 nvfp4_token_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t C, int64_t ldx,
                    uint8_t* __restrict__ q, uint8_t* __restrict__ sf, float* __restrict__ s_tok,
                    int mma_layout, int64_t rows_cover) {
-    __shared__ Nvfp4Table tables[TOK_THREADS / 32];          // one per warp (token row)
+    constexpr int RPW = 32 / LPR;                              // rows per warp
+    __shared__ Nvfp4Table tables[(TOK_THREADS / 32) * RPW];   // one per row
     __shared__ Nvfp4CodeInfo info;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int half = lane / LPR, l = lane % LPR;               // row of the warp, lane within the row
     for (uint32_t c = threadIdx.x; c < 128u; c += TOK_THREADS) nvfp4_code_info_build(info, c);
     __syncthreads();
-    const int64_t row = (int64_t)blockIdx.x * (TOK_THREADS / 32) + warp;
-    if (row >= rows_cover) return;
-    Nvfp4Table& T = tables[warp];
+    const int64_t row0 = ((int64_t)blockIdx.x * (TOK_THREADS / 32) + warp) * RPW;
+    if (row0 >= rows_cover) return;                            // uniform over the warp
+    const int64_t row = row0 + half;
+    const bool covered = row < rows_cover;                     // the second row of a warp may not be
+    Nvfp4Table& T = tables[warp * RPW + half];
     const bool real = row < R;
-    const int64_t nkb = C >> 4;                          // 16-element blocks
-    const int iters = (int)((nkb + 31) >> 5);
-    const uint16_t* xr = x + row * ldx;
+    const int64_t nkb = C >> 4;                                // 16-element blocks
+    const int iters = (int)((nkb + LPR - 1) / LPR);
+    const uint16_t* xr = x + (real ? row : 0) * ldx;
 
     // pass 1: load (into registers where possible) and reduce the row's amax
     uint4 va[TOK_NREG], vb[TOK_NREG];
-    uint32_t mbk[TOK_NREG];                              // block maxima of the register-resident blocks
+    uint32_t mbk[TOK_NREG];                                    // block maxima of the register-resident blocks
     uint32_t m = 0;
 #pragma unroll
     for (int i = 0; i < TOK_NREG; ++i) {
         va[i] = vb[i] = make_uint4(0u, 0u, 0u, 0u);
-        const int64_t kb = (int64_t)i * 32 + lane;
+        const int64_t kb = (int64_t)i * LPR + l;
         if (real && i < iters && kb < nkb) row_block<V8, SWIGLU>(xr + kb * 16, C, va[i], vb[i]);
         mbk[i] = max(absmax_bits_8(va[i]), absmax_bits_8(vb[i]));
         m = max(m, mbk[i]);
     }
     for (int i = TOK_NREG; i < iters; ++i) {
-        const int64_t kb = (int64_t)i * 32 + lane;
+        const int64_t kb = (int64_t)i * LPR + l;
         if (real && kb < nkb) {
             uint4 a, b;
             row_block<V8, SWIGLU>(xr + kb * 16, C, a, b);
@@ -170,35 +223,41 @@ nvfp4_token_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t C, int64_t
         }
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+    for (int o = LPR / 2; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
     const float s = nvfp4_coarse_scale(__uint_as_float(m << 16));
     const Nvfp4Scope sc = make_nvfp4_scope(s);
-    if (real && lane == 0) s_tok[row] = s;
-    if (!sc.exact) nvfp4_table_build_warp(T, s, lane);
+    if (real && l == 0) s_tok[row] = s;
+    if (!sc.exact) nvfp4_table_build_row<LPR>(T, s, l);
     __syncwarp();
 
     // pass 2: per 1x16 block scale and codes (register-resident blocks first, then any reloads)
     TokenRowOut o;
-    o.q = q + row * (C >> 1);
+    o.q = q + (real ? row : 0) * (C >> 1);
     o.nkb = nkb;
     o.mma_layout = mma_layout;
-    o.sf = mma_layout ? sf + mma_sf_offset(row, 0, nkb) : sf + row * nkb;
-    if (!sc.exact) {
+    o.sf = !covered ? nullptr : (mma_layout ? sf + mma_sf_offset(row, 0, nkb) : sf + row * nkb);
+    const bool any_exact = __any_sync(0xffffffffu, sc.exact);
+    const bool all_exact = __all_sync(0xffffffffu, sc.exact);
+    if (!any_exact) {
 #pragma unroll
         for (int i = 0; i < TOK_NREG; ++i)
-            if (i < iters) token_block<false>(va[i], vb[i], mbk[i], i, lane, real, sc, T, info, o);
+            if (i < iters) token_block<false>(va[i], vb[i], mbk[i], (int64_t)i * LPR + l, l, real, sc, T, info, o);
+    } else if (all_exact) {
+#pragma unroll
+        for (int i = 0; i < TOK_NREG; ++i)
+            if (i < iters) token_block<true>(va[i], vb[i], mbk[i], (int64_t)i * LPR + l, l, real, sc, T, info, o);
     } else {
+        // the two rows of the warp take different paths
 #pragma unroll
         for (int i = 0; i < TOK_NREG; ++i)
-            if (i < iters) token_block<true>(va[i], vb[i], mbk[i], i, lane, real, sc, T, info, o);
+            if (i < iters) token_block_mixed(va[i], vb[i], mbk[i], (int64_t)i * LPR + l, l, real, sc, T, info, o);
     }
     for (int i = TOK_NREG; i < iters; ++i) {
-        const int64_t kb = (int64_t)i * 32 + lane;
+        const int64_t kb = (int64_t)i * LPR + l;
         uint4 a = make_uint4(0u, 0u, 0u, 0u), b = a;
         if (real && kb < nkb) row_block<V8, SWIGLU>(xr + kb * 16, C, a, b);
         const uint32_t mb = max(absmax_bits_8(a), absmax_bits_8(b));
-        if (!sc.exact) token_block<false>(a, b, mb, i, lane, real, sc, T, info, o);
-        else token_block<true>(a, b, mb, i, lane, real, sc, T, info, o);
+        token_block_mixed(a, b, mb, kb, l, real, sc, T, info, o);
     }
 }
 
@@ -206,15 +265,21 @@ template <bool SWIGLU>
 static cudaError_t launch_token(const uint16_t* x, int64_t R, int64_t C, int64_t ldx, uint8_t* q, uint8_t* sf,
                                 float* s_tok, int mma_layout, cudaStream_t stream) {
     const int64_t cover = mma_layout ? ((R + 127) & ~int64_t(127)) : R;
-    const int rows_per_cta = TOK_THREADS / 32;
+    // two rows per warp when a row has at most 4 x 16 blocks: all 16 lanes of a row stay busy
+    const bool pair = (C >> 4) <= 4 * 16;
+    const int rows_per_cta = (TOK_THREADS / 32) * (pair ? 2 : 1);
     const int64_t grid = (cover + rows_per_cta - 1) / rows_per_cta;
     const bool v8 = ((reinterpret_cast<uintptr_t>(x) & 31u) == 0) && (ldx % 16 == 0) && (!SWIGLU || C % 16 == 0);
-    if (v8)
-        nvfp4_token_kernel<true, SWIGLU><<<(unsigned)grid, TOK_THREADS, 0, stream>>>(x, R, C, ldx, q, sf, s_tok,
-                                                                                    mma_layout, cover);
-    else
-        nvfp4_token_kernel<false, SWIGLU><<<(unsigned)grid, TOK_THREADS, 0, stream>>>(x, R, C, ldx, q, sf, s_tok,
-                                                                                     mma_layout, cover);
+#define NVQ_TOK(V, L) \
+    nvfp4_token_kernel<V, SWIGLU, L><<<(unsigned)grid, TOK_THREADS, 0, stream>>>(x, R, C, ldx, q, sf, s_tok, mma_layout, cover)
+    if (v8) {
+        if (pair) NVQ_TOK(true, 16);
+        else NVQ_TOK(true, 32);
+    } else {
+        if (pair) NVQ_TOK(false, 16);
+        else NVQ_TOK(false, 32);
+    }
+#undef NVQ_TOK
     const cudaError_t err = cudaGetLastError();
     if (err == cudaSuccess) count_launches(1);
     return err;

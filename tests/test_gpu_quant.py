@@ -170,6 +170,30 @@ def test_nvfp4_tiny_token_scales(nvq, k):
     assert np.array_equal(_np(sf).reshape(sf_ref.shape), sf_ref)
 
 
+@pytest.mark.parametrize("K", [768, 1024, 2048])
+@pytest.mark.parametrize("layout", ["canonical", "mma"])
+def test_nvfp4_rows_on_different_paths(nvq, K, layout):
+    """Rows of one warp whose coarse scales send them down different decision paths (tiny scales
+    take the exact path, others the table path, zero rows have no scale): rows of at most 1024
+    elements are quantized two to a warp, so neighbouring rows mix paths inside one warp."""
+    rng = np.random.default_rng(K)
+    R = 77                                          # odd: the last warp's second row is past the end
+    x = rng.standard_normal((R, K)) * np.exp(rng.uniform(-3, 3, (R, 1)))
+    kind = rng.integers(0, 4, R)
+    x[kind == 1] *= 2688.0 * 2.0 ** -120            # exact path
+    x[kind == 2] = 0.0                              # zero row
+    bits = _bits_of(x)
+    q_ref, sf_ref, s_ref = oracle.nvfp4_quantize_per_token(bits)
+    q, sf, s = nvq.nvfp4_quantize_per_token(_dev(bits), sf_layout=layout)
+    torch.cuda.synchronize()
+    assert np.array_equal(_np(s).view(np.uint32), s_ref.view(np.uint32))
+    assert np.array_equal(_np(q), q_ref)
+    if layout == "canonical":
+        assert np.array_equal(_np(sf).reshape(sf_ref.shape), sf_ref)
+    else:
+        assert np.array_equal(_np(sf), oracle.sf_to_mma_layout(sf_ref))
+
+
 def test_nvfp4_per_token_invariance_on_gpu(nvq):
     # a token's bytes do not depend on the rest of the batch (the scope the pages require)
     bits = family("random", (512, 768), seed=9)
