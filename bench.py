@@ -48,17 +48,17 @@ L2_FLUSH_BYTES = 256 << 20
 # profiles/quant_routed_batch.md (quant). A changed source reports null.
 NCU_TRAFFIC = {
     "dense": {
-        "mxfp8_quantize X row+col": {"bytes": 33600000, "src_sha": "3352a1d55c39ef58"},
-        "mxfp8_quantize W col": {"bytes": 21010000, "src_sha": "3352a1d55c39ef58"},
-        "nvfp4_quantize_per_token X": {"bytes": 33600000, "src_sha": "ef6116dee65ea977"},
-        "nvfp4_quantize_weights W": {"bytes": 41970000, "src_sha": "ef6116dee65ea977"},
-        "block_scaled_gemm MXFP8": {"bytes": 56980000, "src_sha": "437f71369e033858"},
-        "block_scaled_gemm NVFP4": {"bytes": 41770000, "src_sha": "437f71369e033858"},
+        "mxfp8_quantize X row+col": {"bytes": 33600000, "src_sha": "31e38c0af20c14f0"},
+        "mxfp8_quantize W col": {"bytes": 20980000, "src_sha": "31e38c0af20c14f0"},
+        "nvfp4_quantize_per_token X": {"bytes": 33620000, "src_sha": "560b662e7e18c991"},
+        "nvfp4_quantize_weights W": {"bytes": 41990000, "src_sha": "560b662e7e18c991"},
+        "block_scaled_gemm MXFP8": {"bytes": 56970000, "src_sha": "905b1490423e6dd9"},
+        "block_scaled_gemm NVFP4": {"bytes": 41800000, "src_sha": "905b1490423e6dd9"},
         "dequantize_bf16 W": {"bytes": 5910000, "src_sha": "def12a43bb80c45b"},
     },
     "quant": {
-        "mxfp8_quantize X row+col": {"bytes": 1050810000, "src_sha": "3352a1d55c39ef58"},
-        "nvfp4_quantize_per_token X": {"bytes": 677110000, "src_sha": "ef6116dee65ea977"},
+        "mxfp8_quantize X row+col": {"bytes": 1081560000, "src_sha": "31e38c0af20c14f0"},
+        "nvfp4_quantize_per_token X": {"bytes": 675920000, "src_sha": "560b662e7e18c991"},
     },
 }
 
@@ -854,7 +854,7 @@ def _oracle_sample(workload, rows, cols):
     return time.perf_counter() - t0, flops, desc
 
 
-def cpu_baseline(workload, rows=2048, cols=1536):
+def cpu_baseline(workload, rows=4096, cols=3072):
     """Time the oracle in a single-threaded child process (BLAS threads pinned to 1)."""
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
                CUDA_VISIBLE_DEVICES="")
