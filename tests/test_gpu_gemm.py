@@ -389,3 +389,23 @@ def test_bf16_dequantized_backward_dgrad(nvq):
     D, bound = oracle.grouped_gemm_reference("m", oracle.bf16_bits_to_f64(gb), wdq_ref.reshape(E, Kin, Nout), offs)
     rows = ~np.isnan(D[:, 0])
     _check(d[torch.from_numpy(rows).cuda()], D[rows], bound[rows], False)
+
+
+# ------------------------------------------------------------------------------------------------
+# the documented maximum of 1024 groups
+# ------------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4"])
+def test_max_groups(nvq, fmt):
+    """1024 groups (the maximum), most of them empty, a few with rows at 32-row offsets: the tile
+    schedule's group search and the device offset checks at full size."""
+    counts = [0] * 1024
+    for e, c in [(0, 40), (7, 32), (300, 96), (511, 1), (512, 33), (1000, 64), (1023, 130)]:
+        counts[e] = c
+    _run_m(nvq, fmt, counts, 256, 256, seed=77, out_type=nvq.OUT_F32)
+
+
+def test_more_than_max_groups_is_rejected(nvq):
+    x = torch.zeros((64, 128), dtype=torch.uint8, device="cuda")
+    offs = torch.zeros(1026, dtype=torch.int64, device="cuda")
+    with pytest.raises(nvq.NvqError):
+        nvq.block_scaled_grouped_gemm(nvq.MXFP8, nvq.GEMM_GROUP_M, x, x, x, x, offs, m=64, n=128, k=128, groups=1025)
