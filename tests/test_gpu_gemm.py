@@ -401,7 +401,7 @@ def test_max_groups(nvq, fmt):
     counts = [0] * 1024
     for e, c in [(0, 40), (7, 32), (300, 96), (511, 1), (512, 33), (1000, 64), (1023, 130)]:
         counts[e] = c
-    _run_m(nvq, fmt, counts, 256, 256, seed=77, out_type=nvq.OUT_F32)
+    _run_m(nvq, fmt, counts, 128, 128, seed=77, out_type=nvq.OUT_F32)
 
 
 def test_more_than_max_groups_is_rejected(nvq):
