@@ -9,7 +9,10 @@
 // code = E2M1 RNE (saturating) of x / (E4M3(sf) s). Exactness: see nvq_device.cuh.
 //
 // Per-token design: one warp per token row, one 16-element block per lane per step (see the
-// kernel). Weights: one thread per (column, 16-row block) after a shared-memory transpose.
+// kernel). Weights: one thread per (column, 16-row block) after a shared-memory transpose. A scope
+// whose table passes the product-path check (nvq_device.cuh) encodes its elements by one fp32
+// multiply and the hardware E2M1 conversion; any other scope compares each element with its block's
+// exact boundaries.
 #include <algorithm>
 #include <mutex>
 
@@ -75,23 +78,32 @@ __device__ __forceinline__ void row_block(const uint16_t* p, int64_t up, uint4& 
     }
 }
 
+// How a scope's blocks are encoded: by the product path (its table passed the check), by the
+// table's boundary comparisons, or by exact fp64 decisions (a scope with a tiny or zero coarse scale).
+enum : int { ENC_TABLE = 0, ENC_EXACT = 1, ENC_PRODUCT = 2 };
+
 // Scale code and the 16 codes of one block (two uint4 of 8 bf16, magnitude maximum mb as bf16
-// bits): table-driven and branch-free in the fast path; exact fp64 decisions for a scope with a
-// tiny (or zero) coarse scale.
-template <bool EXACT>
+// bits); branch-free in the table and product modes.
+template <int MODE>
 __device__ __forceinline__ uint32_t encode_block(const uint4& a, const uint4& b, uint32_t mb, const Nvfp4Scope& sc,
                                                  const Nvfp4Table& T, const Nvfp4CodeInfo& I, uint32_t& c0,
                                                  uint32_t& c1) {
-    if (EXACT) {
+    if (MODE == ENC_EXACT) {
         const uint32_t sfc = nvfp4_block_scale(__uint_as_float(mb << 16), sc);
         c0 = nvfp4_encode8_exact(a, sfc, sc);
         c1 = nvfp4_encode8_exact(b, sfc, sc);
         return sfc;
     }
     const uint32_t sfc = nvfp4_block_scale_t(mb, sc, T);
-    const E2M1Bounds bd = nvfp4_block_bounds_t(sfc, T, I);
-    c0 = nvfp4_codes8(a, bd);
-    c1 = nvfp4_codes8(b, bd);
+    if (MODE == ENC_PRODUCT) {
+        const float g = nvfp4_block_g(sfc, T, I);
+        c0 = nvfp4_codes8_mul(a, g);
+        c1 = nvfp4_codes8_mul(b, g);
+    } else {
+        const E2M1Bounds bd = nvfp4_block_bounds_t(sfc, T, I);
+        c0 = nvfp4_codes8(a, bd);
+        c1 = nvfp4_codes8(b, bd);
+    }
     return sfc;
 }
 
@@ -125,37 +137,39 @@ __device__ __forceinline__ void token_store(uint32_t sfc, uint32_t c0, uint32_t 
     }
 }
 
-// Encode and store one block; the path (table-driven or exact) is the same for every lane.
-template <bool EXACT>
+// Encode and store one block; the encoding mode is the same for every lane.
+template <int MODE>
 __device__ __forceinline__ void token_block(const uint4& a, const uint4& b, uint32_t mb, int64_t kb, int l, bool real,
                                             const Nvfp4Scope& sc, const Nvfp4Table& T, const Nvfp4CodeInfo& I,
                                             const TokenRowOut& o) {
     uint32_t c0, c1;
-    const uint32_t sfc = encode_block<EXACT>(a, b, mb, sc, T, I, c0, c1);
+    const uint32_t sfc = encode_block<MODE>(a, b, mb, sc, T, I, c0, c1);
     token_store(sfc, c0, c1, kb, l, real, o);
 }
 
 // Encode and store one block when the two rows of a warp may take different paths: the encoding
 // branches per row, the stores (shuffles) run with the whole warp.
 __device__ __forceinline__ void token_block_mixed(const uint4& a, const uint4& b, uint32_t mb, int64_t kb, int l,
-                                                  bool real, const Nvfp4Scope& sc, const Nvfp4Table& T,
+                                                  bool real, int mode, const Nvfp4Scope& sc, const Nvfp4Table& T,
                                                   const Nvfp4CodeInfo& I, const TokenRowOut& o) {
     uint32_t c0, c1, sfc;
-    if (!sc.exact) sfc = encode_block<false>(a, b, mb, sc, T, I, c0, c1);
-    else sfc = encode_block<true>(a, b, mb, sc, T, I, c0, c1);
+    if (mode == ENC_PRODUCT) sfc = encode_block<ENC_PRODUCT>(a, b, mb, sc, T, I, c0, c1);
+    else if (mode == ENC_TABLE) sfc = encode_block<ENC_TABLE>(a, b, mb, sc, T, I, c0, c1);
+    else sfc = encode_block<ENC_EXACT>(a, b, mb, sc, T, I, c0, c1);
     __syncwarp();
     token_store(sfc, c0, c1, kb, l, real, o);
 }
 
-// The scope table of a row built by its LPR lanes (32: nvfp4_table_build_warp; 16: each lane takes
-// the class boundaries of thresholds j and j + 2 (and their j + 4 partners) of class l & 7, and the
-// block-scale boundary of code l).
+// The scope table of a row built by its LPR lanes (32: nvfp4_table_build_warp, with the product
+// path's check; 16: each lane takes the class boundaries of thresholds j and j + 2 (and their
+// j + 4 partners) of class l & 7, and the block-scale boundary of code l). Called by all 32 lanes of
+// the warp together; returns whether the lane's class has a product-path multiplier. Rows of 16
+// lanes never take the product path: with at most four blocks per lane, the check (five candidate
+// multipliers at up to four boundaries per lane) costs more than it saves (measured: the MoE down
+// projection's 768-wide rows and the SwiGLU rows ran 7% and 17% slower with it).
 template <int LPR>
-__device__ __forceinline__ void nvfp4_table_build_row(Nvfp4Table& T, float s, int l) {
-    if (LPR == 32) {
-        nvfp4_table_build_warp(T, s, l);
-        return;
-    }
+__device__ __forceinline__ bool nvfp4_table_build_row(Nvfp4Table& T, float s, int l) {
+    if (LPR == 32) return nvfp4_table_build_warp(T, s, l);
     const uint32_t f = (uint32_t)l & 7u;
     const float v = (float)(8u + f) * 0x1p-9f;                     // value of E4M3 code 8 + f
 #pragma unroll
@@ -173,6 +187,7 @@ __device__ __forceinline__ void nvfp4_table_build_row(Nvfp4Table& T, float s, in
     }
     T.bs[l] = bf16_boundary((float)(3 * (2 * l + 1)) * 0x1p-9f, s, (l & 1) != 0);
     if (l < 12) T.bp[8][l] = l < 7 ? 0x7F007F00u : (l >= 8 && l < 11 ? 0xFF00FF00u : 0u);
+    return false;
 }
 
 // LPR lanes per token row (32: one row per warp; 16: two rows per warp, for rows of at most 64
@@ -227,8 +242,12 @@ nvfp4_token_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t C, int64_t
     const float s = nvfp4_coarse_scale(__uint_as_float(m << 16));
     const Nvfp4Scope sc = make_nvfp4_scope(s);
     if (real && l == 0) s_tok[row] = s;
-    if (!sc.exact) nvfp4_table_build_row<LPR>(T, s, l);
+    // every row builds a table (all lanes take part in its shuffles); an exact-path row ignores it
+    const bool ok = nvfp4_table_build_row<LPR>(T, s, l);
     __syncwarp();
+    const uint32_t bad = __ballot_sync(0xffffffffu, !ok);
+    const uint32_t row_bad = LPR == 32 ? bad : (bad >> (half * LPR)) & ((1u << LPR) - 1u);
+    const int mode = sc.exact ? ENC_EXACT : ((LPR == 32 && row_bad == 0u) ? ENC_PRODUCT : ENC_TABLE);
 
     // pass 2: per 1x16 block scale and codes (register-resident blocks first, then any reloads)
     TokenRowOut o;
@@ -236,28 +255,33 @@ nvfp4_token_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t C, int64_t
     o.nkb = nkb;
     o.mma_layout = mma_layout;
     o.sf = !covered ? nullptr : (mma_layout ? sf + mma_sf_offset(row, 0, nkb) : sf + row * nkb);
-    const bool any_exact = __any_sync(0xffffffffu, sc.exact);
-    const bool all_exact = __all_sync(0xffffffffu, sc.exact);
-    if (!any_exact) {
+    const uint32_t same = __match_any_sync(0xffffffffu, mode);
+    if (same == 0xffffffffu && mode == ENC_PRODUCT) {
 #pragma unroll
         for (int i = 0; i < TOK_NREG; ++i)
-            if (i < iters) token_block<false>(va[i], vb[i], mbk[i], (int64_t)i * LPR + l, l, real, sc, T, info, o);
-    } else if (all_exact) {
+            if (i < iters)
+                token_block<ENC_PRODUCT>(va[i], vb[i], mbk[i], (int64_t)i * LPR + l, l, real, sc, T, info, o);
+    } else if (same == 0xffffffffu && mode == ENC_TABLE) {
 #pragma unroll
         for (int i = 0; i < TOK_NREG; ++i)
-            if (i < iters) token_block<true>(va[i], vb[i], mbk[i], (int64_t)i * LPR + l, l, real, sc, T, info, o);
+            if (i < iters) token_block<ENC_TABLE>(va[i], vb[i], mbk[i], (int64_t)i * LPR + l, l, real, sc, T, info, o);
+    } else if (same == 0xffffffffu) {
+#pragma unroll
+        for (int i = 0; i < TOK_NREG; ++i)
+            if (i < iters) token_block<ENC_EXACT>(va[i], vb[i], mbk[i], (int64_t)i * LPR + l, l, real, sc, T, info, o);
     } else {
-        // the two rows of the warp take different paths
+        // the two rows of the warp take different modes
 #pragma unroll
         for (int i = 0; i < TOK_NREG; ++i)
-            if (i < iters) token_block_mixed(va[i], vb[i], mbk[i], (int64_t)i * LPR + l, l, real, sc, T, info, o);
+            if (i < iters)
+                token_block_mixed(va[i], vb[i], mbk[i], (int64_t)i * LPR + l, l, real, mode, sc, T, info, o);
     }
     for (int i = TOK_NREG; i < iters; ++i) {
         const int64_t kb = (int64_t)i * LPR + l;
         uint4 a = make_uint4(0u, 0u, 0u, 0u), b = a;
         if (real && kb < nkb) row_block<V8, SWIGLU>(xr + kb * 16, C, a, b);
         const uint32_t mb = max(absmax_bits_8(a), absmax_bits_8(b));
-        token_block_mixed(a, b, mb, kb, l, real, sc, T, info, o);
+        token_block_mixed(a, b, mb, kb, l, real, mode, sc, T, info, o);
     }
 }
 
@@ -378,6 +402,8 @@ nvfp4_weight_encode_kernel(const uint16_t* __restrict__ w, int64_t K, int64_t N,
     uint4 A, B;
     if (t_begin < t_end) load(cur, A, B);
     int64_t cur_e = -1;
+    bool new_scope = false;
+    int mode = ENC_EXACT;
     Nvfp4Scope sc = make_nvfp4_scope(0.0f);
     for (int64_t t = t_begin; t < t_end; ++t) {
         uint32_t* buf = tile[(t - t_begin) & 1];
@@ -400,9 +426,17 @@ nvfp4_weight_encode_kernel(const uint16_t* __restrict__ w, int64_t K, int64_t N,
             cur_e = e;
             const float s = nvfp4_coarse_scale(__uint_as_float(amax_bits[e]));
             sc = make_nvfp4_scope(s);
-            if (!sc.exact && threadIdx.x < 32) nvfp4_table_build_warp(T, s, threadIdx.x);
+            if (threadIdx.x < 32) {
+                const bool all = __all_sync(0xffffffffu, nvfp4_table_build_warp(T, s, threadIdx.x));
+                if (threadIdx.x == 0) T.product = all ? 1u : 0u;
+            }
+            new_scope = true;
         }
         __syncthreads();
+        if (new_scope) {
+            mode = sc.exact ? ENC_EXACT : (T.product ? ENC_PRODUCT : ENC_TABLE);
+            new_scope = false;
+        }
 
         const int64_t k0 = cur.kt * WT_K, n = cur.nt * WT_N + en;
         const uint32_t* rowp = buf + en * WT_STRIDE;
@@ -411,8 +445,10 @@ nvfp4_weight_encode_kernel(const uint16_t* __restrict__ w, int64_t K, int64_t N,
         const uint4 hi = *reinterpret_cast<const uint4*>(rowp + ((8 * ekb + 4) ^ sw));
         uint32_t c0, c1;
         const uint32_t mb = max(absmax_bits_8(lo), absmax_bits_8(hi));
-        const uint32_t sfc = sc.exact ? encode_block<true>(lo, hi, mb, sc, T, I, c0, c1)
-                                      : encode_block<false>(lo, hi, mb, sc, T, I, c0, c1);
+        uint32_t sfc;
+        if (mode == ENC_PRODUCT) sfc = encode_block<ENC_PRODUCT>(lo, hi, mb, sc, T, I, c0, c1);
+        else if (mode == ENC_TABLE) sfc = encode_block<ENC_TABLE>(lo, hi, mb, sc, T, I, c0, c1);
+        else sfc = encode_block<ENC_EXACT>(lo, hi, mb, sc, T, I, c0, c1);
         const int64_t kb0 = k0 >> 4, kb = kb0 + ekb;
         const int64_t row = e * N + n;
         if (n < N && kb < nkb) *reinterpret_cast<uint2*>(qT + row * (K >> 1) + kb * 8) = make_uint2(c0, c1);

@@ -248,6 +248,34 @@ def test_nvfp4_weights_tile_ranges_cross_experts(nvq, layout):
         assert np.array_equal(_np(sf), oracle.sf_to_mma_layout(sf_ref.reshape(E * N, K // 16)))
 
 
+@pytest.mark.parametrize("layout", ["canonical", "mma"])
+def test_nvfp4_weights_product_and_boundary_scopes(nvq, layout):
+    """Experts whose coarse scale is a power of two (s = 2^k: ties on the boundaries that no fp32
+    multiplier reproduces, so the boundary comparison) next to experts with generic scales (the
+    product path), in one launch; values on and next to the rounding midpoints."""
+    E, K, N = 12, 256, 192
+    bits = family("boundary", (E * K, N), seed=21).reshape(E, K, N)
+    rng = np.random.default_rng(21)
+    w = oracle.bf16_bits_to_f64(bits)
+    w /= np.abs(w).reshape(E, -1).max(axis=1)[:, None, None]
+    for e in range(E):
+        k = int(rng.integers(-12, 4))
+        amax = 2688.0 * 2.0 ** k if e % 2 == 0 else 2688.0 * 2.0 ** k * 1.37
+        w[e] *= 0.5 * amax
+        w[e, 0, 0] = amax
+    bits = _bits_of(w)
+    q_ref, sf_ref, s_ref = oracle.nvfp4_quantize_weights(bits)
+    assert (s_ref[0::2] == np.exp2(np.round(np.log2(s_ref[0::2])))).all()
+    q, sf, s = nvq.nvfp4_quantize_weights(_dev(bits).contiguous(), sf_layout=layout)
+    torch.cuda.synchronize()
+    assert np.array_equal(_np(s).view(np.uint32), s_ref.view(np.uint32))
+    assert np.array_equal(_np(q), q_ref)
+    if layout == "canonical":
+        assert np.array_equal(_np(sf).reshape(sf_ref.shape), sf_ref)
+    else:
+        assert np.array_equal(_np(sf), oracle.sf_to_mma_layout(sf_ref.reshape(E * N, K // 16)))
+
+
 # ------------------------------------------------------------------------------------------------
 # Dequantize
 # ------------------------------------------------------------------------------------------------
