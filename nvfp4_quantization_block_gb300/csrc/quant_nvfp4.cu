@@ -9,7 +9,7 @@
 // code = E2M1 RNE (saturating) of x / (E4M3(sf) s). Exactness: see nvq_device.cuh.
 //
 // Per-token design: one warp per token row, one 16-element block per lane per step (see the
-// kernel). Weights: one thread per (column, 16-row block) after a shared-memory transpose. A scope
+// kernel). Weights: one warp per 64 x 64 tile, two columns and four 16-row blocks per lane. A scope
 // whose table passes the product-path check (nvq_device.cuh) encodes its elements by one fp32
 // multiply and the hardware E2M1 conversion; any other scope compares each element with its block's
 // exact boundaries.
@@ -325,17 +325,25 @@ cudaError_t launch_nvfp4_swiglu_quantize(const uint16_t* gate_up, int64_t R, int
 // Three kernels: amax per expert (atomic max on the fp32 bits, kept in s_w), encode, finalize
 // (s_w <- RN(amax / 2688)).
 // ------------------------------------------------------------------------------------------------
-constexpr int WT_K = 64, WT_N = 64, WT_THREADS = 256;
-constexpr int WT_STRIDE = 36;            // words per transposed smem row (64 k = 32 k-pair words + 4)
+constexpr int WA_VEC = 4;                // 16-byte vectors in flight per thread in the amax pass
 
 __global__ void __launch_bounds__(256)
 nvfp4_weight_amax_kernel(const uint16_t* __restrict__ w, int64_t per_expert, uint32_t* __restrict__ amax_bits) {
     const int64_t e = blockIdx.y;
     const uint16_t* we = w + e * per_expert;
     const int64_t nvec = per_expert >> 3;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     uint32_t m = 0;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += (int64_t)gridDim.x * blockDim.x)
-        m = max(m, absmax_bits_8(ld_stream_v4(we + i * 8)));
+    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    // WA_VEC independent loads issued before any of them is used
+    for (; i + (WA_VEC - 1) * stride < nvec; i += WA_VEC * stride) {
+        uint4 v[WA_VEC];
+#pragma unroll
+        for (int j = 0; j < WA_VEC; ++j) v[j] = ld_stream_v4(we + (i + j * stride) * 8);
+#pragma unroll
+        for (int j = 0; j < WA_VEC; ++j) m = max(m, absmax_bits_8(v[j]));
+    }
+    for (; i < nvec; i += stride) m = max(m, absmax_bits_8(ld_stream_v4(we + i * 8)));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
     __shared__ uint32_t red[8];
@@ -348,124 +356,177 @@ nvfp4_weight_amax_kernel(const uint16_t* __restrict__ w, int64_t per_expert, uin
     }
 }
 
-// Encode: a persistent loop over tiles of 64 k x 64 n. CTA b takes the contiguous range
-// [total b / G, total (b + 1) / G) of the (expert, k tile, n tile) sequence, so the load is even
-// for any expert count and a CTA rebuilds its scope table only when its range enters the next
-// expert. A tile arrives as row pairs (k, k + 1): byte permutes interleave them into words
-// (x[k][n], x[k+1][n]) stored transposed, [n][k pair], in shared memory, the k-pair index of row
-// n XOR-ed with 4 (n / 8) so that the stores and the 128-bit loads are free of bank conflicts.
-// Each thread then encodes one 16-k block of one column, read with two 128-bit loads. The next
-// tile's rows are in flight while the current tile is encoded (two buffers, one barrier a tile).
-__global__ void __launch_bounds__(WT_THREADS)
+// Encode: every warp works on its own, over a contiguous range of the (expert, n tile, k tile)
+// sequence of 64 k x 64 n tiles, so the load is even for any expert count and a warp rebuilds its
+// scope table only when its range enters the next expert. Lane l owns columns n0 + 2l and
+// n0 + 2l + 1 and the tile's four 16-row blocks: it loads the tile's 64 rows of its two columns (one
+// 4-byte load per row, 128 contiguous bytes per row across the warp; each 32-row half of the next
+// tile is requested as soon as the same half of this one is encoded), so each column's block is
+// the low or high halves of one word per row and no transpose is needed. Its outputs are whole per column: the four blocks' 32 code bytes (one L2 sector, one
+// store) and their 4 scale bytes (one 4-column group). K is the fastest tile index, so a row's
+// scale bytes are written by consecutive tiles of one warp. (Half-sector code stores, 16 bytes per
+// tile, made L2 write partial sectors back: 3.4x the output bytes in DRAM writes.)
+constexpr int WE_K = 64, WE_N = 64, WE_THREADS = 128, WE_WARPS = WE_THREADS / 32;
+
+// Pairs (x[2i], x[2i + 1]) of one column of 8 rows, as the bf16x2 words of the table and exact
+// paths: the column is the low (HI false) or high half of each row's word.
+template <bool HI>
+__device__ __forceinline__ uint4 column_pairs(const uint32_t* r) {
+    constexpr uint32_t sel = HI ? 0x7632u : 0x5410u;
+    return make_uint4(__byte_perm(r[0], r[1], sel), __byte_perm(r[2], r[3], sel), __byte_perm(r[4], r[5], sel),
+                      __byte_perm(r[6], r[7], sel));
+}
+
+// fp32 values of 8 rows of one column, times g, to 8 E2M1 codes (product path)
+template <bool HI>
+__device__ __forceinline__ uint32_t column_codes_mul(const uint32_t* r, float g) {
+    float x[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) x[i] = __fmul_rn(HI ? bf16_hi(r[i]) : bf16_lo(r[i]), g);
+    return cvt_e2m1x8(x[0], x[1], x[2], x[3], x[4], x[5], x[6], x[7]);
+}
+
+struct BlockCodes {
+    uint32_t sfc, c0, c1;
+};
+
+// Table or exact decisions for one column's 16-row block (the four pair words of each half): kept
+// out of line, so the product path's loop stays small.
+__device__ __noinline__ BlockCodes column_block_slow(uint4 a, uint4 b, uint32_t mb, int mode, Nvfp4Scope sc,
+                                                     const Nvfp4Table* T, const Nvfp4CodeInfo* I) {
+    BlockCodes r;
+    if (mode == ENC_TABLE) r.sfc = encode_block<ENC_TABLE>(a, b, mb, sc, *T, *I, r.c0, r.c1);
+    else r.sfc = encode_block<ENC_EXACT>(a, b, mb, sc, *T, *I, r.c0, r.c1);
+    return r;
+}
+
+// Scale code and codes of one column's 16-row block (rows r[0..15], the column in the low or high
+// halves), magnitude maximum mb
+template <bool HI>
+__device__ __forceinline__ BlockCodes column_block(const uint32_t* r, uint32_t mb, int mode, const Nvfp4Scope& sc,
+                                                   const Nvfp4Table& T, const Nvfp4CodeInfo& I) {
+    if (mode == ENC_PRODUCT) {
+        BlockCodes o;
+        o.sfc = nvfp4_block_scale_t(mb, sc, T);
+        const float g = nvfp4_block_g(o.sfc, T, I);
+        o.c0 = column_codes_mul<HI>(r, g);
+        o.c1 = column_codes_mul<HI>(r + 8, g);
+        return o;
+    }
+    return column_block_slow(column_pairs<HI>(r), column_pairs<HI>(r + 8), mb, mode, sc, &T, &I);
+}
+
+__global__ void __launch_bounds__(WE_THREADS, 3)
 nvfp4_weight_encode_kernel(const uint16_t* __restrict__ w, int64_t K, int64_t N, int64_t tiles_k, int64_t tiles_n,
                            int64_t total, uint8_t* __restrict__ qT, uint8_t* __restrict__ sfT,
                            const uint32_t* __restrict__ amax_bits, int mma_layout) {
-    __shared__ __align__(16) uint32_t tile[2][WT_N * WT_STRIDE];
-    __shared__ Nvfp4Table T;                                   // the current expert's scope table
+    __shared__ Nvfp4Table tables[WE_WARPS];                    // each warp's current expert
     __shared__ Nvfp4CodeInfo I;
-    if (threadIdx.x < 128) nvfp4_code_info_build(I, threadIdx.x);
+    for (uint32_t c = threadIdx.x; c < 128u; c += WE_THREADS) nvfp4_code_info_build(I, c);
+    __syncthreads();
 
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    Nvfp4Table& T = tables[warp];
+    const int64_t gw = (int64_t)blockIdx.x * WE_WARPS + warp, nw = (int64_t)gridDim.x * WE_WARPS;
+    const int64_t t_begin = total * gw / nw, t_end = total * (gw + 1) / nw;
+    if (t_begin >= t_end) return;                              // uniform over the warp
     const int64_t per_e = tiles_k * tiles_n;
-    const int64_t t_begin = total * blockIdx.x / gridDim.x, t_end = total * (blockIdx.x + 1) / gridDim.x;
-    const int lp = threadIdx.x >> 3, lc = threadIdx.x & 7;     // loader: k pair, 8-column chunk
-    const int en = threadIdx.x >> 2, ekb = threadIdx.x & 3;    // encoder: column, 16-k block
-    const int64_t nkb = K >> 4;
-
-    // tile cursor (expert, k tile, n tile), advanced without divisions
-    struct Cursor {
-        int64_t e, kt, nt;
-    };
-    auto advance = [&](Cursor& c) {
-        if (++c.nt == tiles_n) {
-            c.nt = 0;
-            if (++c.kt == tiles_k) {
-                c.kt = 0;
-                ++c.e;
-            }
-        }
-    };
-    auto load = [&](const Cursor& c, uint4& A, uint4& B) {
-        const int64_t k = c.kt * WT_K + 2 * lp, n = c.nt * WT_N + 8 * lc;
-        A = B = make_uint4(0u, 0u, 0u, 0u);
-        if (k < K && n < N) {                                  // K even: row k + 1 exists too
-            const uint16_t* src = w + (c.e * K + k) * N + n;
-            A = ld_stream_v4(src);
-            B = ld_stream_v4(src + N);
-        }
-    };
-
-    Cursor cur;
-    cur.e = t_begin / per_e;
-    cur.kt = (t_begin - cur.e * per_e) / tiles_n;
-    cur.nt = t_begin - cur.e * per_e - cur.kt * tiles_n;
-    Cursor nxt = cur;
-    uint4 A, B;
-    if (t_begin < t_end) load(cur, A, B);
+    int64_t e = t_begin / per_e;
+    int64_t nt = (t_begin - e * per_e) / tiles_k;
+    int64_t kt = t_begin - e * per_e - nt * tiles_k;
+    const int64_t nkb = K >> 4, half_k = K >> 1;
+    // whole tiles of K: one 32-byte code store per column (when the rows start on 32 bytes) and
+    // one 4-byte scale store
+    const bool whole_k = (K & 63) == 0;
+    const bool sector_rows = whole_k && ((reinterpret_cast<uintptr_t>(qT) & 31u) == 0);
     int64_t cur_e = -1;
-    bool new_scope = false;
     int mode = ENC_EXACT;
     Nvfp4Scope sc = make_nvfp4_scope(0.0f);
-    for (int64_t t = t_begin; t < t_end; ++t) {
-        uint32_t* buf = tile[(t - t_begin) & 1];
-        {
-            const uint32_t a[4] = {A.x, A.y, A.z, A.w}, b[4] = {B.x, B.y, B.z, B.w};
-            const int col = lp ^ (4 * lc);                     // row n = 8 lc + m: n / 8 = lc
+
+    // rows [0, 32) and [32, 64) of the tile's two columns (low / high half of each word); the next
+    // tile's half is loaded as soon as this tile's half is encoded, so loads stay in flight while
+    // the warp computes
+    uint32_t xa[WE_K / 2], xb[WE_K / 2];
+    auto load_half = [&](uint32_t (&x)[WE_K / 2], int64_t te, int64_t tn, int64_t tk, int h) {
+        const int64_t k0 = tk * WE_K + h * (WE_K / 2), n0 = tn * WE_N + 2 * lane;
+        const bool ok = n0 < N;                                // N even: both columns in or out together
+        const int64_t rows = K - k0;
+        const uint16_t* src = w + (te * K + k0) * N + n0;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int n0 = 8 * lc + 2 * j;                 // word j holds columns n0, n0 + 1
-                buf[n0 * WT_STRIDE + col] = __byte_perm(a[j], b[j], 0x5410);
-                buf[(n0 + 1) * WT_STRIDE + col] = __byte_perm(a[j], b[j], 0x7632);
-            }
-        }
-        cur = nxt;
-        advance(nxt);
-        if (t + 1 < t_end) load(nxt, A, B);
-        const int64_t e = cur.e;
-        if (e != cur_e) {                                      // uniform across the CTA
-            __syncthreads();                                   // the previous expert's table is done
+        for (int r = 0; r < WE_K / 2; ++r) x[r] = ld_stream_u32_if(src + r * N, ok && r < rows);
+    };
+    load_half(xa, e, nt, kt, 0);
+    load_half(xb, e, nt, kt, 1);
+
+    for (int64_t t = t_begin; t < t_end; ++t) {
+        if (e != cur_e) {
+            __syncwarp();                                      // the previous expert's table reads are done
             cur_e = e;
             const float s = nvfp4_coarse_scale(__uint_as_float(amax_bits[e]));
             sc = make_nvfp4_scope(s);
-            if (threadIdx.x < 32) {
-                const bool all = __all_sync(0xffffffffu, nvfp4_table_build_warp(T, s, threadIdx.x));
-                if (threadIdx.x == 0) T.product = all ? 1u : 0u;
+            const bool all = __all_sync(0xffffffffu, nvfp4_table_build_warp(T, s, lane));
+            __syncwarp();
+            mode = sc.exact ? ENC_EXACT : (all ? ENC_PRODUCT : ENC_TABLE);
+        }
+        // the next tile (k fastest)
+        int64_t e1 = e, nt1 = nt, kt1 = kt + 1;
+        if (kt1 == tiles_k) {
+            kt1 = 0;
+            if (++nt1 == tiles_n) {
+                nt1 = 0;
+                ++e1;
             }
-            new_scope = true;
         }
-        __syncthreads();
-        if (new_scope) {
-            mode = sc.exact ? ENC_EXACT : (T.product ? ENC_PRODUCT : ENC_TABLE);
-            new_scope = false;
-        }
-
-        const int64_t k0 = cur.kt * WT_K, n = cur.nt * WT_N + en;
-        const uint32_t* rowp = buf + en * WT_STRIDE;
-        const int sw = 4 * (en >> 3);
-        const uint4 lo = *reinterpret_cast<const uint4*>(rowp + ((8 * ekb) ^ sw));
-        const uint4 hi = *reinterpret_cast<const uint4*>(rowp + ((8 * ekb + 4) ^ sw));
-        uint32_t c0, c1;
-        const uint32_t mb = max(absmax_bits_8(lo), absmax_bits_8(hi));
-        uint32_t sfc;
-        if (mode == ENC_PRODUCT) sfc = encode_block<ENC_PRODUCT>(lo, hi, mb, sc, T, I, c0, c1);
-        else if (mode == ENC_TABLE) sfc = encode_block<ENC_TABLE>(lo, hi, mb, sc, T, I, c0, c1);
-        else sfc = encode_block<ENC_EXACT>(lo, hi, mb, sc, T, I, c0, c1);
-        const int64_t kb0 = k0 >> 4, kb = kb0 + ekb;
-        const int64_t row = e * N + n;
-        if (n < N && kb < nkb) *reinterpret_cast<uint2*>(qT + row * (K >> 1) + kb * 8) = make_uint2(c0, c1);
-        // scale bytes: the 4 lanes of one column hold 4 consecutive blocks
-        const uint32_t s1 = __shfl_down_sync(0xffffffffu, sfc, 1);
-        const uint32_t s2 = __shfl_down_sync(0xffffffffu, sfc, 2);
-        const uint32_t s3 = __shfl_down_sync(0xffffffffu, sfc, 3);
-        if (ekb == 0 && n < N) {
-            const uint32_t word = sfc | (s1 << 8) | (s2 << 16) | (s3 << 24);
-            if (mma_layout) {
-                *reinterpret_cast<uint32_t*>(sfT + mma_sf_offset(row, kb0, nkb)) = word;
-            } else {
+        const bool more = t + 1 < t_end;
+        uint32_t code[2][8], sfw[2] = {0u, 0u};                // [column][word] / [column] scale word
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    if (kb0 + j < nkb) sfT[row * nkb + kb0 + j] = (uint8_t)(word >> (8 * j));
+        for (int b = 0; b < 4; ++b) {
+            const uint32_t* rb = (b < 2 ? xa : xb) + 16 * (b & 1);
+            uint32_t m = 0;
+#pragma unroll
+            for (int r = 0; r < 16; ++r) m = __vmaxu2(m, rb[r] & 0x7FFF7FFFu);
+            const BlockCodes lo = column_block<false>(rb, m & 0xFFFFu, mode, sc, T, I);
+            const BlockCodes hi = column_block<true>(rb, m >> 16, mode, sc, T, I);
+            code[0][2 * b] = lo.c0;
+            code[0][2 * b + 1] = lo.c1;
+            code[1][2 * b] = hi.c0;
+            code[1][2 * b + 1] = hi.c1;
+            sfw[0] |= lo.sfc << (8 * b);                       // blocks past K (zero rows) have scale 0
+            sfw[1] |= hi.sfc << (8 * b);
+            if (b == 1 && more) load_half(xa, e1, nt1, kt1, 0);
+            if (b == 3 && more) load_half(xb, e1, nt1, kt1, 1);
+        }
+        const int64_t n = nt * WE_N + 2 * lane;
+        if (n < N) {
+            const int64_t kb0 = kt * (WE_K / 16);
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int64_t row = e * N + n + j;
+                uint8_t* qd = qT + row * half_k + kb0 * 8;
+                if (sector_rows) {
+                    st_sector(qd, make_uint4(code[j][0], code[j][1], code[j][2], code[j][3]),
+                              make_uint4(code[j][4], code[j][5], code[j][6], code[j][7]));
+                } else {
+#pragma unroll
+                    for (int b = 0; b < 4; ++b)
+                        if (kb0 + b < nkb)
+                            *reinterpret_cast<uint2*>(qd + 8 * b) = make_uint2(code[j][2 * b], code[j][2 * b + 1]);
+                }
+                if (mma_layout) {
+                    // kb0 is a multiple of 4: the word is one whole 4-column group, padding included
+                    *reinterpret_cast<uint32_t*>(sfT + mma_sf_offset(row, kb0, nkb)) = sfw[j];
+                } else if (whole_k) {
+                    *reinterpret_cast<uint32_t*>(sfT + row * nkb + kb0) = sfw[j];
+                } else {
+#pragma unroll
+                    for (int b = 0; b < 4; ++b)
+                        if (kb0 + b < nkb) sfT[row * nkb + kb0 + b] = (uint8_t)(sfw[j] >> (8 * b));
+                }
             }
         }
+        e = e1;
+        nt = nt1;
+        kt = kt1;
     }
 }
 
@@ -516,18 +577,18 @@ cudaError_t launch_nvfp4_quantize_weights(const uint16_t* w, int64_t E, int64_t 
             ++launched;
         }
     }
-    // one resident wave of encode CTAs over every tile of every expert
+    // one resident wave of encode warps over every tile of every expert
     static int enc_per_sm = 0;
     static std::once_flag enc_once;
     std::call_once(enc_once, [] {
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&enc_per_sm, nvfp4_weight_encode_kernel, WT_THREADS, 0) !=
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&enc_per_sm, nvfp4_weight_encode_kernel, WE_THREADS, 0) !=
             cudaSuccess || enc_per_sm < 1)
             enc_per_sm = 1;
     });
-    const int64_t tiles_k = (K + WT_K - 1) / WT_K, tiles_n = (N + WT_N - 1) / WT_N;
+    const int64_t tiles_k = (K + WE_K - 1) / WE_K, tiles_n = (N + WE_N - 1) / WE_N;
     const int64_t total = E * tiles_k * tiles_n;
-    const int64_t enc_grid = std::min<int64_t>(total, (int64_t)sms * enc_per_sm);
-    nvfp4_weight_encode_kernel<<<(unsigned)enc_grid, WT_THREADS, 0, stream>>>(
+    const int64_t enc_grid = std::min<int64_t>((total + WE_WARPS - 1) / WE_WARPS, (int64_t)sms * enc_per_sm);
+    nvfp4_weight_encode_kernel<<<(unsigned)enc_grid, WE_THREADS, 0, stream>>>(
         w, K, N, tiles_k, tiles_n, total, qT, sfT, reinterpret_cast<const uint32_t*>(s_w), mma_layout);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     ++launched;

@@ -207,7 +207,8 @@ def test_nvfp4_per_token_invariance_on_gpu(nvq):
 # ------------------------------------------------------------------------------------------------
 # NVFP4 weights
 # ------------------------------------------------------------------------------------------------
-@pytest.mark.parametrize("shape", [(3, 256, 192), (2, 80, 72), (1, 512, 384), (4, 64, 128)])
+@pytest.mark.parametrize("shape", [(3, 256, 192), (2, 80, 72), (1, 512, 384), (4, 64, 128), (2, 96, 136),
+                                   (3, 48, 40), (1, 2080, 264)])
 @pytest.mark.parametrize("layout", ["canonical", "mma"])
 def test_nvfp4_weights_bit_exact(nvq, shape, layout):
     E, K, N = shape
