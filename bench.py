@@ -18,6 +18,12 @@ the pages ablate, see workloads.py):
   decode   256 tokens, uniform top-8 (2048 routed rows): per-token NVFP4 of the activations and the
            grouped NVFP4 gate_up GEMM against resident NVFP4 weights, plus the BF16 dequantization of
            all gate_up expert weights.
+  dq_backward  the backward shapes with the dequantized-backward mode: BF16 dequantization of the
+           MXFP8 operands and grouped BF16 GEMMs.
+  quant, dispatch, swiglu, weights  (GB/s lines) the quantizers alone on the routed gate_up batch;
+           quantize-once dispatch (per-token NVFP4 of the tokens, then a gather into expert order);
+           the fused SwiGLU + per-token NVFP4 of the down-projection input; NVFP4 quantization of all
+           gate_up and down expert weights.
 
 value = block-scaled GEMM throughput of the step (GEMM flops of the step / device time of the whole
 step, quantizers included) in TFLOPS; the quantizers' GB/s and every kernel's fraction of its
@@ -44,21 +50,26 @@ L2_FLUSH_BYTES = 256 << 20
 
 # ncu DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of the kernels timed
 # here, keyed by workload and kernel, with the sha256 of the source file the capture was taken
-# from. The commands that produced them are in profiles/launches_dense_step.md (dense) and
-# profiles/quant_routed_batch.md (quant). A changed source reports null.
+# from. The commands that produced them are in profiles/launches_dense_step.md (dense),
+# profiles/quant_routed_batch.md (quant) and profiles/quant_nvfp4_weights.md (weights; the amax
+# and encode launches of one call summed). A changed source reports null.
 NCU_TRAFFIC = {
     "dense": {
         "mxfp8_quantize X row+col": {"bytes": 33600000, "src_sha": "31e38c0af20c14f0"},
         "mxfp8_quantize W col": {"bytes": 20980000, "src_sha": "31e38c0af20c14f0"},
-        "nvfp4_quantize_per_token X": {"bytes": 33620000, "src_sha": "560b662e7e18c991"},
-        "nvfp4_quantize_weights W": {"bytes": 41990000, "src_sha": "560b662e7e18c991"},
+        "nvfp4_quantize_per_token X": {"bytes": 33620000, "src_sha": "cb91c4a9236a9d78"},
+        "nvfp4_quantize_weights W": {"bytes": 42020000, "src_sha": "cb91c4a9236a9d78"},
         "block_scaled_gemm MXFP8": {"bytes": 56970000, "src_sha": "905b1490423e6dd9"},
         "block_scaled_gemm NVFP4": {"bytes": 41800000, "src_sha": "905b1490423e6dd9"},
         "dequantize_bf16 W": {"bytes": 5910000, "src_sha": "def12a43bb80c45b"},
     },
+    "weights": {
+        "nvfp4_quantize_weights gate_up": {"bytes": 1841260000, "src_sha": "cb91c4a9236a9d78"},
+        "nvfp4_quantize_weights down": {"bytes": 882260000, "src_sha": "cb91c4a9236a9d78"},
+    },
     "quant": {
         "mxfp8_quantize X row+col": {"bytes": 1081560000, "src_sha": "31e38c0af20c14f0"},
-        "nvfp4_quantize_per_token X": {"bytes": 675920000, "src_sha": "560b662e7e18c991"},
+        "nvfp4_quantize_per_token X": {"bytes": 675930000, "src_sha": "cb91c4a9236a9d78"},
     },
 }
 
@@ -481,6 +492,35 @@ def _workload_quant(torch, nvq, wl, dev):
             "config": config, "dtype": "bf16 -> mxfp8 / nvfp4", "unit": "GB/s"}
 
 
+def _workload_weights(torch, nvq, wl, dev):
+    """NVFP4 expert-weight quantization alone: the MoE gate_up and down matrices of every expert."""
+    E, H, I2, I = wl.EXPERTS, wl.HIDDEN, 2 * wl.INTERMEDIATE, wl.INTERMEDIATE
+    w1 = wl.expert_weights(H, I2, seed=3, device=dev)
+    w2 = wl.expert_weights(I, H, seed=4, device=dev)
+
+    def alloc_w(e, k, n):
+        return (torch.empty((e, n, k // 2), dtype=torch.uint8, device=dev),
+                torch.empty(nvq.sf_bytes(e * n, k, 16), dtype=torch.uint8, device=dev),
+                torch.empty(e, dtype=torch.float32, device=dev))
+
+    b1, b2 = alloc_w(E, H, I2), alloc_w(E, I, H)
+    kernels = [
+        Kernel("nvfp4_quantize_weights gate_up", "hbm", E * H * I2 * 2.5625 + 4 * E, "quant_nvfp4.cu", "hbm", "2.5625 B/elem"),
+        Kernel("nvfp4_quantize_weights down", "hbm", E * I * H * 2.5625 + 4 * E, "quant_nvfp4.cu", "hbm", "2.5625 B/elem"),
+    ]
+
+    def step(timer, xin=None, win=None):
+        wa, wb = (w1, w2) if win is None else win
+        timer.run(kernels[0].name, lambda: nvq.nvfp4_quantize_weights(wa, out=b1))
+        timer.run(kernels[1].name, lambda: nvq.nvfp4_quantize_weights(wb, out=b2))
+        return [b1[2], b2[2]]
+
+    config = {"workload": "NVFP4 expert-weight quantization (Qwen3-30B-A3B MoE: gate_up and down of 128 experts)",
+              "gate_up": [E, H, I2], "down": [E, I, H]}
+    return {"step": step, "kernels": kernels, "gemm_flops": 0.0, "inputs": [w1, w2], "input_groups": ([], [0, 1]),
+            "config": config, "dtype": "bf16 -> nvfp4 (e2m1 + e4m3 + fp32 scale per expert)", "unit": "GB/s"}
+
+
 def _workload_dispatch(torch, nvq, wl, dev):
     """Quantize-once dispatch of the MoE gate_up input: per-token NVFP4 of the 16384 tokens, then the
     gather of their quantized rows into the 132960 expert-sorted routed rows (32-row padded)."""
@@ -547,8 +587,8 @@ def _workload_swiglu(torch, nvq, wl, dev):
 
 WORKLOADS = {"dense": _workload_dense, "quant": _workload_quant, "moe": _workload_moe, "backward": _workload_backward,
              "decode": _workload_decode, "dispatch": _workload_dispatch, "dq_backward": _workload_dq_backward,
-             "swiglu": _workload_swiglu}
-GBS_WORKLOADS = ("quant", "dispatch", "swiglu")
+             "swiglu": _workload_swiglu, "weights": _workload_weights}
+GBS_WORKLOADS = ("quant", "dispatch", "swiglu", "weights")
 
 
 class ClockSampler:
@@ -814,6 +854,15 @@ def _oracle_sample(workload, rows, cols):
         q[idx], sf[idx], s[idx]
         flops = T * K * 2.5625 + 4 * T + 2 * rows * (K // 2 + K // 16 + 4)   # algorithmic bytes
         desc = f"oracle per-token NVFP4 of {T} tokens x {K}, gathered into {rows} rows"
+    elif workload == "weights":
+        import torch
+        K = wl.HIDDEN
+        w = (rng.standard_normal((1, K, cols)) * 0.02).astype(np.float32)
+        wb = wl.to_bits(torch.from_numpy(w).to(torch.bfloat16))
+        t0 = time.perf_counter()
+        oracle.nvfp4_quantize_weights(wb)
+        flops = K * cols * 2.5625 + 4                               # algorithmic bytes, not flops
+        desc = f"oracle NVFP4 weights of one expert matrix [{K} x {cols}]"
     elif workload == "quant":
         import torch
         K = wl.HIDDEN
