@@ -28,8 +28,10 @@
 //   warps 2-5      epilogue: tcgen05.ld 32 columns at a time (the next load in flight while the
 //                  current chunk converts), multiply by s_a[row] s_b[e], round to bf16 into
 //                  registers (the whole 256-column row of each thread), hand TMEM back to the MMA
-//                  warp, then store with 256-bit stores while the next tile's MMAs run (fp32
-//                  output: stored chunk by chunk).
+//                  warp, then store while the next tile's MMAs run: for grouped row-offset GEMMs
+//                  each warp stages 32 x 32 chunks in shared memory (64-byte swizzle) and sends them
+//                  with TMA box stores; otherwise each thread stores its row with 256-bit stores
+//                  (fp32 output: stored chunk by chunk).
 // GROUP_K tiles iterate the group's reduction range in 32-element MMA steps (k-steps outside the
 // group inside a 128-element stage are skipped).
 //
@@ -84,7 +86,12 @@ struct GemmCfg {
         | ((uint32_t)(BN >> 3) << 17)                  // N >> 3
         | ((uint32_t)(BM >> 4) << 24);                 // M >> 4
     static constexpr int BAR_BYTES = 256;
-    static constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + BAR_BYTES + 8 * (MAX_GROUPS + 1);
+    // bf16 output staging for the TMA stores: per epilogue warp, STG_BUFS buffers of 32 rows x 32
+    // columns (2 KB, 64-byte swizzle), 1024-aligned after the stages, barriers and group tables
+    static constexpr size_t STG_OFFSET =
+        ((size_t)STAGES * STAGE_BYTES + BAR_BYTES + 8 * (MAX_GROUPS + 1) + 1023) / 1024 * 1024;
+    static constexpr int STG_BUFS = (1024 + STG_OFFSET + 4 * 2 * 2048 <= 232448) ? 2 : 1;
+    static constexpr size_t SMEM_BYTES = 1024 + STG_OFFSET + 4 * (size_t)STG_BUFS * 2048;
     static_assert(BN + SF_SETS * SF_SET_COLS <= TMEM_COLS, "TMEM columns");
     static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 };
@@ -102,6 +109,7 @@ struct GemmParams {
     void* d;
     int64_t ldd;
     int d_aligned32;        // d and every row of it start on 32 bytes: 256-bit stores
+    int tma_store;          // bf16 output leaves through staged TMA box stores (else per-thread rows)
     int32_t* status;
     int64_t a_rowtiles;     // 128-row scale tiles of A
     int64_t b_rowtiles;     // 128-row scale tiles of B (stacked rows)
@@ -177,6 +185,17 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
         ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
         : "memory");
 }
+
+// Shared -> global tensor copy of one box (bulk-group completion); x, y: element coordinates
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int32_t x, int32_t y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];"
+                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// wait until at most N bulk groups of this thread still read shared memory
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory"); }
 
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
     asm volatile(
@@ -364,7 +383,7 @@ struct StageCursor {
 template <int FMT>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
 block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                         const GemmParams p) {
+                         const __grid_constant__ CUtensorMap tmap_d, const GemmParams p) {
     using C = GemmCfg<FMT>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -669,6 +688,8 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
         // =========================== epilogue ===========================
         const int q = warp & 3;                       // TMEM lane quarter this warp may access
         const int row_in_tile = q * 32 + lane;
+        const uint32_t stg_warp = smem_u32(smem + C::STG_OFFSET) + (uint32_t)(q * C::STG_BUFS * 2048);
+        uint32_t stg_count = 0;                       // chunks this warp has staged
         const uint32_t tbase = tmem_acc + ((uint32_t)(q * 32) << 16);
         uint32_t acc_phase = 0;
         for (int64_t t = first; t < total; t += stride) {
@@ -740,26 +761,61 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
 #pragma unroll
                     for (int j = 0; j < 16; ++j) pk[c][j] = 0u;
             }
-            if (row_ok) {
-                uint16_t* dst = reinterpret_cast<uint16_t*>(p.d) + drow * p.ldd + tl.n0;
+            if (!p.tma_store) {
+                if (row_ok) {
+                    uint16_t* dst = reinterpret_cast<uint16_t*>(p.d) + drow * p.ldd + tl.n0;
+#pragma unroll
+                    for (int c = 0; c < BN / 32; ++c) {
+                        if (tl.n0 + c * 32 >= p.n) break;
+                        if (p.d_aligned32) {
+#pragma unroll
+                            for (int h = 0; h < 2; ++h)
+                                st_v8(dst + c * 32 + h * 16, pk[c][8 * h], pk[c][8 * h + 1], pk[c][8 * h + 2],
+                                      pk[c][8 * h + 3], pk[c][8 * h + 4], pk[c][8 * h + 5], pk[c][8 * h + 6],
+                                      pk[c][8 * h + 7]);
+                        } else {
+#pragma unroll
+                            for (int h = 0; h < 4; ++h)
+                                reinterpret_cast<uint4*>(dst + c * 32)[h] =
+                                    make_uint4(pk[c][4 * h], pk[c][4 * h + 1], pk[c][4 * h + 2], pk[c][4 * h + 3]);
+                        }
+                    }
+                }
+                continue;
+            }
+            // Stores: each 32-column chunk of the warp's 32 rows goes through a 2 KB staging buffer
+            // (row `lane` = 64 bytes, 16-byte pieces placed by the 64-byte swizzle: piece j of row r
+            // at j ^ ((r >> 1) & 3)) and leaves as one TMA box store. Group offsets are multiples of
+            // 32, so the warp's 32 rows lie wholly inside or outside the tile's group.
+            if (tl.a_row0 + q * 32 < tl.row_end) {
 #pragma unroll
                 for (int c = 0; c < BN / 32; ++c) {
                     if (tl.n0 + c * 32 >= p.n) break;
-                    if (p.d_aligned32) {
+                    const uint32_t buf = stg_warp + (uint32_t)((stg_count % C::STG_BUFS) * 2048);
+                    // the buffer's previous store has finished reading it (groups complete in order)
+                    if (lane == 0) bulk_wait_read<C::STG_BUFS - 1>();
+                    __syncwarp();
+                    const uint32_t rowp = buf + (uint32_t)lane * 64;
+                    const uint32_t swz = (uint32_t)(lane >> 1) & 3u;
 #pragma unroll
-                        for (int h = 0; h < 2; ++h)
-                            st_v8(dst + c * 32 + h * 16, pk[c][8 * h], pk[c][8 * h + 1], pk[c][8 * h + 2],
-                                  pk[c][8 * h + 3], pk[c][8 * h + 4], pk[c][8 * h + 5], pk[c][8 * h + 6],
-                                  pk[c][8 * h + 7]);
-                    } else {
-#pragma unroll
-                        for (int h = 0; h < 4; ++h)
-                            reinterpret_cast<uint4*>(dst + c * 32)[h] =
-                                make_uint4(pk[c][4 * h], pk[c][4 * h + 1], pk[c][4 * h + 2], pk[c][4 * h + 3]);
+                    for (int j = 0; j < 4; ++j)
+                        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};"
+                                     ::"r"(rowp + ((j ^ swz) << 4)), "r"(pk[c][4 * j]), "r"(pk[c][4 * j + 1]),
+                                       "r"(pk[c][4 * j + 2]), "r"(pk[c][4 * j + 3])
+                                     : "memory");
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmap_d, buf, (int32_t)(tl.n0 + c * 32), (int32_t)(tl.d_row0 + q * 32));
+                        bulk_commit();
                     }
+                    ++stg_count;
                 }
             }
         }
+        // the staged chunks must be read out before the CTA exits
+        if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+        __syncwarp();
     }
 
     // teardown: every role is done (and has drained the asynchronous work it issued)
@@ -807,6 +863,20 @@ static bool make_tmap(CUtensorMap* map, const void* base, int64_t rows, int64_t 
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D bf16 tensor map over D [rows, n] (row pitch ldd elements) with a 32 x 32 box and 64-byte
+// swizzle, for the epilogue's box stores; columns past n are not written.
+static bool make_tmap_d(CUtensorMap* map, void* base, int64_t rows, int64_t n, int64_t ldd) {
+    EncodeTiledFn enc = get_encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)n, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)ldd * 2};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, base, dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 static int num_sms() {
     int dev = 0, n = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
@@ -820,9 +890,15 @@ static nvq_status launch_gemm(const nvq_gemm_args* a, cudaStream_t stream) {
     const int64_t row_bytes = C::FP4 ? a->k / 2 : (C::SCALED ? a->k : 2 * a->k);
     const int64_t rows_a = a->m;
     const int64_t rows_b = (a->mode == NVQ_GEMM_GROUP_M) ? a->groups * a->n : a->n;
-    CUtensorMap ta, tb;
+    CUtensorMap ta, tb, td;
     if (!make_tmap(&ta, a->a, rows_a, row_bytes, BM) || !make_tmap(&tb, a->b, rows_b, row_bytes, BN))
         return NVQ_ERR_CUDA;
+    if (a->out_type == NVQ_OUT_F32) {
+        td = ta;                                   // unused: fp32 rows are stored by the threads
+    } else {
+        const int64_t rows_d = (a->mode == NVQ_GEMM_GROUP_M) ? a->m : a->groups * a->m;
+        if (!make_tmap_d(&td, a->d, rows_d, a->n, a->ldd)) return NVQ_ERR_CUDA;
+    }
     GemmParams p;
     p.mode = a->mode;
     p.out_f32 = a->out_type == NVQ_OUT_F32;
@@ -838,6 +914,10 @@ static nvq_status launch_gemm(const nvq_gemm_args* a, cudaStream_t stream) {
     p.d = a->d;
     p.ldd = a->ldd;
     p.d_aligned32 = ((reinterpret_cast<uintptr_t>(a->d) & 31u) == 0) && (a->ldd % 16 == 0);
+    // Box stores through shared memory for grouped row-offset GEMMs (MoE forward and data
+    // gradient: measured 5-22% faster); per-thread row stores for one group and for per-expert
+    // weight gradients, which measured 4-8% faster that way.
+    p.tma_store = a->out_type == NVQ_OUT_BF16 && a->mode == NVQ_GEMM_GROUP_M && a->groups > 1;
     p.status = a->status;
     p.a_rowtiles = (rows_a + BM - 1) / BM;
     p.b_rowtiles = (rows_b + BM - 1) / BM;
@@ -853,7 +933,7 @@ static nvq_status launch_gemm(const nvq_gemm_args* a, cudaStream_t stream) {
     if (!attr_ok) return NVQ_ERR_CUDA;
     const int grid = num_sms();
     if (grid <= 0) return NVQ_ERR_CUDA;
-    block_scaled_gemm_kernel<FMT><<<grid, GEMM_THREADS, C::SMEM_BYTES, stream>>>(ta, tb, p);
+    block_scaled_gemm_kernel<FMT><<<grid, GEMM_THREADS, C::SMEM_BYTES, stream>>>(ta, tb, td, p);
     if (cudaGetLastError() != cudaSuccess) return NVQ_ERR_CUDA;
     count_launches(1);
     return NVQ_OK;
