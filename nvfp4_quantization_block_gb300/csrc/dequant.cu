@@ -26,6 +26,7 @@ __device__ __forceinline__ int64_t sf_index(int64_t row, int64_t kb, int64_t nkb
 __global__ void __launch_bounds__(256)
 dequant_mxfp8_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ sf, int64_t rows,
                      int64_t cols, int mma_layout, uint16_t* __restrict__ out) {
+    griddep_begin();
     const int64_t nkb = cols >> 5;
     const int64_t blk = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (blk >= rows * nkb) return;
@@ -66,6 +67,7 @@ __global__ void __launch_bounds__(256)
 dequant_nvfp4_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ sf,
                      const float* __restrict__ s, int64_t rows_per_group, int64_t total_rows,
                      int64_t cols, int scope_matrix, int mma_layout, uint16_t* __restrict__ out) {
+    griddep_begin();
     const int64_t nkb = cols >> 4;
     const int64_t blk = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (blk >= total_rows * nkb) return;
@@ -99,16 +101,17 @@ cudaError_t launch_dequantize_bf16(int fmt_nvfp4, const uint8_t* q, const uint8_
                                    int scope_matrix, int64_t groups, int64_t rows, int64_t cols,
                                    int mma_layout, uint16_t* out, cudaStream_t stream) {
     const int64_t total_rows = groups * rows;
+    cudaError_t lerr;
     if (!fmt_nvfp4) {
         const int64_t nblk = total_rows * (cols >> 5);
-        dequant_mxfp8_kernel<<<(unsigned)((nblk + 255) / 256), 256, 0, stream>>>(q, sf, total_rows, cols,
-                                                                                  mma_layout, out);
+        lerr = launch_pdl(dequant_mxfp8_kernel, dim3((unsigned)((nblk + 255) / 256)), dim3(256), 0, stream, q, sf,
+                          total_rows, cols, mma_layout, out);
     } else {
         const int64_t nblk = total_rows * (cols >> 4);
-        dequant_nvfp4_kernel<<<(unsigned)((nblk + 255) / 256), 256, 0, stream>>>(
-            q, sf, s, rows, total_rows, cols, scope_matrix, mma_layout, out);
+        lerr = launch_pdl(dequant_nvfp4_kernel, dim3((unsigned)((nblk + 255) / 256)), dim3(256), 0, stream, q, sf, s,
+                          rows, total_rows, cols, scope_matrix, mma_layout, out);
     }
-    const cudaError_t err = cudaGetLastError();
+    const cudaError_t err = lerr != cudaSuccess ? lerr : cudaGetLastError();
     if (err == cudaSuccess) count_launches(1);
     return err;
 }

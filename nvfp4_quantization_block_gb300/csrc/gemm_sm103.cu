@@ -384,6 +384,7 @@ template <int FMT>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
 block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                          const __grid_constant__ CUtensorMap tmap_d, const GemmParams p) {
+    griddep_begin();
     using C = GemmCfg<FMT>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -914,10 +915,12 @@ static nvq_status launch_gemm(const nvq_gemm_args* a, cudaStream_t stream) {
     p.d = a->d;
     p.ldd = a->ldd;
     p.d_aligned32 = ((reinterpret_cast<uintptr_t>(a->d) & 31u) == 0) && (a->ldd % 16 == 0);
-    // Box stores through shared memory for grouped row-offset GEMMs (MoE forward and data
-    // gradient: measured 5-22% faster); per-thread row stores for one group and for per-expert
-    // weight gradients, which measured 4-8% faster that way.
-    p.tma_store = a->out_type == NVQ_OUT_BF16 && a->mode == NVQ_GEMM_GROUP_M && a->groups > 1;
+    // Box stores through shared memory for grouped row-offset GEMMs whose groups fill their row
+    // tiles (MoE forward and data gradient: measured 5-22% faster); per-thread row stores for one
+    // group, for per-expert weight gradients (4-8% faster that way) and for groups of a few rows
+    // (decode: most warps of a tile have no rows to store).
+    p.tma_store = a->out_type == NVQ_OUT_BF16 && a->mode == NVQ_GEMM_GROUP_M && a->groups > 1 &&
+                  a->m >= BM * a->groups;
     p.status = a->status;
     p.a_rowtiles = (rows_a + BM - 1) / BM;
     p.b_rowtiles = (rows_b + BM - 1) / BM;
@@ -933,8 +936,13 @@ static nvq_status launch_gemm(const nvq_gemm_args* a, cudaStream_t stream) {
     if (!attr_ok) return NVQ_ERR_CUDA;
     const int grid = num_sms();
     if (grid <= 0) return NVQ_ERR_CUDA;
-    block_scaled_gemm_kernel<FMT><<<grid, GEMM_THREADS, C::SMEM_BYTES, stream>>>(ta, tb, td, p);
-    if (cudaGetLastError() != cudaSuccess) return NVQ_ERR_CUDA;
+    // the staging buffers sit at the end of shared memory: launches that store rows directly leave
+    // them out (a larger shared-memory request shrinks L1; measured on the decode shape)
+    const size_t smem = p.tma_store ? C::SMEM_BYTES : C::SMEM_BYTES - (size_t)4 * C::STG_BUFS * 2048;
+    if (launch_pdl(block_scaled_gemm_kernel<FMT>, dim3(grid), dim3(GEMM_THREADS), smem, stream, ta, tb, td, p) !=
+            cudaSuccess ||
+        cudaGetLastError() != cudaSuccess)
+        return NVQ_ERR_CUDA;
     count_launches(1);
     return NVQ_OK;
 }

@@ -26,6 +26,7 @@ template <bool TO_MMA>
 __global__ void __launch_bounds__(32 * LO_ROWS)
 sf_convert_kernel(const uint8_t* __restrict__ src, int64_t rows, int64_t kb, uint8_t* __restrict__ dst,
                   int64_t rows_cover) {
+    griddep_begin();
     const int64_t r = (int64_t)blockIdx.x * LO_ROWS + threadIdx.y;
     if (r >= rows_cover) return;
     const int64_t words = (kb + 3) >> 2;
@@ -53,11 +54,10 @@ cudaError_t launch_sf_layout_convert(const uint8_t* src, int to_mma, int64_t row
     const int64_t cover = to_mma ? ((rows + 127) & ~int64_t(127)) : rows;
     const dim3 block(32, LO_ROWS);
     const unsigned grid = (unsigned)((cover + LO_ROWS - 1) / LO_ROWS);
-    if (to_mma)
-        sf_convert_kernel<true><<<grid, block, 0, stream>>>(src, rows, kb, dst, cover);
-    else
-        sf_convert_kernel<false><<<grid, block, 0, stream>>>(src, rows, kb, dst, cover);
-    const cudaError_t err = cudaGetLastError();
+    const cudaError_t lerr =
+        to_mma ? launch_pdl(sf_convert_kernel<true>, dim3(grid), block, 0, stream, src, rows, kb, dst, cover)
+               : launch_pdl(sf_convert_kernel<false>, dim3(grid), block, 0, stream, src, rows, kb, dst, cover);
+    const cudaError_t err = lerr != cudaSuccess ? lerr : cudaGetLastError();
     if (err == cudaSuccess) count_launches(1);
     return err;
 }
@@ -70,6 +70,7 @@ gather_rows_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ sf
                    int64_t src_rows, int64_t qbytes, int64_t kb, const int32_t* __restrict__ index, int64_t rows,
                    int64_t rows_cover, uint8_t* __restrict__ q_out, uint8_t* __restrict__ sf_out,
                    float* __restrict__ s_out, int32_t* __restrict__ status) {
+    griddep_begin();
     const int lane = threadIdx.x & 31;
     const int64_t i = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (i >= rows_cover) return;
@@ -118,15 +119,16 @@ cudaError_t launch_quantized_gather_rows(const uint8_t* q, const uint8_t* sf, co
                                          int32_t* status, cudaStream_t stream) {
     const int64_t cover = dst_mma ? ((rows + 127) & ~int64_t(127)) : rows;
     const unsigned grid = (unsigned)((cover + 7) / 8);
-#define NVQ_GATHER(SM, DM)                                                                                   \
-    gather_rows_kernel<SM, DM><<<grid, 256, 0, stream>>>(q, sf, s, src_rows, qbytes, kb, index, rows, cover, \
-                                                         q_out, sf_out, s_out, status)
+    cudaError_t lerr;
+#define NVQ_GATHER(SM, DM)                                                                                 \
+    lerr = launch_pdl(gather_rows_kernel<SM, DM>, dim3(grid), dim3(256), 0, stream, q, sf, s, src_rows, qbytes, \
+                      kb, index, rows, cover, q_out, sf_out, s_out, status)
     if (src_mma && dst_mma) NVQ_GATHER(true, true);
     else if (src_mma) NVQ_GATHER(true, false);
     else if (dst_mma) NVQ_GATHER(false, true);
     else NVQ_GATHER(false, false);
 #undef NVQ_GATHER
-    const cudaError_t err = cudaGetLastError();
+    const cudaError_t err = lerr != cudaSuccess ? lerr : cudaGetLastError();
     if (err == cudaSuccess) count_launches(1);
     return err;
 }

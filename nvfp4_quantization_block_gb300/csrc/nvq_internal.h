@@ -2,9 +2,31 @@
 // and returns the launch status; argument checking happens in api.cu before any of these runs.
 #pragma once
 #include <cstdint>
+#include <utility>
 #include <cuda_runtime.h>
 
 namespace nvq {
+
+// Launch with programmatic stream serialization: the kernel may be scheduled while the kernel
+// before it in the stream is still finishing (its last CTAs), which hides the launch gap between
+// dependent kernels. Every kernel of this library starts with griddep_begin() (nvq_device.cuh):
+// griddepcontrol.wait, so it touches no global memory before its predecessor has completed and
+// its writes are visible.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args&&... args) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 cudaError_t launch_mxfp8_quantize(const uint16_t* x, int64_t R, int64_t C, int64_t ldx,
                                   uint8_t* q_row, uint8_t* sf_row, uint8_t* q_colT, uint8_t* sf_colT,

@@ -40,6 +40,7 @@ __global__ void __launch_bounds__(MX_THREADS, (MxOcc<ROW, COL, STAGED>::value))
 mxfp8_quant_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t C, int64_t ldx,
                    uint8_t* __restrict__ q_row, uint8_t* __restrict__ sf_row,
                    uint8_t* __restrict__ q_colT, uint8_t* __restrict__ sf_colT, int mma_layout) {
+    griddep_begin();
     __shared__ __align__(16) uint32_t tile[MX_TILE][MX_TILE / 2];   // bf16 pairs
     __shared__ __align__(4) uint8_t sfT_stage[MX_TILE][4];
 
@@ -183,8 +184,10 @@ cudaError_t launch_mxfp8_quantize(const uint16_t* x, int64_t R, int64_t C, int64
     });
     // grids deeper than two waves of the register variant are staged through shared memory
     const bool staged = (int64_t)grid.x * grid.y > 2 * 4 * (int64_t)sms;
-#define NVQ_MX(RW, CL, ST) \
-    mxfp8_quant_kernel<RW, CL, ST><<<grid, MX_THREADS, 0, stream>>>(x, R, C, ldx, q_row, sf_row, q_colT, sf_colT, mma_layout)
+    cudaError_t lerr;
+#define NVQ_MX(RW, CL, ST)                                                                                       \
+    lerr = launch_pdl(mxfp8_quant_kernel<RW, CL, ST>, grid, dim3(MX_THREADS), 0, stream, x, R, C, ldx, q_row, sf_row, \
+                      q_colT, sf_colT, mma_layout)
     if (q_row && q_colT) {
         if (staged) NVQ_MX(true, true, true);
         else NVQ_MX(true, true, false);
@@ -195,7 +198,7 @@ cudaError_t launch_mxfp8_quantize(const uint16_t* x, int64_t R, int64_t C, int64
         NVQ_MX(true, false, false);
     }
 #undef NVQ_MX
-    const cudaError_t err = cudaGetLastError();
+    const cudaError_t err = lerr != cudaSuccess ? lerr : cudaGetLastError();
     if (err == cudaSuccess) count_launches(1);
     return err;
 }

@@ -200,6 +200,7 @@ __global__ void __launch_bounds__(TOK_THREADS)
 nvfp4_token_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t C, int64_t ldx,
                    uint8_t* __restrict__ q, uint8_t* __restrict__ sf, float* __restrict__ s_tok,
                    int mma_layout, int64_t rows_cover) {
+    griddep_begin();
     constexpr int RPW = 32 / LPR;                              // rows per warp
     __shared__ Nvfp4Table tables[(TOK_THREADS / 32) * RPW];   // one per row
     __shared__ Nvfp4CodeInfo info;
@@ -294,8 +295,10 @@ static cudaError_t launch_token(const uint16_t* x, int64_t R, int64_t C, int64_t
     const int rows_per_cta = (TOK_THREADS / 32) * (pair ? 2 : 1);
     const int64_t grid = (cover + rows_per_cta - 1) / rows_per_cta;
     const bool v8 = ((reinterpret_cast<uintptr_t>(x) & 31u) == 0) && (ldx % 16 == 0) && (!SWIGLU || C % 16 == 0);
-#define NVQ_TOK(V, L) \
-    nvfp4_token_kernel<V, SWIGLU, L><<<(unsigned)grid, TOK_THREADS, 0, stream>>>(x, R, C, ldx, q, sf, s_tok, mma_layout, cover)
+    cudaError_t lerr;
+#define NVQ_TOK(V, L)                                                                                             \
+    lerr = launch_pdl(nvfp4_token_kernel<V, SWIGLU, L>, dim3((unsigned)grid), dim3(TOK_THREADS), 0, stream, x, R, C, \
+                      ldx, q, sf, s_tok, mma_layout, cover)
     if (v8) {
         if (pair) NVQ_TOK(true, 16);
         else NVQ_TOK(true, 32);
@@ -304,7 +307,7 @@ static cudaError_t launch_token(const uint16_t* x, int64_t R, int64_t C, int64_t
         else NVQ_TOK(false, 32);
     }
 #undef NVQ_TOK
-    const cudaError_t err = cudaGetLastError();
+    const cudaError_t err = lerr != cudaSuccess ? lerr : cudaGetLastError();
     if (err == cudaSuccess) count_launches(1);
     return err;
 }
@@ -329,6 +332,7 @@ constexpr int WA_VEC = 4;                // 16-byte vectors in flight per thread
 
 __global__ void __launch_bounds__(256)
 nvfp4_weight_amax_kernel(const uint16_t* __restrict__ w, int64_t per_expert, uint32_t* __restrict__ amax_bits) {
+    griddep_begin();
     const int64_t e = blockIdx.y;
     const uint16_t* we = w + e * per_expert;
     const int64_t nvec = per_expert >> 3;
@@ -420,6 +424,7 @@ __global__ void __launch_bounds__(WE_THREADS, 3)
 nvfp4_weight_encode_kernel(const uint16_t* __restrict__ w, int64_t K, int64_t N, int64_t tiles_k, int64_t tiles_n,
                            int64_t total, uint8_t* __restrict__ qT, uint8_t* __restrict__ sfT,
                            const uint32_t* __restrict__ amax_bits, int mma_layout) {
+    griddep_begin();
     __shared__ Nvfp4Table tables[WE_WARPS];                    // each warp's current expert
     __shared__ Nvfp4CodeInfo I;
     for (uint32_t c = threadIdx.x; c < 128u; c += WE_THREADS) nvfp4_code_info_build(I, c);
@@ -531,12 +536,14 @@ nvfp4_weight_encode_kernel(const uint16_t* __restrict__ w, int64_t K, int64_t N,
 }
 
 __global__ void nvfp4_weight_finalize_kernel(float* s_w, int64_t E) {
+    griddep_begin();
     const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (e < E) s_w[e] = nvfp4_coarse_scale(__uint_as_float(reinterpret_cast<uint32_t*>(s_w)[e]));
 }
 
 // zero the padding rows of an MMA-layout scale buffer beyond `rows` (rows not multiple of 128)
 __global__ void zero_bytes_kernel(uint8_t* p, int64_t n) {
+    griddep_begin();
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i < n) p[i] = 0;
 }
@@ -547,8 +554,9 @@ cudaError_t launch_nvfp4_quantize_weights(const uint16_t* w, int64_t E, int64_t 
     int launched = 0;
     cudaError_t err;
     // s_w accumulates the amax bits per expert: clear it first
-    zero_bytes_kernel<<<(unsigned)((4 * E + 255) / 256), 256, 0, stream>>>(reinterpret_cast<uint8_t*>(s_w), 4 * E);
-    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    if ((err = launch_pdl(zero_bytes_kernel, dim3((unsigned)((4 * E + 255) / 256)), dim3(256), 0, stream,
+                          reinterpret_cast<uint8_t*>(s_w), 4 * E)) != cudaSuccess)
+        return err;
     ++launched;
     const int64_t per_expert = K * N;
     // enough CTAs in total to fill the GPU a few times over, at least one per expert
@@ -559,9 +567,9 @@ cudaError_t launch_nvfp4_quantize_weights(const uint16_t* w, int64_t E, int64_t 
     const int64_t max_blocks = (per_expert / 8 + 255) / 256;
     if (blocks > max_blocks) blocks = max_blocks;
     if (blocks < 1) blocks = 1;
-    nvfp4_weight_amax_kernel<<<dim3((unsigned)blocks, (unsigned)E), 256, 0, stream>>>(
-        w, per_expert, reinterpret_cast<uint32_t*>(s_w));
-    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    if ((err = launch_pdl(nvfp4_weight_amax_kernel, dim3((unsigned)blocks, (unsigned)E), dim3(256), 0, stream, w,
+                          per_expert, reinterpret_cast<uint32_t*>(s_w))) != cudaSuccess)
+        return err;
     ++launched;
     if (mma_layout) {
         // rows of the stacked [E*N, K/16] scale matrix are padded to 128; the encode kernel writes
@@ -572,8 +580,9 @@ cudaError_t launch_nvfp4_quantize_weights(const uint16_t* w, int64_t E, int64_t 
         if (padded_rows > rows) {
             const int64_t start = mma_sf_offset(padded_rows - 128, 0, kb);
             const int64_t bytes = ((kb + 3) >> 2) * 512;
-            zero_bytes_kernel<<<(unsigned)((bytes + 255) / 256), 256, 0, stream>>>(sfT + start, bytes);
-            if ((err = cudaGetLastError()) != cudaSuccess) return err;
+            if ((err = launch_pdl(zero_bytes_kernel, dim3((unsigned)((bytes + 255) / 256)), dim3(256), 0, stream,
+                                  sfT + start, bytes)) != cudaSuccess)
+                return err;
             ++launched;
         }
     }
@@ -588,12 +597,14 @@ cudaError_t launch_nvfp4_quantize_weights(const uint16_t* w, int64_t E, int64_t 
     const int64_t tiles_k = (K + WE_K - 1) / WE_K, tiles_n = (N + WE_N - 1) / WE_N;
     const int64_t total = E * tiles_k * tiles_n;
     const int64_t enc_grid = std::min<int64_t>((total + WE_WARPS - 1) / WE_WARPS, (int64_t)sms * enc_per_sm);
-    nvfp4_weight_encode_kernel<<<(unsigned)enc_grid, WE_THREADS, 0, stream>>>(
-        w, K, N, tiles_k, tiles_n, total, qT, sfT, reinterpret_cast<const uint32_t*>(s_w), mma_layout);
-    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    if ((err = launch_pdl(nvfp4_weight_encode_kernel, dim3((unsigned)enc_grid), dim3(WE_THREADS), 0, stream, w, K, N,
+                          tiles_k, tiles_n, total, qT, sfT, reinterpret_cast<const uint32_t*>(s_w), mma_layout)) !=
+        cudaSuccess)
+        return err;
     ++launched;
-    nvfp4_weight_finalize_kernel<<<(unsigned)((E + 255) / 256), 256, 0, stream>>>(s_w, E);
-    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    if ((err = launch_pdl(nvfp4_weight_finalize_kernel, dim3((unsigned)((E + 255) / 256)), dim3(256), 0, stream,
+                          s_w, E)) != cudaSuccess)
+        return err;
     count_launches(launched + 1);
     return cudaSuccess;
 }
