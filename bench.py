@@ -55,21 +55,21 @@ L2_FLUSH_BYTES = 256 << 20
 # and encode launches of one call summed). A changed source reports null.
 NCU_TRAFFIC = {
     "dense": {
-        "mxfp8_quantize X row+col": {"bytes": 33600000, "src_sha": "31e38c0af20c14f0"},
-        "mxfp8_quantize W col": {"bytes": 20980000, "src_sha": "31e38c0af20c14f0"},
-        "nvfp4_quantize_per_token X": {"bytes": 33620000, "src_sha": "cb91c4a9236a9d78"},
-        "nvfp4_quantize_weights W": {"bytes": 42020000, "src_sha": "cb91c4a9236a9d78"},
-        "block_scaled_gemm MXFP8": {"bytes": 56970000, "src_sha": "905b1490423e6dd9"},
-        "block_scaled_gemm NVFP4": {"bytes": 41800000, "src_sha": "905b1490423e6dd9"},
-        "dequantize_bf16 W": {"bytes": 5910000, "src_sha": "def12a43bb80c45b"},
+        "mxfp8_quantize X row+col": {"bytes": 33610000, "src_sha": "293d50137682089b"},
+        "mxfp8_quantize W col": {"bytes": 20980000, "src_sha": "293d50137682089b"},
+        "nvfp4_quantize_per_token X": {"bytes": 33620000, "src_sha": "b23bc0aa0fcfb6e6"},
+        "nvfp4_quantize_weights W": {"bytes": 42020000, "src_sha": "b23bc0aa0fcfb6e6"},
+        "block_scaled_gemm MXFP8": {"bytes": 57080000, "src_sha": "d0a34bd987afd406"},
+        "block_scaled_gemm NVFP4": {"bytes": 42240000, "src_sha": "d0a34bd987afd406"},
+        "dequantize_bf16 W": {"bytes": 5910000, "src_sha": "9cc5b769e6d11623"},
     },
     "weights": {
-        "nvfp4_quantize_weights gate_up": {"bytes": 1841260000, "src_sha": "cb91c4a9236a9d78"},
-        "nvfp4_quantize_weights down": {"bytes": 882260000, "src_sha": "cb91c4a9236a9d78"},
+        "nvfp4_quantize_weights gate_up": {"bytes": 1841560000, "src_sha": "b23bc0aa0fcfb6e6"},
+        "nvfp4_quantize_weights down": {"bytes": 882390000, "src_sha": "b23bc0aa0fcfb6e6"},
     },
     "quant": {
-        "mxfp8_quantize X row+col": {"bytes": 1081560000, "src_sha": "31e38c0af20c14f0"},
-        "nvfp4_quantize_per_token X": {"bytes": 675930000, "src_sha": "cb91c4a9236a9d78"},
+        "mxfp8_quantize X row+col": {"bytes": 1081260000, "src_sha": "293d50137682089b"},
+        "nvfp4_quantize_per_token X": {"bytes": 676250000, "src_sha": "b23bc0aa0fcfb6e6"},
     },
 }
 
