@@ -10,8 +10,8 @@
 //          fma(p, s, -t); the remainder's sign sets the last bit of t (round to odd), after which
 //          the bf16 conversion yields the single rounding of the exact product (Boldo & Melquiond,
 //          IEEE TC 2008). Tiny products, where the remainder could underflow, use fp64.
-// One thread produces one 32-element (MXFP8) or 16-element (NVFP4) block: 16- or 8-byte loads,
-// 64- or 32-byte stores, one scale byte, streaming through HBM once. NVFP4 blocks look their 16
+// One thread produces one 32-element (MXFP8) or two 16-element (NVFP4) blocks: 16- or 8-byte loads,
+// 64- or 32-byte stores, one scale byte per block, streaming through HBM once. NVFP4 blocks look their 16
 // results up in a per-block table of the 8 possible bf16 values (byte permutes), so the E2M1
 // conversion instruction, which issues on a low-throughput pipe, is not used per element.
 #include "nvq_device.cuh"
@@ -23,14 +23,29 @@ __device__ __forceinline__ int64_t sf_index(int64_t row, int64_t kb, int64_t nkb
     return mma_layout ? mma_sf_offset(row, kb, nkb) : row * nkb + kb;
 }
 
+// (row, block) of block index blk in a [rows, nkb] block grid; 32-bit division when the grid has
+// fewer than 2^32 blocks (a 64-bit division expands to several dozen instructions)
+__device__ __forceinline__ void block_coords(int64_t blk, int64_t nkb, bool small, int64_t& row, int64_t& kb) {
+    if (small) {
+        const uint32_t r = (uint32_t)blk / (uint32_t)nkb;
+        row = r;
+        kb = (int64_t)((uint32_t)blk - r * (uint32_t)nkb);
+    } else {
+        row = blk / nkb;
+        kb = blk - row * nkb;
+    }
+}
+
 __global__ void __launch_bounds__(256)
 dequant_mxfp8_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ sf, int64_t rows,
                      int64_t cols, int mma_layout, uint16_t* __restrict__ out) {
     griddep_begin();
     const int64_t nkb = cols >> 5;
     const int64_t blk = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (blk >= rows * nkb) return;
-    const int64_t row = blk / nkb, kb = blk - row * nkb;
+    const int64_t nblk = rows * nkb;
+    if (blk >= nblk) return;
+    int64_t row, kb;
+    block_coords(blk, nkb, nblk <= 0xFFFFFFFFll, row, kb);
     const float scale = e8m0_scale(sf[sf_index(row, kb, nkb, mma_layout)]);
     const uint8_t* src = q + row * cols + kb * 32;
     const uint4 a = ld_stream_v4(src), b = ld_stream_v4(src + 16);
@@ -63,18 +78,7 @@ __device__ __forceinline__ float round_odd_product(float p, float s) {
 // One 16-element block: every element takes one of 8 magnitudes times the block's scale product,
 // so the block's 8 possible bf16 results are computed once (round-to-odd products) and the codes
 // select them with byte permutes; the sign bit is copied from the code. No per-element conversion.
-__global__ void __launch_bounds__(256)
-dequant_nvfp4_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ sf,
-                     const float* __restrict__ s, int64_t rows_per_group, int64_t total_rows,
-                     int64_t cols, int scope_matrix, int mma_layout, uint16_t* __restrict__ out) {
-    griddep_begin();
-    const int64_t nkb = cols >> 4;
-    const int64_t blk = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (blk >= total_rows * nkb) return;
-    const int64_t row = blk / nkb, kb = blk - row * nkb;
-    const float coarse = s[scope_matrix ? row / rows_per_group : row];
-    const float v_sf = e4m3_to_f32(sf[sf_index(row, kb, nkb, mma_layout)]);
-    const uint2 packed = *reinterpret_cast<const uint2*>(q + row * (cols >> 1) + kb * 8);
+__device__ __forceinline__ void dequant_nvfp4_block(uint2 packed, float v_sf, float coarse, uint4& d0, uint4& d1) {
     // bf16 results for magnitude codes 0..7 = {0, .5, 1, 1.5, 2, 3, 4, 6} x v_sf x coarse
     const uint32_t p01 = cvt_bf16x2(0.0f, round_odd_product(0.5f * v_sf, coarse));
     const uint32_t p23 = cvt_bf16x2(round_odd_product(v_sf, coarse), round_odd_product(1.5f * v_sf, coarse));
@@ -92,9 +96,42 @@ dequant_nvfp4_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ 
         o[2 * i] = __byte_perm(lo, hi, 0x5140) | ((qq << 12) & 0x8000u) | ((qq << 24) & 0x80000000u);
         o[2 * i + 1] = __byte_perm(lo, hi, 0x7362) | ((qq << 4) & 0x8000u) | ((qq << 16) & 0x80000000u);
     }
-    uint4* dst = reinterpret_cast<uint4*>(out + row * cols + kb * 16);
-    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    d0 = make_uint4(o[0], o[1], o[2], o[3]);
+    d1 = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+// Two blocks per thread: blocks 2t and 2t + 1 of the row-major block grid (the same row unless
+// the row has an odd number of blocks).
+__global__ void __launch_bounds__(256)
+dequant_nvfp4_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ sf,
+                     const float* __restrict__ s, int64_t rows_per_group, int64_t total_rows,
+                     int64_t cols, int scope_matrix, int mma_layout, uint16_t* __restrict__ out) {
+    griddep_begin();
+    const int64_t nkb = cols >> 4;
+    const int64_t nblk = total_rows * nkb;
+    const int64_t blk0 = 2 * ((int64_t)blockIdx.x * blockDim.x + threadIdx.x);
+    if (blk0 >= nblk) return;
+    const bool small = nblk <= 0xFFFFFFFFll;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int64_t blk = blk0 + h;
+        if (blk >= nblk) break;
+        int64_t row, kb;
+        block_coords(blk, nkb, small, row, kb);
+        int64_t scope = row;
+        if (scope_matrix) {
+            if (small) scope = (int64_t)((uint32_t)row / (uint32_t)rows_per_group);
+            else scope = row / rows_per_group;
+        }
+        const float coarse = s[scope];
+        const float v_sf = e4m3_to_f32(sf[sf_index(row, kb, nkb, mma_layout)]);
+        const uint2 packed = *reinterpret_cast<const uint2*>(q + row * (cols >> 1) + kb * 8);
+        uint4 d0, d1;
+        dequant_nvfp4_block(packed, v_sf, coarse, d0, d1);
+        uint4* dst = reinterpret_cast<uint4*>(out + row * cols + kb * 16);
+        dst[0] = d0;
+        dst[1] = d1;
+    }
 }
 
 cudaError_t launch_dequantize_bf16(int fmt_nvfp4, const uint8_t* q, const uint8_t* sf, const float* s,
@@ -108,8 +145,9 @@ cudaError_t launch_dequantize_bf16(int fmt_nvfp4, const uint8_t* q, const uint8_
                           total_rows, cols, mma_layout, out);
     } else {
         const int64_t nblk = total_rows * (cols >> 4);
-        lerr = launch_pdl(dequant_nvfp4_kernel, dim3((unsigned)((nblk + 255) / 256)), dim3(256), 0, stream, q, sf, s,
-                          rows, total_rows, cols, scope_matrix, mma_layout, out);
+        const int64_t threads = (nblk + 1) / 2;
+        lerr = launch_pdl(dequant_nvfp4_kernel, dim3((unsigned)((threads + 255) / 256)), dim3(256), 0, stream, q, sf,
+                          s, rows, total_rows, cols, scope_matrix, mma_layout, out);
     }
     const cudaError_t err = lerr != cudaSuccess ? lerr : cudaGetLastError();
     if (err == cudaSuccess) count_launches(1);
