@@ -151,6 +151,55 @@ def test_many_tiles_per_cta(nvq, fmt):
     _check(d, D, bound, False)
 
 
+@pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4"])
+def test_box_store_epilogue_edges(nvq, fmt):
+    """bf16 output of a grouped GEMM whose groups fill their row tiles (the epilogue's staged box
+    stores): N = 384 (the last 256-column tile half full), an output view with a row pitch wider
+    than N, and buffer rows after the last group; padding columns and those rows stay untouched."""
+    counts = [300, 40, 0, 260, 97]
+    E, K, N = len(counts), 512, 384
+    offs, xb = _routed(counts, K, seed=41)
+    extra = 64
+    xb = np.concatenate([xb, np.zeros((extra, K), dtype=xb.dtype)])
+    M = xb.shape[0]
+    assert offs[-1] >= 128 * E                      # groups fill their tiles: box stores are used
+    rng = np.random.default_rng(42)
+    wb = _bits(rng.standard_normal((E, K, N)) * 0.02 * np.exp(rng.uniform(-2, 2, (E, 1, 1))))
+    x = workloads.from_bits(xb, "cuda")
+    w = workloads.from_bits(wb, "cuda")
+    offs_d = torch.from_numpy(offs).cuda()
+    big = torch.full((M, N + 64), 7.0, dtype=torch.bfloat16, device="cuda")
+    d = big[:, :N]
+    if fmt == "nvfp4":
+        qa, sfa, sa = nvq.nvfp4_quantize_per_token(x)
+        qb, sfb, sb = nvq.nvfp4_quantize_weights(w.contiguous())
+        nvq.block_scaled_grouped_gemm(nvq.NVFP4, nvq.GEMM_GROUP_M, qa, sfa, qb, sfb, offs_d, m=M, n=N, k=K, groups=E,
+                                      s_a=sa, s_b=sb, out=d)
+        qa_r, sfa_r, sa_r = oracle.nvfp4_quantize_per_token(xb)
+        qb_r, sfb_r, sb_r = oracle.nvfp4_quantize_weights(wb)
+        a = oracle.deq_operand("nvfp4", qa_r, sfa_r)
+        b = np.stack([oracle.deq_operand("nvfp4", qb_r[e], sfb_r[e]) for e in range(E)])
+        D, bound = oracle.grouped_gemm_reference("m", a, b, offs, sa_r, sb_r)
+    else:
+        qa = nvq.mxfp8_quantize(x, colwise=False)
+        qb = nvq.mxfp8_quantize(w.transpose(1, 2).contiguous().view(E * N, K), colwise=False)
+        nvq.block_scaled_grouped_gemm(nvq.MXFP8, nvq.GEMM_GROUP_M, qa["q_row"], qa["sf_row"], qb["q_row"],
+                                      qb["sf_row"], offs_d, m=M, n=N, k=K, groups=E, out=d)
+        ra = oracle.mxfp8_quantize(xb, colwise=False)
+        a = oracle.deq_operand("mxfp8", ra["q_row"], ra["sf_row"])
+        b = np.stack([oracle.deq_operand("mxfp8", *oracle.mxfp8_quantize(np.ascontiguousarray(wb[e]),
+                                                                          rowwise=False).values())
+                      for e in range(E)])
+        D, bound = oracle.grouped_gemm_reference("m", a, b, offs)
+    torch.cuda.synchronize()
+    rows = ~np.isnan(D[:, 0])
+    assert rows.sum() == offs[-1]
+    _check(d[torch.from_numpy(rows).cuda()], D[rows], bound[rows], True)
+    host = big.float().cpu().numpy()
+    assert (host[:, N:] == 7.0).all()               # columns past N
+    assert (host[int(offs[-1]):, :] == 7.0).all()   # rows after the last group
+
+
 def test_rows_outside_groups_untouched(nvq):
     E, K, N = 2, 256, 256
     counts = [40, 20]
