@@ -174,7 +174,7 @@ def _workload_dense(torch, nvq, wl, dev):
         Kernel("mxfp8_quantize W col", "hbm", ne_w * (2 + 1 + 1 / 32), "quant_mxfp8.cu", "hbm", "3.03125 B/elem"),
         Kernel("nvfp4_quantize_per_token X", "hbm", ne_x * (2 + 0.5 + 1 / 16) + 4 * M, "quant_nvfp4.cu", "hbm",
                "2.5625 B/elem + 4 B/row"),
-        Kernel("nvfp4_quantize_weights W", "hbm", ne_w * (2 + 0.5 + 1 / 16) + 4, "quant_nvfp4.cu", "hbm",
+        Kernel("nvfp4_quantize_weights W", "hbm", ne_w * (2 + 0.5 + 1 / 16) + 4, "quant_nvfp4_weights.cu", "hbm",
                "2.5625 B/elem (one read; the kernel reads twice)"),
         Kernel("block_scaled_gemm MXFP8", "tensor", gemm_flops, "gemm_sm103.cu", "fp8", "2*M*N*K"),
         Kernel("block_scaled_gemm NVFP4", "tensor", gemm_flops, "gemm_sm103.cu", "fp4", "2*M*N*K"),
@@ -234,10 +234,10 @@ def _workload_moe(torch, nvq, wl, dev):
          "d2": torch.empty((R, H), dtype=torch.bfloat16, device=dev)}
     kernels = [
         Kernel("nvfp4_quantize_per_token gate_up input", "hbm", R * H * 2.5625 + 4 * R, "quant_nvfp4.cu", "hbm", "2.5625 B/elem + 4 B/row"),
-        Kernel("nvfp4_quantize_weights gate_up", "hbm", E * H * I2 * 2.5625 + 4 * E, "quant_nvfp4.cu", "hbm", "2.5625 B/elem"),
+        Kernel("nvfp4_quantize_weights gate_up", "hbm", E * H * I2 * 2.5625 + 4 * E, "quant_nvfp4_weights.cu", "hbm", "2.5625 B/elem"),
         Kernel("block_scaled_gemm NVFP4 gate_up", "tensor", f1, "gemm_sm103.cu", "fp4", "2*sum_e M_e*N*K"),
         Kernel("nvfp4_quantize_per_token down input", "hbm", R * I * 2.5625 + 4 * R, "quant_nvfp4.cu", "hbm", "2.5625 B/elem + 4 B/row"),
-        Kernel("nvfp4_quantize_weights down", "hbm", E * I * H * 2.5625 + 4 * E, "quant_nvfp4.cu", "hbm", "2.5625 B/elem"),
+        Kernel("nvfp4_quantize_weights down", "hbm", E * I * H * 2.5625 + 4 * E, "quant_nvfp4_weights.cu", "hbm", "2.5625 B/elem"),
         Kernel("block_scaled_gemm NVFP4 down", "tensor", f2, "gemm_sm103.cu", "fp4", "2*sum_e M_e*N*K"),
     ]
 
@@ -506,8 +506,8 @@ def _workload_weights(torch, nvq, wl, dev):
 
     b1, b2 = alloc_w(E, H, I2), alloc_w(E, I, H)
     kernels = [
-        Kernel("nvfp4_quantize_weights gate_up", "hbm", E * H * I2 * 2.5625 + 4 * E, "quant_nvfp4.cu", "hbm", "2.5625 B/elem"),
-        Kernel("nvfp4_quantize_weights down", "hbm", E * I * H * 2.5625 + 4 * E, "quant_nvfp4.cu", "hbm", "2.5625 B/elem"),
+        Kernel("nvfp4_quantize_weights gate_up", "hbm", E * H * I2 * 2.5625 + 4 * E, "quant_nvfp4_weights.cu", "hbm", "2.5625 B/elem"),
+        Kernel("nvfp4_quantize_weights down", "hbm", E * I * H * 2.5625 + 4 * E, "quant_nvfp4_weights.cu", "hbm", "2.5625 B/elem"),
     ]
 
     def step(timer, xin=None, win=None):

@@ -1,4 +1,4 @@
-// NVFP4 quantizers: per-token activations and per-expert-matrix weights.
+// NVFP4 per-token quantizer (activations; the expert weights are in quant_nvfp4_weights.cu).
 //
 // Definition [Miles-zh = page "Miles 在 Blackwell GPU 上实现低精度强化学习，降低训练成本":
 // section "为什么需要 Blackwell 原生方案？" (E2M1 values, one E4M3 scale per 16 values rounded to
@@ -8,16 +8,14 @@
 // no fast math)]. Coarse scale s = RN(amax / 2688); block scale = E4M3 RNE of amax_b / (6 s);
 // code = E2M1 RNE (saturating) of x / (E4M3(sf) s). Exactness: see nvq_device.cuh.
 //
-// Per-token design: one warp per token row, one 16-element block per lane per step (see the
-// kernel). Weights: one warp per 64 x 64 tile, two columns and four 16-row blocks per lane. A scope
+// Design: one warp per token row, one 16-element block per lane per step (see the kernel). A scope
 // whose table passes the product-path check (nvq_device.cuh) encodes its elements by one fp32
 // multiply and the hardware E2M1 conversion; any other scope compares each element with its block's
 // exact boundaries.
-#include <algorithm>
-#include <mutex>
 
 #include "nvq_device.cuh"
 #include "nvq_internal.h"
+#include "nvq_nvfp4_encode.cuh"
 
 namespace nvq {
 
@@ -76,35 +74,6 @@ __device__ __forceinline__ void row_block(const uint16_t* p, int64_t up, uint4& 
         a = make_uint4(swiglu2(a.x, ua.x), swiglu2(a.y, ua.y), swiglu2(a.z, ua.z), swiglu2(a.w, ua.w));
         b = make_uint4(swiglu2(b.x, ub.x), swiglu2(b.y, ub.y), swiglu2(b.z, ub.z), swiglu2(b.w, ub.w));
     }
-}
-
-// How a scope's blocks are encoded: by the product path (its table passed the check), by the
-// table's boundary comparisons, or by exact fp64 decisions (a scope with a tiny or zero coarse scale).
-enum : int { ENC_TABLE = 0, ENC_EXACT = 1, ENC_PRODUCT = 2 };
-
-// Scale code and the 16 codes of one block (two uint4 of 8 bf16, magnitude maximum mb as bf16
-// bits); branch-free in the table and product modes.
-template <int MODE>
-__device__ __forceinline__ uint32_t encode_block(const uint4& a, const uint4& b, uint32_t mb, const Nvfp4Scope& sc,
-                                                 const Nvfp4Table& T, const Nvfp4CodeInfo& I, uint32_t& c0,
-                                                 uint32_t& c1) {
-    if (MODE == ENC_EXACT) {
-        const uint32_t sfc = nvfp4_block_scale(__uint_as_float(mb << 16), sc);
-        c0 = nvfp4_encode8_exact(a, sfc, sc);
-        c1 = nvfp4_encode8_exact(b, sfc, sc);
-        return sfc;
-    }
-    const uint32_t sfc = nvfp4_block_scale_t(mb, sc, T);
-    if (MODE == ENC_PRODUCT) {
-        const float g = nvfp4_block_g(sfc, T, I);
-        c0 = nvfp4_codes8_mul(a, g);
-        c1 = nvfp4_codes8_mul(b, g);
-    } else {
-        const E2M1Bounds bd = nvfp4_block_bounds_t(sfc, T, I);
-        c0 = nvfp4_codes8(a, bd);
-        c1 = nvfp4_codes8(b, bd);
-    }
-    return sfc;
 }
 
 // Where one token row's outputs go: its packed codes and its scale bytes (canonical row, or the
@@ -321,292 +290,6 @@ cudaError_t launch_nvfp4_quantize_per_token(const uint16_t* x, int64_t R, int64_
 cudaError_t launch_nvfp4_swiglu_quantize(const uint16_t* gate_up, int64_t R, int64_t I, int64_t ld, uint8_t* q,
                                          uint8_t* sf, float* s_tok, int mma_layout, cudaStream_t stream) {
     return launch_token<true>(gate_up, R, I, ld, q, sf, s_tok, mma_layout, stream);
-}
-
-// ------------------------------------------------------------------------------------------------
-// Weights: W [E, K, N] -> qT [E, N, K/2], sfT [E, N, K/16], s_w [E]; coarse scope = expert matrix.
-// Three kernels: amax per expert (atomic max on the fp32 bits, kept in s_w), encode, finalize
-// (s_w <- RN(amax / 2688)).
-// ------------------------------------------------------------------------------------------------
-constexpr int WA_VEC = 4;                // 16-byte vectors in flight per thread in the amax pass
-
-__global__ void __launch_bounds__(256)
-nvfp4_weight_amax_kernel(const uint16_t* __restrict__ w, int64_t per_expert, uint32_t* __restrict__ amax_bits) {
-    griddep_begin();
-    const int64_t e = blockIdx.y;
-    const uint16_t* we = w + e * per_expert;
-    const int64_t nvec = per_expert >> 3;
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    uint32_t m = 0;
-    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    // WA_VEC independent loads issued before any of them is used
-    for (; i + (WA_VEC - 1) * stride < nvec; i += WA_VEC * stride) {
-        uint4 v[WA_VEC];
-#pragma unroll
-        for (int j = 0; j < WA_VEC; ++j) v[j] = ld_stream_v4(we + (i + j * stride) * 8);
-#pragma unroll
-        for (int j = 0; j < WA_VEC; ++j) m = max(m, absmax_bits_8(v[j]));
-    }
-    for (; i < nvec; i += stride) m = max(m, absmax_bits_8(ld_stream_v4(we + i * 8)));
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
-    __shared__ uint32_t red[8];
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        uint32_t t = red[0];
-        for (int j = 1; j < (int)(blockDim.x >> 5); ++j) t = max(t, red[j]);
-        if (t) atomicMax(amax_bits + e, t << 16);    // non-negative floats order like their bits
-    }
-}
-
-// Encode: every warp works on its own, over a contiguous range of the (expert, n tile, k tile)
-// sequence of 64 k x 64 n tiles, so the load is even for any expert count and a warp rebuilds its
-// scope table only when its range enters the next expert. Lane l owns columns n0 + 2l and
-// n0 + 2l + 1 and the tile's four 16-row blocks: it loads the tile's 64 rows of its two columns (one
-// 4-byte load per row, 128 contiguous bytes per row across the warp; each 32-row half of the next
-// tile is requested as soon as the same half of this one is encoded), so each column's block is
-// the low or high halves of one word per row and no transpose is needed. Its outputs are whole per column: the four blocks' 32 code bytes (one L2 sector, one
-// store) and their 4 scale bytes (one 4-column group). K is the fastest tile index, so a row's
-// scale bytes are written by consecutive tiles of one warp. (Half-sector code stores, 16 bytes per
-// tile, made L2 write partial sectors back: 3.4x the output bytes in DRAM writes.)
-constexpr int WE_K = 64, WE_N = 64, WE_THREADS = 128, WE_WARPS = WE_THREADS / 32;
-
-// Pairs (x[2i], x[2i + 1]) of one column of 8 rows, as the bf16x2 words of the table and exact
-// paths: the column is the low (HI false) or high half of each row's word.
-template <bool HI>
-__device__ __forceinline__ uint4 column_pairs(const uint32_t* r) {
-    constexpr uint32_t sel = HI ? 0x7632u : 0x5410u;
-    return make_uint4(__byte_perm(r[0], r[1], sel), __byte_perm(r[2], r[3], sel), __byte_perm(r[4], r[5], sel),
-                      __byte_perm(r[6], r[7], sel));
-}
-
-// fp32 values of 8 rows of one column, times g, to 8 E2M1 codes (product path)
-template <bool HI>
-__device__ __forceinline__ uint32_t column_codes_mul(const uint32_t* r, float g) {
-    float x[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) x[i] = __fmul_rn(HI ? bf16_hi(r[i]) : bf16_lo(r[i]), g);
-    return cvt_e2m1x8(x[0], x[1], x[2], x[3], x[4], x[5], x[6], x[7]);
-}
-
-struct BlockCodes {
-    uint32_t sfc, c0, c1;
-};
-
-// Table or exact decisions for one column's 16-row block (the four pair words of each half): kept
-// out of line, so the product path's loop stays small.
-__device__ __noinline__ BlockCodes column_block_slow(uint4 a, uint4 b, uint32_t mb, int mode, Nvfp4Scope sc,
-                                                     const Nvfp4Table* T, const Nvfp4CodeInfo* I) {
-    BlockCodes r;
-    if (mode == ENC_TABLE) r.sfc = encode_block<ENC_TABLE>(a, b, mb, sc, *T, *I, r.c0, r.c1);
-    else r.sfc = encode_block<ENC_EXACT>(a, b, mb, sc, *T, *I, r.c0, r.c1);
-    return r;
-}
-
-// Scale code and codes of one column's 16-row block (rows r[0..15], the column in the low or high
-// halves), magnitude maximum mb
-template <bool HI>
-__device__ __forceinline__ BlockCodes column_block(const uint32_t* r, uint32_t mb, int mode, const Nvfp4Scope& sc,
-                                                   const Nvfp4Table& T, const Nvfp4CodeInfo& I) {
-    if (mode == ENC_PRODUCT) {
-        BlockCodes o;
-        o.sfc = nvfp4_block_scale_t(mb, sc, T);
-        const float g = nvfp4_block_g(o.sfc, T, I);
-        o.c0 = column_codes_mul<HI>(r, g);
-        o.c1 = column_codes_mul<HI>(r + 8, g);
-        return o;
-    }
-    return column_block_slow(column_pairs<HI>(r), column_pairs<HI>(r + 8), mb, mode, sc, &T, &I);
-}
-
-__global__ void __launch_bounds__(WE_THREADS, 3)
-nvfp4_weight_encode_kernel(const uint16_t* __restrict__ w, int64_t K, int64_t N, int64_t tiles_k, int64_t tiles_n,
-                           int64_t total, uint8_t* __restrict__ qT, uint8_t* __restrict__ sfT,
-                           const uint32_t* __restrict__ amax_bits, int mma_layout) {
-    griddep_begin();
-    __shared__ Nvfp4Table tables[WE_WARPS];                    // each warp's current expert
-    __shared__ Nvfp4CodeInfo I;
-    for (uint32_t c = threadIdx.x; c < 128u; c += WE_THREADS) nvfp4_code_info_build(I, c);
-    __syncthreads();
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    Nvfp4Table& T = tables[warp];
-    const int64_t gw = (int64_t)blockIdx.x * WE_WARPS + warp, nw = (int64_t)gridDim.x * WE_WARPS;
-    const int64_t t_begin = total * gw / nw, t_end = total * (gw + 1) / nw;
-    if (t_begin >= t_end) return;                              // uniform over the warp
-    const int64_t per_e = tiles_k * tiles_n;
-    int64_t e = t_begin / per_e;
-    int64_t nt = (t_begin - e * per_e) / tiles_k;
-    int64_t kt = t_begin - e * per_e - nt * tiles_k;
-    const int64_t nkb = K >> 4, half_k = K >> 1;
-    // whole tiles of K: one 32-byte code store per column (when the rows start on 32 bytes) and
-    // one 4-byte scale store
-    const bool whole_k = (K & 63) == 0;
-    const bool sector_rows = whole_k && ((reinterpret_cast<uintptr_t>(qT) & 31u) == 0);
-    int64_t cur_e = -1;
-    int mode = ENC_EXACT;
-    Nvfp4Scope sc = make_nvfp4_scope(0.0f);
-
-    // rows [0, 32) and [32, 64) of the tile's two columns (low / high half of each word); the next
-    // tile's half is loaded as soon as this tile's half is encoded, so loads stay in flight while
-    // the warp computes
-    uint32_t xa[WE_K / 2], xb[WE_K / 2];
-    auto load_half = [&](uint32_t (&x)[WE_K / 2], int64_t te, int64_t tn, int64_t tk, int h) {
-        const int64_t k0 = tk * WE_K + h * (WE_K / 2), n0 = tn * WE_N + 2 * lane;
-        const bool ok = n0 < N;                                // N even: both columns in or out together
-        const int64_t rows = K - k0;
-        const uint16_t* src = w + (te * K + k0) * N + n0;
-#pragma unroll
-        for (int r = 0; r < WE_K / 2; ++r) x[r] = ld_stream_u32_if(src + r * N, ok && r < rows);
-    };
-    load_half(xa, e, nt, kt, 0);
-    load_half(xb, e, nt, kt, 1);
-
-    for (int64_t t = t_begin; t < t_end; ++t) {
-        if (e != cur_e) {
-            __syncwarp();                                      // the previous expert's table reads are done
-            cur_e = e;
-            const float s = nvfp4_coarse_scale(__uint_as_float(amax_bits[e]));
-            sc = make_nvfp4_scope(s);
-            const bool all = __all_sync(0xffffffffu, nvfp4_table_build_warp(T, s, lane));
-            __syncwarp();
-            mode = sc.exact ? ENC_EXACT : (all ? ENC_PRODUCT : ENC_TABLE);
-        }
-        // the next tile (k fastest)
-        int64_t e1 = e, nt1 = nt, kt1 = kt + 1;
-        if (kt1 == tiles_k) {
-            kt1 = 0;
-            if (++nt1 == tiles_n) {
-                nt1 = 0;
-                ++e1;
-            }
-        }
-        const bool more = t + 1 < t_end;
-        uint32_t code[2][8], sfw[2] = {0u, 0u};                // [column][word] / [column] scale word
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-            const uint32_t* rb = (b < 2 ? xa : xb) + 16 * (b & 1);
-            uint32_t m = 0;
-#pragma unroll
-            for (int r = 0; r < 16; ++r) m = __vmaxu2(m, rb[r] & 0x7FFF7FFFu);
-            const BlockCodes lo = column_block<false>(rb, m & 0xFFFFu, mode, sc, T, I);
-            const BlockCodes hi = column_block<true>(rb, m >> 16, mode, sc, T, I);
-            code[0][2 * b] = lo.c0;
-            code[0][2 * b + 1] = lo.c1;
-            code[1][2 * b] = hi.c0;
-            code[1][2 * b + 1] = hi.c1;
-            sfw[0] |= lo.sfc << (8 * b);                       // blocks past K (zero rows) have scale 0
-            sfw[1] |= hi.sfc << (8 * b);
-            if (b == 1 && more) load_half(xa, e1, nt1, kt1, 0);
-            if (b == 3 && more) load_half(xb, e1, nt1, kt1, 1);
-        }
-        const int64_t n = nt * WE_N + 2 * lane;
-        if (n < N) {
-            const int64_t kb0 = kt * (WE_K / 16);
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const int64_t row = e * N + n + j;
-                uint8_t* qd = qT + row * half_k + kb0 * 8;
-                if (sector_rows) {
-                    st_sector(qd, make_uint4(code[j][0], code[j][1], code[j][2], code[j][3]),
-                              make_uint4(code[j][4], code[j][5], code[j][6], code[j][7]));
-                } else {
-#pragma unroll
-                    for (int b = 0; b < 4; ++b)
-                        if (kb0 + b < nkb)
-                            *reinterpret_cast<uint2*>(qd + 8 * b) = make_uint2(code[j][2 * b], code[j][2 * b + 1]);
-                }
-                if (mma_layout) {
-                    // kb0 is a multiple of 4: the word is one whole 4-column group, padding included
-                    *reinterpret_cast<uint32_t*>(sfT + mma_sf_offset(row, kb0, nkb)) = sfw[j];
-                } else if (whole_k) {
-                    *reinterpret_cast<uint32_t*>(sfT + row * nkb + kb0) = sfw[j];
-                } else {
-#pragma unroll
-                    for (int b = 0; b < 4; ++b)
-                        if (kb0 + b < nkb) sfT[row * nkb + kb0 + b] = (uint8_t)(sfw[j] >> (8 * b));
-                }
-            }
-        }
-        e = e1;
-        nt = nt1;
-        kt = kt1;
-    }
-}
-
-__global__ void nvfp4_weight_finalize_kernel(float* s_w, int64_t E) {
-    griddep_begin();
-    const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (e < E) s_w[e] = nvfp4_coarse_scale(__uint_as_float(reinterpret_cast<uint32_t*>(s_w)[e]));
-}
-
-// zero the padding rows of an MMA-layout scale buffer beyond `rows` (rows not multiple of 128)
-__global__ void zero_bytes_kernel(uint8_t* p, int64_t n) {
-    griddep_begin();
-    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i < n) p[i] = 0;
-}
-
-cudaError_t launch_nvfp4_quantize_weights(const uint16_t* w, int64_t E, int64_t K, int64_t N,
-                                          uint8_t* qT, uint8_t* sfT, float* s_w, int mma_layout,
-                                          cudaStream_t stream) {
-    int launched = 0;
-    cudaError_t err;
-    // s_w accumulates the amax bits per expert: clear it first
-    if ((err = launch_pdl(zero_bytes_kernel, dim3((unsigned)((4 * E + 255) / 256)), dim3(256), 0, stream,
-                          reinterpret_cast<uint8_t*>(s_w), 4 * E)) != cudaSuccess)
-        return err;
-    ++launched;
-    const int64_t per_expert = K * N;
-    // enough CTAs in total to fill the GPU a few times over, at least one per expert
-    int sms = 0, dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        sms = 148;
-    int64_t blocks = ((int64_t)sms * 8 + E - 1) / E;
-    const int64_t max_blocks = (per_expert / 8 + 255) / 256;
-    if (blocks > max_blocks) blocks = max_blocks;
-    if (blocks < 1) blocks = 1;
-    if ((err = launch_pdl(nvfp4_weight_amax_kernel, dim3((unsigned)blocks, (unsigned)E), dim3(256), 0, stream, w,
-                          per_expert, reinterpret_cast<uint32_t*>(s_w))) != cudaSuccess)
-        return err;
-    ++launched;
-    if (mma_layout) {
-        // rows of the stacked [E*N, K/16] scale matrix are padded to 128; the encode kernel writes
-        // every real row's tile bytes (column padding included), so only trailing pad rows remain:
-        // zero the last row tile before the encode kernel fills its real rows
-        const int64_t rows = E * N, kb = K >> 4;
-        const int64_t padded_rows = (rows + 127) & ~int64_t(127);
-        if (padded_rows > rows) {
-            const int64_t start = mma_sf_offset(padded_rows - 128, 0, kb);
-            const int64_t bytes = ((kb + 3) >> 2) * 512;
-            if ((err = launch_pdl(zero_bytes_kernel, dim3((unsigned)((bytes + 255) / 256)), dim3(256), 0, stream,
-                                  sfT + start, bytes)) != cudaSuccess)
-                return err;
-            ++launched;
-        }
-    }
-    // one resident wave of encode warps over every tile of every expert
-    static int enc_per_sm = 0;
-    static std::once_flag enc_once;
-    std::call_once(enc_once, [] {
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&enc_per_sm, nvfp4_weight_encode_kernel, WE_THREADS, 0) !=
-            cudaSuccess || enc_per_sm < 1)
-            enc_per_sm = 1;
-    });
-    const int64_t tiles_k = (K + WE_K - 1) / WE_K, tiles_n = (N + WE_N - 1) / WE_N;
-    const int64_t total = E * tiles_k * tiles_n;
-    const int64_t enc_grid = std::min<int64_t>((total + WE_WARPS - 1) / WE_WARPS, (int64_t)sms * enc_per_sm);
-    if ((err = launch_pdl(nvfp4_weight_encode_kernel, dim3((unsigned)enc_grid), dim3(WE_THREADS), 0, stream, w, K, N,
-                          tiles_k, tiles_n, total, qT, sfT, reinterpret_cast<const uint32_t*>(s_w), mma_layout)) !=
-        cudaSuccess)
-        return err;
-    ++launched;
-    if ((err = launch_pdl(nvfp4_weight_finalize_kernel, dim3((unsigned)((E + 255) / 256)), dim3(256), 0, stream,
-                          s_w, E)) != cudaSuccess)
-        return err;
-    count_launches(launched + 1);
-    return cudaSuccess;
 }
 
 }  // namespace nvq
