@@ -140,7 +140,8 @@ nvq_status nvfp4_swiglu_quantize_per_token(const void* gate_up, int64_t rows, in
  *   qT   [experts, N, K/2] packed codes.
  *   sfT  [experts, N, K/16] scales, or MMA layout of the stacked [experts*N, K/16] matrix.
  *   s_w  [experts] float32. Used as scratch between the kernels this call enqueues (it holds
- *        the running amax bits until the last kernel writes the scales).
+ *        the running amax bits, then, for more than one expert, the scales with a work-split flag
+ *        in the sign bit, until the last kernel writes the scales).
  * Requires K % 16 == 0 and N % 8 == 0.
  */
 nvq_status nvfp4_quantize_weights(const void* w, int64_t experts, int64_t k, int64_t n,

@@ -21,8 +21,9 @@ namespace nvq {
 
 // ------------------------------------------------------------------------------------------------
 // Weights: W [E, K, N] -> qT [E, N, K/2], sfT [E, N, K/16], s_w [E]; coarse scope = expert matrix.
-// Three kernels: amax per expert (atomic max on the fp32 bits, kept in s_w), encode, finalize
-// (s_w <- RN(amax / 2688)).
+// Kernels: amax per expert (atomic max on the fp32 bits, kept in s_w); for more than one expert a
+// check kernel (s_w <- coarse scale with a product-path flag, for a cost-weighted split of the
+// encode work); encode; finalize (s_w <- RN(amax / 2688), or the flag cleared).
 // ------------------------------------------------------------------------------------------------
 constexpr int WA_VEC = 4;                // 16-byte vectors in flight per thread in the amax pass
 
@@ -58,9 +59,9 @@ nvfp4_weight_amax_kernel(const uint16_t* __restrict__ w, int64_t per_expert, uin
 
 // Encode: the CTA's warps take adjacent 64-column strips of the same 64 rows (a super-tile of
 // WE_WARPS x 64 columns, so each row is read as WE_WARPS x 128 contiguous bytes), and CTAs take
-// contiguous ranges of the (expert, super-strip, k tile) sequence, k fastest, so the load is even
-// for any expert count and a warp rebuilds its scope table only when its range enters the next
-// expert. Each warp stages its strip through a ring of WE_STAGES 32-row half tiles in shared
+// contiguous ranges of the (expert, super-strip, k tile) sequence, k fastest (equal unit counts for
+// one expert, equal shares of the expected cost for several: see the check kernel), so a warp
+// rebuilds its scope table only when its range enters the next expert. Each warp stages its strip through a ring of WE_STAGES 32-row half tiles in shared
 // memory, filled by 16-byte cp.async copies WE_STAGES - 1 half tiles ahead of the one it encodes,
 // so loads stay in flight without holding registers (the encode work per byte is high, and a
 // register pipeline held the warps to 12 per SM). Lane l owns columns n0 + 2l and n0 + 2l + 1: it
@@ -153,22 +154,101 @@ struct WeCursor {
     }
 };
 
+// Weighted split (more than one expert). An expert whose table fails the product-path check
+// encodes each element by boundary comparisons, which measured about 1.5x the product path's time
+// per unit on GB300; with equal unit counts per CTA, the CTAs inside such an expert set the
+// kernel's end while the rest of the GPU idles. So a check kernel (one warp per expert) turns the
+// amax bits into the coarse scale s ahead of the encode kernel and records the outcome of the
+// check in the sign bit of s_w (s >= 0, so the bit is free until the finalize kernel clears it),
+// and the encode kernel gives each CTA an equal share of the summed unit costs. The flag steers
+// only the split: every warp still takes its own mode decision from its table.
+constexpr int WC_WARPS = 4;
+
+__global__ void __launch_bounds__(WC_WARPS * 32)
+nvfp4_weight_check_kernel(uint32_t* __restrict__ s_w, int64_t E) {
+    griddep_begin();
+    __shared__ Nvfp4Table tables[WC_WARPS];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t e = (int64_t)blockIdx.x * WC_WARPS + warp;
+    if (e >= E) return;                                        // uniform over the warp
+    const float s = nvfp4_coarse_scale(__uint_as_float(s_w[e]));
+    const bool exact = make_nvfp4_scope(s).exact;
+    const bool all = __all_sync(0xffffffffu, nvfp4_table_build_warp(tables[warp], s, lane));
+    if (lane == 0) s_w[e] = __float_as_uint(s) | ((exact || !all) ? 0x80000000u : 0u);
+}
+
+// Relative cost of one unit of an expert, from its flagged scale: product path 2, boundary
+// comparisons 3, exact decisions (tiny or zero scale; rare) 6.
+__device__ __forceinline__ int64_t we_unit_cost(uint32_t sbits) {
+    const float s = __uint_as_float(sbits & 0x7FFFFFFFu);
+    return !(s >= NVQ_FAST_MIN_SCALE) ? 6 : ((sbits >> 31) ? 3 : 2);
+}
+
+// Units [u0, u1) of CTA b of G when the CTAs take equal shares of the summed unit costs; units
+// run in expert order, per_e per expert, and a cost position x maps to the first unit whose cost
+// starts at or after x (so neighbouring CTAs meet at the same unit). Called by one whole warp.
+__device__ __noinline__ void we_weighted_range(const uint32_t* __restrict__ s_w, int64_t E, int64_t per_e, int64_t b, int64_t G,
+                                  int lane, int64_t& u0, int64_t& u1) {
+    int64_t t = 0;
+    for (int64_t e = lane; e < E; e += 32) t += we_unit_cost(s_w[e]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+    const int64_t T = t * per_e;
+    const int64_t x0 = T * b / G, x1 = T * (b + 1) / G;
+    int64_t r0 = -1, r1 = -1, P = 0;                           // P: cost of the experts before this chunk
+    for (int64_t base = 0; base < E; base += 32) {
+        const int64_t e = base + lane;
+        const int64_t c = e < E ? we_unit_cost(s_w[e]) : 0;
+        int64_t incl = c * per_e;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int64_t v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        const int64_t end = P + incl, start = end - c * per_e;  // expert e's cost range [start, end)
+        if (c > 0 && x0 >= start && x0 < end) r0 = e * per_e + (x0 - start + c - 1) / c;
+        if (c > 0 && x1 >= start && x1 < end) r1 = e * per_e + (x1 - start + c - 1) / c;
+        P += __shfl_sync(0xffffffffu, incl, 31);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        r0 = max(r0, (int64_t)__shfl_xor_sync(0xffffffffu, r0, o));
+        r1 = max(r1, (int64_t)__shfl_xor_sync(0xffffffffu, r1, o));
+    }
+    u0 = r0 < 0 ? E * per_e : r0;                              // x == T: past the last unit
+    u1 = r1 < 0 ? E * per_e : r1;
+}
+
 __global__ void __launch_bounds__(WE_THREADS, 4)
 nvfp4_weight_encode_kernel(const uint16_t* __restrict__ w, int64_t K, int64_t N, int64_t tiles_k, int64_t strips,
                            int64_t total, uint8_t* __restrict__ qT, uint8_t* __restrict__ sfT,
-                           const uint32_t* __restrict__ amax_bits, int mma_layout) {
+                           const uint32_t* __restrict__ amax_bits, int mma_layout, int weighted) {
     griddep_begin();
     extern __shared__ __align__(128) uint8_t we_stage[];
     __shared__ Nvfp4Table tables[WE_WARPS];                    // each warp's current expert
     __shared__ Nvfp4CodeInfo I;
+    __shared__ int64_t range[2];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t per_e = tiles_k * strips;
     for (uint32_t c = threadIdx.x; c < 128u; c += WE_THREADS) nvfp4_code_info_build(I, c);
+    if (warp == 0) {
+        int64_t b0, b1;
+        if (weighted) {
+            we_weighted_range(amax_bits, total / per_e, per_e, blockIdx.x, gridDim.x, lane, b0, b1);
+        } else {
+            b0 = total * blockIdx.x / gridDim.x;
+            b1 = total * (blockIdx.x + 1) / gridDim.x;
+        }
+        if (lane == 0) {
+            range[0] = b0;
+            range[1] = b1;
+        }
+    }
     __syncthreads();
 
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     Nvfp4Table& T = tables[warp];
-    const int64_t u_begin = total * blockIdx.x / gridDim.x, u_end = total * (blockIdx.x + 1) / gridDim.x;
+    const int64_t u_begin = range[0], u_end = range[1];
     if (u_begin >= u_end) return;                              // uniform over the CTA
-    const int64_t per_e = tiles_k * strips;
     WeCursor cur;                                              // the half tile being encoded
     cur.e = u_begin / per_e;
     cur.st = (u_begin - cur.e * per_e) / tiles_k;
@@ -235,7 +315,8 @@ nvfp4_weight_encode_kernel(const uint16_t* __restrict__ w, int64_t K, int64_t N,
         if (live && e != cur_e) {
             __syncwarp();                                      // the previous expert's table reads are done
             cur_e = e;
-            const float s = nvfp4_coarse_scale(__uint_as_float(amax_bits[e]));
+            const uint32_t sb = amax_bits[e];              // amax bits, or the flagged scale when weighted
+            const float s = weighted ? __uint_as_float(sb & 0x7FFFFFFFu) : nvfp4_coarse_scale(__uint_as_float(sb));
             sc = make_nvfp4_scope(s);
             const bool all = __all_sync(0xffffffffu, nvfp4_table_build_warp(T, s, lane));
             __syncwarp();
@@ -306,10 +387,15 @@ nvfp4_weight_encode_kernel(const uint16_t* __restrict__ w, int64_t K, int64_t N,
     asm volatile("cp.async.wait_group 0;" ::: "memory");
 }
 
-__global__ void nvfp4_weight_finalize_kernel(float* s_w, int64_t E) {
+// s_w <- RN(amax / 2688) from the amax bits, or (weighted) the check kernel's scale without its flag
+__global__ void nvfp4_weight_finalize_kernel(float* s_w, int64_t E, int weighted) {
     griddep_begin();
     const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (e < E) s_w[e] = nvfp4_coarse_scale(__uint_as_float(reinterpret_cast<uint32_t*>(s_w)[e]));
+    uint32_t* bits = reinterpret_cast<uint32_t*>(s_w);
+    if (e < E) {
+        if (weighted) bits[e] &= 0x7FFFFFFFu;
+        else s_w[e] = nvfp4_coarse_scale(__uint_as_float(bits[e]));
+    }
 }
 
 // zero the padding rows of an MMA-layout scale buffer beyond `rows` (rows not multiple of 128)
@@ -342,6 +428,14 @@ cudaError_t launch_nvfp4_quantize_weights(const uint16_t* w, int64_t E, int64_t 
                           per_expert, reinterpret_cast<uint32_t*>(s_w))) != cudaSuccess)
         return err;
     ++launched;
+    // more than one expert: coarse scales and product-path flags for the weighted split
+    const int weighted = E > 1 ? 1 : 0;
+    if (weighted) {
+        if ((err = launch_pdl(nvfp4_weight_check_kernel, dim3((unsigned)((E + WC_WARPS - 1) / WC_WARPS)),
+                              dim3(WC_WARPS * 32), 0, stream, reinterpret_cast<uint32_t*>(s_w), E)) != cudaSuccess)
+            return err;
+        ++launched;
+    }
     if (mma_layout) {
         // rows of the stacked [E*N, K/16] scale matrix are padded to 128; the encode kernel writes
         // every real row's tile bytes (column padding included), so only trailing pad rows remain:
@@ -375,11 +469,11 @@ cudaError_t launch_nvfp4_quantize_weights(const uint16_t* w, int64_t E, int64_t 
     const int64_t enc_grid = std::min<int64_t>(total, (int64_t)sms * enc_per_sm);
     if ((err = launch_pdl(nvfp4_weight_encode_kernel, dim3((unsigned)enc_grid), dim3(WE_THREADS), WE_SMEM_BYTES,
                           stream, w, K, N, tiles_k, strips, total, qT, sfT, reinterpret_cast<const uint32_t*>(s_w),
-                          mma_layout)) != cudaSuccess)
+                          mma_layout, weighted)) != cudaSuccess)
         return err;
     ++launched;
     if ((err = launch_pdl(nvfp4_weight_finalize_kernel, dim3((unsigned)((E + 255) / 256)), dim3(256), 0, stream,
-                          s_w, E)) != cudaSuccess)
+                          s_w, E, weighted)) != cudaSuccess)
         return err;
     count_launches(launched + 1);
     return cudaSuccess;
