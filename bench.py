@@ -52,21 +52,21 @@ L2_FLUSH_BYTES = 256 << 20
 # ncu DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of the kernels timed
 # here, keyed by workload and kernel, with the sha256 of the source file the capture was taken
 # from. The commands that produced them are in profiles/launches_dense_step.md (dense),
-# profiles/quant_routed_batch.md (quant) and profiles/quant_nvfp4_weights.md (weights; the amax
-# and encode launches of one call summed). A changed source reports null.
+# profiles/quant_routed_batch.md (quant) and profiles/quant_nvfp4_weights.md (weights; the
+# launches of one call summed). A changed source reports null.
 NCU_TRAFFIC = {
     "dense": {
-        "mxfp8_quantize X row+col": {"bytes": 33610000, "src_sha": "293d50137682089b"},
+        "mxfp8_quantize X row+col": {"bytes": 33600000, "src_sha": "293d50137682089b"},
         "mxfp8_quantize W col": {"bytes": 20980000, "src_sha": "293d50137682089b"},
-        "nvfp4_quantize_per_token X": {"bytes": 33620000, "src_sha": "b23bc0aa0fcfb6e6"},
-        "nvfp4_quantize_weights W": {"bytes": 42020000, "src_sha": "b23bc0aa0fcfb6e6"},
-        "block_scaled_gemm MXFP8": {"bytes": 57080000, "src_sha": "d0a34bd987afd406"},
-        "block_scaled_gemm NVFP4": {"bytes": 42240000, "src_sha": "d0a34bd987afd406"},
-        "dequantize_bf16 W": {"bytes": 5910000, "src_sha": "9cc5b769e6d11623"},
+        "nvfp4_quantize_per_token X": {"bytes": 33620000, "src_sha": "d4c39c27893902e1"},
+        "nvfp4_quantize_weights W": {"bytes": 42030000, "src_sha": "01d4aff2498125b3"},
+        "block_scaled_gemm MXFP8": {"bytes": 57560000, "src_sha": "d0a34bd987afd406"},
+        "block_scaled_gemm NVFP4": {"bytes": 42080000, "src_sha": "d0a34bd987afd406"},
+        "dequantize_bf16 W": {"bytes": 5920000, "src_sha": "cfde21af131d287f"},
     },
     "weights": {
-        "nvfp4_quantize_weights gate_up": {"bytes": 1841560000, "src_sha": "b23bc0aa0fcfb6e6"},
-        "nvfp4_quantize_weights down": {"bytes": 882390000, "src_sha": "b23bc0aa0fcfb6e6"},
+        "nvfp4_quantize_weights gate_up": {"bytes": 1808570000, "src_sha": "01d4aff2498125b3"},
+        "nvfp4_quantize_weights down": {"bytes": 889070000, "src_sha": "01d4aff2498125b3"},
     },
     "quant": {
         "mxfp8_quantize X row+col": {"bytes": 1081260000, "src_sha": "293d50137682089b"},
@@ -686,13 +686,14 @@ def run_ours(args):
         W["step"](timer)
     barrier()
 
-    # timed region: K steps, per-kernel and per-step CUDA events, L2 flushed before each step
+    # timed region: K steps, one pair of CUDA events per step and nothing between the step's
+    # launches (an event recorded between two kernels keeps the second from launching while the
+    # first drains: 0.207 vs 0.25-0.27 ms per dense step), L2 flushed before each step
     step_ev = []
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.5)                              # let the sampler start before the timed region
     launches0 = nvq.launch_count()
-    timer.active = True
     barrier()
     t0 = time.perf_counter()
     for _ in range(args.steps):
@@ -704,8 +705,16 @@ def run_ours(args):
         step_ev.append((a, b))
     barrier()
     wall = time.perf_counter() - t0
-    timer.active = False
     launches = nvq.launch_count() - launches0
+    # per-kernel pass: the same K steps again, with CUDA events around each launch group, for the
+    # per-kernel durations and the roofline (each duration then includes its launch's latency)
+    timer.active = True
+    barrier()
+    for _ in range(args.steps):
+        flush.zero_()
+        W["step"](timer)
+    barrier()
+    timer.active = False
     clk = clocks.stop()
     step_ms = [a.elapsed_time(b) for a, b in step_ev]
     total_ms = max_over_ranks(sum(step_ms), world, dev)
@@ -830,6 +839,8 @@ def run_ours(args):
                          "peak_source": f"{peaks['source']} (bf16 burst x {'6' if 'NVFP4' in dom['kernel'] else '2'}"
                                         f" for tensor; STREAM copy for HBM)"},
             "kernels": kern,
+            "kernel_timing": "per-kernel durations from a second pass of the K steps with CUDA events around "
+                             "each launch group; value and ms_per_step from the K steps without them",
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches),
             "clocks": clk, "wall_s_timed_region": round(wall, 4),
         }
