@@ -52,13 +52,13 @@ L2_FLUSH_BYTES = 256 << 20
 # ncu DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of the kernels timed
 # here, keyed by workload and kernel, with the sha256 of the source file the capture was taken
 # from. The commands that produced them are in profiles/launches_dense_step.md (dense),
-# profiles/quant_routed_batch.md (quant) and profiles/quant_nvfp4_weights.md (weights; the
-# launches of one call summed). A changed source reports null.
+# profiles/quant_routed_batch.md (quant, swiglu) and profiles/quant_nvfp4_weights.md (weights;
+# the launches of one call summed). A changed source reports null.
 NCU_TRAFFIC = {
     "dense": {
         "mxfp8_quantize X row+col": {"bytes": 33600000, "src_sha": "293d50137682089b"},
         "mxfp8_quantize W col": {"bytes": 20980000, "src_sha": "293d50137682089b"},
-        "nvfp4_quantize_per_token X": {"bytes": 33620000, "src_sha": "d4c39c27893902e1"},
+        "nvfp4_quantize_per_token X": {"bytes": 33620000, "src_sha": "e63b77614b08fbc6"},
         "nvfp4_quantize_weights W": {"bytes": 42030000, "src_sha": "01d4aff2498125b3"},
         "block_scaled_gemm MXFP8": {"bytes": 57560000, "src_sha": "d0a34bd987afd406"},
         "block_scaled_gemm NVFP4": {"bytes": 42080000, "src_sha": "d0a34bd987afd406"},
@@ -69,8 +69,11 @@ NCU_TRAFFIC = {
         "nvfp4_quantize_weights down": {"bytes": 889070000, "src_sha": "01d4aff2498125b3"},
     },
     "quant": {
-        "mxfp8_quantize X row+col": {"bytes": 1081260000, "src_sha": "293d50137682089b"},
-        "nvfp4_quantize_per_token X": {"bytes": 676250000, "src_sha": "b23bc0aa0fcfb6e6"},
+        "mxfp8_quantize X row+col": {"bytes": 1081200000, "src_sha": "293d50137682089b"},
+        "nvfp4_quantize_per_token X": {"bytes": 676190000, "src_sha": "e63b77614b08fbc6"},
+    },
+    "swiglu": {
+        "nvfp4_swiglu_quantize_per_token down input": {"bytes": 454590000, "src_sha": "e63b77614b08fbc6"},
     },
 }
 

@@ -35,32 +35,57 @@ __device__ __forceinline__ void load_block(const uint16_t* p, uint4& a, uint4& b
 // SwiGLU of a fused gate||up activation, rounded to bf16 (the down projection's input). The pages'
 // SwiGLU experts run gate and up as one GEMM [Miles-zh, "逐 Token 激活值缩放"]; the activation is
 // silu(g) u with silu(g) = g / (1 + exp(-g)) (Shazeer 2020), computed in float32 with one rounding
-// per operation (no contraction: __f*_rn), so that it is reproducible bit for bit. exp is our own:
-// Cody and Waite's two-constant range reduction (clamped to [-87, 88] so 2^n stays normal) and a
-// degree-6 Taylor polynomial in Horner order.
-__device__ __forceinline__ float swiglu_exp(float x) {
-    x = fminf(fmaxf(x, -87.0f), 88.0f);
-    const float n = __fsub_rn(__fadd_rn(__fmul_rn(x, (float)1.4426950408889634), 12582912.0f), 12582912.0f);
-    const float r = __fsub_rn(__fsub_rn(x, __fmul_rn(n, 0.693145751953125f)),
-                              __fmul_rn(n, (float)(0.6931471805599453 - 0.693145751953125)));
-    float p = (float)(1.0 / 720.0);
-    p = __fadd_rn(__fmul_rn(p, r), (float)(1.0 / 120.0));
-    p = __fadd_rn(__fmul_rn(p, r), (float)(1.0 / 24.0));
-    p = __fadd_rn(__fmul_rn(p, r), (float)(1.0 / 6.0));
-    p = __fadd_rn(__fmul_rn(p, r), 0.5f);
-    p = __fadd_rn(__fmul_rn(p, r), 1.0f);
-    p = __fadd_rn(__fmul_rn(p, r), 1.0f);
-    return __fmul_rn(p, __int_as_float(((int)n + 127) << 23));
+// per operation (no contraction), so that it is reproducible bit for bit. exp is our own: Cody and
+// Waite's two-constant range reduction (clamped to [-87, 88] so 2^n stays normal) and a degree-6
+// Taylor polynomial in Horner order. The two elements of a bf16x2 word go through every add,
+// subtract and multiply together as one packed f32x2 operation (two IEEE operations, each rounded
+// once, no flush to zero: the same values as the scalar steps); the division is the scalar IEEE one.
+__device__ __forceinline__ void f2_add(float& y0, float& y1, float a0, float a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+        "add.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(y0), "=f"(y1) : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+__device__ __forceinline__ void f2_sub(float& y0, float& y1, float a0, float a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+        "sub.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(y0), "=f"(y1) : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+__device__ __forceinline__ void f2_mul(float& y0, float& y1, float a0, float a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+        "mul.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(y0), "=f"(y1) : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 
-__device__ __forceinline__ float swiglu(float g, float u) {
-    const float d = __fadd_rn(1.0f, swiglu_exp(-g));
-    return __fmul_rn(__fdiv_rn(g, d), u);
-}
-
-// bf16x2 words of SwiGLU(gate, up) for two bf16x2 words
+// bf16x2 word of SwiGLU(gate, up) for the bf16x2 words g and u
 __device__ __forceinline__ uint32_t swiglu2(uint32_t g, uint32_t u) {
-    return cvt_bf16x2(swiglu(bf16_lo(g), bf16_lo(u)), swiglu(bf16_hi(g), bf16_hi(u)));
+    constexpr float L2E = (float)1.4426950408889634, LN2_HI = 0.693145751953125f;
+    constexpr float LN2_LO = (float)(0.6931471805599453 - 0.693145751953125), MAGIC = 12582912.0f;
+    const uint32_t xw = g ^ 0x80008000u;                       // x = -g, both halves
+    const float x0 = fminf(fmaxf(bf16_lo(xw), -87.0f), 88.0f), x1 = fminf(fmaxf(bf16_hi(xw), -87.0f), 88.0f);
+    float t0, t1, m0, m1, n0, n1, a0, a1, r0, r1;
+    f2_mul(t0, t1, x0, x1, L2E, L2E);
+    f2_add(m0, m1, t0, t1, MAGIC, MAGIC);                      // 1.5 * 2^23 + n: n in the low mantissa bits
+    f2_sub(n0, n1, m0, m1, MAGIC, MAGIC);                      // nearest integer to x log2(e), exactly
+    f2_mul(a0, a1, n0, n1, LN2_HI, LN2_HI);
+    f2_sub(r0, r1, x0, x1, a0, a1);
+    f2_mul(a0, a1, n0, n1, LN2_LO, LN2_LO);
+    f2_sub(r0, r1, r0, r1, a0, a1);
+    float p0 = (float)(1.0 / 720.0), p1 = p0;
+    const float c[6] = {(float)(1.0 / 120.0), (float)(1.0 / 24.0), (float)(1.0 / 6.0), 0.5f, 1.0f, 1.0f};
+#pragma unroll
+    for (int i = 0; i < 6; ++i) {
+        f2_mul(p0, p1, p0, p1, r0, r1);
+        f2_add(p0, p1, p0, p1, c[i], c[i]);
+    }
+    // 2^n from the bits of 1.5 * 2^23 + n (n in [-126, 127])
+    const float s0 = __uint_as_float((__float_as_uint(m0) - 0x4B400000u + 127u) << 23);
+    const float s1 = __uint_as_float((__float_as_uint(m1) - 0x4B400000u + 127u) << 23);
+    float e0, e1, d0, d1, h0, h1;
+    f2_mul(e0, e1, p0, p1, s0, s1);                            // exp(-g)
+    f2_add(d0, d1, e0, e1, 1.0f, 1.0f);
+    const float q0 = __fdiv_rn(bf16_lo(g), d0), q1 = __fdiv_rn(bf16_hi(g), d1);
+    f2_mul(h0, h1, q0, q1, bf16_lo(u), bf16_hi(u));
+    return cvt_bf16x2(h0, h1);
 }
 
 // One 16-element block of the row: loaded as is, or (SWIGLU) formed from the gate block at p and
