@@ -9,7 +9,8 @@
 //   GROUP_M: D[i, j] = s_a[i] s_b[e] sum_k deq(A)[i, k] deq(B[e])[j, k]   (rows i of group e)
 //   GROUP_K: D[e][i, j] = sum_{k in group e} deq(A)[i, k] deq(B)[j, k]
 //
-// Design (one CTA per SM, persistent, warp-specialised, 256 threads). A CTA computes 128 x 256
+// Design (one CTA per SM, persistent, warp-specialised; 256 threads for MXFP8, 384 for NVFP4 and
+// BF16 operands). A CTA computes 128 x 256
 // output tiles (tcgen05 M = 128, N = 256) from a ring of stages (MXFP8: 4 x 50 KB, NVFP4: 3 x 58 KB),
 // each holding a 128x128-byte A tile, a 256x128-byte B tile (128B swizzle) and their 512-byte
 // scale tiles. Roles:
@@ -25,10 +26,13 @@
 //                  MXFP8 E4M3 x UE8M0/32, K = 64 for NVFP4 E2M1 x UE4M3/16) into a 256-column fp32
 //                  TMEM accumulator; commits free stages and scale sets and signal the epilogue.
 //                  Warp 1 also allocates and frees TMEM.
-//   warps 2-5      epilogue: tcgen05.ld 32 columns at a time (the next load in flight while the
-//                  current chunk converts), multiply by s_a[row] s_b[e], round to bf16 into
-//                  registers (the whole 256-column row of each thread), hand TMEM back to the MMA
-//                  warp, then store while the next tile's MMAs run: for grouped row-offset GEMMs
+//   warps 2-5      epilogue (and warps 8-11 for NVFP4 and BF16 operands, so that two warps share
+//   (8-11)         each TMEM lane quarter, one per 128-column half, and the accumulator goes back
+//                  to the MMA warp in about half the time; MXFP8's four stages leave no shared
+//                  memory for their staging buffers): tcgen05.ld 32 columns at a time (the next load
+//                  in flight while the current chunk converts), multiply by s_a[row] s_b[e], round to
+//                  bf16 into registers (the thread's row within the warp's columns), hand TMEM back
+//                  to the MMA warp, then store while the next tile's MMAs run: for grouped row-offset GEMMs
 //                  each warp stages 32 x 32 chunks in shared memory (64-byte swizzle) and sends them
 //                  with TMA box stores; otherwise each thread stores its row with 256-bit stores
 //                  (fp32 output: stored chunk by chunk).
@@ -50,8 +54,9 @@
 
 namespace nvq {
 
-constexpr int GEMM_THREADS = 256;
-constexpr int W_PRODUCER = 0, W_MMA = 1, W_EPI0 = 2, W_TRANSPOSER = 6, W_SCALE = 7;
+// Warps 0-7 have fixed roles; warps 8-11 (when a format has 8 epilogue warps) are the second
+// epilogue warp of each TMEM lane quarter.
+constexpr int W_PRODUCER = 0, W_MMA = 1, W_EPI0 = 2, W_TRANSPOSER = 6, W_SCALE = 7, W_EPI1 = 8;
 constexpr int BM = 128, BN = 256, BKB = 128;       // tile rows, tile columns, K bytes per stage
 constexpr int MAX_GROUPS = 1024;
 constexpr uint32_t TMEM_COLS = 512;
@@ -86,12 +91,19 @@ struct GemmCfg {
         | ((uint32_t)(BN >> 3) << 17)                  // N >> 3
         | ((uint32_t)(BM >> 4) << 24);                 // M >> 4
     static constexpr int BAR_BYTES = 256;
+    // Epilogue warps: one per TMEM lane quarter draining all BN columns of its 32 rows, or two per
+    // quarter draining BN / 2 columns each (the accumulator goes back to the MMA warp in about half
+    // the time). MXFP8's four stages leave no shared memory for the second set's staging buffers.
+    static constexpr int EPI_WARPS = (FMT == F_MXFP8) ? 4 : 8;
+    static constexpr int EPI_COLS = BN * 4 / EPI_WARPS;         // accumulator columns per epilogue warp
+    static constexpr int THREADS = 32 * (4 + EPI_WARPS);
     // bf16 output staging for the TMA stores: per epilogue warp, STG_BUFS buffers of 32 rows x 32
     // columns (2 KB, 64-byte swizzle), 1024-aligned after the stages, barriers and group tables
     static constexpr size_t STG_OFFSET =
         ((size_t)STAGES * STAGE_BYTES + BAR_BYTES + 8 * (MAX_GROUPS + 1) + 1023) / 1024 * 1024;
-    static constexpr int STG_BUFS = (1024 + STG_OFFSET + 4 * 2 * 2048 <= 232448) ? 2 : 1;
-    static constexpr size_t SMEM_BYTES = 1024 + STG_OFFSET + 4 * (size_t)STG_BUFS * 2048;
+    static constexpr int STG_BUFS = (1024 + STG_OFFSET + (size_t)EPI_WARPS * 2 * 2048 <= 232448) ? 2 : 1;
+    static constexpr size_t STG_BYTES = (size_t)EPI_WARPS * STG_BUFS * 2048;
+    static constexpr size_t SMEM_BYTES = 1024 + STG_OFFSET + STG_BYTES;
     static_assert(BN + SF_SETS * SF_SET_COLS <= TMEM_COLS, "TMEM columns");
     static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 };
@@ -381,7 +393,7 @@ struct StageCursor {
 // Kernel
 // ------------------------------------------------------------------------------------------------
 template <int FMT>
-__global__ void __launch_bounds__(GEMM_THREADS, 1)
+__global__ void __launch_bounds__(GemmCfg<FMT>::THREADS, 1)
 block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                          const __grid_constant__ CUtensorMap tmap_d, const GemmParams p) {
     griddep_begin();
@@ -468,7 +480,7 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
             }
         }
         mbar_init(tmem_full, 1);
-        mbar_init(tmem_empty, 4);              // one arrival per epilogue warp
+        mbar_init(tmem_empty, C::EPI_WARPS);   // one arrival per epilogue warp
         mbar_init(mma_done, 1);
         mbar_init(cp_done, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -685,13 +697,16 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
                 if (++slot == C::STAGES) slot = 0;
             }
         }
-    } else if (warp >= W_EPI0 && warp < W_EPI0 + 4) {
+    } else if ((warp >= W_EPI0 && warp < W_EPI0 + 4) || (warp >= W_EPI1 && warp < 4 + C::EPI_WARPS)) {
         // =========================== epilogue ===========================
+        constexpr int NCH = C::EPI_COLS / 32;         // 32-column chunks this warp drains per tile
         const int q = warp & 3;                       // TMEM lane quarter this warp may access
+        const int ei = warp < W_EPI1 ? warp - W_EPI0 : warp - 4;   // epilogue warp index 0..EPI_WARPS-1
+        const int cbase = warp < W_EPI1 ? 0 : C::EPI_COLS;         // first accumulator column it drains
         const int row_in_tile = q * 32 + lane;
-        const uint32_t stg_warp = smem_u32(smem + C::STG_OFFSET) + (uint32_t)(q * C::STG_BUFS * 2048);
+        const uint32_t stg_warp = smem_u32(smem + C::STG_OFFSET) + (uint32_t)(ei * C::STG_BUFS * 2048);
         uint32_t stg_count = 0;                       // chunks this warp has staged
-        const uint32_t tbase = tmem_acc + ((uint32_t)(q * 32) << 16);
+        const uint32_t tbase = tmem_acc + ((uint32_t)(q * 32) << 16) + (uint32_t)cbase;
         uint32_t acc_phase = 0;
         for (int64_t t = first; t < total; t += stride) {
             const Tile tl = sched.get(t);
@@ -708,8 +723,8 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
             }
             if (p.out_f32) {
                 // fp32 output: store each 32-column chunk as it leaves TMEM
-                for (int c = 0; c < BN / 32; ++c) {
-                    const int64_t col = tl.n0 + c * 32;
+                for (int c = 0; c < NCH; ++c) {
+                    const int64_t col = tl.n0 + cbase + c * 32;
                     uint32_t r[32];
                     if (!empty) {
                         tmem_ld32_async(tbase + (uint32_t)(c * 32), r);
@@ -738,19 +753,19 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
             // bf16 output: drain the whole accumulator row into registers as packed bf16 (the next
             // 32-column load in flight while the current one converts) and hand TMEM back to the
             // MMA warp before storing, so the stores overlap the next tile's MMAs
-            uint32_t pk[BN / 32][16];
+            uint32_t pk[NCH][16];
             if (!empty) {
                 uint32_t ra[32], rb[32];
                 tmem_ld32_async(tbase, ra);
                 tmem_wait_ld(ra);
 #pragma unroll
-                for (int c = 0; c < BN / 32; c += 2) {
+                for (int c = 0; c < NCH; c += 2) {
                     tmem_ld32_async(tbase + (uint32_t)((c + 1) * 32), rb);
                     pack_scaled(ra, scale, pk[c]);
                     tmem_wait_ld(rb);
-                    if (c + 2 < BN / 32) tmem_ld32_async(tbase + (uint32_t)((c + 2) * 32), ra);
+                    if (c + 2 < NCH) tmem_ld32_async(tbase + (uint32_t)((c + 2) * 32), ra);
                     pack_scaled(rb, scale, pk[c + 1]);
-                    if (c + 2 < BN / 32) tmem_wait_ld(ra);
+                    if (c + 2 < NCH) tmem_wait_ld(ra);
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -758,16 +773,16 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
                 acc_phase ^= 1u;
             } else {
 #pragma unroll
-                for (int c = 0; c < BN / 32; ++c)
+                for (int c = 0; c < NCH; ++c)
 #pragma unroll
                     for (int j = 0; j < 16; ++j) pk[c][j] = 0u;
             }
             if (!p.tma_store) {
                 if (row_ok) {
-                    uint16_t* dst = reinterpret_cast<uint16_t*>(p.d) + drow * p.ldd + tl.n0;
+                    uint16_t* dst = reinterpret_cast<uint16_t*>(p.d) + drow * p.ldd + tl.n0 + cbase;
 #pragma unroll
-                    for (int c = 0; c < BN / 32; ++c) {
-                        if (tl.n0 + c * 32 >= p.n) break;
+                    for (int c = 0; c < NCH; ++c) {
+                        if (tl.n0 + cbase + c * 32 >= p.n) break;
                         if (p.d_aligned32) {
 #pragma unroll
                             for (int h = 0; h < 2; ++h)
@@ -790,8 +805,8 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
             // 32, so the warp's 32 rows lie wholly inside or outside the tile's group.
             if (tl.a_row0 + q * 32 < tl.row_end) {
 #pragma unroll
-                for (int c = 0; c < BN / 32; ++c) {
-                    if (tl.n0 + c * 32 >= p.n) break;
+                for (int c = 0; c < NCH; ++c) {
+                    if (tl.n0 + cbase + c * 32 >= p.n) break;
                     const uint32_t buf = stg_warp + (uint32_t)((stg_count % C::STG_BUFS) * 2048);
                     // the buffer's previous store has finished reading it (groups complete in order)
                     if (lane == 0) bulk_wait_read<C::STG_BUFS - 1>();
@@ -807,7 +822,7 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                     __syncwarp();
                     if (lane == 0) {
-                        tma_store_2d(&tmap_d, buf, (int32_t)(tl.n0 + c * 32), (int32_t)(tl.d_row0 + q * 32));
+                        tma_store_2d(&tmap_d, buf, (int32_t)(tl.n0 + cbase + c * 32), (int32_t)(tl.d_row0 + q * 32));
                         bulk_commit();
                     }
                     ++stg_count;
@@ -938,8 +953,8 @@ static nvq_status launch_gemm(const nvq_gemm_args* a, cudaStream_t stream) {
     if (grid <= 0) return NVQ_ERR_CUDA;
     // the staging buffers sit at the end of shared memory: launches that store rows directly leave
     // them out (a larger shared-memory request shrinks L1; measured on the decode shape)
-    const size_t smem = p.tma_store ? C::SMEM_BYTES : C::SMEM_BYTES - (size_t)4 * C::STG_BUFS * 2048;
-    if (launch_pdl(block_scaled_gemm_kernel<FMT>, dim3(grid), dim3(GEMM_THREADS), smem, stream, ta, tb, td, p) !=
+    const size_t smem = p.tma_store ? C::SMEM_BYTES : C::SMEM_BYTES - C::STG_BYTES;
+    if (launch_pdl(block_scaled_gemm_kernel<FMT>, dim3(grid), dim3(C::THREADS), smem, stream, ta, tb, td, p) !=
             cudaSuccess ||
         cudaGetLastError() != cudaSuccess)
         return NVQ_ERR_CUDA;
