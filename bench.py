@@ -60,8 +60,8 @@ NCU_TRAFFIC = {
         "mxfp8_quantize W col": {"bytes": 20980000, "src_sha": "293d50137682089b"},
         "nvfp4_quantize_per_token X": {"bytes": 33620000, "src_sha": "e63b77614b08fbc6"},
         "nvfp4_quantize_weights W": {"bytes": 42030000, "src_sha": "01d4aff2498125b3"},
-        "block_scaled_gemm MXFP8": {"bytes": 57560000, "src_sha": "d0a34bd987afd406"},
-        "block_scaled_gemm NVFP4": {"bytes": 42080000, "src_sha": "d0a34bd987afd406"},
+        "block_scaled_gemm MXFP8": {"bytes": 57060000, "src_sha": "1530902a93df9546"},
+        "block_scaled_gemm NVFP4": {"bytes": 42040000, "src_sha": "1530902a93df9546"},
         "dequantize_bf16 W": {"bytes": 5920000, "src_sha": "cfde21af131d287f"},
     },
     "weights": {
