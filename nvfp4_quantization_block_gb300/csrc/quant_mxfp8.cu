@@ -182,8 +182,12 @@ cudaError_t launch_mxfp8_quantize(const uint16_t* x, int64_t R, int64_t C, int64
         if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
             sms = 0;
     });
-    // grids deeper than two waves of the register variant are staged through shared memory
-    const bool staged = (int64_t)grid.x * grid.y > 2 * 4 * (int64_t)sms;
+    // grids deeper than two waves of the register variant are staged through shared memory, and so
+    // are grids just past one register wave that fit one wave of the staged variant (its extra
+    // resident CTAs take the whole grid at once instead of leaving a short second round)
+    const int64_t tiles = (int64_t)grid.x * grid.y, reg_wave = (int64_t)MxOcc<true, true, false>::value * sms;
+    const int64_t staged_wave = (int64_t)(q_row ? MxOcc<true, true, true>::value : MxOcc<false, true, true>::value) * sms;
+    const bool staged = tiles > 2 * reg_wave || (tiles > reg_wave && tiles <= staged_wave);
     cudaError_t lerr;
 #define NVQ_MX(RW, CL, ST)                                                                                       \
     lerr = launch_pdl(mxfp8_quant_kernel<RW, CL, ST>, grid, dim3(MX_THREADS), 0, stream, x, R, C, ldx, q_row, sf_row, \

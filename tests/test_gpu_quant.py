@@ -119,6 +119,22 @@ def test_mxfp8_deep_grid_staged_path(nvq, rowwise):
         assert np.array_equal(_np(o["sf_row"]), oracle.sf_to_mma_layout(ref["sf_row"]))
 
 
+@pytest.mark.parametrize("shape,rowwise", [((2048, 5120), False), ((2048, 5632), True)])
+def test_mxfp8_one_wave_staged_path(nvq, shape, rowwise):
+    """Grids just past one wave of the register variant that fit one wave of the staged variant
+    (640 column-only tiles: the dense W_qkv's columnwise copy; 704 row+col tiles) take the staged
+    variant on a 152-SM GPU; bit-exact against the oracle either way."""
+    bits = family("random", shape, seed=23)
+    ref = oracle.mxfp8_quantize(bits, rowwise=rowwise)
+    o = nvq.mxfp8_quantize(_dev(bits), rowwise=rowwise, sf_layout="mma")
+    torch.cuda.synchronize()
+    assert np.array_equal(_np(o["q_colT"]), ref["q_colT"])
+    assert np.array_equal(_np(o["sf_colT"]), oracle.sf_to_mma_layout(ref["sf_colT"]))
+    if rowwise:
+        assert np.array_equal(_np(o["q_row"]), ref["q_row"])
+        assert np.array_equal(_np(o["sf_row"]), oracle.sf_to_mma_layout(ref["sf_row"]))
+
+
 @pytest.mark.parametrize("shape", [(33, 64), (1, 32), (7, 96)])
 def test_mxfp8_rowwise_only_ragged_rows(nvq, shape):
     bits = family("random", shape, seed=3)
