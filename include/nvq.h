@@ -142,7 +142,7 @@ nvq_status nvfp4_swiglu_quantize_per_token(const void* gate_up, int64_t rows, in
  *   s_w  [experts] float32. Used as scratch between the kernels this call enqueues (it holds
  *        the running amax bits, then, for more than one expert, the scales with a work-split flag
  *        in the sign bit, until the last kernel writes the scales).
- * Requires K % 16 == 0 and N % 8 == 0.
+ * Requires K % 16 == 0, N % 8 == 0 and experts <= 65535. experts = 0 is a no-op.
  */
 nvq_status nvfp4_quantize_weights(const void* w, int64_t experts, int64_t k, int64_t n,
                                   uint8_t* qT, uint8_t* sfT, float* s_w,

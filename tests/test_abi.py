@@ -81,6 +81,17 @@ def test_host_validation_rejects_before_launch(lib):
     assert sw(fake, 4, 64, 100, fake, fake, fake, 0, None) == 1    # ld < 2 cols
     assert sw(fake, 4, 64, 132, fake, fake, fake, 0, None) == 2    # ld % 8
     assert sw(fake, 0, 64, 128, None, None, None, 0, None) == 0    # empty is a no-op
+    nw = lib.nvfp4_quantize_weights
+    nw.argtypes = [vp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, vp, vp, vp, ctypes.c_int, vp]
+    nw.restype = ctypes.c_int
+    assert nw(fake, 2, 40, 64, fake, fake, fake, 1, None) == 1        # K % 16
+    assert nw(fake, 2, 64, 60, fake, fake, fake, 1, None) == 1        # N % 8
+    assert nw(fake, 65536, 64, 64, fake, fake, fake, 1, None) == 1    # more experts than the grid allows
+    assert nw(fake, 2, 64, 64, fake, fake, None, 1, None) == 1        # missing s_w
+    assert nw(fake, 2, 64, 64, fake, fake, fake, 3, None) == 1        # bad layout enum
+    assert nw(odd, 2, 64, 64, fake, fake, fake, 1, None) == 2         # misaligned weights
+    assert nw(fake, 2, 64, 64, fake, fake, odd, 1, None) == 2         # misaligned s_w
+    assert nw(fake, 0, 64, 64, None, None, None, 1, None) == 0        # no experts is a no-op
     cv = lib.sf_layout_convert
     cv.argtypes = [vp, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, vp, ctypes.c_int, vp]
     cv.restype = ctypes.c_int
