@@ -114,3 +114,45 @@ def test_host_validation_rejects_before_launch(lib):
     d.restype = ctypes.c_int
     assert d(1, fake, fake, None, 0, 1, 4, 32, 0, fake, None) == 1            # NVFP4 needs s
     assert d(5, fake, fake, None, 0, 1, 4, 32, 0, fake, None) == 1            # bad format
+
+
+class _GemmArgs(ctypes.Structure):
+    # field order and types of nvq_gemm_args in include/nvq.h
+    _fields_ = [("fmt", ctypes.c_int), ("mode", ctypes.c_int), ("out_type", ctypes.c_int),
+                ("groups", ctypes.c_int64), ("m", ctypes.c_int64), ("n", ctypes.c_int64), ("k", ctypes.c_int64),
+                ("a", ctypes.c_void_p), ("sfa", ctypes.c_void_p), ("s_a", ctypes.c_void_p),
+                ("b", ctypes.c_void_p), ("sfb", ctypes.c_void_p), ("s_b", ctypes.c_void_p),
+                ("offsets", ctypes.c_void_p), ("d", ctypes.c_void_p), ("ldd", ctypes.c_int64),
+                ("status", ctypes.c_void_p)]
+
+
+def test_gemm_host_validation_rejects_before_launch(lib):
+    g = lib.block_scaled_grouped_gemm
+    g.argtypes = [ctypes.POINTER(_GemmArgs), ctypes.c_void_p]
+    g.restype = ctypes.c_int
+    fake, odd = 0x10000, 0x10008                    # never dereferenced: each call fails on the host
+
+    def call(**over):
+        a = _GemmArgs(fmt=1, mode=0, out_type=0, groups=2, m=256, n=256, k=256, a=fake, sfa=fake, s_a=None,
+                      b=fake, sfb=fake, s_b=None, offsets=fake, d=fake, ldd=256, status=None)
+        for key, v in over.items():
+            setattr(a, key, v)
+        return g(ctypes.byref(a), None)
+
+    assert g(None, None) == 1                       # no argument block
+    assert call(fmt=3) == 1                         # bad format
+    assert call(mode=2) == 1                        # bad grouping mode
+    assert call(out_type=2) == 1                    # bad output type
+    assert call(k=-128) == 1                        # negative size
+    assert call(groups=0) == 0                      # nothing to do
+    assert call(m=0) == 0
+    assert call(groups=1025) == 3                   # above the 1024-group maximum
+    assert call(sfa=None) == 1                      # block-scaled operands need their scales
+    assert call(fmt=2, sfa=None, sfb=None, n=200) == 1   # N % 128 (BF16 operands need no scales)
+    assert call(k=96) == 1                          # row-grouped block-scaled K % 128
+    assert call(ldd=200) == 1                       # ldd < n
+    assert call(ldd=260) == 1                       # ldd % 8
+    assert call(mode=1) == 3                        # NVFP4 weight gradient: not built
+    assert call(fmt=0, mode=1, m=200) == 1          # weight gradient: M % 128
+    assert call(a=odd) == 2                         # misaligned operand
+    assert call(offsets=fake + 4) == 2              # offsets not 8-byte aligned
