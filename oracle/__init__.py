@@ -36,4 +36,4 @@ from .quant import (  # noqa: F401
 )
 from .layout import sf_to_mma_layout, sf_from_mma_layout, mma_layout_offset, mma_layout_bytes  # noqa: F401
 from .gemm import grouped_gemm_reference, grouped_gemm_entries, deq_operand  # noqa: F401
-from .swiglu import exp_f32, swiglu_bf16_bits, swiglu_rows  # noqa: F401
+from .swiglu import exp_f32, exp_parts, swiglu_f32, swiglu_bf16_bits, swiglu_rows  # noqa: F401
