@@ -111,17 +111,20 @@ nvq_status nvfp4_quantize_per_token(const void* x, int64_t rows, int64_t cols, i
  * fused gate||up GEMM output: SwiGLU, then per-token NVFP4, without writing the bf16 activation.
  *
  * Defines: h[i, j] = RN_bf16(silu(g) * u), g = gate_up[i, j], u = gate_up[i, cols + j], silu(g) =
- * g / (1 + exp(-g)) in float32 with one rounding per operation and exp(x) = p(r) * 2^n (x clamped
- * to [-87, 88]; n the nearest integer to x log2(e); r = (x - n ln2_hi) - n ln2_lo with ln2_hi =
- * 0x3F317200; p the degree-6 Taylor polynomial of e^r in Horner order); then exactly
- * nvfp4_quantize_per_token of h. [Miles-zh, "逐 Token 激活值缩放": SwiGLU experts run gate and up as
- * one fused GEMM; one call emits FP4 values, E4M3 block scales and per-token FP32 scales; "结果":
- * the unfused scaling op is what slowed the training path.]
+ * g / (1 + exp(-g)) with float32 significands and one rounding per operation, exp(x) = p(r) * 2^n
+ * (x = -g clamped to [-87, 300], which changes no result; n the nearest integer to x log2(e);
+ * r = (x - n ln2_hi) - n ln2_lo with ln2_hi = 0x3F317200; p the degree-6 Taylor polynomial of e^r
+ * in Horner order). exp(-g), 1 + exp(-g) and the quotient carry an unbounded exponent (for
+ * x <= 87 these are the plain IEEE float32 steps); the product with u is rounded once to float32
+ * (gradual underflow), then to bf16. Then exactly nvfp4_quantize_per_token of h.
+ * [Miles-zh, "逐 Token 激活值缩放": SwiGLU experts run gate and up as one fused GEMM; one call emits
+ * FP4 values, E4M3 block scales and per-token FP32 scales; "结果": the unfused scaling op is what
+ * slowed the training path.]
  *
  *   gate_up  bf16 [rows, 2*cols], leading dimension ld (>= 2*cols, multiple of 8): gate in the
  *            first cols columns, up in the next cols.
  *   q, sf, s_tok  as nvfp4_quantize_per_token for h [rows, cols].
- * Requires cols % 16 == 0. Inputs whose SwiGLU overflows float32 are outside the contract.
+ * Requires cols % 16 == 0. Inputs whose SwiGLU overflows bf16 are outside the contract.
  */
 nvq_status nvfp4_swiglu_quantize_per_token(const void* gate_up, int64_t rows, int64_t cols, int64_t ld,
                                            uint8_t* q, uint8_t* sf, float* s_tok,

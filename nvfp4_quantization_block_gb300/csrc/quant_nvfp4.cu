@@ -34,12 +34,16 @@ __device__ __forceinline__ void load_block(const uint16_t* p, uint4& a, uint4& b
 
 // SwiGLU of a fused gate||up activation, rounded to bf16 (the down projection's input). The pages'
 // SwiGLU experts run gate and up as one GEMM [Miles-zh, "逐 Token 激活值缩放"]; the activation is
-// silu(g) u with silu(g) = g / (1 + exp(-g)) (Shazeer 2020), computed in float32 with one rounding
-// per operation (no contraction), so that it is reproducible bit for bit. exp is our own: Cody and
-// Waite's two-constant range reduction (clamped to [-87, 88] so 2^n stays normal) and a degree-6
-// Taylor polynomial in Horner order. The two elements of a bf16x2 word go through every add,
-// subtract and multiply together as one packed f32x2 operation (two IEEE operations, each rounded
-// once, no flush to zero: the same values as the scalar steps); the division is the scalar IEEE one.
+// silu(g) u with silu(g) = g / (1 + exp(-g)) (Shazeer 2020), computed with float32 significands and
+// one rounding per operation (no contraction), so that it is reproducible bit for bit. exp is our
+// own: x = -g clamped to [-87, 300] (neither bound changes a result), Cody and Waite's two-constant
+// range reduction x = n ln2 + r, and a degree-6 Taylor polynomial p of e^r in Horner order, so
+// exp(-g) ~ p 2^n. For x <= 87, 2^n is a normal float32 and the steps are plain IEEE float32:
+// e = p 2^n, d = 1 + e, s = g / d, h = s u. For x > 87 exp(-g) may leave float32's range; its
+// exponent is kept apart instead (swiglu_wide), so silu(g) u keeps its value there too. The two
+// elements of a bf16x2 word go through every add, subtract and multiply together as one packed
+// f32x2 operation (two IEEE operations, each rounded once, no flush to zero: the same values as the
+// scalar steps); the divisions are scalar IEEE ones.
 __device__ __forceinline__ void f2_add(float& y0, float& y1, float a0, float a1, float b0, float b1) {
     asm("{\n\t.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
         "add.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
@@ -56,12 +60,24 @@ __device__ __forceinline__ void f2_mul(float& y0, float& y1, float a0, float a1,
         : "=f"(y0), "=f"(y1) : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 
+// h for -g > 87, where exp(-g) = p 2^n may lie beyond float32's range (n up to 433): d = 1 + p 2^n
+// is p 2^n exactly (1 is far below half an ulp of it), so s = g / d = RN(g / p) 2^-n, formed as
+// q = RN((g 2^-16) / p) (finite for any bf16 g, the same rounding), and h = s u rounded once to
+// float32 (gradual underflow) from the exact float64 product q u 2^(16 - n) (24 x 8 significant
+// bits, times a power of two). m = 1.5 2^23 + n as computed by the caller.
+__device__ __noinline__ float swiglu_wide(float g, float u, float p, float m) {
+    const int n = (int)(__float_as_uint(m) - 0x4B400000u);
+    const float q = __fdiv_rn(__fmul_rn(g, 0x1p-16f), p);
+    const double pow2 = __longlong_as_double((long long)(1023 + 16 - n) << 52);
+    return __double2float_rn(__dmul_rn(__dmul_rn((double)q, (double)u), pow2));
+}
+
 // bf16x2 word of SwiGLU(gate, up) for the bf16x2 words g and u
 __device__ __forceinline__ uint32_t swiglu2(uint32_t g, uint32_t u) {
     constexpr float L2E = (float)1.4426950408889634, LN2_HI = 0.693145751953125f;
     constexpr float LN2_LO = (float)(0.6931471805599453 - 0.693145751953125), MAGIC = 12582912.0f;
     const uint32_t xw = g ^ 0x80008000u;                       // x = -g, both halves
-    const float x0 = fminf(fmaxf(bf16_lo(xw), -87.0f), 88.0f), x1 = fminf(fmaxf(bf16_hi(xw), -87.0f), 88.0f);
+    const float x0 = fminf(fmaxf(bf16_lo(xw), -87.0f), 300.0f), x1 = fminf(fmaxf(bf16_hi(xw), -87.0f), 300.0f);
     float t0, t1, m0, m1, n0, n1, a0, a1, r0, r1;
     f2_mul(t0, t1, x0, x1, L2E, L2E);
     f2_add(m0, m1, t0, t1, MAGIC, MAGIC);                      // 1.5 * 2^23 + n: n in the low mantissa bits
@@ -77,7 +93,8 @@ __device__ __forceinline__ uint32_t swiglu2(uint32_t g, uint32_t u) {
         f2_mul(p0, p1, p0, p1, r0, r1);
         f2_add(p0, p1, p0, p1, c[i], c[i]);
     }
-    // 2^n from the bits of 1.5 * 2^23 + n (n in [-126, 127])
+    // 2^n from the bits of 1.5 * 2^23 + n (n in [-126, 126] when x <= 87; the other lanes'
+    // values here are discarded)
     const float s0 = __uint_as_float((__float_as_uint(m0) - 0x4B400000u + 127u) << 23);
     const float s1 = __uint_as_float((__float_as_uint(m1) - 0x4B400000u + 127u) << 23);
     float e0, e1, d0, d1, h0, h1;
@@ -85,6 +102,8 @@ __device__ __forceinline__ uint32_t swiglu2(uint32_t g, uint32_t u) {
     f2_add(d0, d1, e0, e1, 1.0f, 1.0f);
     const float q0 = __fdiv_rn(bf16_lo(g), d0), q1 = __fdiv_rn(bf16_hi(g), d1);
     f2_mul(h0, h1, q0, q1, bf16_lo(u), bf16_hi(u));
+    if (x0 > 87.0f) h0 = swiglu_wide(bf16_lo(g), bf16_lo(u), p0, m0);
+    if (x1 > 87.0f) h1 = swiglu_wide(bf16_hi(g), bf16_hi(u), p1, m1);
     return cvt_bf16x2(h0, h1);
 }
 

@@ -29,8 +29,14 @@ def _gate_up(R, I, seed):
     rng = np.random.default_rng(seed)
     g = rng.standard_normal((R, I)) * np.exp(rng.uniform(-3, 4, (R, 1)))
     u = rng.standard_normal((R, I)) * np.exp(rng.uniform(-3, 3, (R, 1)))
-    g[rng.random((R, I)) < 0.01] *= 60.0          # gates beyond the exp clamp (|g| > 87) in some rows
+    g[rng.random((R, I)) < 0.01] *= 60.0          # gates with |g| > 87 scattered in every row
     g[rng.random((R, I)) < 0.02] = 0.0
+    # rows whose gates make exp(-g) leave float32's range (-g in (87, 300] and beyond the clamp)
+    # with up values large enough that silu(g) u stays a normal number
+    wide = np.arange(R) % 7 == 3
+    g[wide] = -rng.uniform(85.0, 110.0, (wide.sum(), I))
+    g[wide & (np.arange(R) % 14 == 3)] *= rng.choice([1.0, 3.0, 1e36], (int((wide & (np.arange(R) % 14 == 3)).sum()), I))
+    u[wide] = rng.standard_normal((wide.sum(), I)) * 10.0 ** rng.uniform(28, 38, (wide.sum(), 1))
     bits = oracle.f64_to_bf16_bits_rne(np.concatenate([g, u], axis=1))
     bits[:, :I][np.random.default_rng(seed + 1).random((R, I)) < 0.01] = 0x8000   # negative zero gates
     return bits
