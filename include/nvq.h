@@ -206,7 +206,8 @@ nvq_status sf_layout_convert(const uint8_t* src, nvq_sf_layout src_layout, int64
  *   index       device int32 [rows]; values in [-1, src_rows). An out-of-range value sets *status
  *               to NVQ_DEV_BAD_INDEX (when status is non-NULL) and that row is written as a zero row.
  *   q_out, sf_out, s_out  destination rows [rows], sf_out in dst_layout (MMA padding rows zeroed).
- * Requires cols % 16 (NVFP4) or % 32 (MXFP8) == 0. rows = 0 is a no-op.
+ * Requires cols % 16 (NVFP4) or % 32 (MXFP8) == 0. q, sf, q_out and sf_out 16-byte aligned; index,
+ * s, s_out and status 4-byte aligned (NVQ_ERR_MISALIGNED otherwise). rows = 0 is a no-op.
  */
 nvq_status quantized_gather_rows(nvq_format fmt, const uint8_t* q, const uint8_t* sf, const float* s,
                                  int64_t src_rows, int64_t cols, nvq_sf_layout src_layout,
@@ -215,8 +216,8 @@ nvq_status quantized_gather_rows(nvq_format fmt, const uint8_t* q, const uint8_t
 
 /* Device status word values written by block_scaled_grouped_gemm (when `status` is non-NULL). */
 #define NVQ_DEV_OK 0
-#define NVQ_DEV_TIMEOUT 1          /* a pipeline wait exceeded its iteration limit */
-#define NVQ_DEV_BAD_OFFSETS 2      /* offsets not monotone, not multiples of 32, or past the buffer */
+#define NVQ_DEV_TIMEOUT 1          /* a pipeline wait exceeded its time limit (wait_limit_ns) */
+#define NVQ_DEV_BAD_OFFSETS 2      /* offsets not monotone, past the buffer, or (GROUP_K) not multiples of 32 */
 #define NVQ_DEV_BAD_INDEX 3        /* quantized_gather_rows: an index outside [-1, src_rows) */
 
 
@@ -236,11 +237,21 @@ typedef struct {
     const float* s_b;        /* [groups] per-expert FP32 scales or NULL (= 1)                      */
     const int64_t* offsets;  /* device [groups+1]: group e owns rows (GROUP_M) or reduction columns
                                 (GROUP_K) offsets[e] .. offsets[e+1]-1; offsets[0] = 0, monotone,
-                                multiples of 32, offsets[groups] <= m (GROUP_M) or <= k (GROUP_K) */
+                                offsets[groups] <= m (GROUP_M) or <= k (GROUP_K); any row for
+                                GROUP_M, multiples of 32 for GROUP_K (a 32-element block of the
+                                reduction never straddles two groups)                         */
     void* d;                 /* GROUP_M: [m, n] rows of groups written, others untouched;
                                 GROUP_K: [groups, m, n] (empty groups are written as zeros)        */
     int64_t ldd;             /* leading dimension of d in elements (>= n, multiple of 8)           */
     int32_t* status;         /* optional device int32: NVQ_DEV_* after the call (set, never cleared) */
+    int64_t wait_limit_ns;   /* bound of each wait between the kernel's pipeline roles, in ns of
+                                %globaltimer; 0 = 2 s. A wait that runs out sets *status to
+                                NVQ_DEV_TIMEOUT; the kernel then drains its in-flight copies and
+                                tensor-core work, frees its tensor memory and returns (the output
+                                is then incomplete).                                              */
+    int32_t inject_timeout_stage;  /* 0 = off. Fault injection for tests of that watchdog: k > 0
+                                makes the first CTA's load stage k (1-based) never arrive, so the
+                                waits on it run out and the call ends with NVQ_DEV_TIMEOUT.     */
 } nvq_gemm_args;
 
 /*

@@ -65,6 +65,7 @@ class GemmArgs(ctypes.Structure):
         ("a", _vp), ("sfa", _vp), ("s_a", _vp),
         ("b", _vp), ("sfb", _vp), ("s_b", _vp),
         ("offsets", _vp), ("d", _vp), ("ldd", _i64), ("status", _vp),
+        ("wait_limit_ns", _i64), ("inject_timeout_stage", ctypes.c_int32),
     ]
 
 
@@ -249,10 +250,11 @@ def dequantize_bf16(fmt, q, sf, s=None, scope=SCOPE_ROW, groups=1, rows=None, co
 
 
 def block_scaled_grouped_gemm(fmt, mode, a, sfa, b, sfb, offsets, m, n, k, groups, s_a=None, s_b=None,
-                              out=None, out_type=OUT_BF16, status=None):
+                              out=None, out_type=OUT_BF16, status=None, wait_limit_ns=0, inject_timeout_stage=0):
     """Block-scaled grouped GEMM (include/nvq.h). ``offsets`` is a device int64 tensor [groups+1].
 
-    mode GEMM_GROUP_M: D [m, n]; mode GEMM_GROUP_K: D [groups, m, n]. Returns D.
+    mode GEMM_GROUP_M: D [m, n]; mode GEMM_GROUP_K: D [groups, m, n]. Returns D. ``wait_limit_ns``
+    bounds each pipeline wait (0 = 2 s); ``inject_timeout_stage`` > 0 is the watchdog-test hook.
     """
     if _gemm is None:
         raise NvqError(NVQ_ERR_UNSUPPORTED, "block_scaled_grouped_gemm (not built)")
@@ -266,7 +268,8 @@ def block_scaled_grouped_gemm(fmt, mode, a, sfa, b, sfb, offsets, m, n, k, group
     args = GemmArgs(fmt=int(fmt), mode=int(mode), out_type=int(out_type), groups=int(groups), m=int(m),
                     n=int(n), k=int(k), a=_ptr(a), sfa=_ptr(sfa), s_a=_ptr(s_a), b=_ptr(b), sfb=_ptr(sfb),
                     s_b=_ptr(s_b), offsets=_ptr(offsets), d=_ptr(out), ldd=int(out.stride(-2)),
-                    status=_ptr(status))
+                    status=_ptr(status), wait_limit_ns=int(wait_limit_ns),
+                    inject_timeout_stage=int(inject_timeout_stage))
     st = _gemm(ctypes.byref(args), _stream(dev))
     _check(st, "block_scaled_grouped_gemm")
     return out

@@ -15,6 +15,7 @@ void count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order
 namespace {
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 inline nvq_status from_cuda(cudaError_t e) { return e == cudaSuccess ? NVQ_OK : NVQ_ERR_CUDA; }
 
@@ -128,6 +129,10 @@ nvq_status quantized_gather_rows(nvq_format fmt, const uint8_t* q, const uint8_t
     if (src_rows > 0 && (q == nullptr || sf == nullptr)) return NVQ_ERR_INVALID_ARG;
     if (fmt == NVQ_NVFP4 && (s_out == nullptr || (src_rows > 0 && s == nullptr))) return NVQ_ERR_INVALID_ARG;
     if ((q && !aligned16(q)) || (sf && !aligned16(sf)) || !aligned16(q_out) || !aligned16(sf_out))
+        return NVQ_ERR_MISALIGNED;
+    // 32-bit words the kernel reads or writes as such
+    if (!aligned4(index) || (status && !aligned4(status)) ||
+        (fmt == NVQ_NVFP4 && ((s && !aligned4(s)) || !aligned4(s_out))))
         return NVQ_ERR_MISALIGNED;
     const int64_t qbytes = fmt == NVQ_NVFP4 ? cols / 2 : cols;
     return from_cuda(nvq::launch_quantized_gather_rows(q, sf, fmt == NVQ_NVFP4 ? s : nullptr, src_rows, qbytes,

@@ -15,10 +15,10 @@
 // each holding a 128x128-byte A tile, a 256x128-byte B tile (128B swizzle) and their 512-byte
 // scale tiles. Roles:
 //   warp 0 lane 0  TMA producer: A and B tiles (tensor copies) and the scale tiles (bulk copies).
-//   warp 6         A-scale transposer: a GROUP_M tile starts at its group's row offset (a multiple
-//                  of 32), so its 128 rows of A scales straddle two 128-row scale tiles; the producer
-//                  loads both into the stage and the warp rebuilds the tile's own 512-byte scale tile
-//                  (one funnel shift per 16-byte line).
+//   warp 6         A-scale transposer: a GROUP_M tile starts at its group's row offset (any row),
+//                  so its 128 rows of A scales straddle two 128-row scale tiles; the producer loads
+//                  both into the stage and the warp rebuilds the tile's own 512-byte scale tile (each
+//                  16-byte line a 4-word window of one line of the two loaded tiles).
 //   warp 7 lane 0  scale warp: copies each stage's scale tiles smem -> TMEM (tcgen05.cp
 //                  32x128b.warpx4) into one of two TMEM scale sets, so that the copies of the next
 //                  stage are queued while the MMAs of this one run.
@@ -33,9 +33,9 @@
 //                  in flight while the current chunk converts), multiply by s_a[row] s_b[e], round to
 //                  bf16 into registers (the thread's row within the warp's columns), hand TMEM back
 //                  to the MMA warp, then store while the next tile's MMAs run: for grouped row-offset GEMMs
-//                  each warp stages 32 x 32 chunks in shared memory (64-byte swizzle) and sends them
-//                  with TMA box stores; otherwise each thread stores its row with 256-bit stores
-//                  (fp32 output: stored chunk by chunk).
+//                  each warp whose 32 rows all belong to the tile's group stages 32 x 32 chunks in
+//                  shared memory (64-byte swizzle) and sends them with TMA box stores; otherwise each
+//                  thread stores its own row with 256-bit stores (fp32 output: chunk by chunk).
 // GROUP_K tiles iterate the group's reduction range in 32-element MMA steps (k-steps outside the
 // group inside a 128-element stage are skipped).
 //
@@ -60,7 +60,7 @@ constexpr int W_PRODUCER = 0, W_MMA = 1, W_EPI0 = 2, W_TRANSPOSER = 6, W_SCALE =
 constexpr int BM = 128, BN = 256, BKB = 128;       // tile rows, tile columns, K bytes per stage
 constexpr int MAX_GROUPS = 1024;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;    // 2 s: far beyond any legitimate wait
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;    // 2 s: far beyond any legitimate wait (default)
 
 enum { F_MXFP8 = 0, F_NVFP4 = 1, F_BF16 = 2 };       // operand formats (the kernel's template argument)
 
@@ -123,6 +123,8 @@ struct GemmParams {
     int d_aligned32;        // d and every row of it start on 32 bytes: 256-bit stores
     int tma_store;          // bf16 output leaves through staged TMA box stores (else per-thread rows)
     int32_t* status;
+    uint64_t wait_limit_ns; // bound of every pipeline wait (teardown drains keep WAIT_LIMIT_NS)
+    int inject_stage;       // > 0: CTA 0's producer stops before its inject_stage-th stage (watchdog test)
     int64_t a_rowtiles;     // 128-row scale tiles of A
     int64_t b_rowtiles;     // 128-row scale tiles of B (stacked rows)
     int64_t sf_tiles_per_row;   // 4-column scale tiles per row (same for A and B)
@@ -166,16 +168,17 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     return t;
 }
 
-// Bounded wait; returns false (and raises the abort flag / status) when WAIT_LIMIT_NS of wall-clock
+// Bounded wait; returns false (and raises the abort flag / status) when `limit_ns` of wall-clock
 // time pass without the phase completing, or when another role has already aborted.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int32_t* status) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int32_t* status,
+                                          uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 255u) == 0u) {
             if (*abort_flag) return false;
-            if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) break;
+            if (globaltimer_ns() - t0 > limit_ns) break;
         }
     }
     *abort_flag = 1;
@@ -429,8 +432,9 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
     const int64_t limit = (p.mode == NVQ_GEMM_GROUP_M) ? p.m : p.k;
     for (int e = threadIdx.x; e <= G; e += blockDim.x) {
         const int64_t o = p.offsets[e];
-        const bool ok = (o >= 0) && (o <= limit) && ((o & 31) == 0) && (e > 0 || o == 0) &&
-                        (e == 0 || p.offsets[e - 1] <= o);
+        // weight gradients: a 32-element reduction block never straddles two groups
+        const bool ok = (o >= 0) && (o <= limit) && (p.mode == NVQ_GEMM_GROUP_M || (o & 31) == 0) &&
+                        (e > 0 || o == 0) && (e == 0 || p.offsets[e - 1] <= o);
         if (!ok) *bad_flag = 1;
         off32[e] = (int32_t)o;
     }
@@ -509,7 +513,9 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
         for (int i = 0; i < C::STAGES; ++i) sfa_fills[i] = 0;
         StageCursor<C::EPS> cur;
         for (cur.begin(&sched, first, stride); cur.valid; cur.next()) {
-            if (!mbar_wait(&empty_bar[slot], phase ^ 1u, abort_flag, p.status)) break;
+            // watchdog test: stop before this stage, arming nothing, so its consumers' waits run out
+            if (p.inject_stage > 0 && blockIdx.x == 0 && issued + 1 == p.inject_stage) break;
+            if (!mbar_wait(&empty_bar[slot], phase ^ 1u, abort_flag, p.status, p.wait_limit_ns)) break;
             const Tile& tl = cur.tl;
             const int64_t rb_a = tl.a_row0 / BM;
             const bool shifted = C::SCALED && (tl.a_row0 % BM) != 0;
@@ -575,8 +581,8 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
         StageCursor<C::EPS> cur;
         for (cur.begin(&sched, first, stride); cur.valid; cur.next()) {
             const uint32_t set = fill % C::SF_SETS_NZ;
-            if (!mbar_wait(&full_bar[slot], phase, abort_flag, p.status) ||
-                !mbar_wait(&sf_free[set], ((fill / C::SF_SETS_NZ) & 1u) ^ 1u, abort_flag, p.status))
+            if (!mbar_wait(&full_bar[slot], phase, abort_flag, p.status, p.wait_limit_ns) ||
+                !mbar_wait(&sf_free[set], ((fill / C::SF_SETS_NZ) & 1u) ^ 1u, abort_flag, p.status, p.wait_limit_ns))
                 break;
             tc_fence_after();
             const uint32_t ssfa = stage0 + (uint32_t)slot * C::STAGE_BYTES + C::A_BYTES + C::B_BYTES;
@@ -606,14 +612,14 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
         for (int64_t t = first; t < total && ok; t += stride) {
             const Tile tl = sched.get(t);
             if (tl.k_end <= tl.k_begin) continue;
-            if (!mbar_wait(tmem_empty, acc_phase ^ 1u, abort_flag, p.status)) break;
+            if (!mbar_wait(tmem_empty, acc_phase ^ 1u, abort_flag, p.status, p.wait_limit_ns)) break;
             tc_fence_after();
             const int64_t ks0 = tl.k_begin / C::EPS, ks1 = (tl.k_end + C::EPS - 1) / C::EPS;
             uint32_t accumulate = 0;
             for (int64_t ks = ks0; ks < ks1; ++ks) {
                 const uint32_t set = fill % C::SF_SETS_NZ;
-                if (!mbar_wait(&full_bar[slot], phase, abort_flag, p.status) ||
-                    (C::SCALED && !mbar_wait(&sf_ready[set], (fill / C::SF_SETS_NZ) & 1u, abort_flag, p.status))) {
+                if (!mbar_wait(&full_bar[slot], phase, abort_flag, p.status, p.wait_limit_ns) ||
+                    (C::SCALED && !mbar_wait(&sf_ready[set], (fill / C::SF_SETS_NZ) & 1u, abort_flag, p.status, p.wait_limit_ns))) {
                     ok = false;
                     break;
                 }
@@ -647,10 +653,12 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
         mbar_drain(mma_done, 0);
     } else if (C::SCALED && warp == W_TRANSPOSER) {
         // ======================= A-scale transposer =======================
-        // A tile starting 32*g0 rows into a 128-row scale tile needs rows [32 g0, 128) of that tile
-        // followed by rows [0, 32 g0) of the next. In the 512-byte tile layout line l holds the
-        // scales of rows l, l+32, l+64, l+96 as four 4-byte words, so the tile's own line l is the
-        // 16-byte window starting g0 words into (line l of tile 0 ++ line l of tile 1).
+        // A tile starting g rows into a 128-row scale tile needs rows [g, 128) of that tile followed
+        // by rows [0, g) of the next. In the 512-byte tile layout line l holds the scales of rows l,
+        // l+32, l+64, l+96 as four 4-byte words (one word = a row's four scale columns). The tile's
+        // own line l holds its rows l + 32w, i.e. rows g + l + 32w of the two loaded tiles, which
+        // all sit on line L = (g + l) % 32 at words (g + l) / 32 + w of (line L of tile 0 ++ line L
+        // of tile 1): lane l copies that 4-word window.
         int slot = 0;
         uint32_t sfa_phase = 0;                 // bit s: parity of the next sfa_bar[s] phase
         bool ok = true;
@@ -659,15 +667,16 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
             const Tile tl = sched.get(t);
             if (tl.k_end <= tl.k_begin) continue;
             const int64_t ks0 = tl.k_begin / C::EPS, ks1 = (tl.k_end + C::EPS - 1) / C::EPS;
-            const int g0 = (int)((tl.a_row0 % BM) / 32);
-            if (g0 == 0) {
+            const int g = (int)(tl.a_row0 % BM);
+            const uint32_t src_line = (uint32_t)((g + lane) & 31), shift = (uint32_t)((g + lane) >> 5);   // 0..4
+            if (g == 0) {
                 // aligned tile: the producer loaded the scales in place; only keep the ring position
                 slot = (int)((slot + (ks1 - ks0)) % C::STAGES);
                 continue;
             }
             for (int64_t ks = ks0; ks < ks1; ++ks) {
                 int good = 1;
-                if (lane == 0) good = mbar_wait(&sfa_bar[slot], (sfa_phase >> slot) & 1u, abort_flag, p.status) ? 1 : 0;
+                if (lane == 0) good = mbar_wait(&sfa_bar[slot], (sfa_phase >> slot) & 1u, abort_flag, p.status, p.wait_limit_ns) ? 1 : 0;
                 good = __shfl_sync(0xffffffffu, good, 0);
                 if (!good) { ok = false; break; }
                 const uint32_t dst = stage0 + (uint32_t)slot * C::STAGE_BYTES + C::A_BYTES + C::B_BYTES;
@@ -677,16 +686,25 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
                     uint32_t w[8];
                     asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
                                  : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
-                                 : "r"(raw + j * 512 + lane * 16));
+                                 : "r"(raw + j * 512 + src_line * 16));
                     asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
                                  : "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
-                                 : "r"(raw + (C::KGS + j) * 512 + lane * 16));
-                    uint32_t o0 = w[0], o1 = w[1], o2 = w[2], o3 = w[3];
-                    if (g0 == 1) { o0 = w[1]; o1 = w[2]; o2 = w[3]; o3 = w[4]; }
-                    else if (g0 == 2) { o0 = w[2]; o1 = w[3]; o2 = w[4]; o3 = w[5]; }
-                    else if (g0 == 3) { o0 = w[3]; o1 = w[4]; o2 = w[5]; o3 = w[6]; }
+                                 : "r"(raw + (C::KGS + j) * 512 + src_line * 16));
+                    // window of 4 words starting at word `shift` (0..4): barrel shift by 4, 2, 1
+                    if (shift & 4u) {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) w[i] = w[i + 4];
+                    }
+                    if (shift & 2u) {
+#pragma unroll
+                        for (int i = 0; i < 5; ++i) w[i] = w[i + 2];
+                    }
+                    if (shift & 1u) {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) w[i] = w[i + 1];
+                    }
                     asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};"
-                                 ::"r"(dst + j * 512 + lane * 16), "r"(o0), "r"(o1), "r"(o2), "r"(o3)
+                                 ::"r"(dst + j * 512 + lane * 16), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
                                  : "memory");
                 }
                 // make the generic-proxy writes visible to tcgen05.cp (async proxy), then hand over
@@ -718,7 +736,10 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
             if (p.s_b) scale *= p.s_b[tl.e];
             const bool empty = tl.k_end <= tl.k_begin;
             if (!empty) {
-                if (!mbar_wait(tmem_full, acc_phase, abort_flag, p.status)) break;
+                // every lane waits; the warp leaves together if any lane gave up (the TMEM loads
+                // below are warp-wide instructions)
+                const bool good = mbar_wait(tmem_full, acc_phase, abort_flag, p.status, p.wait_limit_ns);
+                if (!__all_sync(0xffffffffu, good)) break;
                 tc_fence_after();
             }
             if (p.out_f32) {
@@ -777,7 +798,9 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
 #pragma unroll
                     for (int j = 0; j < 16; ++j) pk[c][j] = 0u;
             }
-            if (!p.tma_store) {
+            // box stores need the warp's 32 rows inside the tile's group (a group may end at any row)
+            const bool box = p.tma_store && tl.a_row0 + q * 32 + 32 <= tl.row_end;
+            if (!box) {
                 if (row_ok) {
                     uint16_t* dst = reinterpret_cast<uint16_t*>(p.d) + drow * p.ldd + tl.n0 + cbase;
 #pragma unroll
@@ -801,9 +824,8 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __gri
             }
             // Stores: each 32-column chunk of the warp's 32 rows goes through a 2 KB staging buffer
             // (row `lane` = 64 bytes, 16-byte pieces placed by the 64-byte swizzle: piece j of row r
-            // at j ^ ((r >> 1) & 3)) and leaves as one TMA box store. Group offsets are multiples of
-            // 32, so the warp's 32 rows lie wholly inside or outside the tile's group.
-            if (tl.a_row0 + q * 32 < tl.row_end) {
+            // at j ^ ((r >> 1) & 3)) and leaves as one TMA box store.
+            {
 #pragma unroll
                 for (int c = 0; c < NCH; ++c) {
                     if (tl.n0 + cbase + c * 32 >= p.n) break;
@@ -937,6 +959,8 @@ static nvq_status launch_gemm(const nvq_gemm_args* a, cudaStream_t stream) {
     p.tma_store = a->out_type == NVQ_OUT_BF16 && a->mode == NVQ_GEMM_GROUP_M && a->groups > 1 &&
                   a->m >= BM * a->groups;
     p.status = a->status;
+    p.wait_limit_ns = a->wait_limit_ns > 0 ? (uint64_t)a->wait_limit_ns : WAIT_LIMIT_NS;
+    p.inject_stage = a->inject_timeout_stage;
     p.a_rowtiles = (rows_a + BM - 1) / BM;
     p.b_rowtiles = (rows_b + BM - 1) / BM;
     const int64_t kb = a->k / (C::FP4 ? 16 : 32);
@@ -974,7 +998,8 @@ extern "C" nvq_status block_scaled_grouped_gemm(const nvq_gemm_args* a, void* st
         (a->mode != NVQ_GEMM_GROUP_M && a->mode != NVQ_GEMM_GROUP_K) ||
         (a->out_type != NVQ_OUT_BF16 && a->out_type != NVQ_OUT_F32))
         return NVQ_ERR_INVALID_ARG;
-    if (a->groups < 0 || a->m < 0 || a->n < 0 || a->k < 0) return NVQ_ERR_INVALID_ARG;
+    if (a->groups < 0 || a->m < 0 || a->n < 0 || a->k < 0 || a->wait_limit_ns < 0 || a->inject_timeout_stage < 0)
+        return NVQ_ERR_INVALID_ARG;
     if (a->groups == 0 || a->m == 0 || a->n == 0) return NVQ_OK;
     if (a->groups > nvq::MAX_GROUPS) return NVQ_ERR_UNSUPPORTED;
     const bool scaled = a->fmt != NVQ_BF16;

@@ -108,6 +108,11 @@ def test_host_validation_rejects_before_launch(lib):
     assert g(1, fake, fake, fake, 4, 64, 1, None, 8, fake, fake, fake, 1, None, None) == 1   # no index
     assert g(1, odd, fake, fake, 4, 64, 1, fake, 8, fake, fake, fake, 1, None, None) == 2    # misaligned q
     assert g(1, fake, fake, fake, 4, 64, 1, fake, 0, None, None, None, 1, None, None) == 0   # no rows
+    odd4 = vp(0x10002)                                                                       # not 4-byte aligned
+    assert g(1, fake, fake, fake, 4, 64, 1, odd4, 8, fake, fake, fake, 1, None, None) == 2   # index
+    assert g(1, fake, fake, odd4, 4, 64, 1, fake, 8, fake, fake, fake, 1, None, None) == 2   # s
+    assert g(1, fake, fake, fake, 4, 64, 1, fake, 8, fake, fake, odd4, 1, None, None) == 2   # s_out
+    assert g(1, fake, fake, fake, 4, 64, 1, fake, 8, fake, fake, fake, 1, odd4, None) == 2   # status
     d = lib.dequantize_bf16
     d.argtypes = [ctypes.c_int, vp, vp, vp, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                   ctypes.c_int, vp, vp]
@@ -123,7 +128,8 @@ class _GemmArgs(ctypes.Structure):
                 ("a", ctypes.c_void_p), ("sfa", ctypes.c_void_p), ("s_a", ctypes.c_void_p),
                 ("b", ctypes.c_void_p), ("sfb", ctypes.c_void_p), ("s_b", ctypes.c_void_p),
                 ("offsets", ctypes.c_void_p), ("d", ctypes.c_void_p), ("ldd", ctypes.c_int64),
-                ("status", ctypes.c_void_p)]
+                ("status", ctypes.c_void_p), ("wait_limit_ns", ctypes.c_int64),
+                ("inject_timeout_stage", ctypes.c_int32)]
 
 
 def test_gemm_host_validation_rejects_before_launch(lib):
@@ -156,3 +162,5 @@ def test_gemm_host_validation_rejects_before_launch(lib):
     assert call(fmt=0, mode=1, m=200) == 1          # weight gradient: M % 128
     assert call(a=odd) == 2                         # misaligned operand
     assert call(offsets=fake + 4) == 2              # offsets not 8-byte aligned
+    assert call(wait_limit_ns=-1) == 1              # negative wait limit
+    assert call(inject_timeout_stage=-1) == 1       # negative injection stage

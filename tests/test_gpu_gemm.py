@@ -35,8 +35,8 @@ def _check(d_gpu, D, bound, bf16_out):
                            f"{(err / np.maximum(bound, 1e-300)).max():.3e}")
 
 
-def _routed(counts, k, seed, scale_rows=True):
-    offs = workloads.padded_offsets(counts, 32)
+def _routed(counts, k, seed, scale_rows=True, align=32):
+    offs = workloads.padded_offsets(counts, align)
     rng = np.random.default_rng(seed)
     x = rng.standard_normal((int(offs[-1]), k))
     if scale_rows:
@@ -48,9 +48,15 @@ def _routed(counts, k, seed, scale_rows=True):
 # ------------------------------------------------------------------------------------------------
 # forward / data-gradient (rows grouped by expert)
 # ------------------------------------------------------------------------------------------------
-def _run_m(nvq, fmt, counts, K, N, seed, out_type):
+def _run_m(nvq, fmt, counts, K, N, seed, out_type, align=32, offsets=None):
     E = len(counts)
-    offs, xb = _routed(counts, K, seed)
+    offs, xb = _routed(counts, K, seed, align=align)
+    if offsets is not None:                       # explicit offsets (rows between groups are zero)
+        offs = np.asarray(offsets, dtype=np.int64)
+        xb = np.zeros((int(offs[-1]), K), dtype=np.uint16)
+        rng0 = np.random.default_rng(seed)
+        for e, c in enumerate(counts):
+            xb[offs[e]:offs[e] + c] = _bits(rng0.standard_normal((c, K)) * np.exp(rng0.uniform(-4, 4, (c, 1))))
     rng = np.random.default_rng(seed + 1)
     wb = _bits(rng.standard_normal((E, K, N)) * 0.02 * np.exp(rng.uniform(-2, 2, (E, 1, 1))))
     x = workloads.from_bits(xb, "cuda")
@@ -110,13 +116,35 @@ def test_grouped_rows(nvq, fmt, counts, K, N):
 
 
 @pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4"])
-def test_many_tiles_per_cta(nvq, fmt):
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+@pytest.mark.parametrize("counts,K,N", [
+    ([1, 16, 33, 250], 256, 256),            # group offsets 0, 1, 17, 50, 300: any row
+    ([300, 41, 263, 97, 133], 512, 384),     # groups fill their tiles: bf16 box stores with ragged ends
+    ([1, 31, 64, 0, 0, 129, 7], 384, 512),   # single rows, empty groups, K ragged against the FP4 stage
+    ([127, 129, 255, 1, 128], 256, 256),     # every shift of a 128-row scale tile boundary nearby
+])
+def test_grouped_rows_any_offset(nvq, fmt, out, counts, K, N):
+    _run_m(nvq, fmt, counts, K, N, seed=sum(counts) + K + 1, out_type=nvq.OUT_F32 if out == "f32" else nvq.OUT_BF16,
+           align=1)
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4"])
+def test_explicit_offsets_with_gaps(nvq, fmt):
+    # offsets [0, 1, 17, 50, 300] with fewer real rows than each segment holds (rows between the
+    # groups' rows are zero and belong to the groups), then a second call with gaps left out
+    _run_m(nvq, fmt, [1, 16, 33, 250], 256, 256, seed=90, out_type=nvq.OUT_BF16, offsets=[0, 1, 17, 50, 300])
+    _run_m(nvq, fmt, [1, 10, 20, 100], 256, 256, seed=91, out_type=nvq.OUT_F32, offsets=[0, 1, 17, 50, 300])
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4"])
+@pytest.mark.parametrize("align", [32, 1])
+def test_many_tiles_per_cta(nvq, fmt, align):
     # More tiles than CTAs: each CTA runs several tiles, so every stage ring wraps repeatedly, with
     # tiles starting inside a scale tile (32-row group offsets) mixed among aligned ones, and the
     # scale ring runs ahead of the operand ring across tile boundaries.
     counts = [150, 33, 260, 0, 121, 97, 201, 64, 180, 5, 140, 230]
     E, K, N = len(counts), 1024, 2560
-    offs, xb = _routed(counts, K, seed=21)
+    offs, xb = _routed(counts, K, seed=21, align=align)
     rng = np.random.default_rng(22)
     wb = _bits(rng.standard_normal((E, K, N)) * 0.02 * np.exp(rng.uniform(-2, 2, (E, 1, 1))))
     x = workloads.from_bits(xb, "cuda")
@@ -222,18 +250,28 @@ def test_rows_outside_groups_untouched(nvq):
 def test_bad_offsets_set_status_and_write_nothing(nvq):
     K, N = 256, 256
     x = workloads.normal_bf16((64, K), device="cuda")
-    w = workloads.normal_bf16((1, K, N), 0.02, device="cuda")
+    w = workloads.normal_bf16((2, K, N), 0.02, device="cuda")
     qa, sfa, sa = nvq.nvfp4_quantize_per_token(x, sf_layout="mma")
     qb, sfb, sb = nvq.nvfp4_quantize_weights(w, sf_layout="mma")
     d = torch.full((64, N), 3.0, dtype=torch.float32, device="cuda")
-    for bad in ([0, 48], [0, 96], [16, 64]):            # not a multiple of 32 / past the buffer / [0] != 0
+    for bad in ([0, 96, 64], [0, 32, 16], [16, 64, 64]):   # past the buffer / not monotone / [0] != 0
         status = torch.zeros(1, dtype=torch.int32, device="cuda")
         nvq.block_scaled_grouped_gemm(nvq.NVFP4, nvq.GEMM_GROUP_M, qa, sfa, qb, sfb,
                                       torch.tensor(bad, dtype=torch.int64, device="cuda"), m=64, n=N, k=K,
-                                      groups=1, s_a=sa, s_b=sb, out=d, out_type=nvq.OUT_F32, status=status)
+                                      groups=2, s_a=sa, s_b=sb, out=d, out_type=nvq.OUT_F32, status=status)
         torch.cuda.synchronize()
         assert int(status.item()) == nvq.DEV_BAD_OFFSETS
         assert torch.all(d == 3.0)
+    # weight gradients: reduction offsets must be multiples of 32
+    qx = nvq.mxfp8_quantize(workloads.normal_bf16((64, 128), device="cuda"), rowwise=False)
+    dk = torch.full((2, 128, 128), 3.0, dtype=torch.float32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    nvq.block_scaled_grouped_gemm(nvq.MXFP8, nvq.GEMM_GROUP_K, qx["q_colT"], qx["sf_colT"], qx["q_colT"],
+                                  qx["sf_colT"], torch.tensor([0, 48, 64], dtype=torch.int64, device="cuda"),
+                                  m=128, n=128, k=64, groups=2, out=dk, out_type=nvq.OUT_F32, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == nvq.DEV_BAD_OFFSETS
+    assert torch.all(dk == 3.0)
 
 
 def test_host_rejects_bad_shapes(nvq):
@@ -366,9 +404,9 @@ def test_full_size_weight_gradient_sampled(nvq):
 # ------------------------------------------------------------------------------------------------
 # BF16 grouped GEMM (high-precision and dequantized backward) [Miles-zh, "高精度反向和去量化反向"]
 # ------------------------------------------------------------------------------------------------
-def _bf16_m(nvq, counts, K, N, seed, out_type):
+def _bf16_m(nvq, counts, K, N, seed, out_type, align=32):
     E = len(counts)
-    offs, xb = _routed(counts, K, seed)
+    offs, xb = _routed(counts, K, seed, align=align)
     rng = np.random.default_rng(seed + 1)
     wb = _bits(rng.standard_normal((E, N, K)) * 0.02 * np.exp(rng.uniform(-2, 2, (E, 1, 1))))   # B[e] [N, K]
     x = workloads.from_bits(xb, "cuda")
@@ -397,6 +435,12 @@ def test_bf16_grouped_rows(nvq, counts, K, N, out):
 def test_bf16_many_tiles_per_cta(nvq):
     # more tiles than CTAs: the stage ring wraps across tiles of different groups
     _bf16_m(nvq, [150, 33, 260, 0, 121, 97, 201, 64, 180, 5, 140, 230], 1024, 2560, seed=31, out_type=nvq.OUT_F32)
+
+
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_bf16_any_offset(nvq, out):
+    _bf16_m(nvq, [300, 41, 263, 97, 133, 1], 256, 384, seed=33,
+            out_type=nvq.OUT_F32 if out == "f32" else nvq.OUT_BF16, align=1)
 
 
 @pytest.mark.parametrize("counts,Kin,Nout", [([500, 40], 384, 256), ([100, 0, 250, 33], 256, 384)])
