@@ -5,14 +5,17 @@
 Prints ONE JSON line (rank 0). Workloads (synthetic, seeded; shapes of the Qwen3-30B-A3B RL workload
 the pages ablate, see workloads.py):
 
-  dense    (default) X bf16 [8192, 2048] with per-row scales, W_qkv bf16 [2048, 5120]. One step is the
-           whole hot path on that batch: MXFP8 rowwise + columnwise quantization of X, MXFP8
+  moe      (default) one routed MoE expert layer forward in per-token NVFP4, Qwen3-30B-A3B shapes:
+           16384 tokens, top-8 of 128 experts with Zipf(1.1) loads (131072 routed rows, expert
+           segments at any row): per-token NVFP4 of the routed gate_up input [R, 2048], NVFP4 of
+           W_gate_up [128, 2048, 1536] and W_down [128, 768, 2048] (one FP32 scale per expert), the
+           grouped gate_up GEMM, the fused SwiGLU + per-token NVFP4 of its bf16 output, and the
+           grouped down GEMM.
+  dense    X bf16 [8192, 2048] with per-row scales, W_qkv bf16 [2048, 5120]. One step is every
+           quantizer and GEMM on that batch: MXFP8 rowwise + columnwise quantization of X, MXFP8
            columnwise quantization of W, per-token NVFP4 of X, NVFP4 of W (one matrix scope), the
            MXFP8 and the NVFP4 block-scaled GEMM (bf16 out), and the BF16 dequantization of the NVFP4
            W (dequantized-backward operand).
-  moe      16384 tokens, top-8 of 128 experts with Zipf(1.1) loads: per-token NVFP4 of the routed
-           gate_up input [R, 2048] and down input [R, 768], NVFP4 of W_gate_up [128, 2048, 1536] and
-           W_down [128, 768, 2048], and both grouped NVFP4 GEMMs.
   backward the moe shapes in MXFP8 backward: row+col quantization of the routed X and dY, rowwise
            MXFP8 of the expert weights, grouped data-gradient GEMMs and grouped weight-gradient GEMMs.
   decode   256 tokens, uniform top-8 (2048 routed rows): per-token NVFP4 of the activations and the
@@ -51,9 +54,8 @@ L2_FLUSH_BYTES = 256 << 20
 
 # ncu DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of the kernels timed
 # here, keyed by workload and kernel, with the sha256 of the source file the capture was taken
-# from. The commands that produced them are in profiles/launches_dense_step.md (dense),
-# profiles/quant_routed_batch.md (quant, swiglu) and profiles/quant_nvfp4_weights.md (weights;
-# the launches of one call summed). A changed source reports null.
+# from; each figure comes from a capture of that one kernel (a launch or two, after the warm-up
+# steps) of this script's own command. A changed source reports null.
 NCU_TRAFFIC = {
     "dense": {
         "mxfp8_quantize X row+col": {"bytes": 33610000, "src_sha": "60a437b5be6eb37a"},
@@ -213,12 +215,15 @@ def _workload_dense(torch, nvq, wl, dev):
 
 
 def _workload_moe(torch, nvq, wl, dev):
-    counts, offs_np = wl.moe_routing()
+    """One routed MoE expert layer forward in per-token NVFP4: quantize the routed gate_up input per
+    token and both expert weight matrices (one FP32 scale per expert), the grouped gate_up GEMM, the
+    fused SwiGLU + per-token NVFP4 of its bf16 output, and the grouped down GEMM. Expert segments
+    start at any row (no padding)."""
+    counts, offs_np = wl.moe_routing(align=1)
     offs = torch.from_numpy(offs_np).to(dev)
     R = int(offs_np[-1])
     E, H, I2, I = wl.EXPERTS, wl.HIDDEN, 2 * wl.INTERMEDIATE, wl.INTERMEDIATE
     x1 = wl.routed_activations(counts, offs_np, H, seed=1, device=dev)
-    x2 = wl.routed_activations(counts, offs_np, I, seed=2, device=dev)
     w1 = wl.expert_weights(H, I2, seed=3, device=dev)
     w2 = wl.expert_weights(I, H, seed=4, device=dev)
     real = float(counts.sum())
@@ -238,35 +243,41 @@ def _workload_moe(torch, nvq, wl, dev):
          "d1": torch.empty((R, I2), dtype=torch.bfloat16, device=dev),
          "d2": torch.empty((R, H), dtype=torch.bfloat16, device=dev)}
     kernels = [
-        Kernel("nvfp4_quantize_per_token gate_up input", "hbm", R * H * 2.5625 + 4 * R, "quant_nvfp4.cu", "hbm", "2.5625 B/elem + 4 B/row"),
-        Kernel("nvfp4_quantize_weights gate_up", "hbm", E * H * I2 * 2.5625 + 4 * E, "quant_nvfp4_weights.cu", "hbm", "2.5625 B/elem"),
+        Kernel("nvfp4_quantize_per_token gate_up input", "hbm", R * H * 2.5625 + 4 * R, "quant_nvfp4.cu", "hbm",
+               "2.5625 B/elem + 4 B/row"),
+        Kernel("nvfp4_quantize_weights gate_up", "hbm", E * H * I2 * 2.5625 + 4 * E, "quant_nvfp4_weights.cu", "hbm",
+               "2.5625 B/elem"),
         Kernel("block_scaled_gemm NVFP4 gate_up", "tensor", f1, "gemm_sm103.cu", "fp4", "2*sum_e M_e*N*K"),
-        Kernel("nvfp4_quantize_per_token down input", "hbm", R * I * 2.5625 + 4 * R, "quant_nvfp4.cu", "hbm", "2.5625 B/elem + 4 B/row"),
-        Kernel("nvfp4_quantize_weights down", "hbm", E * I * H * 2.5625 + 4 * E, "quant_nvfp4_weights.cu", "hbm", "2.5625 B/elem"),
+        Kernel("nvfp4_swiglu_quantize_per_token down input", "hbm", R * (2 * I * 2 + I / 2 + I / 16 + 4),
+               "quant_nvfp4.cu", "hbm", "4 B read per h element (gate and up bf16) + 0.5625 B written + 4 B/row"),
+        Kernel("nvfp4_quantize_weights down", "hbm", E * I * H * 2.5625 + 4 * E, "quant_nvfp4_weights.cu", "hbm",
+               "2.5625 B/elem"),
         Kernel("block_scaled_gemm NVFP4 down", "tensor", f2, "gemm_sm103.cu", "fp4", "2*sum_e M_e*N*K"),
     ]
 
     def step(timer, xin=None, win=None):
-        xa, xb = (x1, x2) if xin is None else xin
+        xa = x1 if xin is None else xin[0]
         wa, wb = (w1, w2) if win is None else win
         timer.run(kernels[0].name, lambda: nvq.nvfp4_quantize_per_token(xa, out=b["a1"]))
         timer.run(kernels[1].name, lambda: nvq.nvfp4_quantize_weights(wa, out=b["b1"]))
         timer.run(kernels[2].name, lambda: nvq.block_scaled_grouped_gemm(
             nvq.NVFP4, nvq.GEMM_GROUP_M, b["a1"][0], b["a1"][1], b["b1"][0], b["b1"][1], offs, m=R, n=I2, k=H,
             groups=E, s_a=b["a1"][2], s_b=b["b1"][2], out=b["d1"]))
-        timer.run(kernels[3].name, lambda: nvq.nvfp4_quantize_per_token(xb, out=b["a2"]))
+        timer.run(kernels[3].name, lambda: nvq.nvfp4_swiglu_quantize_per_token(b["d1"], out=b["a2"]))
         timer.run(kernels[4].name, lambda: nvq.nvfp4_quantize_weights(wb, out=b["b2"]))
         timer.run(kernels[5].name, lambda: nvq.block_scaled_grouped_gemm(
             nvq.NVFP4, nvq.GEMM_GROUP_M, b["a2"][0], b["a2"][1], b["b2"][0], b["b2"][1], offs, m=R, n=H, k=I,
             groups=E, s_a=b["a2"][2], s_b=b["b2"][2], out=b["d2"]))
-        return [b["d1"], b["d2"]]
+        return [b["d2"]]
 
-    config = {"workload": "per-token NVFP4 MoE expert forward (gate_up and down), Qwen3-30B-A3B shapes",
-              "tokens": 16384, "experts": E, "topk": 8, "routing": "Gumbel-top-8, p_r ~ r^-1.1",
-              "routed_rows": int(real), "buffer_rows": R, "row_alignment": 32,
-              "expert_rows_min_max": [int(counts.min()), int(counts.max())]}
-    return {"step": step, "kernels": kernels, "gemm_flops": f1 + f2, "inputs": [x1, x2, w1, w2],
-            "input_groups": ([0, 1], [2, 3]), "config": config,
+    config = {"workload": "per-token NVFP4 MoE expert layer forward, Qwen3-30B-A3B shapes: 16384 tokens, "
+                          "top-8 of 128 experts (Zipf 1.1 loads), 131072 routed rows; quantize, gate_up GEMM, "
+                          "SwiGLU + NVFP4, down GEMM",
+              "tokens": 16384, "hidden": H, "intermediate": I, "experts": E, "topk": 8,
+              "routing": "Gumbel-top-8, p_r ~ r^-1.1", "routed_rows": int(real), "buffer_rows": R,
+              "row_alignment": 1, "expert_rows_min_max": [int(counts.min()), int(counts.max())]}
+    return {"step": step, "kernels": kernels, "gemm_flops": f1 + f2, "inputs": [x1, w1, w2],
+            "input_groups": ([0], [1, 2]), "config": config,
             "dtype": "nvfp4(e2m1+e4m3+fp32) -> fp32 accumulate -> bf16"}
 
 
@@ -428,7 +439,7 @@ def _workload_dq_backward(torch, nvq, wl, dev):
 
 def _workload_decode(torch, nvq, wl, dev):
     counts = wl.route_counts(256, zipf_s=0.0, seed=0)
-    offs_np = wl.padded_offsets(counts, 32)
+    offs_np = wl.padded_offsets(counts, 1)                # expert segments start at any row
     offs = torch.from_numpy(offs_np).to(dev)
     R = int(offs_np[-1])
     E, H, I2 = wl.EXPERTS, wl.HIDDEN, 2 * wl.INTERMEDIATE
@@ -529,11 +540,11 @@ def _workload_weights(torch, nvq, wl, dev):
 
 def _workload_dispatch(torch, nvq, wl, dev):
     """Quantize-once dispatch of the MoE gate_up input: per-token NVFP4 of the 16384 tokens, then the
-    gather of their quantized rows into the 132960 expert-sorted routed rows (32-row padded)."""
+    gather of their quantized rows into the 131072 expert-sorted routed rows."""
     T, H = 16384, wl.HIDDEN
     choices = wl.route_choices(T)
     counts = wl.route_counts(T)
-    offs_np = wl.padded_offsets(counts, 32)
+    offs_np = wl.padded_offsets(counts, 1)
     R = int(offs_np[-1])
     idx = torch.from_numpy(wl.dispatch_index(choices, offs_np)).to(dev)
     x = wl.normal_bf16((T, H), 1.0, seed=21, device=dev)
@@ -559,7 +570,7 @@ def _workload_dispatch(torch, nvq, wl, dev):
         return [routed[0], routed[1], routed[2]]
 
     config = {"workload": "quantize-once dispatch: per-token NVFP4 of 16384 tokens x 2048, gathered into "
-                          "the top-8 expert-sorted routed rows (Zipf 1.1, 32-row padding)",
+                          "the top-8 expert-sorted routed rows (Zipf 1.1)",
               "tokens": [T, H], "routed_rows": R}
     return {"step": step, "kernels": kernels, "gemm_flops": 0.0, "inputs": [x], "input_groups": ([0], []),
             "config": config, "dtype": "bf16 -> nvfp4 (gathered)", "unit": "GB/s"}
@@ -567,8 +578,8 @@ def _workload_dispatch(torch, nvq, wl, dev):
 
 def _workload_swiglu(torch, nvq, wl, dev):
     """The down projection's NVFP4 input straight from the gate_up GEMM output: SwiGLU + per-token
-    NVFP4 in one pass over the 132960 x (768 + 768) routed activation."""
-    counts, offs_np = wl.moe_routing()
+    NVFP4 in one pass over the 131072 x (768 + 768) routed activation."""
+    counts, offs_np = wl.moe_routing(align=1)
     R = int(offs_np[-1])
     I = wl.INTERMEDIATE
     x = wl.routed_activations(counts, offs_np, 2 * I, seed=12, device=dev)
@@ -920,9 +931,9 @@ def _oracle_sample(workload, rows, cols):
         flops = rows * K * (4.0625 + 2.5625) + 4 * rows            # algorithmic bytes, not flops
         desc = f"oracle MXFP8 row+col and per-token NVFP4 of {rows} rows x {K}"
     else:
-        counts, offs = wl.moe_routing() if workload != "decode" else (None, None)
         K = wl.HIDDEN
         N = 2 * wl.INTERMEDIATE
+        cols = min(cols, N)
         x = rng.standard_normal((rows, K)).astype(np.float32)
         w = (rng.standard_normal((K, N)) * 0.02).astype(np.float32)
         import torch
@@ -945,26 +956,105 @@ def _oracle_sample(workload, rows, cols):
             oracle.grouped_gemm_reference("m", a, b[None], [0, rows], s, sw)
         flops = 2.0 * rows * cols * K
         desc = f"oracle on {rows} routed rows x {cols} output columns, K={K} (one expert's GEMM block + its quantizers)"
-        del counts, offs
     return time.perf_counter() - t0, flops, desc
 
 
+# The moe sample on all host cores: the oracle's own steps, split into independent units run by a
+# pool of single-threaded worker processes. Phase 1 quantizes blocks of expert-weight columns (the
+# expert's FP32 scale from its amax first), phase 2 quantizes blocks of routed rows per token and
+# multiplies them by the dequantized weights. Module-level so that spawned workers can import them.
+def _moe_w_unit(job):
+    import numpy as np
+
+    import oracle
+    w_cols_bits, s_w = job                                 # [c, K] bf16 bits: columns of W as rows
+    return oracle.nvfp4_quantize_rows(oracle.bf16_bits_to_f64(w_cols_bits), np.full(len(w_cols_bits), s_w))
+
+
+def _moe_x_unit(job):
+    import numpy as np
+
+    import oracle
+    xb, wq, wsf, s_w = job
+    q, sf, s = oracle.nvfp4_quantize_per_token(xb)
+    a = oracle.deq_operand("nvfp4", q, sf)
+    b = oracle.deq_operand("nvfp4", wq, wsf)
+    oracle.grouped_gemm_reference("m", a, b[None], [0, len(xb)], s, np.array([s_w], dtype=np.float32))
+    return 2.0 * len(xb) * len(wq) * xb.shape[1]
+
+
+def _ready(_):
+    import oracle  # noqa: F401
+    return os.getpid()
+
+
+def _oracle_moe_parallel(rows, cols, procs):
+    """Wall time of the moe oracle sample (rows routed rows x cols weight columns, K = 2048) on
+    ``procs`` worker processes; returns (seconds, flops, description)."""
+    import multiprocessing as mp
+
+    import numpy as np
+    import torch
+
+    import workloads as wl
+    rng = np.random.default_rng(0)
+    K, N = wl.HIDDEN, 2 * wl.INTERMEDIATE
+    cols = min(cols, N)
+    xb = wl.to_bits(torch.from_numpy(rng.standard_normal((rows, K)).astype(np.float32)).to(torch.bfloat16))
+    wb = wl.to_bits(torch.from_numpy((rng.standard_normal((K, N)) * 0.02).astype(np.float32)).to(torch.bfloat16))
+    wt = np.ascontiguousarray(wb[:, :cols].T)
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(procs) as pool:
+        pool.map(_ready, range(procs))                     # workers started and the oracle imported
+        t0 = time.perf_counter()
+        import oracle
+        s_w = float(oracle.nvfp4_token_scale(np.abs(oracle.bf16_bits_to_f64(wt)).max()))
+        parts = pool.map(_moe_w_unit, [(c, s_w) for c in np.array_split(wt, procs)])
+        wq = np.concatenate([p[0] for p in parts])
+        wsf = np.concatenate([p[1] for p in parts])
+        flops = sum(pool.map(_moe_x_unit, [(x, wq, wsf, s_w) for x in np.array_split(xb, procs)]))
+        sec = time.perf_counter() - t0
+    desc = (f"oracle on {rows} routed rows x {cols} weight columns, K={K}: per-token NVFP4 of the rows, "
+            f"NVFP4 of the weight columns, the GEMM block; {procs} worker processes (weight column "
+            f"blocks, then row blocks)")
+    return sec, flops, desc
+
+
+def _host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
 def cpu_baseline(workload, rows=4096, cols=3072):
-    """Time the oracle in a single-threaded child process (BLAS threads pinned to 1)."""
+    """Time the oracle in child processes with BLAS threads pinned to 1: single-threaded, and (moe)
+    on every host core as a pool of single-threaded workers. ``value`` / ``cores`` are the all-core
+    figure where there is one, with the single-threaded one beside it."""
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
                CUDA_VISIBLE_DEVICES="")
-    cmd = [sys.executable, os.path.abspath(__file__), "--oracle-sample", workload, "--rows", str(rows),
-           "--cols", str(cols)]
-    try:
-        out = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=600)
+    unit, scale = ("GB/s", 1e9) if workload in GBS_WORKLOADS else ("TFLOPS", 1e12)
+
+    def run(procs):
+        cmd = [sys.executable, os.path.abspath(__file__), "--oracle-sample", workload, "--rows", str(rows),
+               "--cols", str(cols), "--procs", str(procs)]
+        out = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=900)
         res = json.loads(out.stdout.strip().splitlines()[-1])
-    except (subprocess.SubprocessError, ValueError, IndexError) as e:
-        return {"value": None, "unit": "TFLOPS", "cores": 1, "kind": "oracle", "sample": f"failed: {e}"}
-    if workload in GBS_WORKLOADS:
-        return {"value": res["flops"] / res["seconds"] / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+        return {"value": res["flops"] / res["seconds"] / scale, "unit": unit, "cores": procs, "kind": "oracle",
                 "sample": res["sample"], "seconds": round(res["seconds"], 3)}
-    return {"value": res["flops"] / res["seconds"] / 1e12, "unit": "TFLOPS", "cores": 1, "kind": "oracle",
-            "sample": res["sample"], "seconds": round(res["seconds"], 3)}
+
+    try:
+        single = run(1)
+    except (subprocess.SubprocessError, ValueError, IndexError) as e:
+        return {"value": None, "unit": unit, "cores": 1, "kind": "oracle", "sample": f"failed: {e}"}
+    cores = _host_cores()
+    if workload != "moe" or cores <= 1:
+        return single
+    try:
+        allc = run(cores)
+    except (subprocess.SubprocessError, ValueError, IndexError) as e:
+        return dict(single, all_cores=f"failed: {e}")
+    return dict(allc, single_thread={k: single[k] for k in ("value", "cores", "seconds", "sample")})
 
 
 def run_reference(args):
@@ -1004,15 +1094,19 @@ def main():
                     help="timed steps (default: enough for about 2 s of device time, at least 20)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="dense")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="moe")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--oracle-sample", default=None, help=argparse.SUPPRESS)
     ap.add_argument("--rows", type=int, default=512, help=argparse.SUPPRESS)
     ap.add_argument("--cols", type=int, default=512, help=argparse.SUPPRESS)
+    ap.add_argument("--procs", type=int, default=1, help=argparse.SUPPRESS)
     args = ap.parse_args()
     if args.oracle_sample:
-        t, f, d = _oracle_sample(args.oracle_sample, args.rows, args.cols)
+        if args.procs > 1 and args.oracle_sample == "moe":
+            t, f, d = _oracle_moe_parallel(args.rows, args.cols, args.procs)
+        else:
+            t, f, d = _oracle_sample(args.oracle_sample, args.rows, args.cols)
         print(json.dumps({"seconds": t, "flops": f, "sample": d}))
         return
     if args.warmup < 3 and args.impl == "ours":
