@@ -1027,13 +1027,15 @@ def _host_cores():
         return os.cpu_count() or 1
 
 
-def cpu_baseline(workload, rows=4096, cols=3072):
+def cpu_baseline(workload, rows=None, cols=3072):
     """Time the oracle in child processes with BLAS threads pinned to 1: single-threaded, and (moe)
     on every host core as a pool of single-threaded workers. ``value`` / ``cores`` are the all-core
     figure where there is one, with the single-threaded one beside it."""
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
                CUDA_VISIBLE_DEVICES="")
     unit, scale = ("GB/s", 1e9) if workload in GBS_WORKLOADS else ("TFLOPS", 1e12)
+    if rows is None:
+        rows = 16384 if workload == "moe" else 4096     # several seconds of single-threaded oracle work
 
     def run(procs):
         cmd = [sys.executable, os.path.abspath(__file__), "--oracle-sample", workload, "--rows", str(rows),
