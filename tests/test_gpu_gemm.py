@@ -323,6 +323,16 @@ def _sample_pairs(rng, rows, n, count):
     return rng.choice(rows, count), rng.integers(0, n, count)
 
 
+def _oracle_weight_columns(w_e_bits, cols):
+    """Oracle NVFP4 of selected output columns of one expert matrix W[e] [K, N] (bf16 bits): the
+    expert's FP32 scale from the whole matrix's amax, then the columns' 1x16 blocks along K.
+    Returns (dequantized rows [len(cols), K] without the FP32 scale, the FP32 scale)."""
+    wf = oracle.bf16_bits_to_f64(w_e_bits)
+    s_w = oracle.nvfp4_token_scale(np.abs(wf).max())
+    q, sf = oracle.nvfp4_quantize_rows(np.ascontiguousarray(wf[:, cols].T), np.full(len(cols), s_w))
+    return oracle.deq_operand("nvfp4", q, sf), float(s_w)
+
+
 def test_full_size_dense_mxfp8_sampled(nvq):
     inp = workloads.dense_inputs(seed=0, device="cuda")
     x, w = inp["x"], inp["w"]
@@ -347,9 +357,13 @@ def test_full_size_dense_mxfp8_sampled(nvq):
     _check(got, Dv, bd, True)
 
 
-def test_full_size_moe_nvfp4_sampled(nvq):
-    counts, offs = workloads.moe_routing()
-    K, N = workloads.HIDDEN, 2 * workloads.INTERMEDIATE
+@pytest.mark.parametrize("layer,align", [("gate_up", 1), ("gate_up", 32), ("down", 1)])
+def test_full_size_moe_nvfp4_sampled(nvq, layer, align):
+    # the bench's MoE layer (unpadded expert segments) and the 32-row padded layout: gate_up
+    # (K = 2048, N = 1536) and down (K = 768, N = 2048) over the 131072 Zipf-routed rows
+    counts, offs = workloads.moe_routing(align=align)
+    K, N = (workloads.HIDDEN, 2 * workloads.INTERMEDIATE) if layer == "gate_up" else \
+        (workloads.INTERMEDIATE, workloads.HIDDEN)
     x = workloads.routed_activations(counts, offs, K, seed=1, device="cuda")
     w = workloads.expert_weights(K, N, seed=2, device="cuda")
     qa, sfa, sa = nvq.nvfp4_quantize_per_token(x)
@@ -359,7 +373,7 @@ def test_full_size_moe_nvfp4_sampled(nvq):
                                       m=M, n=N, k=K, groups=E, s_a=sa, s_b=sb)
     torch.cuda.synchronize()
     rng = np.random.default_rng(1)
-    experts = rng.choice(E, 6, replace=False)
+    experts = np.concatenate([rng.choice(E, 6, replace=False), [int(np.argmax(counts)), int(np.argmin(counts))]])
     for e in experts:
         if counts[e] == 0:
             continue
@@ -367,11 +381,72 @@ def test_full_size_moe_nvfp4_sampled(nvq):
         cols = rng.integers(0, N, 64)
         xa = workloads.to_bits(x[torch.from_numpy(rows).cuda()])
         q_r, sf_r, s_r = oracle.nvfp4_quantize_per_token(xa)
-        wq_r, wsf_r, ws_r = oracle.nvfp4_quantize_weights(workloads.to_bits(w[int(e)])[None])
         A = oracle.deq_operand("nvfp4", q_r, sf_r)
-        B = oracle.deq_operand("nvfp4", wq_r[0][cols], wsf_r[0][cols])
-        Dv, bd = oracle.grouped_gemm_entries("m", A, B, np.tile([0, K], (64, 1)), s_r.astype(np.float64) * float(ws_r[0]))
+        B, s_w = _oracle_weight_columns(workloads.to_bits(w[int(e)]), cols)
+        Dv, bd = oracle.grouped_gemm_entries("m", A, B, np.tile([0, K], (64, 1)), s_r.astype(np.float64) * s_w)
         got = d[torch.from_numpy(rows).cuda(), torch.from_numpy(cols).cuda()]
+        _check(got, Dv, bd, True)
+
+
+@pytest.mark.parametrize("layer", ["gate_up", "down"])
+def test_full_size_mxfp8_data_gradient_sampled(nvq, layer):
+    # the backward workload's data gradients: dX = dY W[e]^T per expert, A = rowwise MXFP8 of dY
+    # [R, N] (blocks along N), B = rowwise MXFP8 of W stacked [E*K, N] (W[e] [K, N])
+    counts, offs = workloads.moe_routing()
+    K, N = (workloads.HIDDEN, 2 * workloads.INTERMEDIATE) if layer == "gate_up" else \
+        (workloads.INTERMEDIATE, workloads.HIDDEN)
+    E = len(counts)
+    g = workloads.routed_activations(counts, offs, N, std=1e-3, seed=5, device="cuda")
+    w = workloads.expert_weights(K, N, seed=3, device="cuda").view(E * K, N)
+    qg = nvq.mxfp8_quantize(g, colwise=False)
+    qw = nvq.mxfp8_quantize(w, colwise=False)
+    M = g.shape[0]
+    d = nvq.block_scaled_grouped_gemm(nvq.MXFP8, nvq.GEMM_GROUP_M, qg["q_row"], qg["sf_row"], qw["q_row"],
+                                      qw["sf_row"], torch.from_numpy(offs).cuda(), m=M, n=K, k=N, groups=E)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(4)
+    for e in np.concatenate([rng.choice(E, 5, replace=False), [int(np.argmax(counts))]]):
+        if counts[e] == 0:
+            continue
+        rows = offs[e] + rng.integers(0, counts[e], 64)
+        cols = rng.integers(0, K, 64)
+        ga = workloads.to_bits(g[torch.from_numpy(rows).cuda()])
+        wr = workloads.to_bits(w[torch.from_numpy(int(e) * K + cols).cuda()])
+        A = oracle.deq_operand("mxfp8", *oracle.mxfp8_quantize(ga, colwise=False).values())
+        B = oracle.deq_operand("mxfp8", *oracle.mxfp8_quantize(wr, colwise=False).values())
+        Dv, bd = oracle.grouped_gemm_entries("m", A, B, np.tile([0, N], (64, 1)), np.ones(64))
+        got = d[torch.from_numpy(rows).cuda(), torch.from_numpy(cols).cuda()]
+        _check(got, Dv, bd, True)
+
+
+def test_full_size_decode_nvfp4(nvq):
+    # the decode workload: 256 tokens, uniform top-8 over 128 experts (9..25 rows each, 2048 rows,
+    # unpadded), K = 2048, N = 1536; every row of 24 experts checked on 96 columns
+    counts = workloads.route_counts(256, zipf_s=0.0, seed=0)
+    offs = workloads.padded_offsets(counts, 1)
+    K, N, E = workloads.HIDDEN, 2 * workloads.INTERMEDIATE, workloads.EXPERTS
+    x = workloads.routed_activations(counts, offs, K, seed=1, device="cuda")
+    w = workloads.expert_weights(K, N, seed=3, device="cuda")
+    qa, sfa, sa = nvq.nvfp4_quantize_per_token(x)
+    qb, sfb, sb = nvq.nvfp4_quantize_weights(w)
+    M = x.shape[0]
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    d = nvq.block_scaled_grouped_gemm(nvq.NVFP4, nvq.GEMM_GROUP_M, qa, sfa, qb, sfb, torch.from_numpy(offs).cuda(),
+                                      m=M, n=N, k=K, groups=E, s_a=sa, s_b=sb, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0 and M == 2048
+    q_r, sf_r, s_r = oracle.nvfp4_quantize_per_token(workloads.to_bits(x))
+    A = oracle.deq_operand("nvfp4", q_r, sf_r)
+    rng = np.random.default_rng(6)
+    experts = np.concatenate([rng.choice(E, 22, replace=False), [int(np.argmax(counts)), int(np.argmin(counts))]])
+    for e in experts:
+        cols = rng.integers(0, N, 96)
+        B, s_w = _oracle_weight_columns(workloads.to_bits(w[int(e)]), cols)
+        rows = np.arange(offs[e], offs[e + 1])
+        ii, jj = np.repeat(rows, 96), np.tile(np.arange(96), len(rows))
+        Dv, bd = oracle.grouped_gemm_entries("m", A[ii], B[jj], np.tile([0, K], (len(ii), 1)),
+                                             s_r[ii].astype(np.float64) * s_w)
+        got = d[torch.from_numpy(ii).cuda(), torch.from_numpy(cols[jj]).cuda()]
         _check(got, Dv, bd, True)
 
 
