@@ -293,6 +293,30 @@ def test_nvfp4_weights_product_and_boundary_scopes(nvq, layout):
         assert np.array_equal(_np(sf), oracle.sf_to_mma_layout(sf_ref.reshape(E * N, K // 16)))
 
 
+@pytest.mark.parametrize("layer", ["gate_up", "down"])
+def test_full_size_expert_weights_sampled(nvq, layer):
+    """All 128 expert matrices of the MoE layer in the bench's launch (MMA layout): every expert's
+    scale, and 64 sampled output columns of 12 experts byte for byte."""
+    K, N = (workloads.HIDDEN, 2 * workloads.INTERMEDIATE) if layer == "gate_up" else \
+        (workloads.INTERMEDIATE, workloads.HIDDEN)
+    w = workloads.expert_weights(K, N, seed=3, device="cuda")
+    E = w.shape[0]
+    q, sf, s = nvq.nvfp4_quantize_weights(w)
+    torch.cuda.synchronize()
+    amax = w.abs().reshape(E, -1).max(dim=1).values.float().cpu().numpy().astype(np.float64)
+    s_ref = oracle.nvfp4_token_scale(amax)
+    assert np.array_equal(_np(s).view(np.uint32), s_ref.view(np.uint32))
+    rng = np.random.default_rng(11)
+    kb = K // 16
+    for e in rng.choice(E, 12, replace=False):
+        cols = np.sort(rng.choice(N, 64, replace=False))
+        we = oracle.bf16_bits_to_f64(workloads.to_bits(w[int(e)]))
+        q_r, sf_r = oracle.nvfp4_quantize_rows(np.ascontiguousarray(we[:, cols].T), np.full(64, s_ref[e]))
+        assert np.array_equal(_np(q[int(e)])[cols], q_r)
+        r_idx, c_idx = np.meshgrid(int(e) * N + cols, np.arange(kb), indexing="ij")
+        assert np.array_equal(_np(sf)[oracle.mma_layout_offset(r_idx, c_idx, kb)], sf_r)
+
+
 # ------------------------------------------------------------------------------------------------
 # Dequantize
 # ------------------------------------------------------------------------------------------------
