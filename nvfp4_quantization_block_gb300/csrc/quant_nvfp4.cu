@@ -72,8 +72,44 @@ __device__ __noinline__ float swiglu_wide(float g, float u, float p, float m) {
     return __double2float_rn(__dmul_rn(__dmul_rn((double)q, (double)u), pow2));
 }
 
-// bf16x2 word of SwiGLU(gate, up) for the bf16x2 words g and u
-__device__ __forceinline__ uint32_t swiglu2(uint32_t g, uint32_t u) {
+// bf16x2 word of SwiGLU(gate, up) for the bf16x2 words g and u; `rare` is set when an element
+// needs the exact path (swiglu2_exact below): a gate with -g > 87 or a quotient the fast
+// division does not cover.
+__device__ __forceinline__ uint32_t swiglu2_fast(uint32_t g, uint32_t u, bool& rare) {
+    constexpr float L2E = (float)1.4426950408889634, LN2_HI = 0.693145751953125f;
+    constexpr float LN2_LO = (float)(0.6931471805599453 - 0.693145751953125), MAGIC = 12582912.0f;
+    const uint32_t xw = g ^ 0x80008000u;                       // x = -g, both halves
+    const float x0 = fminf(fmaxf(bf16_lo(xw), -87.0f), 300.0f), x1 = fminf(fmaxf(bf16_hi(xw), -87.0f), 300.0f);
+    float t0, t1, m0, m1, n0, n1, a0, a1, r0, r1;
+    f2_mul(t0, t1, x0, x1, L2E, L2E);
+    f2_add(m0, m1, t0, t1, MAGIC, MAGIC);                      // 1.5 * 2^23 + n: n in the low mantissa bits
+    f2_sub(n0, n1, m0, m1, MAGIC, MAGIC);                      // nearest integer to x log2(e), exactly
+    f2_mul(a0, a1, n0, n1, LN2_HI, LN2_HI);
+    f2_sub(r0, r1, x0, x1, a0, a1);
+    f2_mul(a0, a1, n0, n1, LN2_LO, LN2_LO);
+    f2_sub(r0, r1, r0, r1, a0, a1);
+    float p0 = (float)(1.0 / 720.0), p1 = p0;
+    const float c[6] = {(float)(1.0 / 120.0), (float)(1.0 / 24.0), (float)(1.0 / 6.0), 0.5f, 1.0f, 1.0f};
+#pragma unroll
+    for (int i = 0; i < 6; ++i) {
+        f2_mul(p0, p1, p0, p1, r0, r1);
+        f2_add(p0, p1, p0, p1, c[i], c[i]);
+    }
+    // 2^n from the bits of 1.5 * 2^23 + n (n in [-126, 126] when x <= 87)
+    const float s0 = __uint_as_float((__float_as_uint(m0) - 0x4B400000u + 127u) << 23);
+    const float s1 = __uint_as_float((__float_as_uint(m1) - 0x4B400000u + 127u) << 23);
+    float e0, e1, d0, d1, h0, h1;
+    f2_mul(e0, e1, p0, p1, s0, s1);                            // exp(-g)
+    f2_add(d0, d1, e0, e1, 1.0f, 1.0f);
+    bool ok0, ok1;
+    const float q0 = div_markstein(bf16_lo(g), d0, ok0), q1 = div_markstein(bf16_hi(g), d1, ok1);
+    f2_mul(h0, h1, q0, q1, bf16_lo(u), bf16_hi(u));
+    rare = rare || !(ok0 && ok1 && x0 <= 87.0f && x1 <= 87.0f);
+    return cvt_bf16x2(h0, h1);
+}
+
+// bf16x2 word of SwiGLU(gate, up) for the bf16x2 words g and u (every element exact)
+__device__ __noinline__ uint32_t swiglu2(uint32_t g, uint32_t u) {
     constexpr float L2E = (float)1.4426950408889634, LN2_HI = 0.693145751953125f;
     constexpr float LN2_LO = (float)(0.6931471805599453 - 0.693145751953125), MAGIC = 12582912.0f;
     const uint32_t xw = g ^ 0x80008000u;                       // x = -g, both halves
@@ -115,8 +151,20 @@ __device__ __forceinline__ void row_block(const uint16_t* p, int64_t up, uint4& 
     if (SWIGLU) {
         uint4 ua, ub;
         load_block<V8>(p + up, ua, ub);
-        a = make_uint4(swiglu2(a.x, ua.x), swiglu2(a.y, ua.y), swiglu2(a.z, ua.z), swiglu2(a.w, ua.w));
-        b = make_uint4(swiglu2(b.x, ub.x), swiglu2(b.y, ub.y), swiglu2(b.z, ub.z), swiglu2(b.w, ub.w));
+        // the fast steps for the whole block; a block with any element outside their range (rare)
+        // is formed again element by element with the exact steps
+        bool rare = false;
+        a = make_uint4(swiglu2_fast(a.x, ua.x, rare), swiglu2_fast(a.y, ua.y, rare), swiglu2_fast(a.z, ua.z, rare),
+                       swiglu2_fast(a.w, ua.w, rare));
+        b = make_uint4(swiglu2_fast(b.x, ub.x, rare), swiglu2_fast(b.y, ub.y, rare), swiglu2_fast(b.z, ub.z, rare),
+                       swiglu2_fast(b.w, ub.w, rare));
+        if (rare) {
+            // the block's gate and up words again (rare: no registers kept for them)
+            load_block<V8>(p, a, b);
+            load_block<V8>(p + up, ua, ub);
+            a = make_uint4(swiglu2(a.x, ua.x), swiglu2(a.y, ua.y), swiglu2(a.z, ua.z), swiglu2(a.w, ua.w));
+            b = make_uint4(swiglu2(b.x, ub.x), swiglu2(b.y, ub.y), swiglu2(b.z, ub.z), swiglu2(b.w, ub.w));
+        }
     }
 }
 

@@ -64,6 +64,25 @@ def test_swiglu_quantize_bit_exact(nvq, R, I, layout):
     _check(nvq, bits, layout, out)
 
 
+def test_swiglu_quantize_division_ranges(nvq):
+    # the division g / (1 + exp(-g)) over the ranges its fast steps cover and those they leave to
+    # IEEE division: quotients near 2^-100 (tiny gates, huge exp(-g)), subnormal and zero gates
+    R, I = 64, 512
+    rng = np.random.default_rng(17)
+    g = rng.standard_normal((R, I))
+    kind = np.arange(R) % 4
+    g[kind == 0] = -rng.uniform(55.0, 87.0, ((kind == 0).sum(), I))          # exp(-g) up to 2^125
+    g[kind == 1] = np.sign(rng.standard_normal(((kind == 1).sum(), I))) * 2.0 ** rng.uniform(-133, -90, ((kind == 1).sum(), I))
+    g[kind == 2] *= 2.0 ** rng.integers(-110, 10, ((kind == 2).sum(), I))
+    u = rng.standard_normal((R, I)) * 10.0 ** rng.uniform(-3, 35, (R, 1))
+    bits = oracle.f64_to_bf16_bits_rne(np.concatenate([g, u], axis=1))
+    bits[3, :I:7] = 0x8000                                                   # negative zero gates
+    bits[3, 1:I:7] = 0x0000
+    out = nvq.nvfp4_swiglu_quantize_per_token(workloads.from_bits(bits, "cuda"), sf_layout="canonical")
+    torch.cuda.synchronize()
+    _check(nvq, bits, "canonical", out)
+
+
 def test_swiglu_quantize_strided_rows(nvq):
     R, I = 96, 256
     bits = _gate_up(R, I, seed=3)
