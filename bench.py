@@ -51,33 +51,21 @@ if ROOT not in sys.path:
 
 METRIC = "quantize GB/s (% HBM peak); block-scaled MoE GEMM TFLOPS (% dense peak)"
 L2_FLUSH_BYTES = 256 << 20
+COPY_STREAMS = 4
 
 # ncu DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of the kernels timed
 # here, keyed by workload and kernel, with the sha256 of the source file the capture was taken
 # from; each figure comes from a capture of that one kernel (a launch or two, after the warm-up
 # steps) of this script's own command. A changed source reports null.
 NCU_TRAFFIC = {
-    "dense": {
-        "mxfp8_quantize X row+col": {"bytes": 33610000, "src_sha": "60a437b5be6eb37a"},
-        "mxfp8_quantize W col": {"bytes": 20980000, "src_sha": "60a437b5be6eb37a"},
-        "nvfp4_quantize_per_token X": {"bytes": 33620000, "src_sha": "797c83c205b3c5dc"},
-        "nvfp4_quantize_weights W": {"bytes": 42030000, "src_sha": "01d4aff2498125b3"},
-        "block_scaled_gemm MXFP8": {"bytes": 57060000, "src_sha": "1530902a93df9546"},
-        "block_scaled_gemm NVFP4": {"bytes": 42040000, "src_sha": "1530902a93df9546"},
-        "dequantize_bf16 W": {"bytes": 5920000, "src_sha": "cfde21af131d287f"},
-    },
-    "weights": {
-        "nvfp4_quantize_weights gate_up": {"bytes": 1808570000, "src_sha": "01d4aff2498125b3"},
-        "nvfp4_quantize_weights down": {"bytes": 889070000, "src_sha": "01d4aff2498125b3"},
-    },
-    "quant": {
-        "mxfp8_quantize X row+col": {"bytes": 1081250000, "src_sha": "60a437b5be6eb37a"},
-        "nvfp4_quantize_per_token X": {"bytes": 676190000, "src_sha": "797c83c205b3c5dc"},
-    },
-    # per-token entries: the file's later change (the SwiGLU variant's launch bounds) leaves the
-    # per-token kernels' source as captured; the SwiGLU entry predates that change and reads null
-    "swiglu": {
-        "nvfp4_swiglu_quantize_per_token down input": {"bytes": 454590000, "src_sha": "e63b77614b08fbc6"},
+    # the weight quantizers: amax + encode launches of one call (check, finalize and zeroing move < 0.1 MB)
+    "moe": {
+        "nvfp4_quantize_per_token gate_up input": {"bytes": 669702912, "src_sha": "b8a0d1f96e2dd418"},
+        "nvfp4_quantize_weights gate_up": {"bytes": 1814151424, "src_sha": "01d4aff2498125b3"},
+        "block_scaled_gemm NVFP4 gate_up": {"bytes": 758652672, "src_sha": "7bb9e84f2d517b90"},
+        "nvfp4_swiglu_quantize_per_token down input": {"bytes": 447336704, "src_sha": "b8a0d1f96e2dd418"},
+        "nvfp4_quantize_weights down": {"bytes": 888688896, "src_sha": "01d4aff2498125b3"},
+        "block_scaled_gemm NVFP4 down": {"bytes": 662566400, "src_sha": "7bb9e84f2d517b90"},
     },
 }
 
@@ -777,8 +765,17 @@ def run_ours(args):
         h2d = sum(t.numel() * t.element_size() for t in host_in)
         d2h = sum(t.numel() * t.element_size() for t in host_out[0])
         groups = W.get("input_groups")
-        s_in, s_cmp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
-        ev_cmp, ev_out = [None, None], [None, None]
+        # host<->device copies split into 64 MiB pieces over COPY_STREAMS streams each way, so that
+        # several copy engines move one step's inputs and outputs at once
+        s_ins = [torch.cuda.Stream() for _ in range(COPY_STREAMS)]
+        s_outs = [torch.cuda.Stream() for _ in range(COPY_STREAMS)]
+        s_in, s_cmp, s_out = s_ins[0], torch.cuda.Stream(), s_outs[0]
+        ev_cmp, ev_out = [None, None], [[], []]
+
+        def pieces(dst, src):
+            a, b = dst.view(-1).view(torch.uint8), src.view(-1).view(torch.uint8)
+            step = 64 << 20
+            return [(a[o:o + step], b[o:o + step]) for o in range(0, a.numel(), step)]
 
         def run_step(j, din):
             if groups is None:
@@ -789,26 +786,35 @@ def run_ours(args):
 
         def e2e_step(i):
             j = i & 1
-            with torch.cuda.stream(s_in):
-                if ev_cmp[j] is not None:
-                    s_in.wait_event(ev_cmp[j])             # step i-2 has finished reading set j
-                for h, dv in zip(host_in, dev_in[j]):
-                    dv.copy_(h, non_blocking=True)
-                ev_in = torch.cuda.Event()
-                ev_in.record(s_in)
+            ev_ins = []
+            jobs = [pc for h, dv in zip(host_in, dev_in[j]) for pc in pieces(dv, h)]
+            for c, st in enumerate(s_ins):
+                with torch.cuda.stream(st):
+                    if ev_cmp[j] is not None:
+                        st.wait_event(ev_cmp[j])           # step i-2 has finished reading set j
+                    for dv, h in jobs[c::COPY_STREAMS]:
+                        dv.copy_(h, non_blocking=True)
+                    ev = torch.cuda.Event()
+                    ev.record(st)
+                    ev_ins.append(ev)
             with torch.cuda.stream(s_cmp):
-                s_cmp.wait_event(ev_in)
-                if ev_out[j] is not None:
-                    s_cmp.wait_event(ev_out[j])            # step i-2's outputs have been copied out
+                for ev in ev_ins:
+                    s_cmp.wait_event(ev)
+                for ev in ev_out[j]:
+                    s_cmp.wait_event(ev)                   # step i-2's outputs have been copied out
                 res = run_step(j, dev_in[j])
                 ev_cmp[j] = torch.cuda.Event()
                 ev_cmp[j].record(s_cmp)
-            with torch.cuda.stream(s_out):
-                s_out.wait_event(ev_cmp[j])
-                for o, h in zip(res, host_out[j]):
-                    h.copy_(o, non_blocking=True)
-                ev_out[j] = torch.cuda.Event()
-                ev_out[j].record(s_out)
+            jobs = [pc for o, h in zip(res, host_out[j]) for pc in pieces(h, o)]
+            ev_out[j] = []
+            for c, st in enumerate(s_outs):
+                with torch.cuda.stream(st):
+                    st.wait_event(ev_cmp[j])
+                    for h, o in jobs[c::COPY_STREAMS]:
+                        h.copy_(o, non_blocking=True)
+                    ev = torch.cuda.Event()
+                    ev.record(st)
+                    ev_out[j].append(ev)
 
         warm = max(2, args.warmup)
         for i in range(warm):
@@ -817,10 +823,14 @@ def run_ours(args):
         barrier()
         e2e_steps = min(args.steps, 100)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(s_in)
+        a.record(s_cmp)
+        for st in s_ins:
+            st.wait_event(a)                               # the timed copies start after a
         for i in range(warm, warm + e2e_steps):
             e2e_step(i)
-        b.record(s_out)                                    # after the last step's output copy
+        for ev in ev_out[(warm + e2e_steps - 1) & 1]:
+            s_cmp.wait_event(ev)
+        b.record(s_cmp)                                    # after the last step's output copies
         torch.cuda.synchronize()
         barrier()
         e2e_ms = max_over_ranks(a.elapsed_time(b), world, dev)
@@ -831,7 +841,8 @@ def run_ours(args):
         e2e = {"value": round(e2e_val, 2),
                "unit": W.get("unit", "TFLOPS"), "ms_per_step": round(e2e_ms / e2e_steps, 4), "steps": e2e_steps,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "pipelined": "3 streams: copy-in of step i+1, compute of step i, copy-out of step i-1"}
+               "pipelined": f"copy-in of step i+1 ({COPY_STREAMS} streams), compute of step i, copy-out of "
+                            f"step i-1 ({COPY_STREAMS} streams)"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
