@@ -129,6 +129,21 @@ def test_grouped_rows_any_offset(nvq, fmt, out, counts, K, N):
 
 
 @pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4"])
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+@pytest.mark.parametrize("counts,K,N", [
+    ([16, 9, 25, 0, 17, 130, 1, 40], 512, 384),    # a group of more than 128 rows: two row tiles
+    ([1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11, 12], 384, 256),
+    ([33] * 20, 1024, 640),                        # many tiles per CTA, 33 rows each (MMA N = 48)
+])
+def test_few_rows_per_group(nvq, fmt, out, counts, K, N):
+    # decode-like groups (at most 64 rows on average, one of them over 128), unpadded offsets that
+    # start anywhere inside the scale tiles
+    assert sum(counts) <= 64 * len(counts)
+    _run_m(nvq, fmt, counts, K, N, seed=sum(counts) + K + 3, out_type=nvq.OUT_F32 if out == "f32" else nvq.OUT_BF16,
+           align=1)
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4"])
 def test_explicit_offsets_with_gaps(nvq, fmt):
     # offsets [0, 1, 17, 50, 300] with fewer real rows than each segment holds (rows between the
     # groups' rows are zero and belong to the groups), then a second call with gaps left out
@@ -510,6 +525,12 @@ def test_bf16_grouped_rows(nvq, counts, K, N, out):
 def test_bf16_many_tiles_per_cta(nvq):
     # more tiles than CTAs: the stage ring wraps across tiles of different groups
     _bf16_m(nvq, [150, 33, 260, 0, 121, 97, 201, 64, 180, 5, 140, 230], 1024, 2560, seed=31, out_type=nvq.OUT_F32)
+
+
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_bf16_few_rows_per_group(nvq, out):
+    _bf16_m(nvq, [16, 9, 25, 0, 17, 130, 1, 40], 272, 384, seed=34,
+            out_type=nvq.OUT_F32 if out == "f32" else nvq.OUT_BF16, align=1)
 
 
 @pytest.mark.parametrize("out", ["f32", "bf16"])

@@ -75,3 +75,32 @@ def test_wait_that_runs_out_sets_status_and_frees_the_gpu(nvq, fmt, stage):
     assert int(status.item()) == nvq.DEV_OK
     err = np.abs(d.cpu().numpy().astype(np.float64) - D)
     assert (err <= 2e-3 * bound).all()
+
+
+@pytest.mark.parametrize("stage", [1, 4])
+def test_wait_that_runs_out_in_the_few_rows_per_group_layout(nvq, stage):
+    # 8 experts of 24 rows each: every tile starts inside a scale tile (the transposer's waits too)
+    E, rows, K, N = 8, 24, 1024, 256
+    rng = np.random.default_rng(40 + stage)
+    xb = oracle.f64_to_bf16_bits_rne(rng.standard_normal((E * rows, K)))
+    wb = oracle.f64_to_bf16_bits_rne(rng.standard_normal((E, K, N)) * 0.02)
+    qa, sfa, sa = nvq.nvfp4_quantize_per_token(workloads.from_bits(xb, "cuda"))
+    qb, sfb, sb = nvq.nvfp4_quantize_weights(workloads.from_bits(wb, "cuda").contiguous())
+    offs_np = np.arange(E + 1, dtype=np.int64) * rows
+    offs = torch.from_numpy(offs_np).cuda()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    call = (nvq.NVFP4, nvq.GEMM_GROUP_M, qa, sfa, qb, sfb, offs)
+    nvq.block_scaled_grouped_gemm(*call, m=E * rows, n=N, k=K, groups=E, s_a=sa, s_b=sb, out_type=nvq.OUT_F32,
+                                  status=status, wait_limit_ns=2_000_000, inject_timeout_stage=stage)
+    torch.cuda.synchronize()
+    assert int(status.item()) == nvq.DEV_TIMEOUT
+    status.zero_()
+    d = nvq.block_scaled_grouped_gemm(*call, m=E * rows, n=N, k=K, groups=E, s_a=sa, s_b=sb, out_type=nvq.OUT_F32,
+                                      status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == nvq.DEV_OK
+    q_r, sf_r, s_r = oracle.nvfp4_quantize_per_token(xb)
+    wq_r, wsf_r, ws_r = oracle.nvfp4_quantize_weights(wb)
+    b = np.stack([oracle.deq_operand("nvfp4", wq_r[e], wsf_r[e]) for e in range(E)])
+    D, bound = oracle.grouped_gemm_reference("m", oracle.deq_operand("nvfp4", q_r, sf_r), b, offs_np, s_r, ws_r)
+    assert (np.abs(d.cpu().numpy().astype(np.float64) - D) <= 2e-3 * bound).all()
