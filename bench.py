@@ -54,26 +54,30 @@ L2_FLUSH_BYTES = 256 << 20
 COPY_STREAMS = 4
 
 # ncu DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of the kernels timed
-# here, keyed by workload and kernel, with the sha256 of the source file the capture was taken
-# from; each figure comes from a capture of that one kernel (a launch or two, after the warm-up
-# steps) of this script's own command. A changed source reports null.
+# here, keyed by workload and kernel, with the sha256 of the source file (and the csrc headers) the
+# capture was taken from; each figure comes from a capture of that one kernel (a launch or two,
+# after the warm-up steps) of this script's own command. A changed source reports null.
 NCU_TRAFFIC = {
     # the weight quantizers: amax + encode launches of one call (check, finalize and zeroing move < 0.1 MB)
     "moe": {
-        "nvfp4_quantize_per_token gate_up input": {"bytes": 669702912, "src_sha": "b8a0d1f96e2dd418"},
-        "nvfp4_quantize_weights gate_up": {"bytes": 1814151424, "src_sha": "01d4aff2498125b3"},
-        "block_scaled_gemm NVFP4 gate_up": {"bytes": 758652672, "src_sha": "7bb9e84f2d517b90"},
-        "nvfp4_swiglu_quantize_per_token down input": {"bytes": 447336704, "src_sha": "b8a0d1f96e2dd418"},
-        "nvfp4_quantize_weights down": {"bytes": 888688896, "src_sha": "01d4aff2498125b3"},
-        "block_scaled_gemm NVFP4 down": {"bytes": 662566400, "src_sha": "7bb9e84f2d517b90"},
+        "nvfp4_quantize_per_token gate_up input": {"bytes": 668907008, "src_sha": "ebde99e2a08fc259"},
+        "nvfp4_quantize_weights gate_up": {"bytes": 1808085760, "src_sha": "a29b226b014f5c46"},
+        "block_scaled_gemm NVFP4 gate_up": {"bytes": 755845120, "src_sha": "0190987686acf6ff"},
+        "nvfp4_swiglu_quantize_per_token down input": {"bytes": 447070208, "src_sha": "ebde99e2a08fc259"},
+        "nvfp4_quantize_weights down": {"bytes": 888271360, "src_sha": "a29b226b014f5c46"},
+        "block_scaled_gemm NVFP4 down": {"bytes": 663325696, "src_sha": "0190987686acf6ff"},
     },
 }
 
 
 def _src_hash(name):
-    path = os.path.join(ROOT, "nvfp4_quantization_block_gb300", "csrc", name)
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """sha256 (16 hex digits) of a kernel's source file and of the csrc headers it may include."""
+    csrc = os.path.join(ROOT, "nvfp4_quantization_block_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in [name] + sorted(x for x in os.listdir(csrc) if x.endswith((".cuh", ".h"))):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
 
 
 def _load_peaks():

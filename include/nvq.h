@@ -100,7 +100,8 @@ nvq_status mxfp8_quantize(const void* x, int64_t rows, int64_t cols, int64_t ldx
  *   q      [rows, cols/2] packed codes (dense).
  *   sf     [rows, cols/16] scales, or MMA layout of that.
  *   s_tok  [rows] float32 coarse scales (decode multipliers: x ~ E2M1 * E4M3(sf) * s_tok).
- * Requires cols % 16 == 0. rows = 0 is a no-op.
+ * Requires cols % 16 == 0, cols <= 2^30 and rows <= 2^32 (NVQ_ERR_INVALID_ARG otherwise). rows = 0
+ * is a no-op.
  */
 nvq_status nvfp4_quantize_per_token(const void* x, int64_t rows, int64_t cols, int64_t ldx,
                                     uint8_t* q, uint8_t* sf, float* s_tok,
@@ -124,7 +125,8 @@ nvq_status nvfp4_quantize_per_token(const void* x, int64_t rows, int64_t cols, i
  *   gate_up  bf16 [rows, 2*cols], leading dimension ld (>= 2*cols, multiple of 8): gate in the
  *            first cols columns, up in the next cols.
  *   q, sf, s_tok  as nvfp4_quantize_per_token for h [rows, cols].
- * Requires cols % 16 == 0. Inputs whose SwiGLU overflows bf16 are outside the contract.
+ * Requires cols % 16 == 0, cols <= 2^30 and rows <= 2^32. Inputs whose SwiGLU overflows bf16 are
+ * outside the contract.
  */
 nvq_status nvfp4_swiglu_quantize_per_token(const void* gate_up, int64_t rows, int64_t cols, int64_t ld,
                                            uint8_t* q, uint8_t* sf, float* s_tok,

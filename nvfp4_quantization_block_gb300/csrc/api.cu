@@ -21,6 +21,10 @@ inline nvq_status from_cuda(cudaError_t e) { return e == cudaSuccess ? NVQ_OK : 
 
 inline bool valid_layout(nvq_sf_layout l) { return l == NVQ_SF_CANONICAL || l == NVQ_SF_MMA; }
 
+// per-token quantizers: block counts per row fit an int, and the grid (4 rows per CTA) fits its x limit
+constexpr int64_t NVQ_TOKEN_MAX_COLS = int64_t(1) << 30;
+constexpr int64_t NVQ_TOKEN_MAX_ROWS = int64_t(1) << 32;
+
 }  // namespace
 
 extern "C" {
@@ -71,6 +75,7 @@ nvq_status nvfp4_quantize_per_token(const void* x, int64_t rows, int64_t cols, i
     if (rows == 0) return NVQ_OK;
     if (x == nullptr || q == nullptr || sf == nullptr || s_tok == nullptr) return NVQ_ERR_INVALID_ARG;
     if (cols == 0 || cols % 16 || ldx < cols) return NVQ_ERR_INVALID_ARG;
+    if (cols > NVQ_TOKEN_MAX_COLS || rows > NVQ_TOKEN_MAX_ROWS) return NVQ_ERR_INVALID_ARG;
     if (!aligned16(x) || ldx % 8 || !aligned16(q) || !aligned16(sf) || !aligned16(s_tok))
         return NVQ_ERR_MISALIGNED;
     return from_cuda(nvq::launch_nvfp4_quantize_per_token(static_cast<const uint16_t*>(x), rows, cols, ldx, q,
@@ -85,6 +90,7 @@ nvq_status nvfp4_swiglu_quantize_per_token(const void* gate_up, int64_t rows, in
     if (rows == 0) return NVQ_OK;
     if (gate_up == nullptr || q == nullptr || sf == nullptr || s_tok == nullptr) return NVQ_ERR_INVALID_ARG;
     if (cols == 0 || cols % 16 || ld < 2 * cols) return NVQ_ERR_INVALID_ARG;
+    if (cols > NVQ_TOKEN_MAX_COLS || rows > NVQ_TOKEN_MAX_ROWS) return NVQ_ERR_INVALID_ARG;
     if (!aligned16(gate_up) || ld % 8 || !aligned16(q) || !aligned16(sf) || !aligned16(s_tok))
         return NVQ_ERR_MISALIGNED;
     return from_cuda(nvq::launch_nvfp4_swiglu_quantize(static_cast<const uint16_t*>(gate_up), rows, cols, ld, q, sf,

@@ -168,87 +168,96 @@ __device__ __forceinline__ void row_block(const uint16_t* p, int64_t up, uint4& 
     }
 }
 
-// Where one token row's outputs go: its packed codes and its scale bytes (canonical row, or the
-// row's place in the MMA tile layout, to which a 4-block group adds (kb / 4) * 512).
-struct TokenRowOut {
-    uint8_t* q;          // row of packed codes
-    uint8_t* sf;         // canonical: row of scale bytes; MMA: row's base inside its tile column
-    int64_t nkb;
-    int mma_layout;
+// Where one lane's outputs of one token row go: the lane holds blocks l, l + LPR, l + 2 LPR, ...
+// of the row (step i: block i LPR + l), with their packed codes at q + i LPR 8 and their scale
+// bytes at sf + i sf_step (canonical rows: consecutive bytes; MMA layout: the row's place in its
+// tile column, LPR / 4 tile columns further per step).
+struct TokenLaneOut {
+    uint8_t* q;          // codes of the lane's block of step 0
+    uint8_t* sf;         // scale byte of the lane's block of step 0, or nullptr (row not covered)
+    int sf_step;
+    int nkb_lane;        // the row's blocks from block l on: step i holds codes when i LPR < nkb_lane
+    int nsf_lane;        // the same for scale bytes (MMA layout: up to the padded multiple of 4 blocks,
+                         // whose padding bytes are the zero codes of the zero blocks beyond the row)
 };
 
-// Stores of one 16-element block kb of the row (codes c0, c1, scale code sfc), one block per lane:
-// the four lanes l..l+3 (l a multiple of 4 within the row's lanes) hold four consecutive blocks and
-// share one scale word. Called by all 32 lanes of the warp together (shuffles).
-__device__ __forceinline__ void token_store(uint32_t sfc, uint32_t c0, uint32_t c1, int64_t kb, int l, bool real,
-                                            const TokenRowOut& o) {
-    if (real && kb < o.nkb) *reinterpret_cast<uint2*>(o.q + kb * 8) = make_uint2(c0, c1);
-    const uint32_t s1 = __shfl_down_sync(0xffffffffu, sfc, 1);
-    const uint32_t s2 = __shfl_down_sync(0xffffffffu, sfc, 2);
-    const uint32_t s3 = __shfl_down_sync(0xffffffffu, sfc, 3);
-    if ((l & 3) == 0 && kb < o.nkb && o.sf != nullptr) {
-        const uint32_t word = sfc | (s1 << 8) | (s2 << 16) | (s3 << 24);
-        if (o.mma_layout) {
-            *reinterpret_cast<uint32_t*>(o.sf + ((kb >> 2) << 9)) = word;
-        } else {
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                if (kb + j < o.nkb) o.sf[kb + j] = (uint8_t)(word >> (8 * j));
-        }
-    }
+// Stores of the lane's block of step i (codes c0, c1, scale code sfc); each lane stores its own
+// scale byte (the four bytes of a scale word come from four neighbouring lanes in one instruction).
+template <int LPR>
+__device__ __forceinline__ void token_store(uint32_t sfc, uint32_t c0, uint32_t c1, int i, bool real,
+                                            const TokenLaneOut& o) {
+    if (real && i * LPR < o.nkb_lane) *reinterpret_cast<uint2*>(o.q + (int64_t)i * LPR * 8) = make_uint2(c0, c1);
+    if (o.sf != nullptr && i * LPR < o.nsf_lane) o.sf[(int64_t)i * o.sf_step] = (uint8_t)sfc;
 }
 
 // Encode and store one block; the encoding mode is the same for every lane.
-template <int MODE>
-__device__ __forceinline__ void token_block(const uint4& a, const uint4& b, uint32_t mb, int64_t kb, int l, bool real,
+template <int MODE, int LPR>
+__device__ __forceinline__ void token_block(const uint4& a, const uint4& b, uint32_t mb, int i, bool real,
                                             const Nvfp4Scope& sc, const Nvfp4Table& T, const Nvfp4CodeInfo& I,
-                                            const TokenRowOut& o) {
+                                            const TokenLaneOut& o) {
     uint32_t c0, c1;
     const uint32_t sfc = encode_block<MODE>(a, b, mb, sc, T, I, c0, c1);
-    token_store(sfc, c0, c1, kb, l, real, o);
+    token_store<LPR>(sfc, c0, c1, i, real, o);
 }
 
-// Encode and store one block when the two rows of a warp may take different paths: the encoding
-// branches per row, the stores (shuffles) run with the whole warp.
-__device__ __forceinline__ void token_block_mixed(const uint4& a, const uint4& b, uint32_t mb, int64_t kb, int l,
-                                                  bool real, int mode, const Nvfp4Scope& sc, const Nvfp4Table& T,
-                                                  const Nvfp4CodeInfo& I, const TokenRowOut& o) {
+// Encode and store one block when the two rows of a warp may take different paths.
+template <int LPR>
+__device__ __forceinline__ void token_block_mixed(const uint4& a, const uint4& b, uint32_t mb, int i, bool real,
+                                                  int mode, const Nvfp4Scope& sc, const Nvfp4Table& T,
+                                                  const Nvfp4CodeInfo& I, const TokenLaneOut& o) {
     uint32_t c0, c1, sfc;
     if (mode == ENC_PRODUCT) sfc = encode_block<ENC_PRODUCT>(a, b, mb, sc, T, I, c0, c1);
     else if (mode == ENC_TABLE) sfc = encode_block<ENC_TABLE>(a, b, mb, sc, T, I, c0, c1);
     else sfc = encode_block<ENC_EXACT>(a, b, mb, sc, T, I, c0, c1);
-    __syncwarp();
-    token_store(sfc, c0, c1, kb, l, real, o);
+    token_store<LPR>(sfc, c0, c1, i, real, o);
 }
 
-// The scope table of a row built by its LPR lanes (32: nvfp4_table_build_warp, with the product
-// path's check; 16: each lane takes the class boundaries of thresholds j and j + 2 (and their
-// j + 4 partners) of class l & 7, and the block-scale boundary of code l). Called by all 32 lanes of
-// the warp together; returns whether the lane's class has a product-path multiplier. Rows of 16
-// lanes never take the product path: with at most four blocks per lane, the check (five candidate
-// multipliers at up to four boundaries per lane) costs more than it saves (measured: the MoE down
-// projection's 768-wide rows and the SwiGLU rows ran 7% and 17% slower with it).
-template <int LPR>
+// The scope table of a row built by its LPR lanes, with the product path's multipliers (32:
+// nvfp4_table_build_warp; 16: lane l takes thresholds j = (l >> 3) + 2t, t = 0, 1, of class l & 7
+// and their j + 4 partners, and the block-scale boundary of code l; a class's two lanes are l and
+// l ^ 8 of the same half-warp). Called by all 32 lanes of the warp together; returns whether the
+// lane's class has a product-path multiplier. SwiGLU rows of 16 lanes skip the search and take the
+// boundary comparison: with three blocks per lane the search costs them more than it saves
+// (131072 x 768 SwiGLU rows: 0.175 ms without it, 0.181 with it; plain 768-wide rows: 0.076 ms
+// without, 0.072 with).
+template <int LPR, bool SEARCH>
 __device__ __forceinline__ bool nvfp4_table_build_row(Nvfp4Table& T, float s, int l) {
     if (LPR == 32) return nvfp4_table_build_warp(T, s, l);
-    const uint32_t f = (uint32_t)l & 7u;
+    const uint32_t f = (uint32_t)l & 7u, jb = (uint32_t)l >> 3;
     const float v = (float)(8u + f) * 0x1p-9f;                     // value of E4M3 code 8 + f
+    const uint32_t g0 = nvfp4_class_g0(v, s);
+    uint32_t bd[4];                                                // thresholds jb, jb + 4, jb + 2, jb + 6
 #pragma unroll
     for (uint32_t t = 0; t < 2; ++t) {
-        const uint32_t j = ((uint32_t)l >> 3) + 2u * t;            // 0..3
-        uint32_t b = bf16_boundary((float)(2u * j + 1u) * 0.25f * v, s, (j & 1u) != 0u);
+        const uint32_t j = jb + 2u * t;                            // 0..3
+        const uint32_t b = bf16_boundary((float)(2u * j + 1u) * 0.25f * v, s, (j & 1u) != 0u);
         T.bp[f][j] = b | (b << 16);
         if (j < 3u) T.bp[f][8u + j] = (b | (b << 16)) ^ 0x80008000u;
+        bd[2 * t] = b;
+        bd[2 * t + 1] = 0u;
         const uint32_t j2 = j + 4u;
         if (j2 < 7u) {
             const float m = (j2 == 6u) ? 5.0f : (float)j2 - 1.5f;
-            b = bf16_boundary(m * v, s, (j2 & 1u) != 0u);
-            T.bp[f][j2] = b | (b << 16);
+            const uint32_t b2 = bf16_boundary(m * v, s, (j2 & 1u) != 0u);
+            T.bp[f][j2] = b2 | (b2 << 16);
+            bd[2 * t + 1] = b2;
         }
     }
+    const uint32_t g = !SEARCH ? 0u : nvfp4_search_multiplier(g0, [&](uint32_t gk) {
+        uint32_t m = 0u;
+#pragma unroll
+        for (uint32_t t = 0; t < 2; ++t) {
+            const uint32_t j = jb + 2u * t;
+            m |= nvfp4_product_miss(bd[2 * t], j, __uint_as_float(gk));
+            if (j + 4u < 7u) m |= nvfp4_product_miss(bd[2 * t + 1], j + 4u, __uint_as_float(gk));
+        }
+        return m | __shfl_xor_sync(0xffffffffu, m, 8);
+    });
     T.bs[l] = bf16_boundary((float)(3 * (2 * l + 1)) * 0x1p-9f, s, (l & 1) != 0);
     if (l < 12) T.bp[8][l] = l < 7 ? 0x7F007F00u : (l >= 8 && l < 11 ? 0xFF00FF00u : 0u);
-    return false;
+    if (l < 8) T.g[l] = g;
+    if (l == 8) T.g[8] = 0u;
+    return g != 0u;
 }
 
 // LPR lanes per token row (32: one row per warp; 16: two rows per warp, for rows of at most 64
@@ -280,7 +289,8 @@ nvfp4_token_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t C, int64_t
     const bool real = row < R;
     const int64_t nkb = C >> 4;                                // 16-element blocks
     const int iters = (int)((nkb + LPR - 1) / LPR);
-    const uint16_t* xr = x + (real ? row : 0) * ldx;
+    const int nkb_lane = (int)(nkb - l);                       // step i holds a block when i LPR < nkb_lane
+    const uint16_t* xl = x + (real ? row : 0) * ldx + l * 16;  // the lane's block of step 0
 
     // pass 1: load (into registers where possible) and reduce the row's amax
     uint4 va[TOK_NREG], vb[TOK_NREG];
@@ -289,17 +299,15 @@ nvfp4_token_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t C, int64_t
 #pragma unroll
     for (int i = 0; i < TOK_NREG; ++i) {
         va[i] = vb[i] = make_uint4(0u, 0u, 0u, 0u);
-        const int64_t kb = (int64_t)i * LPR + l;
-        if (real && i < iters && kb < nkb) row_block<V8, SWIGLU>(xr + kb * 16, C, va[i], vb[i]);
-        mbk[i] = max(absmax_bits_8(va[i]), absmax_bits_8(vb[i]));
+        if (real && i * LPR < nkb_lane) row_block<V8, SWIGLU>(xl + i * LPR * 16, C, va[i], vb[i]);
+        mbk[i] = absmax_bits_16(va[i], vb[i]);
         m = max(m, mbk[i]);
     }
     for (int i = TOK_NREG; i < iters; ++i) {
-        const int64_t kb = (int64_t)i * LPR + l;
-        if (real && kb < nkb) {
+        if (real && i * LPR < nkb_lane) {
             uint4 a, b;
-            row_block<V8, SWIGLU>(xr + kb * 16, C, a, b);
-            m = max(m, max(absmax_bits_8(a), absmax_bits_8(b)));
+            row_block<V8, SWIGLU>(xl + (int64_t)i * LPR * 16, C, a, b);
+            m = max(m, absmax_bits_16(a, b));
         }
     }
 #pragma unroll
@@ -308,45 +316,43 @@ nvfp4_token_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t C, int64_t
     const Nvfp4Scope sc = make_nvfp4_scope(s);
     if (real && l == 0) s_tok[row] = s;
     // every row builds a table (all lanes take part in its shuffles); an exact-path row ignores it
-    const bool ok = nvfp4_table_build_row<LPR>(T, s, l);
+    constexpr bool SEARCH = LPR == 32 || !SWIGLU;              // rows that may take the product path
+    const bool ok = nvfp4_table_build_row<LPR, SEARCH>(T, s, l);
     __syncwarp();
     const uint32_t bad = __ballot_sync(0xffffffffu, !ok);
     const uint32_t row_bad = LPR == 32 ? bad : (bad >> (half * LPR)) & ((1u << LPR) - 1u);
-    const int mode = sc.exact ? ENC_EXACT : ((LPR == 32 && row_bad == 0u) ? ENC_PRODUCT : ENC_TABLE);
+    const int mode = sc.exact ? ENC_EXACT : ((SEARCH && row_bad == 0u) ? ENC_PRODUCT : ENC_TABLE);
 
     // pass 2: per 1x16 block scale and codes (register-resident blocks first, then any reloads)
-    TokenRowOut o;
-    o.q = q + (real ? row : 0) * (C >> 1);
-    o.nkb = nkb;
-    o.mma_layout = mma_layout;
-    o.sf = !covered ? nullptr : (mma_layout ? sf + mma_sf_offset(row, 0, nkb) : sf + row * nkb);
+    TokenLaneOut o;
+    o.q = q + (real ? row : 0) * (C >> 1) + l * 8;
+    o.nkb_lane = nkb_lane;
+    o.nsf_lane = (int)((mma_layout ? (nkb + 3) & ~int64_t(3) : nkb) - l);
+    o.sf = !covered ? nullptr : (mma_layout ? sf + mma_sf_offset(row, l, nkb) : sf + row * nkb + l);
+    o.sf_step = mma_layout ? (LPR / 4) * 512 : LPR;
     const uint32_t same = __match_any_sync(0xffffffffu, mode);
     if (same == 0xffffffffu && mode == ENC_PRODUCT) {
 #pragma unroll
         for (int i = 0; i < TOK_NREG; ++i)
-            if (i < iters)
-                token_block<ENC_PRODUCT>(va[i], vb[i], mbk[i], (int64_t)i * LPR + l, l, real, sc, T, info, o);
+            if (i < iters) token_block<ENC_PRODUCT, LPR>(va[i], vb[i], mbk[i], i, real, sc, T, info, o);
     } else if (same == 0xffffffffu && mode == ENC_TABLE) {
 #pragma unroll
         for (int i = 0; i < TOK_NREG; ++i)
-            if (i < iters) token_block<ENC_TABLE>(va[i], vb[i], mbk[i], (int64_t)i * LPR + l, l, real, sc, T, info, o);
+            if (i < iters) token_block<ENC_TABLE, LPR>(va[i], vb[i], mbk[i], i, real, sc, T, info, o);
     } else if (same == 0xffffffffu) {
 #pragma unroll
         for (int i = 0; i < TOK_NREG; ++i)
-            if (i < iters) token_block<ENC_EXACT>(va[i], vb[i], mbk[i], (int64_t)i * LPR + l, l, real, sc, T, info, o);
+            if (i < iters) token_block<ENC_EXACT, LPR>(va[i], vb[i], mbk[i], i, real, sc, T, info, o);
     } else {
         // the two rows of the warp take different modes
 #pragma unroll
         for (int i = 0; i < TOK_NREG; ++i)
-            if (i < iters)
-                token_block_mixed(va[i], vb[i], mbk[i], (int64_t)i * LPR + l, l, real, mode, sc, T, info, o);
+            if (i < iters) token_block_mixed<LPR>(va[i], vb[i], mbk[i], i, real, mode, sc, T, info, o);
     }
     for (int i = TOK_NREG; i < iters; ++i) {
-        const int64_t kb = (int64_t)i * LPR + l;
         uint4 a = make_uint4(0u, 0u, 0u, 0u), b = a;
-        if (real && kb < nkb) row_block<V8, SWIGLU>(xr + kb * 16, C, a, b);
-        const uint32_t mb = max(absmax_bits_8(a), absmax_bits_8(b));
-        token_block_mixed(a, b, mb, kb, l, real, mode, sc, T, info, o);
+        if (real && i * LPR < nkb_lane) row_block<V8, SWIGLU>(xl + (int64_t)i * LPR * 16, C, a, b);
+        token_block_mixed<LPR>(a, b, absmax_bits_16(a, b), i, real, mode, sc, T, info, o);
     }
 }
 

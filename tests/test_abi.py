@@ -74,6 +74,8 @@ def test_host_validation_rejects_before_launch(lib):
     assert t(fake, 4, 40, 40, fake, fake, fake, 0, None) == 1                 # cols % 16
     assert t(fake, 4, 64, 64, fake, fake, None, 0, None) == 1                 # missing s_tok
     assert t(fake, 0, 64, 64, None, None, None, 0, None) == 0
+    assert t(fake, 4, (1 << 30) + 16, (1 << 30) + 16, fake, fake, fake, 0, None) == 1   # cols > 2^30
+    assert t(fake, (1 << 32) + 1, 64, 64, fake, fake, fake, 0, None) == 1               # rows > 2^32
     sw = lib.nvfp4_swiglu_quantize_per_token
     sw.argtypes = [vp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, vp, vp, vp, ctypes.c_int, vp]
     sw.restype = ctypes.c_int
@@ -81,6 +83,7 @@ def test_host_validation_rejects_before_launch(lib):
     assert sw(fake, 4, 64, 100, fake, fake, fake, 0, None) == 1    # ld < 2 cols
     assert sw(fake, 4, 64, 132, fake, fake, fake, 0, None) == 2    # ld % 8
     assert sw(fake, 0, 64, 128, None, None, None, 0, None) == 0    # empty is a no-op
+    assert sw(fake, 4, (1 << 30) + 16, (1 << 31) + 32, fake, fake, fake, 0, None) == 1   # cols > 2^30
     nw = lib.nvfp4_quantize_weights
     nw.argtypes = [vp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, vp, vp, vp, ctypes.c_int, vp]
     nw.restype = ctypes.c_int

@@ -181,3 +181,75 @@ def test_the_check_catches_a_wrong_multiplier():
         if not np.array_equal(_prod_mag(x, g_off), ex):
             bad += 1
     assert bad > 0
+
+
+def _class_pairs(f, s):
+    v = (8 + f) * 2.0 ** -9
+    x, _ = _bf16_window(v * float(s) * 2.0 ** -4, v * float(s) * 2.0 ** 4)
+    ex = _exact_mag(x, v, s)
+    pairs = []
+    for j in range(7):
+        i = int(np.argmax(ex > j))
+        pairs.append((j, x[i], x[i - 1]))
+    return pairs
+
+
+def _miss(pairs, g):
+    # bit 0: some boundary's product keeps its code at or below the threshold (g too small);
+    # bit 1: some value just below a boundary gets a code above it (g too large)
+    m = 0
+    for j, b, below in pairs:
+        if _prod_mag(np.array([b]), g)[0] <= j:
+            m |= 1
+        if _prod_mag(np.array([below]), g)[0] > j:
+            m |= 2
+    return m
+
+
+def _directed_multiplier(f, s):
+    """The kernels' search as they run it: candidate 0, then up to two steps (1 and 2 ulps) towards
+    the side it missed on, stopping at the first pass or at a miss on the other side."""
+    v = (8 + f) * 2.0 ** -9
+    g0 = _class_g0(v, s)
+    if g0 == 0:
+        return None
+    pairs = _class_pairs(f, s)
+    m0 = _miss(pairs, g0)
+    if m0 == 0:
+        return g0
+    if m0 == 3:
+        return None
+    step = 1 if m0 == 1 else -1
+    for k in (1, 2):
+        g = np.array(int(np.array(g0, dtype=F32).view(np.uint32)) + k * step, dtype=np.uint32).view(F32)
+        mk = _miss(pairs, g)
+        if mk == 0:
+            return g
+        if mk != m0:
+            return None
+    return None
+
+
+@pytest.mark.parametrize("kind,seed", [("random", 11), ("amax", 12), ("amax", 13)])
+def test_directed_search_picks_the_first_passing_candidate(kind, seed):
+    # the candidates that pass form one run around RN(1 / RN(v s)) (both codes are monotone in g),
+    # so stepping away from the side candidate 0 misses on finds what the order 0, -1, +1, -2, +2 finds
+    scopes = _random_scopes(12, seed) if kind == "random" else _amax_scopes(24, seed)
+    moved = 0
+    for s in scopes:
+        for f in range(8):
+            want = _class_multiplier(f, s)
+            got = _directed_multiplier(f, s)
+            assert (want is None) == (got is None), (float(s), f)
+            if want is not None:
+                assert F32(want) == F32(got), (float(s), f)
+                moved += F32(want) != _class_g0((8 + f) * 2.0 ** -9, s)
+            # the passing candidates are consecutive
+            g0 = _class_g0((8 + f) * 2.0 ** -9, s)
+            if g0 != 0:
+                pairs = _class_pairs(f, s)
+                ok = [_miss(pairs, _candidate(g0, c)) == 0 for c in (3, 1, 0, 2, 4)]   # -2 .. +2
+                runs = sum(1 for i in range(5) if ok[i] and (i == 0 or not ok[i - 1]))
+                assert runs <= 1, (float(s), f, ok)
+    if kind == "amax":
+        assert moved > 0                     # scopes of bf16 maxima do need the steps
