@@ -79,7 +79,8 @@ __device__ __forceinline__ uint32_t swiglu2_fast(uint32_t g, uint32_t u, bool& r
     constexpr float L2E = (float)1.4426950408889634, LN2_HI = 0.693145751953125f;
     constexpr float LN2_LO = (float)(0.6931471805599453 - 0.693145751953125), MAGIC = 12582912.0f;
     const uint32_t xw = g ^ 0x80008000u;                       // x = -g, both halves
-    const float x0 = fminf(fmaxf(bf16_lo(xw), -87.0f), 300.0f), x1 = fminf(fmaxf(bf16_hi(xw), -87.0f), 300.0f);
+    // (no upper clamp here: an element with x > 87 sends its block to the exact steps anyway)
+    const float x0 = fmaxf(bf16_lo(xw), -87.0f), x1 = fmaxf(bf16_hi(xw), -87.0f);
     float t0, t1, m0, m1, n0, n1, a0, a1, r0, r1;
     f2_mul(t0, t1, x0, x1, L2E, L2E);
     f2_add(m0, m1, t0, t1, MAGIC, MAGIC);                      // 1.5 * 2^23 + n: n in the low mantissa bits
@@ -170,12 +171,11 @@ __device__ __forceinline__ void row_block(const uint16_t* p, int64_t up, uint4& 
 
 // Where one lane's outputs of one token row go: the lane holds blocks l, l + LPR, l + 2 LPR, ...
 // of the row (step i: block i LPR + l), with their packed codes at q + i LPR 8 and their scale
-// bytes at sf + i sf_step (canonical rows: consecutive bytes; MMA layout: the row's place in its
+// bytes at sf + i SF_STEP (canonical rows: consecutive bytes; MMA layout: the row's place in its
 // tile column, LPR / 4 tile columns further per step).
 struct TokenLaneOut {
     uint8_t* q;          // codes of the lane's block of step 0
     uint8_t* sf;         // scale byte of the lane's block of step 0, or nullptr (row not covered)
-    int sf_step;
     int nkb_lane;        // the row's blocks from block l on: step i holds codes when i LPR < nkb_lane
     int nsf_lane;        // the same for scale bytes (MMA layout: up to the padded multiple of 4 blocks,
                          // whose padding bytes are the zero codes of the zero blocks beyond the row)
@@ -183,25 +183,28 @@ struct TokenLaneOut {
 
 // Stores of the lane's block of step i (codes c0, c1, scale code sfc); each lane stores its own
 // scale byte (the four bytes of a scale word come from four neighbouring lanes in one instruction).
-template <int LPR>
+// FULL: every lane of the warp has a block at every step taken, in a real row (no guards).
+template <int LPR, bool FULL, bool MMA>
 __device__ __forceinline__ void token_store(uint32_t sfc, uint32_t c0, uint32_t c1, int i, bool real,
                                             const TokenLaneOut& o) {
-    if (real && i * LPR < o.nkb_lane) *reinterpret_cast<uint2*>(o.q + (int64_t)i * LPR * 8) = make_uint2(c0, c1);
-    if (o.sf != nullptr && i * LPR < o.nsf_lane) o.sf[(int64_t)i * o.sf_step] = (uint8_t)sfc;
+    constexpr int SF_STEP = MMA ? (LPR / 4) * 512 : LPR;
+    if (FULL || (real && i * LPR < o.nkb_lane))
+        *reinterpret_cast<uint2*>(o.q + (int64_t)i * LPR * 8) = make_uint2(c0, c1);
+    if (FULL || (o.sf != nullptr && i * LPR < o.nsf_lane)) o.sf[(int64_t)i * SF_STEP] = (uint8_t)sfc;
 }
 
 // Encode and store one block; the encoding mode is the same for every lane.
-template <int MODE, int LPR>
+template <int MODE, int LPR, bool FULL, bool MMA>
 __device__ __forceinline__ void token_block(const uint4& a, const uint4& b, uint32_t mb, int i, bool real,
                                             const Nvfp4Scope& sc, const Nvfp4Table& T, const Nvfp4CodeInfo& I,
                                             const TokenLaneOut& o) {
     uint32_t c0, c1;
     const uint32_t sfc = encode_block<MODE>(a, b, mb, sc, T, I, c0, c1);
-    token_store<LPR>(sfc, c0, c1, i, real, o);
+    token_store<LPR, FULL, MMA>(sfc, c0, c1, i, real, o);
 }
 
 // Encode and store one block when the two rows of a warp may take different paths.
-template <int LPR>
+template <int LPR, bool FULL, bool MMA>
 __device__ __forceinline__ void token_block_mixed(const uint4& a, const uint4& b, uint32_t mb, int i, bool real,
                                                   int mode, const Nvfp4Scope& sc, const Nvfp4Table& T,
                                                   const Nvfp4CodeInfo& I, const TokenLaneOut& o) {
@@ -209,7 +212,7 @@ __device__ __forceinline__ void token_block_mixed(const uint4& a, const uint4& b
     if (mode == ENC_PRODUCT) sfc = encode_block<ENC_PRODUCT>(a, b, mb, sc, T, I, c0, c1);
     else if (mode == ENC_TABLE) sfc = encode_block<ENC_TABLE>(a, b, mb, sc, T, I, c0, c1);
     else sfc = encode_block<ENC_EXACT>(a, b, mb, sc, T, I, c0, c1);
-    token_store<LPR>(sfc, c0, c1, i, real, o);
+    token_store<LPR, FULL, MMA>(sfc, c0, c1, i, real, o);
 }
 
 // The scope table of a row built by its LPR lanes, with the product path's multipliers (32:
@@ -260,33 +263,14 @@ __device__ __forceinline__ bool nvfp4_table_build_row(Nvfp4Table& T, float s, in
     return g != 0u;
 }
 
-// LPR lanes per token row (32: one row per warp; 16: two rows per warp, for rows of at most 64
-// blocks, so that rows of 48 blocks keep every lane busy), one 16-element block per lane per step:
-// the row is loaded once with 32-byte coalesced loads (held in registers up to TOK_NREG steps),
-// reduced to its amax with shuffles among the row's lanes, and encoded from registers, so each
-// input byte is read from HBM once.
-template <bool V8, bool SWIGLU, int LPR>
-// 6 CTAs per SM (80 registers, no spills; 24 warps keep enough row loads in flight: 131072 x 2048
-// rows 0.218 ms at 142 registers, 0.179 at 128, 0.158 at 96, 0.146 at 80); the SwiGLU variant keeps
-// 5 (96 registers; at 80 it spills).
-__global__ void __launch_bounds__(TOK_THREADS, SWIGLU ? 5 : 6)
-nvfp4_token_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t C, int64_t ldx,
-                   uint8_t* __restrict__ q, uint8_t* __restrict__ sf, float* __restrict__ s_tok,
-                   int mma_layout, int64_t rows_cover) {
-    griddep_begin();
-    constexpr int RPW = 32 / LPR;                              // rows per warp
-    __shared__ Nvfp4Table tables[(TOK_THREADS / 32) * RPW];   // one per row
-    __shared__ Nvfp4CodeInfo info;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int half = lane / LPR, l = lane % LPR;               // row of the warp, lane within the row
-    for (uint32_t c = threadIdx.x; c < 128u; c += TOK_THREADS) nvfp4_code_info_build(info, c);
-    __syncthreads();
-    const int64_t row0 = ((int64_t)blockIdx.x * (TOK_THREADS / 32) + warp) * RPW;
-    if (row0 >= rows_cover) return;                            // uniform over the warp
-    const int64_t row = row0 + half;
-    const bool covered = row < rows_cover;                     // the second row of a warp may not be
-    Nvfp4Table& T = tables[warp * RPW + half];
-    const bool real = row < R;
+// The rows of one warp (LPR lanes each), from their loads to their stores. FULL: every row of the
+// warp is real and every lane has a block at each of the row's steps (the block count a multiple of
+// LPR, at most TOK_NREG steps), so no load or store needs a guard.
+template <bool V8, bool SWIGLU, int LPR, bool FULL, bool MMA>
+__device__ __forceinline__ void token_rows(const uint16_t* __restrict__ x, int64_t C, int64_t ldx,
+                                           uint8_t* __restrict__ q, uint8_t* __restrict__ sf,
+                                           float* __restrict__ s_tok, int64_t row, bool covered, bool real,
+                                           int l, int half, Nvfp4Table& T, const Nvfp4CodeInfo& info) {
     const int64_t nkb = C >> 4;                                // 16-element blocks
     const int iters = (int)((nkb + LPR - 1) / LPR);
     const int nkb_lane = (int)(nkb - l);                       // step i holds a block when i LPR < nkb_lane
@@ -298,16 +282,22 @@ nvfp4_token_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t C, int64_t
     uint32_t m = 0;
 #pragma unroll
     for (int i = 0; i < TOK_NREG; ++i) {
-        va[i] = vb[i] = make_uint4(0u, 0u, 0u, 0u);
-        if (real && i * LPR < nkb_lane) row_block<V8, SWIGLU>(xl + i * LPR * 16, C, va[i], vb[i]);
+        if (FULL && i < iters) {
+            row_block<V8, SWIGLU>(xl + i * LPR * 16, C, va[i], vb[i]);
+        } else {
+            va[i] = vb[i] = make_uint4(0u, 0u, 0u, 0u);
+            if (!FULL && real && i * LPR < nkb_lane) row_block<V8, SWIGLU>(xl + i * LPR * 16, C, va[i], vb[i]);
+        }
         mbk[i] = absmax_bits_16(va[i], vb[i]);
         m = max(m, mbk[i]);
     }
-    for (int i = TOK_NREG; i < iters; ++i) {
-        if (real && i * LPR < nkb_lane) {
-            uint4 a, b;
-            row_block<V8, SWIGLU>(xl + (int64_t)i * LPR * 16, C, a, b);
-            m = max(m, absmax_bits_16(a, b));
+    if (!FULL) {
+        for (int i = TOK_NREG; i < iters; ++i) {
+            if (real && i * LPR < nkb_lane) {
+                uint4 a, b;
+                row_block<V8, SWIGLU>(xl + (int64_t)i * LPR * 16, C, a, b);
+                m = max(m, absmax_bits_16(a, b));
+            }
         }
     }
 #pragma unroll
@@ -327,33 +317,70 @@ nvfp4_token_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t C, int64_t
     TokenLaneOut o;
     o.q = q + (real ? row : 0) * (C >> 1) + l * 8;
     o.nkb_lane = nkb_lane;
-    o.nsf_lane = (int)((mma_layout ? (nkb + 3) & ~int64_t(3) : nkb) - l);
-    o.sf = !covered ? nullptr : (mma_layout ? sf + mma_sf_offset(row, l, nkb) : sf + row * nkb + l);
-    o.sf_step = mma_layout ? (LPR / 4) * 512 : LPR;
+    o.nsf_lane = (int)((MMA ? (nkb + 3) & ~int64_t(3) : nkb) - l);
+    o.sf = !covered ? nullptr : (MMA ? sf + mma_sf_offset(row, l, nkb) : sf + row * nkb + l);
     const uint32_t same = __match_any_sync(0xffffffffu, mode);
     if (same == 0xffffffffu && mode == ENC_PRODUCT) {
 #pragma unroll
         for (int i = 0; i < TOK_NREG; ++i)
-            if (i < iters) token_block<ENC_PRODUCT, LPR>(va[i], vb[i], mbk[i], i, real, sc, T, info, o);
+            if (i < iters) token_block<ENC_PRODUCT, LPR, FULL, MMA>(va[i], vb[i], mbk[i], i, real, sc, T, info, o);
     } else if (same == 0xffffffffu && mode == ENC_TABLE) {
 #pragma unroll
         for (int i = 0; i < TOK_NREG; ++i)
-            if (i < iters) token_block<ENC_TABLE, LPR>(va[i], vb[i], mbk[i], i, real, sc, T, info, o);
+            if (i < iters) token_block<ENC_TABLE, LPR, FULL, MMA>(va[i], vb[i], mbk[i], i, real, sc, T, info, o);
     } else if (same == 0xffffffffu) {
 #pragma unroll
         for (int i = 0; i < TOK_NREG; ++i)
-            if (i < iters) token_block<ENC_EXACT, LPR>(va[i], vb[i], mbk[i], i, real, sc, T, info, o);
+            if (i < iters) token_block<ENC_EXACT, LPR, FULL, MMA>(va[i], vb[i], mbk[i], i, real, sc, T, info, o);
     } else {
         // the two rows of the warp take different modes
 #pragma unroll
         for (int i = 0; i < TOK_NREG; ++i)
-            if (i < iters) token_block_mixed<LPR>(va[i], vb[i], mbk[i], i, real, mode, sc, T, info, o);
+            if (i < iters) token_block_mixed<LPR, FULL, MMA>(va[i], vb[i], mbk[i], i, real, mode, sc, T, info, o);
     }
-    for (int i = TOK_NREG; i < iters; ++i) {
-        uint4 a = make_uint4(0u, 0u, 0u, 0u), b = a;
-        if (real && i * LPR < nkb_lane) row_block<V8, SWIGLU>(xl + (int64_t)i * LPR * 16, C, a, b);
-        token_block_mixed<LPR>(a, b, absmax_bits_16(a, b), i, real, mode, sc, T, info, o);
+    if (!FULL) {
+        for (int i = TOK_NREG; i < iters; ++i) {
+            uint4 a = make_uint4(0u, 0u, 0u, 0u), b = a;
+            if (real && i * LPR < nkb_lane) row_block<V8, SWIGLU>(xl + (int64_t)i * LPR * 16, C, a, b);
+            token_block_mixed<LPR, FULL, MMA>(a, b, absmax_bits_16(a, b), i, real, mode, sc, T, info, o);
+        }
     }
+}
+
+// LPR lanes per token row (32: one row per warp; 16: two rows per warp, for rows of at most 64
+// blocks, so that rows of 48 blocks keep every lane busy), one 16-element block per lane per step:
+// the row is loaded once with 32-byte coalesced loads (held in registers up to TOK_NREG steps),
+// reduced to its amax with shuffles among the row's lanes, and encoded from registers, so each
+// input byte is read from HBM once. MMA: scale bytes in the tile layout (else canonical rows).
+template <bool V8, bool SWIGLU, int LPR, bool MMA>
+// 6 CTAs per SM (80 registers, no spills; 24 warps keep enough row loads in flight: 131072 x 2048
+// rows 0.218 ms at 142 registers, 0.179 at 128, 0.158 at 96, 0.146 at 80); the SwiGLU variant keeps
+// 5 (96 registers; at 80 it spills).
+__global__ void __launch_bounds__(TOK_THREADS, SWIGLU ? 5 : 6)
+nvfp4_token_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t C, int64_t ldx,
+                   uint8_t* __restrict__ q, uint8_t* __restrict__ sf, float* __restrict__ s_tok,
+                   int64_t rows_cover) {
+    griddep_begin();
+    constexpr int RPW = 32 / LPR;                              // rows per warp
+    __shared__ Nvfp4Table tables[(TOK_THREADS / 32) * RPW];   // one per row
+    __shared__ Nvfp4CodeInfo info;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int half = lane / LPR, l = lane % LPR;               // row of the warp, lane within the row
+    for (uint32_t c = threadIdx.x; c < 128u; c += TOK_THREADS) nvfp4_code_info_build(info, c);
+    __syncthreads();
+    const int64_t row0 = ((int64_t)blockIdx.x * (TOK_THREADS / 32) + warp) * RPW;
+    if (row0 >= rows_cover) return;                            // uniform over the warp
+    const int64_t row = row0 + half;
+    const bool covered = row < rows_cover;                     // the second row of a warp may not be
+    Nvfp4Table& T = tables[warp * RPW + half];
+    const bool real = row < R;
+    const int64_t nkb = C >> 4;
+    // uniform over the warp: whole steps for every lane, and every row of the warp real
+    const bool full = nkb % LPR == 0 && nkb <= (int64_t)TOK_NREG * LPR && row0 + RPW - 1 < R;
+    if (full)
+        token_rows<V8, SWIGLU, LPR, true, MMA>(x, C, ldx, q, sf, s_tok, row, covered, real, l, half, T, info);
+    else
+        token_rows<V8, SWIGLU, LPR, false, MMA>(x, C, ldx, q, sf, s_tok, row, covered, real, l, half, T, info);
 }
 
 template <bool SWIGLU>
@@ -366,16 +393,20 @@ static cudaError_t launch_token(const uint16_t* x, int64_t R, int64_t C, int64_t
     const int64_t grid = (cover + rows_per_cta - 1) / rows_per_cta;
     const bool v8 = ((reinterpret_cast<uintptr_t>(x) & 31u) == 0) && (ldx % 16 == 0) && (!SWIGLU || C % 16 == 0);
     cudaError_t lerr;
-#define NVQ_TOK(V, L)                                                                                             \
-    lerr = launch_pdl(nvfp4_token_kernel<V, SWIGLU, L>, dim3((unsigned)grid), dim3(TOK_THREADS), 0, stream, x, R, C, \
-                      ldx, q, sf, s_tok, mma_layout, cover)
+#define NVQ_TOK(V, L, M)                                                                                          \
+    lerr = launch_pdl(nvfp4_token_kernel<V, SWIGLU, L, M>, dim3((unsigned)grid), dim3(TOK_THREADS), 0, stream, x, R, \
+                      C, ldx, q, sf, s_tok, cover)
+#define NVQ_TOK_L(V, M)                                                                                           \
+    if (pair) NVQ_TOK(V, 16, M);                                                                                  \
+    else NVQ_TOK(V, 32, M)
     if (v8) {
-        if (pair) NVQ_TOK(true, 16);
-        else NVQ_TOK(true, 32);
+        if (mma_layout) NVQ_TOK_L(true, true);
+        else NVQ_TOK_L(true, false);
     } else {
-        if (pair) NVQ_TOK(false, 16);
-        else NVQ_TOK(false, 32);
+        if (mma_layout) NVQ_TOK_L(false, true);
+        else NVQ_TOK_L(false, false);
     }
+#undef NVQ_TOK_L
 #undef NVQ_TOK
     const cudaError_t err = lerr != cudaSuccess ? lerr : cudaGetLastError();
     if (err == cudaSuccess) count_launches(1);
