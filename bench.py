@@ -206,16 +206,28 @@ def _workload_dense(torch, nvq, wl, dev):
             "config": config, "dtype": "mxfp8(e4m3+e8m0)/nvfp4(e2m1+e4m3+fp32) -> fp32 accumulate -> bf16"}
 
 
-def _workload_moe(torch, nvq, wl, dev):
-    """One routed MoE expert layer forward in per-token NVFP4: quantize the routed gate_up input per
-    token and both expert weight matrices (one FP32 scale per expert), the grouped gate_up GEMM, the
+def _workload_moe(torch, nvq, wl, dev, quantize_once=True):
+    """One routed MoE expert layer forward in per-token NVFP4: the gate_up input quantized per token,
+    both expert weight matrices quantized (one FP32 scale per expert), the grouped gate_up GEMM, the
     fused SwiGLU + per-token NVFP4 of its bf16 output, and the grouped down GEMM. Expert segments
-    start at any row (no padding)."""
-    counts, offs_np = wl.moe_routing(align=1)
+    start at any row (no padding).
+
+    quantize_once (the default line): the layer's input is the 16384 tokens and their routing; the
+    tokens are quantized once and their quantized rows gathered into the 131072 expert-sorted routed
+    rows (per-token scales make this equal, byte for byte, to quantizing the gathered bf16 rows).
+    Otherwise (workload moe_rows) the input is 131072 routed bf16 rows, quantized as they are."""
+    import numpy as np
+    T, E, H, I2, I = 16384, wl.EXPERTS, wl.HIDDEN, 2 * wl.INTERMEDIATE, wl.INTERMEDIATE
+    choices = wl.route_choices(T)
+    counts = np.bincount(choices.reshape(-1), minlength=E).astype(np.int64)
+    offs_np = wl.padded_offsets(counts, 1)
     offs = torch.from_numpy(offs_np).to(dev)
     R = int(offs_np[-1])
-    E, H, I2, I = wl.EXPERTS, wl.HIDDEN, 2 * wl.INTERMEDIATE, wl.INTERMEDIATE
-    x1 = wl.routed_activations(counts, offs_np, H, seed=1, device=dev)
+    if quantize_once:
+        x1 = wl.normal_bf16((T, H), 1.0, seed=1, device=dev)                 # the layer's tokens
+        idx = torch.from_numpy(wl.dispatch_index(choices, offs_np)).to(dev)
+    else:
+        x1 = wl.routed_activations(counts, offs_np, H, seed=1, device=dev)  # routed rows, as given
     w1 = wl.expert_weights(H, I2, seed=3, device=dev)
     w2 = wl.expert_weights(I, H, seed=4, device=dev)
     real = float(counts.sum())
@@ -234,9 +246,22 @@ def _workload_moe(torch, nvq, wl, dev):
     b = {"a1": alloc_tok(R, H), "a2": alloc_tok(R, I), "b1": alloc_w(E, H, I2), "b2": alloc_w(E, I, H),
          "d1": torch.empty((R, I2), dtype=torch.bfloat16, device=dev),
          "d2": torch.empty((R, H), dtype=torch.bfloat16, device=dev)}
-    kernels = [
-        Kernel("nvfp4_quantize_per_token gate_up input", "hbm", R * H * 2.5625 + 4 * R, "quant_nvfp4.cu", "hbm",
-               "2.5625 B/elem + 4 B/row"),
+    if quantize_once:
+        b["tok"] = alloc_tok(T, H)
+        row_bytes = H // 2 + H // 16 + 4
+        kernels = [
+            Kernel("nvfp4_quantize_per_token tokens", "hbm", T * H * 2.5625 + 4 * T, "quant_nvfp4.cu", "hbm",
+                   "2.5625 B/elem + 4 B/row"),
+            Kernel("quantized_gather_rows routed gate_up input", "hbm", (real + R) * row_bytes, "layout_ops.cu", "hbm",
+                   "read K/2 + K/16 + 4 B per routed row, write the same per routed row"),
+        ]
+    else:
+        kernels = [
+            Kernel("nvfp4_quantize_per_token gate_up input", "hbm", R * H * 2.5625 + 4 * R, "quant_nvfp4.cu", "hbm",
+                   "2.5625 B/elem + 4 B/row"),
+        ]
+    nq = len(kernels)
+    kernels += [
         Kernel("nvfp4_quantize_weights gate_up", "hbm", E * H * I2 * 2.5625 + 4 * E, "quant_nvfp4_weights.cu", "hbm",
                "2.5625 B/elem"),
         Kernel("block_scaled_gemm NVFP4 gate_up", "tensor", f1, "gemm_sm103.cu", "fp4", "2*sum_e M_e*N*K"),
@@ -250,27 +275,42 @@ def _workload_moe(torch, nvq, wl, dev):
     def step(timer, xin=None, win=None):
         xa = x1 if xin is None else xin[0]
         wa, wb = (w1, w2) if win is None else win
-        timer.run(kernels[0].name, lambda: nvq.nvfp4_quantize_per_token(xa, out=b["a1"]))
-        timer.run(kernels[1].name, lambda: nvq.nvfp4_quantize_weights(wa, out=b["b1"]))
-        timer.run(kernels[2].name, lambda: nvq.block_scaled_grouped_gemm(
+        if quantize_once:
+            timer.run(kernels[0].name, lambda: nvq.nvfp4_quantize_per_token(xa, out=b["tok"]))
+            timer.run(kernels[1].name, lambda: nvq.quantized_gather_rows(
+                nvq.NVFP4, b["tok"][0], b["tok"][1], b["tok"][2], idx, H, out=b["a1"]))
+        else:
+            timer.run(kernels[0].name, lambda: nvq.nvfp4_quantize_per_token(xa, out=b["a1"]))
+        timer.run(kernels[nq].name, lambda: nvq.nvfp4_quantize_weights(wa, out=b["b1"]))
+        timer.run(kernels[nq + 1].name, lambda: nvq.block_scaled_grouped_gemm(
             nvq.NVFP4, nvq.GEMM_GROUP_M, b["a1"][0], b["a1"][1], b["b1"][0], b["b1"][1], offs, m=R, n=I2, k=H,
             groups=E, s_a=b["a1"][2], s_b=b["b1"][2], out=b["d1"]))
-        timer.run(kernels[3].name, lambda: nvq.nvfp4_swiglu_quantize_per_token(b["d1"], out=b["a2"]))
-        timer.run(kernels[4].name, lambda: nvq.nvfp4_quantize_weights(wb, out=b["b2"]))
-        timer.run(kernels[5].name, lambda: nvq.block_scaled_grouped_gemm(
+        timer.run(kernels[nq + 2].name, lambda: nvq.nvfp4_swiglu_quantize_per_token(b["d1"], out=b["a2"]))
+        timer.run(kernels[nq + 3].name, lambda: nvq.nvfp4_quantize_weights(wb, out=b["b2"]))
+        timer.run(kernels[nq + 4].name, lambda: nvq.block_scaled_grouped_gemm(
             nvq.NVFP4, nvq.GEMM_GROUP_M, b["a2"][0], b["a2"][1], b["b2"][0], b["b2"][1], offs, m=R, n=H, k=I,
             groups=E, s_a=b["a2"][2], s_b=b["b2"][2], out=b["d2"]))
         return [b["d2"]]
 
+    what = ("16384 tokens quantized once and their NVFP4 rows gathered into the expert-sorted routed rows"
+            if quantize_once else "the routed bf16 rows quantized as given")
     config = {"workload": "per-token NVFP4 MoE expert layer forward, Qwen3-30B-A3B shapes: 16384 tokens, "
-                          "top-8 of 128 experts (Zipf 1.1 loads), 131072 routed rows; quantize, gate_up GEMM, "
-                          "SwiGLU + NVFP4, down GEMM",
-              "tokens": 16384, "hidden": H, "intermediate": I, "experts": E, "topk": 8,
+                          "top-8 of 128 experts (Zipf 1.1 loads), 131072 routed rows; " + what +
+                          ", both expert weight stacks quantized, gate_up GEMM, SwiGLU + NVFP4, down GEMM",
+              "tokens": T, "hidden": H, "intermediate": I, "experts": E, "topk": 8,
               "routing": "Gumbel-top-8, p_r ~ r^-1.1", "routed_rows": int(real), "buffer_rows": R,
-              "row_alignment": 1, "expert_rows_min_max": [int(counts.min()), int(counts.max())]}
+              "row_alignment": 1, "expert_rows_min_max": [int(counts.min()), int(counts.max())],
+              "activation_input": "tokens [16384, 2048] + routing (quantize once, gather)" if quantize_once
+              else "routed rows [131072, 2048]"}
     return {"step": step, "kernels": kernels, "gemm_flops": f1 + f2, "inputs": [x1, w1, w2],
             "input_groups": ([0], [1, 2]), "config": config,
             "dtype": "nvfp4(e2m1+e4m3+fp32) -> fp32 accumulate -> bf16"}
+
+
+def _workload_moe_rows(torch, nvq, wl, dev):
+    """The routed MoE layer forward with the 131072 routed bf16 rows as its input (no quantize-once
+    dispatch): the per-token quantizer runs on every routed row."""
+    return _workload_moe(torch, nvq, wl, dev, quantize_once=False)
 
 
 def _workload_backward(torch, nvq, wl, dev):
@@ -594,7 +634,8 @@ def _workload_swiglu(torch, nvq, wl, dev):
             "config": config, "dtype": "bf16 -> swiglu (fp32) -> nvfp4", "unit": "GB/s"}
 
 
-WORKLOADS = {"dense": _workload_dense, "quant": _workload_quant, "moe": _workload_moe, "backward": _workload_backward,
+WORKLOADS = {"dense": _workload_dense, "quant": _workload_quant, "moe": _workload_moe, "moe_rows": _workload_moe_rows,
+             "backward": _workload_backward,
              "decode": _workload_decode, "dispatch": _workload_dispatch, "dq_backward": _workload_dq_backward,
              "swiglu": _workload_swiglu, "weights": _workload_weights}
 GBS_WORKLOADS = ("quant", "dispatch", "swiglu", "weights")
@@ -1050,7 +1091,7 @@ def cpu_baseline(workload, rows=None, cols=3072):
                CUDA_VISIBLE_DEVICES="")
     unit, scale = ("GB/s", 1e9) if workload in GBS_WORKLOADS else ("TFLOPS", 1e12)
     if rows is None:
-        rows = 16384 if workload == "moe" else 4096     # several seconds of single-threaded oracle work
+        rows = 16384 if workload in ("moe", "moe_rows") else 4096     # several seconds of single-threaded oracle work
 
     def run(procs):
         cmd = [sys.executable, os.path.abspath(__file__), "--oracle-sample", workload, "--rows", str(rows),
@@ -1065,7 +1106,7 @@ def cpu_baseline(workload, rows=None, cols=3072):
     except (subprocess.SubprocessError, ValueError, IndexError) as e:
         return {"value": None, "unit": unit, "cores": 1, "kind": "oracle", "sample": f"failed: {e}"}
     cores = _host_cores()
-    if workload != "moe" or cores <= 1:
+    if workload not in ("moe", "moe_rows") or cores <= 1:
         return single
     try:
         allc = run(cores)

@@ -111,14 +111,15 @@ def test_gather_bad_index_sets_status_and_writes_zero_row(nvq):
     assert int(sfg.view(5, K // 16)[2:4].sum()) == 0
 
 
-def test_full_size_quantize_once_dispatch(nvq):
-    """16384 tokens x 2048, top-8 of 128 experts (Zipf 1.1), 32-row padded segments: gathering the
-    quantized tokens equals quantizing the gathered rows, byte for byte (the whole batch), and
-    sampled rows equal the oracle."""
+@pytest.mark.parametrize("align", [1, 32])
+def test_full_size_quantize_once_dispatch(nvq, align):
+    """16384 tokens x 2048, top-8 of 128 experts (Zipf 1.1), segments unpadded (the MoE bench step's
+    layout) or padded to 32 rows: gathering the quantized tokens equals quantizing the gathered rows,
+    byte for byte (the whole batch), and sampled rows equal the oracle."""
     T, K = 16384, workloads.HIDDEN
     choices = workloads.route_choices(T)
     counts = np.bincount(choices.reshape(-1), minlength=workloads.EXPERTS)
-    offs = workloads.padded_offsets(counts, 32)
+    offs = workloads.padded_offsets(counts, align)
     idx = workloads.dispatch_index(choices, offs)
     x = workloads.normal_bf16((T, K), 1.0, seed=21, device="cuda")
     q, sf, s = nvq.nvfp4_quantize_per_token(x)
