@@ -24,7 +24,7 @@ the pages ablate, see workloads.py):
   dq_backward  the backward shapes with the dequantized-backward mode: BF16 dequantization of the
            MXFP8 operands and grouped BF16 GEMMs.
   quant, dispatch, swiglu, weights  (GB/s lines) the quantizers alone on the routed gate_up batch;
-           quantize-once dispatch (per-token NVFP4 of the tokens, then a gather into expert order);
+           quantize-once dispatch (per-token NVFP4 of the tokens, each written to its routed rows);
            the fused SwiGLU + per-token NVFP4 of the down-projection input; NVFP4 quantization of all
            gate_up and down expert weights.
 
@@ -212,9 +212,9 @@ def _workload_moe(torch, nvq, wl, dev, quantize_once=True):
     fused SwiGLU + per-token NVFP4 of its bf16 output, and the grouped down GEMM. Expert segments
     start at any row (no padding).
 
-    quantize_once (the default line): the layer's input is the 16384 tokens and their routing; the
-    tokens are quantized once and their quantized rows gathered into the 131072 expert-sorted routed
-    rows (per-token scales make this equal, byte for byte, to quantizing the gathered bf16 rows).
+    quantize_once (the default line): the layer's input is the 16384 tokens and their routing; each
+    token is quantized once and written to its 8 expert-sorted routed rows by nvfp4_quantize_dispatch
+    (per-token scales make this equal, byte for byte, to quantizing the gathered bf16 rows).
     Otherwise (workload moe_rows) the input is 131072 routed bf16 rows, quantized as they are."""
     import numpy as np
     T, E, H, I2, I = 16384, wl.EXPERTS, wl.HIDDEN, 2 * wl.INTERMEDIATE, wl.INTERMEDIATE
@@ -225,7 +225,7 @@ def _workload_moe(torch, nvq, wl, dev, quantize_once=True):
     R = int(offs_np[-1])
     if quantize_once:
         x1 = wl.normal_bf16((T, H), 1.0, seed=1, device=dev)                 # the layer's tokens
-        idx = torch.from_numpy(wl.dispatch_index(choices, offs_np)).to(dev)
+        dest = torch.from_numpy(wl.dispatch_dest(choices, offs_np)).to(dev)  # routed row of each (token, k)
     else:
         x1 = wl.routed_activations(counts, offs_np, H, seed=1, device=dev)  # routed rows, as given
     w1 = wl.expert_weights(H, I2, seed=3, device=dev)
@@ -247,13 +247,10 @@ def _workload_moe(torch, nvq, wl, dev, quantize_once=True):
          "d1": torch.empty((R, I2), dtype=torch.bfloat16, device=dev),
          "d2": torch.empty((R, H), dtype=torch.bfloat16, device=dev)}
     if quantize_once:
-        b["tok"] = alloc_tok(T, H)
         row_bytes = H // 2 + H // 16 + 4
         kernels = [
-            Kernel("nvfp4_quantize_per_token tokens", "hbm", T * H * 2.5625 + 4 * T, "quant_nvfp4.cu", "hbm",
-                   "2.5625 B/elem + 4 B/row"),
-            Kernel("quantized_gather_rows routed gate_up input", "hbm", (real + R) * row_bytes, "layout_ops.cu", "hbm",
-                   "read K/2 + K/16 + 4 B per routed row, write the same per routed row"),
+            Kernel("nvfp4_quantize_dispatch tokens -> routed gate_up input", "hbm", T * H * 2 + real * row_bytes,
+                   "quant_nvfp4.cu", "hbm", "2 B read per token element + K/2 + K/16 + 4 B written per routed row"),
         ]
     else:
         kernels = [
@@ -276,9 +273,7 @@ def _workload_moe(torch, nvq, wl, dev, quantize_once=True):
         xa = x1 if xin is None else xin[0]
         wa, wb = (w1, w2) if win is None else win
         if quantize_once:
-            timer.run(kernels[0].name, lambda: nvq.nvfp4_quantize_per_token(xa, out=b["tok"]))
-            timer.run(kernels[1].name, lambda: nvq.quantized_gather_rows(
-                nvq.NVFP4, b["tok"][0], b["tok"][1], b["tok"][2], idx, H, out=b["a1"]))
+            timer.run(kernels[0].name, lambda: nvq.nvfp4_quantize_dispatch(xa, dest, R, out=b["a1"]))
         else:
             timer.run(kernels[0].name, lambda: nvq.nvfp4_quantize_per_token(xa, out=b["a1"]))
         timer.run(kernels[nq].name, lambda: nvq.nvfp4_quantize_weights(wa, out=b["b1"]))
@@ -292,7 +287,7 @@ def _workload_moe(torch, nvq, wl, dev, quantize_once=True):
             groups=E, s_a=b["a2"][2], s_b=b["b2"][2], out=b["d2"]))
         return [b["d2"]]
 
-    what = ("16384 tokens quantized once and their NVFP4 rows gathered into the expert-sorted routed rows"
+    what = ("16384 tokens quantized once, each written to its 8 expert-sorted routed rows"
             if quantize_once else "the routed bf16 rows quantized as given")
     config = {"workload": "per-token NVFP4 MoE expert layer forward, Qwen3-30B-A3B shapes: 16384 tokens, "
                           "top-8 of 128 experts (Zipf 1.1 loads), 131072 routed rows; " + what +
@@ -300,7 +295,7 @@ def _workload_moe(torch, nvq, wl, dev, quantize_once=True):
               "tokens": T, "hidden": H, "intermediate": I, "experts": E, "topk": 8,
               "routing": "Gumbel-top-8, p_r ~ r^-1.1", "routed_rows": int(real), "buffer_rows": R,
               "row_alignment": 1, "expert_rows_min_max": [int(counts.min()), int(counts.max())],
-              "activation_input": "tokens [16384, 2048] + routing (quantize once, gather)" if quantize_once
+              "activation_input": "tokens [16384, 2048] + routing (quantize once, dispatch)" if quantize_once
               else "routed rows [131072, 2048]"}
     return {"step": step, "kernels": kernels, "gemm_flops": f1 + f2, "inputs": [x1, w1, w2],
             "input_groups": ([0], [1, 2]), "config": config,
@@ -571,41 +566,35 @@ def _workload_weights(torch, nvq, wl, dev):
 
 
 def _workload_dispatch(torch, nvq, wl, dev):
-    """Quantize-once dispatch of the MoE gate_up input: per-token NVFP4 of the 16384 tokens, then the
-    gather of their quantized rows into the 131072 expert-sorted routed rows."""
+    """Quantize-once dispatch of the MoE gate_up input: per-token NVFP4 of the 16384 tokens, each
+    token written to its 8 expert-sorted routed rows (nvfp4_quantize_dispatch, one pass)."""
+    import numpy as np
     T, H = 16384, wl.HIDDEN
     choices = wl.route_choices(T)
-    counts = wl.route_counts(T)
+    counts = np.bincount(choices.reshape(-1), minlength=wl.EXPERTS)
     offs_np = wl.padded_offsets(counts, 1)
     R = int(offs_np[-1])
-    idx = torch.from_numpy(wl.dispatch_index(choices, offs_np)).to(dev)
+    dest = torch.from_numpy(wl.dispatch_dest(choices, offs_np)).to(dev)
     x = wl.normal_bf16((T, H), 1.0, seed=21, device=dev)
-    tok = (torch.empty((T, H // 2), dtype=torch.uint8, device=dev),
-           torch.empty(nvq.sf_bytes(T, H, 16), dtype=torch.uint8, device=dev),
-           torch.empty(T, dtype=torch.float32, device=dev))
     routed = (torch.empty((R, H // 2), dtype=torch.uint8, device=dev),
               torch.empty(nvq.sf_bytes(R, H, 16), dtype=torch.uint8, device=dev),
               torch.empty(R, dtype=torch.float32, device=dev))
     row_bytes = H // 2 + H // 16 + 4
     kernels = [
-        Kernel("nvfp4_quantize_per_token tokens", "hbm", T * H * 2.5625 + 4 * T, "quant_nvfp4.cu", "hbm",
-               "2.5625 B/elem + 4 B/row"),
-        Kernel("quantized_gather_rows routed", "hbm", (int(counts.sum()) + R) * row_bytes, "layout_ops.cu", "hbm",
-               "read K/2 + K/16 + 4 B per real routed row, write the same per routed row"),
+        Kernel("nvfp4_quantize_dispatch tokens -> routed rows", "hbm", T * H * 2 + int(counts.sum()) * row_bytes,
+               "quant_nvfp4.cu", "hbm", "2 B read per token element + K/2 + K/16 + 4 B written per routed row"),
     ]
 
     def step(timer, xin=None, win=None):
         xx = x if xin is None else xin[0]
-        timer.run(kernels[0].name, lambda: nvq.nvfp4_quantize_per_token(xx, out=tok))
-        timer.run(kernels[1].name, lambda: nvq.quantized_gather_rows(nvq.NVFP4, tok[0], tok[1], tok[2], idx, H,
-                                                                     out=routed))
+        timer.run(kernels[0].name, lambda: nvq.nvfp4_quantize_dispatch(xx, dest, R, out=routed))
         return [routed[0], routed[1], routed[2]]
 
-    config = {"workload": "quantize-once dispatch: per-token NVFP4 of 16384 tokens x 2048, gathered into "
-                          "the top-8 expert-sorted routed rows (Zipf 1.1)",
+    config = {"workload": "quantize-once dispatch: per-token NVFP4 of 16384 tokens x 2048, each token written to "
+                          "its top-8 expert-sorted routed rows (Zipf 1.1)",
               "tokens": [T, H], "routed_rows": R}
     return {"step": step, "kernels": kernels, "gemm_flops": 0.0, "inputs": [x], "input_groups": ([0], []),
-            "config": config, "dtype": "bf16 -> nvfp4 (gathered)", "unit": "GB/s"}
+            "config": config, "dtype": "bf16 -> nvfp4 (dispatched)", "unit": "GB/s"}
 
 
 def _workload_swiglu(torch, nvq, wl, dev):

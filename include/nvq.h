@@ -108,6 +108,34 @@ nvq_status nvfp4_quantize_per_token(const void* x, int64_t rows, int64_t cols, i
                                     nvq_sf_layout sf_layout, void* stream);
 
 /*
+ * nvfp4_quantize_dispatch — quantize-once dispatch: per-token NVFP4 of each token, written straight
+ * to every routed row the token is dispatched to (its top-k experts' segments), in one pass.
+ *
+ * Defines: for every token t and k < topk with r = dest[t * topk + k] >= 0, routed row r of the
+ * outputs (codes, block scales, token scale) is byte for byte nvfp4_quantize_per_token of row t of x.
+ * Because a token's per-token bytes depend on that row only, this equals quantizing the routed
+ * (gathered) bf16 rows, and equals nvfp4_quantize_per_token of the tokens followed by
+ * quantized_gather_rows with the inverse index. [Miles-zh, "逐 Token 激活值缩放": one FP32 scale per
+ * token computed online, so the rollout can quantize once and dispatch the packed values.]
+ *
+ *   x      bf16 [tokens, cols], leading dimension ldx.
+ *   dest   device int32 [tokens, topk]: the routed row of each (token, k), or -1 (not dispatched).
+ *          Any other value outside [0, rows) sets *status to NVQ_DEV_BAD_INDEX (when status is
+ *          non-NULL) and that entry is skipped. Each routed row should be named at most once (otherwise one of the
+ *          tokens naming it wins).
+ *   rows   routed rows of the outputs.
+ *   q      [rows, cols/2] packed codes; sf [rows, cols/16] scales or MMA layout of that (its padding
+ *          rows below `rows` are zeroed); s_tok [rows] float32.
+ *   Routed rows that no entry of dest names are left as they were.
+ * Requires cols % 16 == 0, 0 < cols <= 16384, 1 <= topk <= 32, tokens <= 2^32, rows < 2^31;
+ * x, q and sf 16-byte aligned, dest, s_tok and status 4-byte aligned. tokens = rows = 0 is a no-op.
+ */
+nvq_status nvfp4_quantize_dispatch(const void* x, int64_t tokens, int64_t cols, int64_t ldx,
+                                   const int32_t* dest, int32_t topk, int64_t rows,
+                                   uint8_t* q, uint8_t* sf, float* s_tok, nvq_sf_layout sf_layout,
+                                   int32_t* status, void* stream);
+
+/*
  * nvfp4_swiglu_quantize_per_token — the down projection's per-token NVFP4 input straight from the
  * fused gate||up GEMM output: SwiGLU, then per-token NVFP4, without writing the bf16 activation.
  *
@@ -220,7 +248,7 @@ nvq_status quantized_gather_rows(nvq_format fmt, const uint8_t* q, const uint8_t
 #define NVQ_DEV_OK 0
 #define NVQ_DEV_TIMEOUT 1          /* a pipeline wait exceeded its time limit (wait_limit_ns) */
 #define NVQ_DEV_BAD_OFFSETS 2      /* offsets not monotone, past the buffer, or (GROUP_K) not multiples of 32 */
-#define NVQ_DEV_BAD_INDEX 3        /* quantized_gather_rows: an index outside [-1, src_rows) */
+#define NVQ_DEV_BAD_INDEX 3        /* quantized_gather_rows / nvfp4_quantize_dispatch: an index out of range */
 
 
 typedef struct {

@@ -47,6 +47,8 @@ _sf_bytes = _sig("nvq_sf_bytes", [_i64, _i64, _i32, ctypes.c_int], _i64)
 _launch_count = _sig("nvq_launch_count", [], ctypes.c_uint64)
 _mxfp8_quantize = _sig("mxfp8_quantize", [_vp, _i64, _i64, _i64, _vp, _vp, _vp, _vp, ctypes.c_int, _vp])
 _nvfp4_quantize_per_token = _sig("nvfp4_quantize_per_token", [_vp, _i64, _i64, _i64, _vp, _vp, _vp, ctypes.c_int, _vp])
+_nvfp4_quantize_dispatch = _sig("nvfp4_quantize_dispatch", [_vp, _i64, _i64, _i64, _vp, _i32, _i64, _vp, _vp, _vp,
+                                                             ctypes.c_int, _vp, _vp])
 _nvfp4_swiglu_quantize = _sig("nvfp4_swiglu_quantize_per_token", [_vp, _i64, _i64, _i64, _vp, _vp, _vp,
                                                                   ctypes.c_int, _vp])
 _nvfp4_quantize_weights = _sig("nvfp4_quantize_weights", [_vp, _i64, _i64, _i64, _vp, _vp, _vp, ctypes.c_int, _vp])
@@ -181,6 +183,28 @@ def nvfp4_swiglu_quantize_per_token(gate_up, sf_layout="mma", out=None):
     st = _nvfp4_swiglu_quantize(_ptr(gate_up), T, I, gate_up.stride(0) if T else I2, _ptr(q), _ptr(sf), _ptr(s),
                                 lay, _stream(dev))
     _check(st, "nvfp4_swiglu_quantize_per_token")
+    return q, sf, s
+
+
+def nvfp4_quantize_dispatch(x, dest, rows, sf_layout="mma", out=None, status=None):
+    """Quantize-once dispatch: per-token NVFP4 of the tokens x [T, K] (bf16 CUDA), written to the
+    routed rows dest [T, topk] (int32 CUDA, -1 = not dispatched) of (q [rows, K/2], sf, s [rows]).
+    Routed rows named by no entry are left as they are (fresh outputs: undefined there)."""
+    if not x.is_cuda or x.dtype != torch.bfloat16 or x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("expected a 2-D bf16 CUDA tensor with unit column stride")
+    if dest.dtype != torch.int32 or dest.dim() != 2 or not dest.is_contiguous() or dest.shape[0] != x.shape[0]:
+        raise ValueError("dest must be a contiguous int32 [tokens, topk] tensor")
+    T, K = x.shape
+    lay = _layout(sf_layout)
+    dev = x.device
+    if out is None:
+        out = (torch.empty((rows, K // 2), dtype=torch.uint8, device=dev),
+               torch.empty(sf_bytes(rows, K, 16, lay), dtype=torch.uint8, device=dev),
+               torch.empty(rows, dtype=torch.float32, device=dev))
+    q, sf, s = out
+    st = _nvfp4_quantize_dispatch(_ptr(x), T, K, x.stride(0), _ptr(dest), int(dest.shape[1]), int(rows), _ptr(q),
+                                  _ptr(sf), _ptr(s), lay, _ptr(status), _stream(dev))
+    _check(st, "nvfp4_quantize_dispatch")
     return q, sf, s
 
 

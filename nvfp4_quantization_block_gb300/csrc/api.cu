@@ -83,6 +83,24 @@ nvq_status nvfp4_quantize_per_token(const void* x, int64_t rows, int64_t cols, i
                                                           static_cast<cudaStream_t>(stream)));
 }
 
+nvq_status nvfp4_quantize_dispatch(const void* x, int64_t tokens, int64_t cols, int64_t ldx, const int32_t* dest,
+                                   int32_t topk, int64_t rows, uint8_t* q, uint8_t* sf, float* s_tok,
+                                   nvq_sf_layout sf_layout, int32_t* status, void* stream) {
+    if (tokens < 0 || cols < 0 || rows < 0 || !valid_layout(sf_layout)) return NVQ_ERR_INVALID_ARG;
+    if (topk < 1 || topk > 32) return NVQ_ERR_INVALID_ARG;
+    if (tokens == 0 && rows == 0) return NVQ_OK;
+    if (cols == 0 || cols % 16 || cols > 16384 || ldx < cols) return NVQ_ERR_INVALID_ARG;
+    if (tokens > NVQ_TOKEN_MAX_ROWS || rows > ((int64_t)1 << 31) - 1) return NVQ_ERR_INVALID_ARG;
+    if (q == nullptr || sf == nullptr || s_tok == nullptr || (tokens > 0 && (x == nullptr || dest == nullptr)))
+        return NVQ_ERR_INVALID_ARG;
+    if ((x && !aligned16(x)) || ldx % 8 || !aligned16(q) || !aligned16(sf) || !aligned4(s_tok) ||
+        (dest && !aligned4(dest)) || (status && !aligned4(status)))
+        return NVQ_ERR_MISALIGNED;
+    return from_cuda(nvq::launch_nvfp4_quantize_dispatch(static_cast<const uint16_t*>(x), tokens, cols, ldx, dest, topk,
+                                                         rows, q, sf, s_tok, sf_layout == NVQ_SF_MMA, status,
+                                                         static_cast<cudaStream_t>(stream)));
+}
+
 nvq_status nvfp4_swiglu_quantize_per_token(const void* gate_up, int64_t rows, int64_t cols, int64_t ld,
                                            uint8_t* q, uint8_t* sf, float* s_tok, nvq_sf_layout sf_layout,
                                            void* stream) {

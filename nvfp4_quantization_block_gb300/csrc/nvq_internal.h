@@ -36,6 +36,10 @@ cudaError_t launch_nvfp4_quantize_per_token(const uint16_t* x, int64_t R, int64_
                                             uint8_t* q, uint8_t* sf, float* s_tok, int mma_layout,
                                             cudaStream_t stream);
 
+cudaError_t launch_nvfp4_quantize_dispatch(const uint16_t* x, int64_t T, int64_t C, int64_t ldx, const int32_t* dest,
+                                           int topk, int64_t R, uint8_t* q, uint8_t* sf, float* s_tok, int mma_layout,
+                                           int32_t* status, cudaStream_t stream);
+
 cudaError_t launch_nvfp4_swiglu_quantize(const uint16_t* gate_up, int64_t R, int64_t I, int64_t ld, uint8_t* q,
                                          uint8_t* sf, float* s_tok, int mma_layout, cudaStream_t stream);
 

@@ -13,6 +13,7 @@
 // multiply and the hardware E2M1 conversion; any other scope compares each element with its block's
 // exact boundaries.
 
+#include "../../include/nvq.h"
 #include "nvq_device.cuh"
 #include "nvq_internal.h"
 #include "nvq_nvfp4_encode.cuh"
@@ -409,6 +410,115 @@ static cudaError_t launch_token(const uint16_t* x, int64_t R, int64_t C, int64_t
 #undef NVQ_TOK_L
 #undef NVQ_TOK
     const cudaError_t err = lerr != cudaSuccess ? lerr : cudaGetLastError();
+    if (err == cudaSuccess) count_launches(1);
+    return err;
+}
+
+// ------------------------------------------------------------------------------------------------
+// Quantize-once dispatch. Per-token scales make a token's NVFP4 bytes independent of every other
+// row [Miles-zh, "逐 Token 激活值缩放"], so a routed MoE layer can quantize each token once and copy
+// its bytes to every expert segment it is routed to. One warp per token: the token is quantized by
+// the per-token path above (one row of 32 lanes) into the warp's staging area in shared memory
+// (codes, canonical scale bytes, token scale), then the warp writes the staged row to each of the
+// token's routed rows: 16-byte code stores (8-byte when a row of codes is not a multiple of 16
+// bytes), one 4-byte scale word per 4-column group, the token scale. Warps past the tokens zero the
+// MMA layout's padding rows below the last routed row (what the gather and the per-token quantizer
+// leave there). Each input byte is read once; each routed row is written once.
+// ------------------------------------------------------------------------------------------------
+constexpr int64_t DSP_MAX_COLS = 16384;
+
+__host__ __device__ __forceinline__ int64_t dsp_stage_bytes(int64_t C) {
+    const int64_t qb = C >> 1, nkb4 = ((C >> 4) + 3) & ~int64_t(3);
+    return ((qb + nkb4 + 15) & ~int64_t(15)) + 16;             // codes, scale bytes, token scale
+}
+
+template <bool V8, bool MMA>
+__global__ void __launch_bounds__(TOK_THREADS, 5)
+nvfp4_dispatch_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t C, int64_t ldx,
+                      const int32_t* __restrict__ dest, int topk, int64_t R, int64_t pad_rows,
+                      uint8_t* __restrict__ q, uint8_t* __restrict__ sf, float* __restrict__ s_tok,
+                      int32_t* __restrict__ status) {
+    griddep_begin();
+    extern __shared__ __align__(16) uint8_t dsp_stage[];
+    __shared__ Nvfp4Table tables[TOK_THREADS / 32];
+    __shared__ Nvfp4CodeInfo info;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (uint32_t c = threadIdx.x; c < 128u; c += TOK_THREADS) nvfp4_code_info_build(info, c);
+    __syncthreads();
+    const int64_t w = (int64_t)blockIdx.x * (TOK_THREADS / 32) + warp;   // token w, then padding rows
+    const int64_t nkb = C >> 4, qb = C >> 1, ngr = (nkb + 3) >> 2;       // blocks, code bytes, scale words
+    if (w >= T) {
+        const int64_t r = R + (w - T);                         // uniform over the warp
+        if (MMA && r < R + pad_rows)
+            for (int64_t g = lane; g < ngr; g += 32) *reinterpret_cast<uint32_t*>(sf + mma_sf_offset(r, 4 * g, nkb)) = 0u;
+        return;
+    }
+    const int64_t sb = dsp_stage_bytes(C);
+    uint8_t* sq = dsp_stage + warp * sb;                       // staged codes [qb]
+    uint8_t* ssf = sq + qb;                                    // staged scale bytes [nkb]
+    float* ss = reinterpret_cast<float*>(sq + sb - 16);        // staged token scale
+    // the token quantized as a one-row batch (rows of 32 lanes, canonical scale bytes)
+    const uint16_t* xt = x + w * ldx;
+    if (nkb % 32 == 0 && nkb <= (int64_t)TOK_NREG * 32)
+        token_rows<V8, false, 32, true, false>(xt, C, ldx, sq, ssf, ss, 0, true, true, lane, 0, tables[warp], info);
+    else
+        token_rows<V8, false, 32, false, false>(xt, C, ldx, sq, ssf, ss, 0, true, true, lane, 0, tables[warp], info);
+    __syncwarp();
+    const float s = *ss;
+    const int32_t mine = lane < topk ? dest[w * topk + lane] : -1;
+    for (int k = 0; k < topk; ++k) {
+        const int32_t r = __shfl_sync(0xffffffffu, mine, k);
+        if (r == -1) continue;                                 // uniform over the warp
+        if (r < 0 || r >= R) {
+            if (lane == 0 && status != nullptr) atomicExch(status, NVQ_DEV_BAD_INDEX);
+            continue;
+        }
+        uint8_t* qd = q + (int64_t)r * qb;
+        if ((qb & 15) == 0) {
+            for (int64_t c = lane * 16; c < qb; c += 32 * 16)
+                *reinterpret_cast<uint4*>(qd + c) = *reinterpret_cast<const uint4*>(sq + c);
+        } else {
+            for (int64_t c = lane * 8; c < qb; c += 32 * 8)
+                *reinterpret_cast<uint2*>(qd + c) = *reinterpret_cast<const uint2*>(sq + c);
+        }
+        for (int64_t g = lane; g < ngr; g += 32) {
+            uint32_t word = *reinterpret_cast<const uint32_t*>(ssf + 4 * g);
+            const int64_t valid = nkb - 4 * g;                 // scale bytes of this group that exist
+            if (valid < 4) word &= (1u << (8 * valid)) - 1u;
+            if (MMA) {
+                *reinterpret_cast<uint32_t*>(sf + mma_sf_offset(r, 4 * g, nkb)) = word;
+            } else if ((nkb & 3) == 0) {
+                *reinterpret_cast<uint32_t*>(sf + (int64_t)r * nkb + 4 * g) = word;
+            } else {
+                for (int64_t j = 0; j < 4 && j < valid; ++j) sf[(int64_t)r * nkb + 4 * g + j] = (uint8_t)(word >> (8 * j));
+            }
+        }
+        if (lane == 0) s_tok[r] = s;
+    }
+}
+
+cudaError_t launch_nvfp4_quantize_dispatch(const uint16_t* x, int64_t T, int64_t C, int64_t ldx, const int32_t* dest,
+                                           int topk, int64_t R, uint8_t* q, uint8_t* sf, float* s_tok, int mma_layout,
+                                           int32_t* status, cudaStream_t stream) {
+    const int64_t pad_rows = mma_layout ? (((R + 127) & ~int64_t(127)) - R) : 0;
+    const int64_t warps = T + pad_rows;
+    if (warps == 0) return cudaSuccess;
+    const int64_t grid = (warps + TOK_THREADS / 32 - 1) / (TOK_THREADS / 32);
+    const size_t smem = (size_t)(TOK_THREADS / 32) * (size_t)dsp_stage_bytes(C);
+    const bool v8 = ((reinterpret_cast<uintptr_t>(x) & 31u) == 0) && (ldx % 16 == 0);
+    cudaError_t err;
+    if (v8) {
+        if (mma_layout) err = launch_pdl(nvfp4_dispatch_kernel<true, true>, dim3((unsigned)grid), dim3(TOK_THREADS), smem,
+                                         stream, x, T, C, ldx, dest, topk, R, pad_rows, q, sf, s_tok, status);
+        else err = launch_pdl(nvfp4_dispatch_kernel<true, false>, dim3((unsigned)grid), dim3(TOK_THREADS), smem,
+                              stream, x, T, C, ldx, dest, topk, R, pad_rows, q, sf, s_tok, status);
+    } else {
+        if (mma_layout) err = launch_pdl(nvfp4_dispatch_kernel<false, true>, dim3((unsigned)grid), dim3(TOK_THREADS), smem,
+                                         stream, x, T, C, ldx, dest, topk, R, pad_rows, q, sf, s_tok, status);
+        else err = launch_pdl(nvfp4_dispatch_kernel<false, false>, dim3((unsigned)grid), dim3(TOK_THREADS), smem,
+                              stream, x, T, C, ldx, dest, topk, R, pad_rows, q, sf, s_tok, status);
+    }
+    if (err == cudaSuccess) err = cudaGetLastError();
     if (err == cudaSuccess) count_launches(1);
     return err;
 }

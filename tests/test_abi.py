@@ -95,6 +95,22 @@ def test_host_validation_rejects_before_launch(lib):
     assert nw(odd, 2, 64, 64, fake, fake, fake, 1, None) == 2         # misaligned weights
     assert nw(fake, 2, 64, 64, fake, fake, odd, 1, None) == 2         # misaligned s_w
     assert nw(fake, 0, 64, 64, None, None, None, 1, None) == 0        # no experts is a no-op
+    dq = lib.nvfp4_quantize_dispatch
+    dq.argtypes = [vp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, vp, ctypes.c_int32, ctypes.c_int64, vp, vp,
+                   vp, ctypes.c_int, vp, vp]
+    dq.restype = ctypes.c_int
+    assert dq(fake, 4, 40, 64, fake, 2, 8, fake, fake, fake, 1, None, None) == 1       # cols % 16
+    assert dq(fake, 4, 64, 64, fake, 0, 8, fake, fake, fake, 1, None, None) == 1       # topk < 1
+    assert dq(fake, 4, 64, 64, fake, 33, 8, fake, fake, fake, 1, None, None) == 1      # topk > 32
+    assert dq(fake, 4, 16400, 16400, fake, 2, 8, fake, fake, fake, 1, None, None) == 1  # cols > 16384
+    assert dq(fake, 4, 64, 48, fake, 2, 8, fake, fake, fake, 1, None, None) == 1       # ldx < cols
+    assert dq(fake, 4, 64, 64, None, 2, 8, fake, fake, fake, 1, None, None) == 1       # missing dest
+    assert dq(fake, 4, 64, 64, fake, 2, 8, fake, fake, fake, 2, None, None) == 1       # bad layout enum
+    assert dq(odd, 4, 64, 64, fake, 2, 8, fake, fake, fake, 1, None, None) == 2        # misaligned x
+    assert dq(fake, 4, 64, 68, fake, 2, 8, fake, fake, fake, 1, None, None) == 2       # ldx % 8
+    assert dq(fake, 4, 64, 64, fake, 2, 8, fake, fake, vp(0x10002), 1, None, None) == 2  # s_tok not 4-aligned
+    assert dq(fake, 4, 64, 64, vp(0x10002), 2, 8, fake, fake, fake, 1, None, None) == 2  # dest not 4-aligned
+    assert dq(fake, 0, 64, 64, None, 2, 0, None, None, None, 1, None, None) == 0       # empty is a no-op
     cv = lib.sf_layout_convert
     cv.argtypes = [vp, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, vp, ctypes.c_int, vp]
     cv.restype = ctypes.c_int

@@ -26,3 +26,19 @@ def test_route_counts_unchanged_by_the_refactor():
     # the 16384-token Zipf(1.1) routing the MoE configuration is quoted on
     c = workloads.route_counts(16384)
     assert c.sum() == 131072 and c.min() == 173 and c.max() == 14749
+
+
+def test_dispatch_dest_inverts_dispatch_index():
+    T = 3000
+    choices = workloads.route_choices(T)
+    counts = np.bincount(choices.reshape(-1), minlength=workloads.EXPERTS)
+    for align in (1, 32):
+        offs = workloads.padded_offsets(counts, align)
+        idx = workloads.dispatch_index(choices, offs)
+        dest = workloads.dispatch_dest(choices, offs)
+        assert dest.shape == choices.shape and dest.dtype == np.int32
+        # every (token, k) names a distinct real routed row of its own token and expert
+        assert len(np.unique(dest)) == dest.size
+        assert np.array_equal(idx[dest], np.repeat(np.arange(T)[:, None], workloads.TOPK, axis=1))
+        e_of_row = np.searchsorted(offs, dest, side="right") - 1
+        assert np.array_equal(e_of_row, choices)

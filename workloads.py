@@ -101,6 +101,23 @@ def dispatch_index(choices, offsets, experts=EXPERTS):
     return idx
 
 
+def dispatch_dest(choices, offsets, experts=EXPERTS):
+    """Routed row of every (token, k) of ``choices`` in the layout of ``dispatch_index`` (expert-sorted,
+    each expert's tokens in token order, segments starting at ``offsets``): int32 [tokens, topk]."""
+    choices = np.asarray(choices)
+    tokens, topk = choices.shape
+    flat_e = choices.reshape(-1)
+    order = np.argsort(flat_e, kind="stable")
+    counts = np.bincount(flat_e, minlength=experts)
+    dest = np.empty(flat_e.size, dtype=np.int32)
+    pos = 0
+    for e in range(experts):
+        c = int(counts[e])
+        dest[order[pos:pos + c]] = np.arange(int(offsets[e]), int(offsets[e]) + c, dtype=np.int32)
+        pos += c
+    return dest.reshape(tokens, topk)
+
+
 def padded_offsets(counts, align):
     """Segment starts [E+1]: each expert's rows padded up to a multiple of ``align``."""
     c = np.asarray(counts, dtype=np.int64)
