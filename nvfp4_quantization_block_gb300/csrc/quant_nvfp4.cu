@@ -61,6 +61,31 @@ __device__ __forceinline__ void f2_mul(float& y0, float& y1, float a0, float a1,
         : "=f"(y0), "=f"(y1) : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 
+__device__ __forceinline__ void f2_fma(float& y0, float& y1, float a0, float a1, float b0, float b1, float c0,
+                                       float c1) {
+    asm("{\n\t.reg .b64 a, b, c, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\tmov.b64 c, {%6, %7};\n\t"
+        "fma.rn.f32x2 d, a, b, c;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(y0), "=f"(y1) : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+
+// div_markstein (nvq_device.cuh) for the two elements of a word at once: the same steps, each an
+// IEEE operation on both elements (packed f32x2: one rounding each, no flush to zero), so the
+// same quotients; `ok` covers both.
+__device__ __forceinline__ void div_markstein2(float g0, float g1, float d0, float d1, float& q0, float& q1, bool& ok) {
+    float y00, y01;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y00) : "f"(d0));
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y01) : "f"(d1));
+    const float n0 = __uint_as_float(__float_as_uint(d0) ^ 0x80000000u);   // -d, exactly
+    const float n1 = __uint_as_float(__float_as_uint(d1) ^ 0x80000000u);
+    float e0, e1, y0, y1, a0, a1, r0, r1;
+    f2_fma(e0, e1, n0, n1, y00, y01, 1.0f, 1.0f);              // 1 - d y0
+    f2_fma(y0, y1, y00, y01, e0, e1, y00, y01);                // y = y0 + y0 (1 - d y0)
+    f2_mul(a0, a1, g0, g1, y0, y1);                            // q0 = RN(g y)
+    f2_fma(r0, r1, n0, n1, a0, a1, g0, g1);                    // r = g - d q0 (exact)
+    f2_fma(q0, q1, r0, r1, y0, y1, a0, a1);                    // RN(q0 + r y)
+    ok = fabsf(a0) >= 0x1p-100f && fabsf(a1) >= 0x1p-100f;
+}
+
 // h for -g > 87, where exp(-g) = p 2^n may lie beyond float32's range (n up to 433): d = 1 + p 2^n
 // is p 2^n exactly (1 is far below half an ulp of it), so s = g / d = RN(g / p) 2^-n, formed as
 // q = RN((g 2^-16) / p) (finite for any bf16 g, the same rounding), and h = s u rounded once to
@@ -79,9 +104,11 @@ __device__ __noinline__ float swiglu_wide(float g, float u, float p, float m) {
 __device__ __forceinline__ uint32_t swiglu2_fast(uint32_t g, uint32_t u, bool& rare) {
     constexpr float L2E = (float)1.4426950408889634, LN2_HI = 0.693145751953125f;
     constexpr float LN2_LO = (float)(0.6931471805599453 - 0.693145751953125), MAGIC = 12582912.0f;
-    const uint32_t xw = g ^ 0x80008000u;                       // x = -g, both halves
-    // (no upper clamp here: an element with x > 87 sends its block to the exact steps anyway)
-    const float x0 = fmaxf(bf16_lo(xw), -87.0f), x1 = fmaxf(bf16_hi(xw), -87.0f);
+    // x = -g clamped below at -87 in both halves at once (bf16 comparisons are exact; -87 = 0xC2AE);
+    // no upper clamp here: an element with x > 87 sends its block to the exact steps anyway
+    uint32_t xc;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(xc) : "r"(g ^ 0x80008000u), "r"(0xC2AEC2AEu));
+    const float x0 = bf16_lo(xc), x1 = bf16_hi(xc);
     float t0, t1, m0, m1, n0, n1, a0, a1, r0, r1;
     f2_mul(t0, t1, x0, x1, L2E, L2E);
     f2_add(m0, m1, t0, t1, MAGIC, MAGIC);                      // 1.5 * 2^23 + n: n in the low mantissa bits
@@ -103,10 +130,11 @@ __device__ __forceinline__ uint32_t swiglu2_fast(uint32_t g, uint32_t u, bool& r
     float e0, e1, d0, d1, h0, h1;
     f2_mul(e0, e1, p0, p1, s0, s1);                            // exp(-g)
     f2_add(d0, d1, e0, e1, 1.0f, 1.0f);
-    bool ok0, ok1;
-    const float q0 = div_markstein(bf16_lo(g), d0, ok0), q1 = div_markstein(bf16_hi(g), d1, ok1);
+    bool ok;
+    float q0, q1;
+    div_markstein2(bf16_lo(g), bf16_hi(g), d0, d1, q0, q1, ok);
     f2_mul(h0, h1, q0, q1, bf16_lo(u), bf16_hi(u));
-    rare = rare || !(ok0 && ok1 && x0 <= 87.0f && x1 <= 87.0f);
+    rare = rare || !(ok && x0 <= 87.0f && x1 <= 87.0f);
     return cvt_bf16x2(h0, h1);
 }
 
@@ -453,6 +481,7 @@ nvfp4_dispatch_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t C, int6
             for (int64_t g = lane; g < ngr; g += 32) *reinterpret_cast<uint32_t*>(sf + mma_sf_offset(r, 4 * g, nkb)) = 0u;
         return;
     }
+    const int32_t mine = lane < topk ? dest[w * topk + lane] : -1;   // in flight while the token is quantized
     const int64_t sb = dsp_stage_bytes(C);
     uint8_t* sq = dsp_stage + warp * sb;                       // staged codes [qb]
     uint8_t* ssf = sq + qb;                                    // staged scale bytes [nkb]
@@ -465,7 +494,6 @@ nvfp4_dispatch_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t C, int6
         token_rows<V8, false, 32, false, false>(xt, C, ldx, sq, ssf, ss, 0, true, true, lane, 0, tables[warp], info);
     __syncwarp();
     const float s = *ss;
-    const int32_t mine = lane < topk ? dest[w * topk + lane] : -1;
     for (int k = 0; k < topk; ++k) {
         const int32_t r = __shfl_sync(0xffffffffu, mine, k);
         if (r == -1) continue;                                 // uniform over the warp
