@@ -124,9 +124,10 @@ __device__ __forceinline__ uint32_t swiglu2_fast(uint32_t g, uint32_t u, bool& r
         f2_mul(p0, p1, p0, p1, r0, r1);
         f2_add(p0, p1, p0, p1, c[i], c[i]);
     }
-    // 2^n from the bits of 1.5 * 2^23 + n (n in [-126, 126] when x <= 87)
-    const float s0 = __uint_as_float((__float_as_uint(m0) - 0x4B400000u + 127u) << 23);
-    const float s1 = __uint_as_float((__float_as_uint(m1) - 0x4B400000u + 127u) << 23);
+    // 2^n from the bits of 1.5 * 2^23 + n (n in [-126, 126] when x <= 87): (bits - 0x4B400000 + 127)
+    // << 23 equals (bits << 23) + 0x3F800000 modulo 2^32 (0x4B400000 << 23 wraps to 0)
+    const float s0 = __uint_as_float((__float_as_uint(m0) << 23) + 0x3F800000u);
+    const float s1 = __uint_as_float((__float_as_uint(m1) << 23) + 0x3F800000u);
     float e0, e1, d0, d1, h0, h1;
     f2_mul(e0, e1, p0, p1, s0, s1);                            // exp(-g)
     f2_add(d0, d1, e0, e1, 1.0f, 1.0f);
