@@ -60,12 +60,12 @@ COPY_STREAMS = 4
 NCU_TRAFFIC = {
     # the weight quantizers: amax + encode launches of one call (check, finalize and zeroing move < 0.1 MB)
     "moe": {
-        "nvfp4_quantize_per_token gate_up input": {"bytes": 668907008, "src_sha": "ebde99e2a08fc259"},
-        "nvfp4_quantize_weights gate_up": {"bytes": 1808085760, "src_sha": "a29b226b014f5c46"},
-        "block_scaled_gemm NVFP4 gate_up": {"bytes": 755845120, "src_sha": "0190987686acf6ff"},
-        "nvfp4_swiglu_quantize_per_token down input": {"bytes": 447070208, "src_sha": "ebde99e2a08fc259"},
-        "nvfp4_quantize_weights down": {"bytes": 888271360, "src_sha": "a29b226b014f5c46"},
-        "block_scaled_gemm NVFP4 down": {"bytes": 663325696, "src_sha": "0190987686acf6ff"},
+        "nvfp4_quantize_dispatch tokens -> routed gate_up input": {"bytes": 166387712, "src_sha": "8e3db3ad43581994"},
+        "nvfp4_quantize_weights gate_up": {"bytes": 1814086912, "src_sha": "43bc634262ccb6ed"},
+        "block_scaled_gemm NVFP4 gate_up": {"bytes": 758438144, "src_sha": "b555bf0a103e30fb"},
+        "nvfp4_swiglu_quantize_per_token down input": {"bytes": 450689792, "src_sha": "8e3db3ad43581994"},
+        "nvfp4_quantize_weights down": {"bytes": 888220672, "src_sha": "43bc634262ccb6ed"},
+        "block_scaled_gemm NVFP4 down": {"bytes": 663508224, "src_sha": "b555bf0a103e30fb"},
     },
 }
 
