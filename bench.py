@@ -206,7 +206,7 @@ def _workload_dense(torch, nvq, wl, dev):
             "config": config, "dtype": "mxfp8(e4m3+e8m0)/nvfp4(e2m1+e4m3+fp32) -> fp32 accumulate -> bf16"}
 
 
-def _workload_moe(torch, nvq, wl, dev, quantize_once=True):
+def _workload_moe(torch, nvq, wl, dev, quantize_once=True, concurrent=True):
     """One routed MoE expert layer forward in per-token NVFP4: the gate_up input quantized per token,
     both expert weight matrices quantized (one FP32 scale per expert), the grouped gate_up GEMM, the
     fused SwiGLU + per-token NVFP4 of its bf16 output, and the grouped down GEMM. Expert segments
@@ -269,19 +269,53 @@ def _workload_moe(torch, nvq, wl, dev, quantize_once=True):
         Kernel("block_scaled_gemm NVFP4 down", "tensor", f2, "gemm_sm103.cu", "fp4", "2*sum_e M_e*N*K"),
     ]
 
+    # The expert-weight quantizations depend on nothing else in the step, so the timed step runs
+    # them on a side stream: W_gate_up next to the activation quantization, W_down next to the
+    # fused SwiGLU (after the gate_up GEMM, which holds every SM), each joined by an event before
+    # the GEMM that reads it. The per-kernel pass (timer active) runs the same launches in order on
+    # one stream, so each kernel's duration is its own.
+    side = torch.cuda.Stream(device=dev)
+    evs = [torch.cuda.Event() for _ in range(4)]
+
     def step(timer, xin=None, win=None):
         xa = x1 if xin is None else xin[0]
         wa, wb = (w1, w2) if win is None else win
-        if quantize_once:
-            timer.run(kernels[0].name, lambda: nvq.nvfp4_quantize_dispatch(xa, dest, R, out=b["a1"]))
+        serial = timer.active or not concurrent
+        cur = torch.cuda.current_stream(dev)
+
+        def act():
+            if quantize_once:
+                timer.run(kernels[0].name, lambda: nvq.nvfp4_quantize_dispatch(xa, dest, R, out=b["a1"]))
+            else:
+                timer.run(kernels[0].name, lambda: nvq.nvfp4_quantize_per_token(xa, out=b["a1"]))
+
+        def wq(k, w, out, ev_wait, ev_done):
+            if serial:
+                timer.run(kernels[k].name, lambda: nvq.nvfp4_quantize_weights(w, out=out))
+                return
+            ev_wait.record(cur)
+            side.wait_event(ev_wait)
+            with torch.cuda.stream(side):
+                nvq.nvfp4_quantize_weights(w, out=out)
+                ev_done.record(side)
+
+        if serial:
+            act()
+            wq(nq, wa, b["b1"], None, None)
         else:
-            timer.run(kernels[0].name, lambda: nvq.nvfp4_quantize_per_token(xa, out=b["a1"]))
-        timer.run(kernels[nq].name, lambda: nvq.nvfp4_quantize_weights(wa, out=b["b1"]))
+            wq(nq, wa, b["b1"], evs[0], evs[1])
+            act()
+            cur.wait_event(evs[1])
         timer.run(kernels[nq + 1].name, lambda: nvq.block_scaled_grouped_gemm(
             nvq.NVFP4, nvq.GEMM_GROUP_M, b["a1"][0], b["a1"][1], b["b1"][0], b["b1"][1], offs, m=R, n=I2, k=H,
             groups=E, s_a=b["a1"][2], s_b=b["b1"][2], out=b["d1"]))
-        timer.run(kernels[nq + 2].name, lambda: nvq.nvfp4_swiglu_quantize_per_token(b["d1"], out=b["a2"]))
-        timer.run(kernels[nq + 3].name, lambda: nvq.nvfp4_quantize_weights(wb, out=b["b2"]))
+        if serial:
+            timer.run(kernels[nq + 2].name, lambda: nvq.nvfp4_swiglu_quantize_per_token(b["d1"], out=b["a2"]))
+            wq(nq + 3, wb, b["b2"], None, None)
+        else:
+            wq(nq + 3, wb, b["b2"], evs[2], evs[3])
+            nvq.nvfp4_swiglu_quantize_per_token(b["d1"], out=b["a2"])
+            cur.wait_event(evs[3])
         timer.run(kernels[nq + 4].name, lambda: nvq.block_scaled_grouped_gemm(
             nvq.NVFP4, nvq.GEMM_GROUP_M, b["a2"][0], b["a2"][1], b["b2"][0], b["b2"][1], offs, m=R, n=H, k=I,
             groups=E, s_a=b["a2"][2], s_b=b["b2"][2], out=b["d2"]))
@@ -305,7 +339,7 @@ def _workload_moe(torch, nvq, wl, dev, quantize_once=True):
 def _workload_moe_rows(torch, nvq, wl, dev):
     """The routed MoE layer forward with the 131072 routed bf16 rows as its input (no quantize-once
     dispatch): the per-token quantizer runs on every routed row."""
-    return _workload_moe(torch, nvq, wl, dev, quantize_once=False)
+    return _workload_moe(torch, nvq, wl, dev, quantize_once=False, concurrent=False)
 
 
 def _workload_backward(torch, nvq, wl, dev):
