@@ -249,10 +249,9 @@ __device__ __forceinline__ void token_block_mixed(const uint4& a, const uint4& b
 // nvfp4_table_build_warp; 16: lane l takes thresholds j = (l >> 3) + 2t, t = 0, 1, of class l & 7
 // and their j + 4 partners, and the block-scale boundary of code l; a class's two lanes are l and
 // l ^ 8 of the same half-warp). Called by all 32 lanes of the warp together; returns whether the
-// lane's class has a product-path multiplier. SwiGLU rows of 16 lanes skip the search and take the
-// boundary comparison: with three blocks per lane the search costs them more than it saves
-// (131072 x 768 SwiGLU rows: 0.175 ms without it, 0.181 with it; plain 768-wide rows: 0.076 ms
-// without, 0.072 with).
+// lane's class has a product-path multiplier. Every row searches (131072 x 768 SwiGLU rows: 0.1604
+// ms without the search, 0.1584-0.1593 with it, once the SwiGLU divisions ran packed; plain
+// 768-wide rows: 0.076 ms without, 0.072 with).
 template <int LPR, bool SEARCH>
 __device__ __forceinline__ bool nvfp4_table_build_row(Nvfp4Table& T, float s, int l) {
     if (LPR == 32) return nvfp4_table_build_warp(T, s, l);
@@ -336,7 +335,7 @@ __device__ __forceinline__ void token_rows(const uint16_t* __restrict__ x, int64
     const Nvfp4Scope sc = make_nvfp4_scope(s);
     if (real && l == 0) s_tok[row] = s;
     // every row builds a table (all lanes take part in its shuffles); an exact-path row ignores it
-    constexpr bool SEARCH = LPR == 32 || !SWIGLU;              // rows that may take the product path
+    constexpr bool SEARCH = true;                              // rows that may take the product path
     const bool ok = nvfp4_table_build_row<LPR, SEARCH>(T, s, l);
     __syncwarp();
     const uint32_t bad = __ballot_sync(0xffffffffu, !ok);
