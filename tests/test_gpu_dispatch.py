@@ -82,6 +82,29 @@ def test_dispatch_equals_oracle(nvq, layout, T, K, topk, R):
     assert np.array_equal(_np(sf).reshape(-1), sfe)
 
 
+@pytest.mark.parametrize("K,pad", [(2048, 8), (272, 24)])
+def test_dispatch_strided_tokens(nvq, K, pad):
+    """Token rows with a pitch that is not a multiple of 16 elements (the 16-byte load path): the
+    same bytes as the oracle."""
+    T, topk, R = 96, 4, 500
+    rng = np.random.default_rng(K + pad)
+    bits = _tokens(T, K, K)
+    wide = np.zeros((T, K + pad), np.uint16)
+    wide[:, :K] = bits
+    x = workloads.from_bits(wide, "cuda")[:, :K]
+    assert x.stride(0) == K + pad and (K + pad) % 16 != 0
+    dest = rng.permutation(R)[:T * topk].reshape(T, topk).astype(np.int32)
+    qe, sfe, se = _expected(bits, dest, R, "mma")
+    out = (torch.full((R, K // 2), 0xAB, dtype=torch.uint8, device="cuda"),
+           torch.full((nvq.sf_bytes(R, K, 16),), 0xAB, dtype=torch.uint8, device="cuda"),
+           torch.full((R,), 0xABABABAB - 2 ** 32, dtype=torch.int32, device="cuda").view(torch.float32))
+    q, sf, s = nvq.nvfp4_quantize_dispatch(x, torch.from_numpy(dest).cuda(), R, out=out)
+    torch.cuda.synchronize()
+    assert np.array_equal(_np(q), qe)
+    assert np.array_equal(_np(s).view(np.uint32), se)
+    assert np.array_equal(_np(sf).reshape(-1), sfe)
+
+
 def test_dispatch_bad_index_sets_status_and_skips_the_entry(nvq):
     T, K, R = 4, 64, 16
     bits = _tokens(T, K, 3)
