@@ -1,6 +1,6 @@
-"""The bench's MoE step (the default line) as it is timed: the expert-weight quantizations run on a
-side stream joined by events, and its output must be bit-identical to the same launches run in
-order on one stream (the GEMMs accumulate in a fixed order, so any missing join would show)."""
+"""The bench's MoE and dense steps as they are timed: weight quantizations run on a side stream
+joined by events, and the output must be bit-identical to the same launches run in order on one
+stream (the GEMMs accumulate in a fixed order, so any missing join would show)."""
 import importlib.util
 import os
 
@@ -35,6 +35,28 @@ def test_moe_step_concurrent_equals_serial():
         torch.cuda.synchronize()
         timer.active = active                 # inactive: the timed schedule (side stream + joins)
         res = W["step"](timer, [x], (w1, w2))
+        torch.cuda.synchronize()
+        outs.append([o.clone() for o in res])
+    for other in outs[1:]:
+        for u, v in zip(outs[0], other):
+            assert torch.equal(u.view(torch.int16), v.view(torch.int16))
+
+
+def test_dense_step_concurrent_equals_serial():
+    import nvfp4_quantization_block_gb300 as nvq
+    import workloads
+    b = _bench()
+    dev = torch.device("cuda:0")
+    W = b.WORKLOADS["dense"](torch, nvq, workloads, dev)
+    x, w = W["inputs"]
+    timer = b.Timer(torch)
+    outs = []
+    for active in (False, True, False):
+        timer.active = True
+        W["step"](timer, x * 0.5, w * 2.0)    # other inputs: every intermediate buffer changes
+        torch.cuda.synchronize()
+        timer.active = active
+        res = W["step"](timer, x, w)
         torch.cuda.synchronize()
         outs.append([o.clone() for o in res])
     for other in outs[1:]:
