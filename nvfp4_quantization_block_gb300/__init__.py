@@ -202,7 +202,8 @@ def nvfp4_quantize_dispatch(x, dest, rows, sf_layout="mma", out=None, status=Non
                torch.empty(sf_bytes(rows, K, 16, lay), dtype=torch.uint8, device=dev),
                torch.empty(rows, dtype=torch.float32, device=dev))
     q, sf, s = out
-    st = _nvfp4_quantize_dispatch(_ptr(x), T, K, x.stride(0), _ptr(dest), int(dest.shape[1]), int(rows), _ptr(q),
+    ldx = x.stride(0) if T else K                        # an empty tensor may report stride 0
+    st = _nvfp4_quantize_dispatch(_ptr(x), T, K, ldx, _ptr(dest), int(dest.shape[1]), int(rows), _ptr(q),
                                   _ptr(sf), _ptr(s), lay, _ptr(status), _stream(dev))
     _check(st, "nvfp4_quantize_dispatch")
     return q, sf, s
