@@ -190,7 +190,7 @@ def nvfp4_quantize_dispatch(x, dest, rows, sf_layout="mma", out=None, status=Non
     """Quantize-once dispatch: per-token NVFP4 of the tokens x [T, K] (bf16 CUDA), written to the
     routed rows dest [T, topk] (int32 CUDA, -1 = not dispatched) of (q [rows, K/2], sf, s [rows]).
     Routed rows named by no entry are left as they are (fresh outputs: undefined there)."""
-    if not x.is_cuda or x.dtype != torch.bfloat16 or x.dim() != 2 or x.stride(1) != 1:
+    if not x.is_cuda or x.dtype != torch.bfloat16 or x.dim() != 2 or (x.shape[0] and x.stride(1) != 1):
         raise ValueError("expected a 2-D bf16 CUDA tensor with unit column stride")
     if dest.dtype != torch.int32 or dest.dim() != 2 or not dest.is_contiguous() or dest.shape[0] != x.shape[0]:
         raise ValueError("dest must be a contiguous int32 [tokens, topk] tensor")
