@@ -60,10 +60,10 @@ COPY_STREAMS = 4
 NCU_TRAFFIC = {
     # the weight quantizers: amax + encode launches of one call (check, finalize and zeroing move < 0.1 MB)
     "moe": {
-        "nvfp4_quantize_dispatch tokens -> routed gate_up input": {"bytes": 166387712, "src_sha": "8e3db3ad43581994"},
+        "nvfp4_quantize_dispatch tokens -> routed gate_up input": {"bytes": 164628608, "src_sha": "0bcc02f7ce47fa98"},
         "nvfp4_quantize_weights gate_up": {"bytes": 1814086912, "src_sha": "43bc634262ccb6ed"},
         "block_scaled_gemm NVFP4 gate_up": {"bytes": 758438144, "src_sha": "b555bf0a103e30fb"},
-        "nvfp4_swiglu_quantize_per_token down input": {"bytes": 450689792, "src_sha": "8e3db3ad43581994"},
+        "nvfp4_swiglu_quantize_per_token down input": {"bytes": 449146368, "src_sha": "0bcc02f7ce47fa98"},
         "nvfp4_quantize_weights down": {"bytes": 888220672, "src_sha": "43bc634262ccb6ed"},
         "block_scaled_gemm NVFP4 down": {"bytes": 663508224, "src_sha": "b555bf0a103e30fb"},
     },
