@@ -173,6 +173,22 @@ def test_nvfp4_per_token_bit_exact(nvq, fam, shape, layout):
     assert np.array_equal(_np(sf).reshape(want.shape), want)
 
 
+@pytest.mark.parametrize("shape", [(16001, 256), (7500, 1040)])
+def test_nvfp4_per_token_many_row_groups_per_warp(nvq, shape):
+    """More row groups than a 152-SM GPU holds resident warps, so each warp takes two or three in
+    turn and the last turn is ragged (two rows per warp at 256 columns, one at 1040): every byte
+    equals the oracle's in both scale layouts."""
+    bits = family("random", shape, seed=_seed("random", shape, 7))
+    q_ref, sf_ref, s_ref = oracle.nvfp4_quantize_per_token(bits)
+    for layout in ("canonical", "mma"):
+        q, sf, s = nvq.nvfp4_quantize_per_token(_dev(bits), sf_layout=layout)
+        torch.cuda.synchronize()
+        assert np.array_equal(_np(s).view(np.uint32), s_ref.view(np.uint32))
+        assert np.array_equal(_np(q), q_ref)
+        want = sf_ref if layout == "canonical" else oracle.sf_to_mma_layout(sf_ref)
+        assert np.array_equal(_np(sf).reshape(want.shape), want)
+
+
 @pytest.mark.parametrize("k", [-149, -140, -127, -120, -100, -91, -89])
 def test_nvfp4_tiny_token_scales(nvq, k):
     # tokens whose coarse scale is subnormal or just around the fp32 fast-path threshold

@@ -64,6 +64,22 @@ def test_swiglu_quantize_bit_exact(nvq, R, I, layout):
     _check(nvq, bits, layout, out)
 
 
+def test_swiglu_quantize_many_row_groups_per_warp(nvq):
+    # 13001 rows of 256 + 256: 6501 two-row groups, more than a 152-SM GPU holds resident warps, so
+    # each warp takes two or three in turn and the last turn is ragged (moderate gates and up values:
+    # over this many rows the extreme rows of _gate_up can overflow bf16)
+    R, I = 13001, 256
+    rng = np.random.default_rng(21)
+    g = rng.standard_normal((R, I)) * np.exp(rng.uniform(-3, 4, (R, 1)))
+    u = rng.standard_normal((R, I)) * np.exp(rng.uniform(-3, 3, (R, 1)))
+    g[rng.random((R, I)) < 0.01] *= 60.0                  # gates with |g| > 87 in most rows
+    bits = oracle.f64_to_bf16_bits_rne(np.concatenate([g, u], axis=1))
+    for layout in ("canonical", "mma"):
+        out = nvq.nvfp4_swiglu_quantize_per_token(workloads.from_bits(bits, "cuda"), sf_layout=layout)
+        torch.cuda.synchronize()
+        _check(nvq, bits, layout, out)
+
+
 def test_swiglu_quantize_division_ranges(nvq):
     # the division g / (1 + exp(-g)) over the ranges its fast steps cover and those they leave to
     # IEEE division: quotients near 2^-100 (tiny gates, huge exp(-g)), subnormal and zero gates
