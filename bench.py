@@ -18,9 +18,9 @@ the pages ablate, see workloads.py):
            W (dequantized-backward operand).
   backward the moe shapes in MXFP8 backward: row+col quantization of the routed X and dY, rowwise
            MXFP8 of the expert weights, grouped data-gradient GEMMs and grouped weight-gradient GEMMs.
-  decode   256 tokens, uniform top-8 (2048 routed rows): per-token NVFP4 of the activations and the
-           grouped NVFP4 gate_up GEMM against resident NVFP4 weights, plus the BF16 dequantization of
-           all gate_up expert weights.
+  decode   256 tokens, uniform top-8 (2048 routed rows): per-token NVFP4 of the activations, the
+           grouped NVFP4 gate_up GEMM, the fused SwiGLU + NVFP4 and the grouped NVFP4 down GEMM against
+           both resident NVFP4 weight stacks, plus the BF16 dequantization of all gate_up weights.
   dq_backward  the backward shapes with the dequantized-backward mode: BF16 dequantization of the
            MXFP8 operands and grouped BF16 GEMMs.
   quant, dispatch, swiglu, weights  (GB/s lines) the quantizers alone on the routed gate_up batch;
@@ -527,44 +527,65 @@ def _workload_dq_backward(torch, nvq, wl, dev):
 
 
 def _workload_decode(torch, nvq, wl, dev):
+    """One rollout-decode pass of the MoE expert layer: 256 tokens, uniform top-8 over 128 experts
+    (about 16 routed rows per expert), both NVFP4 weight stacks resident (quantized once, untimed)
+    and streamed by the two grouped GEMMs, plus the dequantized-backward copy of the gate_up weights."""
     counts = wl.route_counts(256, zipf_s=0.0, seed=0)
     offs_np = wl.padded_offsets(counts, 1)                # expert segments start at any row
     offs = torch.from_numpy(offs_np).to(dev)
     R = int(offs_np[-1])
-    E, H, I2 = wl.EXPERTS, wl.HIDDEN, 2 * wl.INTERMEDIATE
+    E, H, I = wl.EXPERTS, wl.HIDDEN, wl.INTERMEDIATE
+    I2 = 2 * I
     x = wl.routed_activations(counts, offs_np, H, seed=1, device=dev)
-    w = wl.expert_weights(H, I2, seed=3, device=dev)
-    wq = nvq.nvfp4_quantize_weights(w)          # resident NVFP4 weights (quantized once, untimed)
-    del w
+    w1 = wl.expert_weights(H, I2, seed=3, device=dev)
+    wq1 = nvq.nvfp4_quantize_weights(w1)        # resident NVFP4 weights (quantized once, untimed)
+    del w1
+    w2 = wl.expert_weights(I, H, seed=4, device=dev)
+    wq2 = nvq.nvfp4_quantize_weights(w2)
+    del w2
     real = float(counts.sum())
-    flops = 2.0 * real * I2 * H
-    a = (torch.empty((R, H // 2), dtype=torch.uint8, device=dev),
-         torch.empty(nvq.sf_bytes(R, H, 16), dtype=torch.uint8, device=dev),
-         torch.empty(R, dtype=torch.float32, device=dev))
-    d = torch.empty((R, I2), dtype=torch.bfloat16, device=dev)
+    f1, f2 = 2.0 * real * I2 * H, 2.0 * real * H * I
+    a1 = (torch.empty((R, H // 2), dtype=torch.uint8, device=dev),
+          torch.empty(nvq.sf_bytes(R, H, 16), dtype=torch.uint8, device=dev),
+          torch.empty(R, dtype=torch.float32, device=dev))
+    d1 = torch.empty((R, I2), dtype=torch.bfloat16, device=dev)
+    a2 = (torch.empty((R, I // 2), dtype=torch.uint8, device=dev),
+          torch.empty(nvq.sf_bytes(R, I, 16), dtype=torch.uint8, device=dev),
+          torch.empty(R, dtype=torch.float32, device=dev))
+    d2 = torch.empty((R, H), dtype=torch.bfloat16, device=dev)
     wdq = torch.empty((E * I2, H), dtype=torch.bfloat16, device=dev)
-    wbytes = E * I2 * H * (0.5 + 1 / 16) + 4 * E
+    wbytes1 = E * I2 * H * (0.5 + 1 / 16) + 4 * E
+    wbytes2 = E * H * I * (0.5 + 1 / 16) + 4 * E
     kernels = [
         Kernel("nvfp4_quantize_per_token decode activations", "hbm", R * H * 2.5625 + 4 * R, "quant_nvfp4.cu", "hbm", "2.5625 B/elem + 4 B/row"),
-        Kernel("block_scaled_gemm NVFP4 decode gate_up", "hbm", wbytes + R * H * 0.5625 + real * I2 * 2, "gemm_sm103.cu", "hbm",
+        Kernel("block_scaled_gemm NVFP4 decode gate_up", "hbm", wbytes1 + R * H * 0.5625 + real * I2 * 2, "gemm_sm103.cu", "hbm",
+               "NVFP4 weight bytes + activation bytes + bf16 output (memory-bound)"),
+        Kernel("nvfp4_swiglu_quantize_per_token decode down input", "hbm", R * I * 4.5625 + 4 * R, "quant_nvfp4.cu", "hbm",
+               "4 B read per h element (gate and up bf16) + 0.5625 B written + 4 B/row"),
+        Kernel("block_scaled_gemm NVFP4 decode down", "hbm", wbytes2 + R * I * 0.5625 + real * H * 2, "gemm_sm103.cu", "hbm",
                "NVFP4 weight bytes + activation bytes + bf16 output (memory-bound)"),
         Kernel("dequantize_bf16 gate_up weights", "hbm", E * I2 * H * (0.5625 + 2), "dequant.cu", "hbm", "2.5625 B/elem"),
     ]
 
     def step(timer, xin=None, win=None):
         xx = x if xin is None else xin[0]
-        timer.run(kernels[0].name, lambda: nvq.nvfp4_quantize_per_token(xx, out=a))
+        timer.run(kernels[0].name, lambda: nvq.nvfp4_quantize_per_token(xx, out=a1))
         timer.run(kernels[1].name, lambda: nvq.block_scaled_grouped_gemm(
-            nvq.NVFP4, nvq.GEMM_GROUP_M, a[0], a[1], wq[0], wq[1], offs, m=R, n=I2, k=H, groups=E,
-            s_a=a[2], s_b=wq[2], out=d))
-        timer.run(kernels[2].name, lambda: nvq.dequantize_bf16(
-            nvq.NVFP4, wq[0], wq[1], wq[2], nvq.SCOPE_MATRIX, groups=E, rows=I2, cols=H, out=wdq))
-        return [d]
+            nvq.NVFP4, nvq.GEMM_GROUP_M, a1[0], a1[1], wq1[0], wq1[1], offs, m=R, n=I2, k=H, groups=E,
+            s_a=a1[2], s_b=wq1[2], out=d1))
+        timer.run(kernels[2].name, lambda: nvq.nvfp4_swiglu_quantize_per_token(d1, out=a2))
+        timer.run(kernels[3].name, lambda: nvq.block_scaled_grouped_gemm(
+            nvq.NVFP4, nvq.GEMM_GROUP_M, a2[0], a2[1], wq2[0], wq2[1], offs, m=R, n=H, k=I, groups=E,
+            s_a=a2[2], s_b=wq2[2], out=d2))
+        timer.run(kernels[4].name, lambda: nvq.dequantize_bf16(
+            nvq.NVFP4, wq1[0], wq1[1], wq1[2], nvq.SCOPE_MATRIX, groups=E, rows=I2, cols=H, out=wdq))
+        return [d2]
 
-    config = {"workload": "rollout-decode NVFP4 expert GEMM (256 tokens, uniform top-8) + dequantize all gate_up weights",
+    config = {"workload": "rollout-decode NVFP4 MoE expert layer (256 tokens, uniform top-8): gate_up GEMM, "
+                          "SwiGLU + NVFP4, down GEMM, + dequantize all gate_up weights",
               "tokens": 256, "experts": E, "routed_rows": int(real), "buffer_rows": R,
-              "weights_nvfp4_mb": round(wbytes / 1e6, 1)}
-    return {"step": step, "kernels": kernels, "gemm_flops": flops, "inputs": [x], "input_groups": ([0], []),
+              "weights_nvfp4_mb": round((wbytes1 + wbytes2) / 1e6, 1)}
+    return {"step": step, "kernels": kernels, "gemm_flops": f1 + f2, "inputs": [x], "input_groups": ([0], []),
             "config": config, "dtype": "nvfp4(e2m1+e4m3+fp32) -> fp32 accumulate -> bf16"}
 
 

@@ -434,14 +434,18 @@ def test_full_size_mxfp8_data_gradient_sampled(nvq, layer):
         _check(got, Dv, bd, True)
 
 
-def test_full_size_decode_nvfp4(nvq):
+@pytest.mark.parametrize("layer", ["gate_up", "down"])
+def test_full_size_decode_nvfp4(nvq, layer):
     # the decode workload: 256 tokens, uniform top-8 over 128 experts (9..25 rows each, 2048 rows,
-    # unpadded), K = 2048, N = 1536; every row of 24 experts checked on 96 columns
+    # unpadded); gate_up K = 2048, N = 1536 or down K = 768, N = 2048; every row of 24 experts
+    # checked on 96 columns
     counts = workloads.route_counts(256, zipf_s=0.0, seed=0)
     offs = workloads.padded_offsets(counts, 1)
-    K, N, E = workloads.HIDDEN, 2 * workloads.INTERMEDIATE, workloads.EXPERTS
+    K, N = (workloads.HIDDEN, 2 * workloads.INTERMEDIATE) if layer == "gate_up" else \
+        (workloads.INTERMEDIATE, workloads.HIDDEN)
+    E = workloads.EXPERTS
     x = workloads.routed_activations(counts, offs, K, seed=1, device="cuda")
-    w = workloads.expert_weights(K, N, seed=3, device="cuda")
+    w = workloads.expert_weights(K, N, seed=3 if layer == "gate_up" else 4, device="cuda")
     qa, sfa, sa = nvq.nvfp4_quantize_per_token(x)
     qb, sfb, sb = nvq.nvfp4_quantize_weights(w)
     M = x.shape[0]
