@@ -10,10 +10,11 @@
 //          fma(p, s, -t); the remainder's sign sets the last bit of t (round to odd), after which
 //          the bf16 conversion yields the single rounding of the exact product (Boldo & Melquiond,
 //          IEEE TC 2008). Tiny products, where the remainder could underflow, use fp64.
-// One thread produces one 32-element (MXFP8) or two 16-element (NVFP4) blocks: 16- or 8-byte loads,
-// 64- or 32-byte stores, one scale byte per block, streaming through HBM once. NVFP4 blocks look their 16
-// results up in a per-block table of the 8 possible bf16 values (byte permutes), so the E2M1
-// conversion instruction, which issues on a low-throughput pipe, is not used per element.
+// One thread produces one 32-element (MXFP8) block, or four (rows of a multiple of 64 elements) or
+// two 16-element NVFP4 blocks, with one scale byte per block, streaming through HBM once. NVFP4
+// blocks look their 16 results up in a per-block table of the 8 possible bf16 values (byte
+// permutes), so the E2M1 conversion instruction, which issues on a low-throughput pipe, is not
+// used per element.
 #include "nvq_device.cuh"
 #include "nvq_internal.h"
 
@@ -134,6 +135,43 @@ dequant_nvfp4_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ 
     }
 }
 
+// Four blocks per thread (64 elements of one row: blocks 4t .. 4t + 3 of the row-major grid of
+// 4-block groups): one 32-byte code load, the four scale bytes as one word (a row's four
+// consecutive blocks are adjacent bytes in both scale layouts), and four 256-bit stores that each
+// fill one whole 32-byte sector, so a warp's store instruction writes 32 complete sectors. For rows
+// of a multiple of 64 elements with q and out 32-byte aligned and sf 4-byte aligned.
+__global__ void __launch_bounds__(256)
+dequant_nvfp4_x4_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ sf,
+                        const float* __restrict__ s, int64_t rows_per_group, int64_t total_rows,
+                        int64_t cols, int scope_matrix, int mma_layout, uint16_t* __restrict__ out) {
+    griddep_begin();
+    const int64_t nkb = cols >> 4;                             // a multiple of 4
+    const int64_t ngrp = total_rows * (nkb >> 2);
+    const int64_t grp = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (grp >= ngrp) return;
+    const bool small = ngrp <= 0xFFFFFFFFll;
+    int64_t row, kq;
+    block_coords(grp, nkb >> 2, small, row, kq);
+    const int64_t kb = 4 * kq;
+    int64_t scope = row;
+    if (scope_matrix) {
+        if (small) scope = (int64_t)((uint32_t)row / (uint32_t)rows_per_group);
+        else scope = row / rows_per_group;
+    }
+    const float coarse = s[scope];
+    const uint32_t sfw = *reinterpret_cast<const uint32_t*>(sf + sf_index(row, kb, nkb, mma_layout));
+    uint4 a, b;
+    ld_v8(q + row * (cols >> 1) + kb * 8, a, b);
+    const uint2 packed[4] = {make_uint2(a.x, a.y), make_uint2(a.z, a.w), make_uint2(b.x, b.y), make_uint2(b.z, b.w)};
+    uint16_t* dst = out + row * cols + kb * 16;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        uint4 d0, d1;
+        dequant_nvfp4_block(packed[i], e4m3_to_f32((uint8_t)(sfw >> (8 * i))), coarse, d0, d1);
+        st_sector(dst + 16 * i, d0, d1);
+    }
+}
+
 cudaError_t launch_dequantize_bf16(int fmt_nvfp4, const uint8_t* q, const uint8_t* sf, const float* s,
                                    int scope_matrix, int64_t groups, int64_t rows, int64_t cols,
                                    int mma_layout, uint16_t* out, cudaStream_t stream) {
@@ -143,6 +181,11 @@ cudaError_t launch_dequantize_bf16(int fmt_nvfp4, const uint8_t* q, const uint8_
         const int64_t nblk = total_rows * (cols >> 5);
         lerr = launch_pdl(dequant_mxfp8_kernel, dim3((unsigned)((nblk + 255) / 256)), dim3(256), 0, stream, q, sf,
                           total_rows, cols, mma_layout, out);
+    } else if (cols % 64 == 0 && (reinterpret_cast<uintptr_t>(q) & 31u) == 0 &&
+               (reinterpret_cast<uintptr_t>(out) & 31u) == 0 && (reinterpret_cast<uintptr_t>(sf) & 3u) == 0) {
+        const int64_t threads = total_rows * (cols >> 6);
+        lerr = launch_pdl(dequant_nvfp4_x4_kernel, dim3((unsigned)((threads + 255) / 256)), dim3(256), 0, stream, q,
+                          sf, s, rows, total_rows, cols, scope_matrix, mma_layout, out);
     } else {
         const int64_t nblk = total_rows * (cols >> 4);
         const int64_t threads = (nblk + 1) / 2;

@@ -351,30 +351,40 @@ def test_dequantize_mxfp8_bit_exact(nvq, fam, layout):
 
 @pytest.mark.parametrize("fam", FAMILIES + ["tiny"])
 @pytest.mark.parametrize("layout", ["canonical", "mma"])
-def test_dequantize_nvfp4_rows_bit_exact(nvq, fam, layout):
+@pytest.mark.parametrize("shape", [(96, 272), (100, 512)])     # two-block path; four-block path
+def test_dequantize_nvfp4_rows_bit_exact(nvq, fam, layout, shape):
+    R, C = shape
     if fam == "tiny":
-        x = np.random.default_rng(6).standard_normal((96, 272)) * 2.0 ** -120
+        x = np.random.default_rng(6).standard_normal(shape) * 2.0 ** -120
         bits = _bits_of(x)
     else:
-        bits = family(fam, (96, 272), seed=6)
+        bits = family(fam, shape, seed=6)
     q, sf, s = oracle.nvfp4_quantize_per_token(bits)
     want = oracle.dequantize_nvfp4(q, sf, s)
     sfl = sf if layout == "canonical" else oracle.sf_to_mma_layout(sf)
     out = nvq.dequantize_bf16(nvq.NVFP4, torch.from_numpy(q).cuda(), torch.from_numpy(sfl).cuda(),
-                              torch.from_numpy(s).cuda(), nvq.SCOPE_ROW, rows=96, cols=272, sf_layout=layout)
+                              torch.from_numpy(s).cuda(), nvq.SCOPE_ROW, rows=R, cols=C, sf_layout=layout)
     got = out.view(torch.int16).cpu().numpy().view(np.uint16)
     assert np.array_equal(got, want)
 
 
-def test_dequantize_nvfp4_weights_matrix_scope(nvq):
+@pytest.mark.parametrize("layout", ["canonical", "mma"])
+@pytest.mark.parametrize("out_offset", [0, 8])   # 8 bf16 = 16 bytes: output off the 32-byte grid
+def test_dequantize_nvfp4_weights_matrix_scope(nvq, layout, out_offset):
+    # K = 128: rows of a multiple of 64 elements take the four-block path when the output is
+    # 32-byte aligned and the two-block path otherwise; both give the oracle's bits
     E, K, N = 3, 128, 64
     rng = np.random.default_rng(7)
     bits = _bits_of(rng.standard_normal((E, K, N)) * 0.02)
     q, sf, s_w = oracle.nvfp4_quantize_weights(bits)
-    want = oracle.dequantize_nvfp4(q.reshape(E * N, K // 2), sf.reshape(E * N, K // 16), np.repeat(s_w, N))
-    out = nvq.dequantize_bf16(nvq.NVFP4, torch.from_numpy(q).cuda(), torch.from_numpy(sf).cuda(),
-                              torch.from_numpy(s_w).cuda(), nvq.SCOPE_MATRIX, groups=E, rows=N, cols=K,
-                              sf_layout="canonical")
+    sf2 = sf.reshape(E * N, K // 16)
+    want = oracle.dequantize_nvfp4(q.reshape(E * N, K // 2), sf2, np.repeat(s_w, N))
+    sfl = sf2 if layout == "canonical" else oracle.sf_to_mma_layout(sf2)
+    buf = torch.empty(E * N * K + 16, dtype=torch.bfloat16, device="cuda")
+    out = buf[out_offset:out_offset + E * N * K].view(E * N, K)
+    nvq.dequantize_bf16(nvq.NVFP4, torch.from_numpy(q).cuda(), torch.from_numpy(sfl).cuda(),
+                        torch.from_numpy(s_w).cuda(), nvq.SCOPE_MATRIX, groups=E, rows=N, cols=K,
+                        sf_layout=layout, out=out)
     got = out.view(torch.int16).cpu().numpy().view(np.uint16)
     assert np.array_equal(got, want)
 
