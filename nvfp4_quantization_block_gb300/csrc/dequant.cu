@@ -60,9 +60,16 @@ dequant_mxfp8_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ 
         o[2 * i] = cvt_bf16x2(f0 * scale, f1 * scale);
         o[2 * i + 1] = cvt_bf16x2(f2 * scale, f3 * scale);
     }
-    uint4* dst = reinterpret_cast<uint4*>(out + row * cols + kb * 32);
+    // the block's 64 output bytes: two 256-bit stores of whole sectors when out is 32-byte aligned
+    uint16_t* dst = out + row * cols + kb * 32;
+    if ((reinterpret_cast<uintptr_t>(out) & 31u) == 0) {
+        st_sector(dst, make_uint4(o[0], o[1], o[2], o[3]), make_uint4(o[4], o[5], o[6], o[7]));
+        st_sector(dst + 16, make_uint4(o[8], o[9], o[10], o[11]), make_uint4(o[12], o[13], o[14], o[15]));
+    } else {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+        for (int i = 0; i < 4; ++i)
+            reinterpret_cast<uint4*>(dst)[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+    }
 }
 
 // RN_bf16(p * s) for exact fp32 p and s (both finite).

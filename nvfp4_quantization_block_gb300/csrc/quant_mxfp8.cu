@@ -145,12 +145,19 @@ mxfp8_quant_kernel(const uint16_t* __restrict__ x, int64_t R, int64_t C, int64_t
             ohi[i] = cvt_e4m3x2(bf16_hi(a[0]) * inv_hi, bf16_hi(a[1]) * inv_hi) |
                      (cvt_e4m3x2(bf16_hi(a[2]) * inv_hi, bf16_hi(a[3]) * inv_hi) << 16);
         }
-        uint4* plo = reinterpret_cast<uint4*>(q_colT + c * R + rs);
-        uint4* phi = reinterpret_cast<uint4*>(q_colT + (c + 1) * R + rs);
-        plo[0] = make_uint4(olo[0], olo[1], olo[2], olo[3]);
-        plo[1] = make_uint4(olo[4], olo[5], olo[6], olo[7]);
-        phi[0] = make_uint4(ohi[0], ohi[1], ohi[2], ohi[3]);
-        phi[1] = make_uint4(ohi[4], ohi[5], ohi[6], ohi[7]);
+        // each column's 32 codes are one 32-byte sector (R % 32 == 0, rs a multiple of 32): one
+        // 256-bit store when q_colT is 32-byte aligned, so no store instruction writes half sectors
+        uint8_t* plo = q_colT + c * R + rs;
+        uint8_t* phi = q_colT + (c + 1) * R + rs;
+        if ((reinterpret_cast<uintptr_t>(q_colT) & 31u) == 0) {
+            st_sector(plo, make_uint4(olo[0], olo[1], olo[2], olo[3]), make_uint4(olo[4], olo[5], olo[6], olo[7]));
+            st_sector(phi, make_uint4(ohi[0], ohi[1], ohi[2], ohi[3]), make_uint4(ohi[4], ohi[5], ohi[6], ohi[7]));
+        } else {
+            reinterpret_cast<uint4*>(plo)[0] = make_uint4(olo[0], olo[1], olo[2], olo[3]);
+            reinterpret_cast<uint4*>(plo)[1] = make_uint4(olo[4], olo[5], olo[6], olo[7]);
+            reinterpret_cast<uint4*>(phi)[0] = make_uint4(ohi[0], ohi[1], ohi[2], ohi[3]);
+            reinterpret_cast<uint4*>(phi)[1] = make_uint4(ohi[4], ohi[5], ohi[6], ohi[7]);
+        }
     }
     sfT_stage[2 * cp][rb] = (uint8_t)sf_lo;
     sfT_stage[2 * cp + 1][rb] = (uint8_t)sf_hi;

@@ -146,6 +146,21 @@ def test_mxfp8_rowwise_only_ragged_rows(nvq, shape):
         assert np.array_equal(_np(out["sf_row"]).reshape(want.shape), want)
 
 
+def test_mxfp8_columnwise_output_off_the_32_byte_grid(nvq):
+    # q_colT 16 bytes past a 32-byte boundary: the columnwise codes take 16-byte stores instead of
+    # one 256-bit store per column and block; the bytes are the same
+    R, C = 96, 160
+    bits = family("random", (R, C), seed=8)
+    ref = oracle.mxfp8_quantize(bits)
+    buf = torch.empty(C * R + 32, dtype=torch.uint8, device="cuda")
+    qT = buf[16:16 + C * R].view(C, R)
+    out = nvq.mxfp8_quantize(_dev(bits), sf_layout="canonical", out={"q_colT": qT})
+    torch.cuda.synchronize()
+    assert np.array_equal(_np(out["q_colT"]), ref["q_colT"])
+    assert np.array_equal(_np(out["sf_colT"]).reshape(ref["sf_colT"].shape), ref["sf_colT"])
+    assert np.array_equal(_np(out["q_row"]), ref["q_row"])
+
+
 def test_mxfp8_strided_input(nvq):
     bits = family("random", (128, 256), seed=4)
     big = torch.zeros((128, 320), dtype=torch.bfloat16, device="cuda")
@@ -338,13 +353,16 @@ def test_full_size_expert_weights_sampled(nvq, layer):
 # ------------------------------------------------------------------------------------------------
 @pytest.mark.parametrize("fam", FAMILIES)
 @pytest.mark.parametrize("layout", ["canonical", "mma"])
-def test_dequantize_mxfp8_bit_exact(nvq, fam, layout):
+@pytest.mark.parametrize("out_offset", [0, 8])   # 8 bf16 = 16 bytes: output off the 32-byte grid
+def test_dequantize_mxfp8_bit_exact(nvq, fam, layout, out_offset):
     bits = family(fam, (160, 224), seed=5)
     ref = oracle.mxfp8_quantize(bits, colwise=False)
     want = oracle.dequantize_mxfp8(ref["q_row"], ref["sf_row"])
     sf = ref["sf_row"] if layout == "canonical" else oracle.sf_to_mma_layout(ref["sf_row"])
-    out = nvq.dequantize_bf16(nvq.MXFP8, torch.from_numpy(ref["q_row"]).cuda(), torch.from_numpy(sf).cuda(),
-                              rows=160, cols=224, sf_layout=layout)
+    buf = torch.empty(160 * 224 + 16, dtype=torch.bfloat16, device="cuda")
+    out = buf[out_offset:out_offset + 160 * 224].view(160, 224)
+    nvq.dequantize_bf16(nvq.MXFP8, torch.from_numpy(ref["q_row"]).cuda(), torch.from_numpy(sf).cuda(),
+                        rows=160, cols=224, sf_layout=layout, out=out)
     got = out.view(torch.int16).cpu().numpy().view(np.uint16)
     assert np.array_equal(got, want)
 
