@@ -494,6 +494,44 @@ nvfp4_dispatch_kernel(const uint16_t* __restrict__ x, int64_t T, int64_t C, int6
         token_rows<V8, false, 32, false, false>(xt, C, ldx, sq, ssf, ss, 0, true, true, lane, 0, tables[warp], info);
     __syncwarp();
     const float s = *ss;
+    if (qb <= 1024 && (qb & 15) == 0) {
+        // rows of at most 2048 elements: each lane's share of the staged token (two 16-byte code
+        // pieces and one scale word) is read from shared memory once and stored from registers to
+        // every routed row
+        const int64_t o0 = (int64_t)lane * 16, o1 = o0 + 512;
+        uint4 c0 = make_uint4(0u, 0u, 0u, 0u), c1 = c0;
+        if (o0 < qb) c0 = *reinterpret_cast<const uint4*>(sq + o0);
+        if (o1 < qb) c1 = *reinterpret_cast<const uint4*>(sq + o1);
+        uint32_t word = 0u;
+        const int64_t valid = nkb - 4 * (int64_t)lane;         // scale bytes of the lane's group that exist
+        if (lane < ngr) {
+            word = *reinterpret_cast<const uint32_t*>(ssf + 4 * lane);
+            if (valid < 4) word &= (1u << (8 * valid)) - 1u;
+        }
+        for (int k = 0; k < topk; ++k) {
+            const int32_t r = __shfl_sync(0xffffffffu, mine, k);
+            if (r == -1) continue;                             // uniform over the warp
+            if (r < 0 || r >= R) {
+                if (lane == 0 && status != nullptr) atomicExch(status, NVQ_DEV_BAD_INDEX);
+                continue;
+            }
+            uint8_t* qd = q + (int64_t)r * qb;
+            if (o0 < qb) *reinterpret_cast<uint4*>(qd + o0) = c0;
+            if (o1 < qb) *reinterpret_cast<uint4*>(qd + o1) = c1;
+            if (lane < ngr) {
+                if (MMA) {
+                    *reinterpret_cast<uint32_t*>(sf + mma_sf_offset(r, 4 * lane, nkb)) = word;
+                } else if ((nkb & 3) == 0) {
+                    *reinterpret_cast<uint32_t*>(sf + (int64_t)r * nkb + 4 * lane) = word;
+                } else {
+                    for (int64_t j = 0; j < 4 && j < valid; ++j)
+                        sf[(int64_t)r * nkb + 4 * lane + j] = (uint8_t)(word >> (8 * j));
+                }
+            }
+            if (lane == 0) s_tok[r] = s;
+        }
+        return;
+    }
     for (int k = 0; k < topk; ++k) {
         const int32_t r = __shfl_sync(0xffffffffu, mine, k);
         if (r == -1) continue;                                 // uniform over the warp

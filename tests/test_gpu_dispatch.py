@@ -60,7 +60,7 @@ def _expected(bits, dest, R, layout):
 
 @pytest.mark.parametrize("layout", ["canonical", "mma"])
 @pytest.mark.parametrize("T,K,topk,R", [(200, 272, 3, 700), (64, 2048, 8, 600), (33, 4096, 2, 70), (9, 16, 5, 50),
-                                        (130, 768, 8, 1100), (8, 16384, 2, 20), (0, 64, 4, 200)])
+                                        (130, 768, 8, 1100), (8, 16384, 2, 20), (0, 64, 4, 200), (40, 96, 3, 150)])
 def test_dispatch_equals_oracle(nvq, layout, T, K, topk, R):
     rng = np.random.default_rng(T + K + topk)
     bits = _tokens(T, K, T * K) if T else np.zeros((0, K), np.uint16)   # T = 0: only the padding rows
